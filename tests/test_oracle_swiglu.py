@@ -1,0 +1,83 @@
+"""Pins of the oracle's SwiGLU specification: the exponential against
+float64 exp, the activation against a float64 SiLU(g)*u, and the special
+cases that reduce to closed forms."""
+
+import numpy as np
+import torch
+
+import oracle as O
+from w8a16_linear_gb300 import synth
+
+
+def test_exp_spec_accuracy_dense_sweep():
+    t = np.linspace(-87.0, 88.0, 3_000_001).astype(np.float32)
+    e = O.exp_spec(t).astype(np.float64)
+    ref = np.exp(t.astype(np.float64))
+    ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    normal = ref > 2.0 ** -126
+    assert (np.abs(e - ref) / ulp)[normal].max() <= 2.0
+
+
+def test_exp_spec_special_values():
+    t = np.array([0.0, -0.0, 88.5, np.inf, -88.5, -np.inf], np.float32)
+    e = O.exp_spec(t)
+    assert e[0] == 1.0 and e[1] == 1.0
+    assert np.isinf(e[2]) and np.isinf(e[3])
+    assert e[4] == 0.0 and e[5] == 0.0
+
+
+def test_swiglu_against_float64_silu():
+    g = synth.random_bf16_bits(0, (200_000,))
+    u = synth.activations_bf16(1, (200_000,), 1.0)
+    gf, uf = O.bf16_decode(g), O.bf16_decode(u)
+    ok = np.isfinite(gf) & (np.abs(gf) < 1e30) & np.isfinite(uf)
+    g, u, gf, uf = g[ok], u[ok], gf[ok].astype(np.float64), uf[ok].astype(np.float64)
+    with np.errstate(over="ignore"):
+        ref = gf * uf / (1.0 + np.exp(-gf))
+    h = O.swiglu_h(g, u).astype(np.float64)
+    fin = np.isfinite(ref) & (np.abs(ref) > 2.0 ** -120) & (np.abs(ref) < 3e38)
+    ulp = np.spacing(np.abs(ref[fin]).astype(np.float32)).astype(np.float64)
+    assert (np.abs(h[fin] - ref[fin]) / ulp).max() <= 4.0
+
+
+def test_swiglu_closed_forms():
+    def bits(v):
+        return torch.tensor(v, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    g = bits([0.0, 20.0, 100.0, -100.0, 30.0])
+    u = bits([5.0, 1.5, -0.75, 3.0, 2.0])
+    h = O.swiglu_h(g, u)
+    assert h[0] == 0.0                       # silu(0) = 0
+    assert h[1] == np.float32(30.0)          # exp(-20) < 2^-24: 1 + e rounds to 1
+    assert h[2] == np.float32(-75.0)
+    assert h[3] == 0.0                       # exp(100) = inf: p / inf
+    s = np.float32(0.25)
+    assert O.swiglu_2in_fp8(g, u, s)[4] == O.e4m3_encode(np.array([240.0], np.float32))[0]
+
+
+def test_swiglu_fp8_codes_agree_with_float64_away_from_midpoints():
+    """FP8 codes equal those of the float64 value except where that value is
+    within 2^-18 (relative) of an E4M3 rounding boundary."""
+    g = synth.activations_bf16(3, (300_000,), 2.0)
+    u = synth.activations_bf16(4, (300_000,), 1.0)
+    s = np.float32(0.01)
+    gf, uf = O.bf16_decode(g).astype(np.float64), O.bf16_decode(u).astype(np.float64)
+    v = gf * uf / (1.0 + np.exp(-gf)) / float(s)
+    code64 = O.e4m3_encode(v.astype(np.float32))  # the float32 rounding of v is within 2^-24
+    got = O.swiglu_2in_fp8(g, u, s)
+    # distance of v to the nearest E4M3 decision midpoint
+    codes, vals = O.e4m3_all_values()
+    fv = np.sort(np.unique(np.abs(vals[~np.isnan(vals)])).astype(np.float64))
+    mids = (fv[1:] + fv[:-1]) / 2
+    idx = np.clip(np.searchsorted(mids, np.abs(v)), 1, len(mids) - 1)
+    dist = np.minimum(np.abs(np.abs(v) - mids[idx]), np.abs(np.abs(v) - mids[idx - 1]))
+    near = dist <= np.abs(v) * 2.0 ** -18
+    assert np.array_equal(got[~near], code64[~near])
+    assert near.mean() < 1e-3
+
+
+def test_swiglu_bf16_output_is_rounded_h():
+    g = synth.activations_bf16(5, (1000,), 2.0)
+    u = synth.activations_bf16(6, (1000,), 1.0)
+    assert np.array_equal(O.swiglu_2in_bf16(g, u), O.bf16_round(O.swiglu_h(g, u)))
+    ref = torch.from_numpy(O.swiglu_h(g, u)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.swiglu_2in_bf16(g, u), ref)
