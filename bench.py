@@ -1,0 +1,383 @@
+"""Benchmark of the static per-tensor FP8 linear path on GB300.
+
+Workload (the headline): split Q/K/V with one shared activation
+quantization, 20670 tokens (a 13x30x53 latent grid), hidden 4096, three
+4096x4096 E4M3 weights with distinct weight scales and one static input
+scale.  One step = ``qkv_shared_quant_gemm`` in W8A8 mode: one quantization
+kernel plus one persistent tcgen05 GEMM launch over the three projections.
+Metric: W8A8 FP8 linear TFLOPS (3 * 2 * M * N * K per step / step time).
+
+Other kernels of the path (W8A16 group, SwiGLU FP8/bf16, the gated-MLP
+projections) are timed after the headline and reported under "breakdown".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torchrun; every rank runs an independent replica (the
+path has no cross-GPU step) and rank 0 prints the aggregate.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_TOK, HID, INTER = 20670, 4096, 16384
+GEMM_FLOPS = 3 * 2.0 * M_TOK * HID * HID
+METRIC = "W8A8 FP8 linear TFLOPS (M≈20k, K=N=4096) and % of GB300 dense FP8 peak"
+WORKLOAD = "split QKV, shared static-FP8 activation quant, M=20670 (13x30x53), 3 x 4096x4096"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:  # noqa: BLE001
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.dev = dev_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:  # noqa: BLE001
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- inputs
+
+def make_inputs(dev, seed=0):
+    """Synthetic device-resident inputs (drawn on the GPU with torch's seeded
+    generator; E4M3 weights from scaled normal draws with amax calibration)."""
+    g = torch.Generator(device=dev).manual_seed(seed)
+    x = torch.randn((M_TOK, HID), generator=g, device=dev) * 0.25
+    k = int(x.numel() * 0.001)
+    idx = torch.randint(0, x.numel(), (k,), generator=g, device=dev)
+    x.view(-1)[idx] *= 8.0
+    x = x.to(torch.bfloat16)
+    s_in = (x.float().abs().amax() / 448.0).reshape(1).contiguous()
+
+    def weight(n, kk, mult):
+        w = torch.randn((n, kk), generator=g, device=dev) * (0.02 * mult)
+        s = (w.abs().amax() / 448.0).reshape(1).contiguous()
+        q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        return q.contiguous(), s
+
+    c = (torch.rand(3, generator=g, device=dev) * 0.5 + 0.5).tolist()
+    qkv = [weight(HID, HID, c[i]) for i in range(3)]
+    return x, s_in, qkv, weight
+
+
+def flush_l2(buf):
+    buf.add_(1.0)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, dev):
+    import w8a16_linear_gb300 as W
+    W.device_check()
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    x, s_in, qkv, weight = make_inputs(dev)
+    ws_q = [q for q, _ in qkv]
+    ws_s = [s for _, s in qkv]
+    ys = [torch.empty((M_TOK, HID), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    qx = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        W.qkv_shared_quant_gemm(W.MODE_A8, x, s_in, ws_q, ws_s, outs=ys, ws=qx)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    W.poll_device_error()
+
+    # ---- timed region: K steps, L2 flushed between steps (outside the events)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        flush_l2(flush)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    W.poll_device_error()
+
+    # ---- dominant kernel: the 3-projection GEMM launch alone, same stream
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_l2(flush)
+        gev[i][0].record(stream)
+        W.fp8_linear_w8a8_group(qx, s_in, ws_q, ws_s, outs=ys)
+        gev[i][1].record(stream)
+    torch.cuda.synchronize()
+    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in gev)
+
+    # ---- end to end through the public API with host buffers
+    xh = x.cpu().pin_memory()
+    yh = [torch.empty((M_TOK, HID), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    xd = torch.empty_like(x)
+    e2e_steps = max(3, min(args.steps, 10))
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush_l2(flush)
+        eev[i][0].record(stream)
+        xd.copy_(xh, non_blocking=True)
+        W.qkv_shared_quant_gemm(W.MODE_A8, xd, s_in, ws_q, ws_s, outs=ys, ws=qx)
+        for y, h in zip(ys, yh):
+            h.copy_(y, non_blocking=True)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+
+    breakdown = breakdown_ours(W, dev, stream, x, s_in, ws_q, ws_s, ys, qx, weight, flush, args)
+
+    return {"total_ms": total_ms, "step_ms": step_ms, "gemm_ms": gemm_ms, "e2e_ms": e2e_ms,
+            "h2d": x.numel() * 2, "d2h": 3 * M_TOK * HID * 2, "clocks": clk,
+            "breakdown": breakdown}
+
+
+def _time(fn, flush, stream, n):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    fn()
+    for i in range(n):
+        flush_l2(flush)
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def breakdown_ours(W, dev, stream, x, s_in, ws_q, ws_s, ys, qx, weight, flush, args):
+    n = max(3, min(args.steps, 10))
+    out = {}
+    ms = _time(lambda: W.fp8_quant_static(x, s_in, out=qx), flush, stream, n)
+    out["fp8_quant_static"] = {"us": ms * 1e3, "GB_s": 3 * x.numel() / ms / 1e6}
+    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, ws_q, ws_s, outs=ys), flush, stream, n)
+    out["qkv_w8a16_group"] = {"us": ms * 1e3, "TFLOPS": GEMM_FLOPS / ms / 1e9}
+    ms = _time(lambda: W.fp8_linear_w8a8_group(qx, s_in, ws_q[:1], ws_s[:1], outs=ys[:1]), flush, stream, n)
+    out["w8a8_single_4096"] = {"us": ms * 1e3, "TFLOPS": GEMM_FLOPS / 3 / ms / 1e9}
+    del ys
+    g = torch.randn((M_TOK, INTER), device=dev).to(torch.bfloat16)
+    u = torch.randn((M_TOK, INTER), device=dev).to(torch.bfloat16)
+    h8 = torch.empty((M_TOK, INTER), dtype=torch.uint8, device=dev)
+    h16 = torch.empty((M_TOK, INTER), dtype=torch.bfloat16, device=dev)
+    s_out = torch.tensor([0.02], device=dev)
+    ms = _time(lambda: W.swiglu_2in_fp8(g, u, s_out, out=h8), flush, stream, n)
+    out["swiglu_2in_fp8"] = {"us": ms * 1e3, "GB_s": 5 * g.numel() / ms / 1e6}
+    ms = _time(lambda: W.swiglu_2in_bf16(g, u, out=h16), flush, stream, n)
+    out["swiglu_2in_bf16"] = {"us": ms * 1e3, "GB_s": 6 * g.numel() / ms / 1e6}
+    del h16
+    qg, sg = weight(INTER, HID, 0.8)
+    qd, sd = weight(HID, INTER, 0.9)
+    yg = torch.empty((M_TOK, INTER), dtype=torch.bfloat16, device=dev)
+    ms = _time(lambda: W.fp8_linear_w8a8_group(qx, s_in, [qg], [sg], outs=[yg]), flush, stream, n)
+    out["w8a8_gate_4096x16384"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
+    yd = torch.empty((M_TOK, HID), dtype=torch.bfloat16, device=dev)
+    ms = _time(lambda: W.fp8_linear_w8a8_group(h8, s_out, [qd], [sd], outs=[yd]), flush, stream, n)
+    out["w8a8_down_16384x4096"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
+    torch.cuda.synchronize()
+    W.poll_device_error()
+    return out
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def run_oracle_sample(rows=512, seed=0):
+    """The CPU oracle on a bounded sample of the workload: ``rows`` tokens of
+    the split-QKV step (quantization plus the three W8A8 projections)."""
+    import oracle as O
+    from w8a16_linear_gb300 import synth
+    x = synth.activations_bf16(seed, (rows, HID), 0.25, outlier_frac=0.001)
+    s_in = np.float32(np.abs(O.bf16_decode(x)).max() / 448)
+    qws, s_ws = [], []
+    for i in range(3):
+        w = synth.normal_f32(10 + i, (HID, HID), 0.02)
+        s = np.float32(np.abs(w).max() / 448)
+        qws.append(O.e4m3_encode(w / s))
+        s_ws.append(s)
+    t0 = time.perf_counter()
+    O.qkv_shared_quant_gemm("A8", x, s_in, qws, s_ws)
+    dt = time.perf_counter() - t0
+    flops = 3 * 2.0 * rows * HID * HID
+    return flops / dt / 1e12, dt, rows
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:  # noqa: BLE001
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        run_oracle_sample(rows=64)
+    vals, secs = [], []
+    rows = 512
+    for _ in range(args.steps):
+        v, dt, _ = run_oracle_sample(rows=rows)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.mean(vals)
+    ms = statistics.mean(secs) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_rows": rows, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{rows} of {M_TOK} tokens of the split-QKV step per bench step"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__ as g
+    if rank == 0:
+        g.build()
+    if world > 1:
+        torch.distributed.barrier()
+    g.build()
+
+    r = run_ours(args, rank, world, dev)
+    total_ms = r["total_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * GEMM_FLOPS * args.steps / (total_ms / 1e3) / 1e12
+
+    if rank == 0:
+        peaks = load_peaks()
+        fp8_peak = peaks["bf16_tflops"] * 2.0          # nominal FP8:BF16 dense ratio 4.5:2.25
+        achieved = GEMM_FLOPS / (r["gemm_ms"] / 1e3) / 1e12
+        cpu = None
+        if not args.no_cpu_baseline:
+            v, dt, rows = run_oracle_sample(rows=512)
+            cpu = {"value": v, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+                   "sample": f"{rows} of {M_TOK} tokens of the split-QKV step ({dt:.1f} s)"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M_TOK, "K": HID, "N": HID, "projections": 3,
+                       "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "kernel": "gemm_kernel<W8A8> (3-projection launch)",
+                         "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                         "frac": achieved / fp8_peak, "traffic": None,
+                         "peak_note": f"{peaks['source']} bf16 burst x 2 (nominal FP8/BF16 ratio)"},
+            "pct_of_5pf_fp8": value / 5000.0,
+            "cpu_baseline": cpu,
+            "e2e": {"value": GEMM_FLOPS / (r["e2e_ms"] / 1e3) / 1e12, "unit": "TFLOPS",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": 2 * args.steps,
+            "clocks": r["clocks"],
+            "breakdown": r["breakdown"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,223 @@
+/*
+ * w8lin.h — C ABI of the static per-tensor FP8 linear layer for GB300 (sm_103a).
+ *
+ * Sources of the operations (web pages; cited by title and section):
+ *  [P1] diffusers issue #15170, "Cosmos 3 docs: FP8 snippet fails at the first
+ *       W8A8 step without importing ModelOpt's FP8 GEMM backend".
+ *  [P2] cosmos-framework PR #157, "feat: load ModelOpt static-FP8 checkpoints
+ *       via TorchAO".
+ *  [P3] diffusers PR #14664, "[Cosmos3] Mixed W8A8/W8A16 denoising for
+ *       ModelOpt FP8 checkpoints".
+ *  [P4] TensorRT-LLM PR #17476, "Load static FP8 Cosmos3 Nano/Super
+ *       checkpoints without re-quantizing them".
+ *
+ * Conventions shared by every entry point
+ *  - Data pointers are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or retains them.  Tensors are dense row-major:
+ *    activations [M, K], weights [N, K] (the exported nn.Linear.weight),
+ *    outputs [M, N].  There is no bias ([P1] Logs: bias=False).
+ *  - bf16 values travel as uint16_t bit patterns, E4M3 codes as uint8_t
+ *    (OCP E4M3 "fn": 4 exponent bits, bias 7, 3 mantissa bits, max 448).
+ *  - Scales are `const float*` to ONE float in device memory, never read on
+ *    the host: reading a scale on the hot path would synchronise the device
+ *    ([P4] What changed: the shared-scale invariant is checked at load, never
+ *    in forward).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every compute
+ *    entry point only enqueues work on it and returns; results are ready when
+ *    the stream reaches that point.
+ *  - Base pointers must be 16-byte aligned and K (and N for outputs) multiples
+ *    of 16 (E4M3 rows) / 8 (bf16 rows) so that every row starts on a 16-byte
+ *    boundary, as the tensor-memory-accelerator copies require.
+ *  - M == 0 is a no-op that returns W8_OK without launching anything (zero-row
+ *    inputs; [P2] Commits: the zero-row limitation it works around).
+ *    Tensors of rank > 2 are flattened to [M, K] by the caller.
+ *  - Arguments are validated on the host before any CUDA call; an invalid
+ *    argument returns its error code and enqueues nothing.  Thread-local
+ *    detail is available from w8_last_error().
+ *  - Kernels never trap.  A GEMM whose internal pipeline wait runs past its
+ *    deadline (2 s) stops, records W8_ERR_TIMEOUT in a device error word and
+ *    returns; w8_poll_device_error() reports and clears it.
+ */
+#ifndef W8LIN_H
+#define W8LIN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  W8_OK = 0,
+  W8_ERR_NULL = 1,     /* a required pointer is NULL */
+  W8_ERR_SHAPE = 2,    /* negative or unsupported size, or group size outside 1..3 */
+  W8_ERR_ALIGN = 3,    /* a pointer or row pitch is not 16-byte aligned */
+  W8_ERR_STRIDE = 4,   /* reserved: non-dense layouts are rejected by the binding */
+  W8_ERR_DTYPE = 5,    /* activation dtype not accepted by this path */
+  W8_ERR_ARCH = 6,     /* current device is not sm_103 */
+  W8_ERR_POLICY = 7,   /* step policy refused (schema, window, step range) */
+  W8_ERR_TIMEOUT = 8,  /* a kernel's bounded pipeline wait expired */
+  W8_ERR_CUDA = 9,     /* a CUDA runtime/driver call failed */
+  W8_ERR_SCALE = 10    /* projections of a sharing group carry different input scales */
+} w8_status;
+
+typedef enum { W8_DTYPE_BF16 = 0, W8_DTYPE_E4M3 = 1 } w8_dtype;
+
+/* Activation precision of one denoising step ([P3] Behavior). */
+typedef enum { W8_MODE_A8 = 0, W8_MODE_A16 = 1 } w8_mode;
+
+/* Per-denoising-step precision policy ([P4] Denoising-step activation
+ * precision: quantization_config.runtime.diffusion_step_policy). */
+typedef struct {
+  int32_t schema_version; /* must be 1 */
+  int32_t enabled;        /* 0 = the checkpoint carries no policy: every step W8A8 */
+  int32_t first_steps;    /* leading steps run W8A16 (published policy: 3) */
+  int32_t last_steps;     /* trailing steps run W8A16 (published policy: 3) */
+} w8_step_policy;
+
+/* Version of this ABI (bumped on any signature change). */
+int w8_abi_version(void);
+
+/* Thread-local text of the last error returned on this thread ("" if none). */
+const char* w8_last_error(void);
+
+/* W8_OK if the current CUDA device is an sm_103 part, else W8_ERR_ARCH. */
+w8_status w8_device_check(void);
+
+/* Synchronises `stream`, then returns W8_ERR_TIMEOUT (and clears the word)
+ * if any GEMM launched so far on the current device recorded a pipeline
+ * timeout, else W8_OK. */
+w8_status w8_poll_device_error(void* stream);
+
+/*
+ * fp8_quant_static — static per-tensor activation quantization.
+ * q[i] = E4M3_satRNE( fl32( x[i] / s_in ) ) for all M*K elements: one
+ * correctly rounded binary32 division, then one round-to-nearest-even to
+ * E4M3 with saturation at +-448 ([P2] Verification: div -> clamp ->
+ * round-to-float8 with the exported input_scale).  NaN inputs give a NaN code.
+ *   x    bf16 [M, K], device, read-only
+ *   s_in float scalar, device
+ *   q    E4M3 [M, K], device, written
+ * Errors: NULL, SHAPE (M<0, K<=0, K%16), ALIGN, ARCH, CUDA.
+ */
+w8_status fp8_quant_static(const uint16_t* x, int64_t M, int64_t K, const float* s_in, uint8_t* q,
+                           void* stream);
+
+/*
+ * fp8_linear_w8a8 — W8A8 FP8 linear.
+ * y = bf16_RNE( fl32(s_in * s_w) * sum_k dec(qx[m,k]) * dec(w[n,k]) ), F32
+ * accumulation on the tcgen05 tensor cores ([P2] Verification: _scaled_mm
+ * with the two per-tensor scales; [P3] Behavior: native W8A8 on middle steps).
+ *   x       activation [M, K]: bf16 if x_dtype == W8_DTYPE_BF16 (quantized
+ *           first with s_in into `ws`), or E4M3 codes already quantized with
+ *           s_in if x_dtype == W8_DTYPE_E4M3 (pass-through: [P4] What changed,
+ *           a pre-quantized input goes straight to the GEMM)
+ *   w       E4M3 weight [N, K]; s_in, s_w device float scalars
+ *   y       bf16 output [M, N], written
+ *   ws      E4M3 scratch [M, K], required iff x_dtype == W8_DTYPE_BF16,
+ *           else ignored (may be NULL)
+ * Errors: NULL, SHAPE (K%16, N%16), DTYPE, ALIGN, ARCH, CUDA.
+ */
+w8_status fp8_linear_w8a8(const void* x, int32_t x_dtype, int64_t M, int64_t K, const uint8_t* w,
+                          int64_t N, const float* s_in, const float* s_w, uint16_t* y, uint8_t* ws,
+                          void* stream);
+
+/*
+ * fp8_linear_w8a16 — W8A16 linear on the same E4M3 weight.
+ * y = bf16_RNE( sum_k x[m,k] * Wd[n,k] ), Wd = bf16_RNE( fl32(dec(w) * s_w) ),
+ * the dequantization done inside the GEMM with no dequantized copy in global
+ * memory; input_scale is unused ([P3] Behavior: dequant + F.linear; [P4]
+ * Denoising-step activation precision: same weights, same scales).
+ *   x_dtype must be W8_DTYPE_BF16: an already-quantized activation is refused
+ *   with W8_ERR_DTYPE ([P4] Denoising-step activation precision: the W8A16
+ *   linear raises rather than accept an already-quantized activation).
+ * Errors: NULL, SHAPE (K%16, N%16), DTYPE, ALIGN, ARCH, CUDA.
+ */
+w8_status fp8_linear_w8a16(const void* x, int32_t x_dtype, int64_t M, int64_t K, const uint8_t* w,
+                           int64_t N, const float* s_w, uint16_t* y, void* stream);
+
+/*
+ * qkv_shared_quant_gemm — a group of G projections sharing one activation
+ * (G = 3: split Q/K/V; G = 2: split gate/up), each with its own weight,
+ * weight scale and contiguous output ([P4] Description and What changed:
+ * projections stay split, the shared activation is quantized once and the
+ * same FP8 tensor is handed to every projection).
+ *   mode == W8_MODE_A8:  one fp8_quant_static of x into ws, then one
+ *                        persistent W8A8 launch over the tiles of all G
+ *                        projections, all reading ws.
+ *   mode == W8_MODE_A16: no quantization (sharing stands down on 16-bit
+ *                        steps, [P4] Denoising-step activation precision);
+ *                        one W8A16 launch over all G projections.
+ *   x          bf16 [M, K], device
+ *   s_in       device float scalar shared by the group (A8 only)
+ *   w, N, s_w, y  HOST arrays of G entries: device weight [N_g, K], its row
+ *              count, device weight scale, device output [M, N_g]
+ *   ws         E4M3 scratch [M, K] (A8 only; may be NULL for A16)
+ * Errors: NULL, SHAPE (G outside 2..3 or 1, K%16, N_g%16), ALIGN, ARCH, CUDA.
+ */
+w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int64_t K,
+                                const float* s_in, int32_t G, const uint8_t* const* w,
+                                const int64_t* N, const float* const* s_w, uint16_t* const* y,
+                                uint8_t* ws, void* stream);
+
+/*
+ * fp8_linear_w8a8_group — the GEMM half of qkv_shared_quant_gemm in A8 mode:
+ * G projections (1..3) over an activation that is ALREADY E4M3, quantized
+ * with s_in (for example by fp8_quant_static or swiglu_2in_fp8), in one
+ * persistent launch.  y_g = bf16_RNE( fl32(s_in * s_w[g]) * qx . w_g^T ).
+ *   qx   E4M3 [M, K], device;  w, N, s_w, y: HOST arrays of G entries as in
+ *   qkv_shared_quant_gemm.
+ * Errors: NULL, SHAPE, ALIGN, ARCH, CUDA.
+ */
+w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const float* s_in,
+                                int32_t G, const uint8_t* const* w, const int64_t* N,
+                                const float* const* s_w, uint16_t* const* y, void* stream);
+
+/*
+ * swiglu_2in_fp8 — out = E4M3_satRNE( fl32( h / s_out ) ) with
+ * h = fl32( fl32(g * u) / fl32(1 + exp_spec(-g)) ), SiLU(gate) * up from two
+ * separate tensors written straight to FP8 for the down projection
+ * ([P4] What changed: two-input SwiGLU quantizing directly for the FP8
+ * down_proj).  exp_spec is the library's binary32 exponential (Cody-Waite
+ * reduction, degree-7 Taylor polynomial; stated in the kernel source).
+ *   gate, up  bf16 [M, I], device;  s_out device float scalar (the down
+ *   projection's input_scale);  out E4M3 [M, I], device.
+ * Errors: NULL, SHAPE (I%16), ALIGN, ARCH, CUDA.
+ */
+w8_status swiglu_2in_fp8(const uint16_t* gate, const uint16_t* up, int64_t M, int64_t I,
+                         const float* s_out, uint8_t* out, void* stream);
+
+/* swiglu_2in_bf16 — bf16_RNE(h) with h as above; the 16-bit-step variant in
+ * which the FP8 output stands down ([P4] Denoising-step activation precision). */
+w8_status swiglu_2in_bf16(const uint16_t* gate, const uint16_t* up, int64_t M, int64_t I,
+                          uint16_t* out, void* stream);
+
+/*
+ * step_policy_dispatch — host-only, pure function of (policy, step, num_steps).
+ * policy == NULL or enabled == 0: W8_MODE_A8 on every step (a checkpoint with
+ * no policy runs fully quantized).  num_steps == 1: W8_MODE_A8 (the one-step
+ * carve-out, [P3] Tests: 1-step stays native).  Otherwise W8_MODE_A16 iff
+ * step < first_steps or step >= num_steps - last_steps ([P3] Behavior: first
+ * 3 + last 3 steps W8A16).  Steps are zero-based.
+ * Errors: NULL (mode_out), POLICY (schema_version != 1, negative window,
+ * step outside [0, num_steps)) — refused rather than partially honoured
+ * ([P4] Denoising-step activation precision).
+ */
+w8_status step_policy_dispatch(const w8_step_policy* policy, int32_t step, int32_t num_steps,
+                               int32_t* mode_out);
+
+/*
+ * w8_check_group_scales — load-time check that the G projections of a
+ * sharing group carry bit-identical input scales ([P4] What changed: the
+ * invariant the sharing rests on, validated in post_load_weights(), never
+ * in forward).  Reads the G device scalars and synchronises the device.
+ *   s_in  HOST array of G device pointers.
+ * Errors: NULL, SHAPE (G < 1), SCALE (scales differ), CUDA.
+ */
+w8_status w8_check_group_scales(const float* const* s_in, int32_t G);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8LIN_H */

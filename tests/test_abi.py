@@ -1,0 +1,111 @@
+"""CPU tests of the C ABI: the library builds and loads, exports every
+symbol the header declares, and its host-side logic (argument validation,
+step policy, M == 0) behaves as the header states.  No call here reaches
+the GPU."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def L():
+    from w8a16_linear_gb300 import build as B
+    from w8a16_linear_gb300 import binding
+    B.build()
+    return binding.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "w8lin.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_symbols_exported(L):
+    from w8a16_linear_gb300 import binding
+    names = _declared_functions()
+    assert set(names) == set(binding.SIGNATURES), names
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in binding.SIGNATURES, n
+    assert L.w8_abi_version() == 1
+
+
+def test_policy_matches_oracle_everywhere(L):
+    from w8a16_linear_gb300 import binding as b
+    for first in range(0, 5):
+        for last in range(0, 5):
+            pol = b.StepPolicy(1, 1, first, last)
+            opol = O.StepPolicy(1, True, first, last)
+            for n in range(1, 40):
+                for s in range(n):
+                    got = b.step_policy_dispatch(pol, s, n)
+                    want = O.step_mode(opol, s, n)
+                    assert got == (b.MODE_A16 if want == "A16" else b.MODE_A8)
+
+
+def test_policy_refusals(L):
+    from w8a16_linear_gb300 import binding as b
+    for pol, step, n in [(b.StepPolicy(2, 1, 3, 3), 0, 8), (b.StepPolicy(1, 1, -1, 3), 0, 8),
+                         (b.StepPolicy(1, 1, 3, -1), 0, 8), (b.StepPolicy(1, 1, 3, 3), 8, 8),
+                         (b.StepPolicy(1, 1, 3, 3), -1, 8), (b.StepPolicy(1, 1, 3, 3), 0, 0)]:
+        with pytest.raises(b.W8Error) as ei:
+            b.step_policy_dispatch(pol, step, n)
+        assert ei.value.status == 7
+    assert all(b.step_policy_dispatch(None, s, 8) == b.MODE_A8 for s in range(8))
+    assert L.step_policy_dispatch(None, 0, 8, None) == 1          # NULL mode_out
+
+
+def _u(v):
+    return ctypes.c_void_p(v)
+
+
+def test_validation_before_any_cuda_call(L):
+    # Non-null fake device addresses; validation must reject before use.
+    p16 = _u(0x10000)
+    # NULL pointers
+    assert L.fp8_quant_static(None, 4, 16, p16, p16, None) == 1
+    # K not a multiple of 16 / negative M
+    assert L.fp8_quant_static(p16, 4, 24, p16, p16, None) == 2
+    assert L.fp8_quant_static(p16, -1, 16, p16, p16, None) == 2
+    # misaligned
+    assert L.fp8_quant_static(_u(0x10008), 4, 16, p16, p16, None) == 3
+    # W8A16 refuses an already-quantized (E4M3) activation
+    assert L.fp8_linear_w8a16(p16, 1, 4, 16, p16, 16, p16, p16, None) == 5
+    assert b"already-quantized" in L.w8_last_error()
+    # unknown dtype, N not a multiple of 16, missing workspace for bf16 input
+    assert L.fp8_linear_w8a8(p16, 7, 4, 16, p16, 16, p16, p16, p16, None, None) == 5
+    assert L.fp8_linear_w8a8(p16, 1, 4, 16, p16, 24, p16, p16, p16, None, None) == 2
+    assert L.fp8_linear_w8a8(p16, 0, 4, 16, p16, 16, p16, p16, p16, None, None) == 1
+    # group size and mode
+    arr = (ctypes.c_void_p * 3)(0x10000, 0x10000, 0x10000)
+    ns = (ctypes.c_int64 * 3)(16, 16, 16)
+    assert L.qkv_shared_quant_gemm(0, p16, 4, 16, p16, 4, arr, ns, arr, arr, p16, None) == 2
+    assert L.qkv_shared_quant_gemm(5, p16, 4, 16, p16, 3, arr, ns, arr, arr, p16, None) == 2
+    assert L.qkv_shared_quant_gemm(0, p16, 4, 16, p16, 3, arr, ns, arr, arr, None, None) == 1
+    # swiglu
+    assert L.swiglu_2in_fp8(p16, p16, 4, 24, p16, p16, None) == 2
+    assert L.swiglu_2in_fp8(p16, p16, 4, 16, None, p16, None) == 1
+    assert L.swiglu_2in_bf16(p16, _u(0x10004), 4, 16, p16, None) == 3
+    # group-scale check arguments
+    assert L.w8_check_group_scales(None, 3) == 1
+    assert L.w8_check_group_scales(arr, 0) == 2
+
+
+def test_zero_rows_is_a_noop(L):
+    p16 = _u(0x10000)
+    arr = (ctypes.c_void_p * 3)(0x10000, 0x10000, 0x10000)
+    ns = (ctypes.c_int64 * 3)(16, 16, 16)
+    assert L.fp8_quant_static(p16, 0, 16, p16, p16, None) == 0
+    assert L.fp8_linear_w8a8(p16, 0, 0, 16, p16, 16, p16, p16, p16, None, None) == 0
+    assert L.fp8_linear_w8a16(p16, 0, 0, 16, p16, 16, p16, p16, None) == 0
+    assert L.qkv_shared_quant_gemm(0, p16, 0, 16, p16, 3, arr, ns, arr, arr, None, None) == 0
+    assert L.swiglu_2in_fp8(p16, p16, 0, 16, p16, p16, None) == 0
+    assert L.swiglu_2in_bf16(p16, p16, 0, 16, p16, None) == 0

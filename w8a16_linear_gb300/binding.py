@@ -1,0 +1,276 @@
+"""Thin ctypes binding of ``libw8lin.so`` (the C ABI in ``include/w8lin.h``).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  When the
+library is missing the calls raise instead of falling back to anything else.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw8lin.so")
+
+W8_OK = 0
+STATUS_NAMES = {
+    0: "W8_OK", 1: "W8_ERR_NULL", 2: "W8_ERR_SHAPE", 3: "W8_ERR_ALIGN", 4: "W8_ERR_STRIDE",
+    5: "W8_ERR_DTYPE", 6: "W8_ERR_ARCH", 7: "W8_ERR_POLICY", 8: "W8_ERR_TIMEOUT",
+    9: "W8_ERR_CUDA", 10: "W8_ERR_SCALE",
+}
+DTYPE_BF16, DTYPE_E4M3 = 0, 1
+MODE_A8, MODE_A16 = 0, 1
+
+# Every symbol the header declares, with its ctypes signature.
+_c_void_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+SIGNATURES = {
+    "w8_abi_version": (ctypes.c_int, []),
+    "w8_last_error": (ctypes.c_char_p, []),
+    "w8_device_check": (ctypes.c_int, []),
+    "w8_poll_device_error": (ctypes.c_int, [_c_void_p]),
+    "fp8_quant_static": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "fp8_linear_w8a8": (ctypes.c_int, [_c_void_p, _i32, _i64, _i64, _c_void_p, _i64, _c_void_p,
+                                       _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "fp8_linear_w8a16": (ctypes.c_int, [_c_void_p, _i32, _i64, _i64, _c_void_p, _i64, _c_void_p,
+                                        _c_void_p, _c_void_p]),
+    "qkv_shared_quant_gemm": (ctypes.c_int, [_i32, _c_void_p, _i64, _i64, _c_void_p, _i32,
+                                             ctypes.POINTER(_c_void_p), ctypes.POINTER(_i64),
+                                             ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
+                                             _c_void_p, _c_void_p]),
+    "fp8_linear_w8a8_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i32,
+                                             ctypes.POINTER(_c_void_p), ctypes.POINTER(_i64),
+                                             ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
+                                             _c_void_p]),
+    "swiglu_2in_fp8": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p,
+                                      _c_void_p]),
+    "swiglu_2in_bf16": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
+    "step_policy_dispatch": (ctypes.c_int, [_c_void_p, _i32, _i32, ctypes.POINTER(_i32)]),
+    "w8_check_group_scales": (ctypes.c_int, [ctypes.POINTER(_c_void_p), _i32]),
+}
+
+
+class W8Error(RuntimeError):
+    def __init__(self, status, detail):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {detail}")
+
+
+class StepPolicy(ctypes.Structure):
+    """Mirror of ``w8_step_policy``."""
+    _fields_ = [("schema_version", _i32), ("enabled", _i32),
+                ("first_steps", _i32), ("last_steps", _i32)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(status):
+    if status != W8_OK:
+        raise W8Error(status, lib().w8_last_error().decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dense(t, name):
+    if not t.is_contiguous():
+        raise W8Error(4, f"{name}: non-contiguous tensors are rejected")
+    if not t.is_cuda:
+        raise W8Error(1, f"{name}: must be a CUDA tensor")
+    return t
+
+
+def _as_u8(t, name):
+    _dense(t, name)
+    if t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+        return t.view(torch.uint8)
+    raise W8Error(5, f"{name}: expected E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+
+
+def _as_bf16(t, name):
+    _dense(t, name)
+    if t.dtype != torch.bfloat16:
+        raise W8Error(5, f"{name}: expected bfloat16, got {t.dtype}")
+    return t
+
+
+def _flat2(t):
+    return t.reshape(-1, t.shape[-1])
+
+
+def _scalar(t, name):
+    _dense(t, name)
+    if t.dtype != torch.float32 or t.numel() != 1:
+        raise W8Error(5, f"{name}: expected a one-element float32 device tensor")
+    return t
+
+
+# ---------------------------------------------------------------- entry points
+
+def abi_version():
+    return lib().w8_abi_version()
+
+
+def device_check():
+    _check(lib().w8_device_check())
+
+
+def poll_device_error(stream=None):
+    _check(lib().w8_poll_device_error(_stream(stream)))
+
+
+def fp8_quant_static(x, s_in, out=None, stream=None):
+    """E4M3 codes (uint8) of ``x / s_in``; same shape as ``x``."""
+    x = _as_bf16(x, "x")
+    x2 = _flat2(x)
+    M, K = x2.shape
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    o = _as_u8(out, "out")
+    _check(lib().fp8_quant_static(_ptr(x2), M, K, _ptr(_scalar(s_in, "s_in")), _ptr(o), _stream(stream)))
+    return out
+
+
+def fp8_linear_w8a8(x, w, s_in, s_w, out=None, ws=None, stream=None):
+    """W8A8 linear.  ``x`` bf16 (quantized into ``ws``) or E4M3 codes."""
+    if x.dtype == torch.bfloat16:
+        xd, dt = _as_bf16(x, "x"), DTYPE_BF16
+    else:
+        xd, dt = _as_u8(x, "x"), DTYPE_E4M3
+    x2 = _flat2(xd)
+    M, K = x2.shape
+    wq = _as_u8(w, "w")
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty(*x.shape[:-1], N, dtype=torch.bfloat16, device=x.device)
+    _as_bf16(out, "out")
+    if dt == DTYPE_BF16 and ws is None:
+        ws = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_linear_w8a8(_ptr(x2), dt, M, K, _ptr(wq), N, _ptr(_scalar(s_in, "s_in")),
+                                 _ptr(_scalar(s_w, "s_w")), _ptr(out),
+                                 _ptr(_as_u8(ws, "ws") if ws is not None else None), _stream(stream)))
+    return out
+
+
+def fp8_linear_w8a16(x, w, s_w, out=None, stream=None):
+    """W8A16 linear (dequantization inside the GEMM).  ``x`` must be bf16."""
+    dt = DTYPE_BF16 if x.dtype == torch.bfloat16 else DTYPE_E4M3
+    xd = _dense(x, "x")
+    x2 = _flat2(xd)
+    M, K = x2.shape
+    wq = _as_u8(w, "w")
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty(*x.shape[:-1], N, dtype=torch.bfloat16, device=x.device)
+    _as_bf16(out, "out")
+    _check(lib().fp8_linear_w8a16(_ptr(x2), dt, M, K, _ptr(wq), N, _ptr(_scalar(s_w, "s_w")),
+                                  _ptr(out), _stream(stream)))
+    return out
+
+
+def qkv_shared_quant_gemm(mode, x, s_in, weights, weight_scales, outs=None, ws=None, stream=None):
+    """A projection group sharing one activation (mode MODE_A8 or MODE_A16)."""
+    x = _as_bf16(x, "x")
+    x2 = _flat2(x)
+    M, K = x2.shape
+    G = len(weights)
+    ws_q = [_as_u8(w, f"w[{i}]") for i, w in enumerate(weights)]
+    if outs is None:
+        outs = [torch.empty(*x.shape[:-1], w.shape[0], dtype=torch.bfloat16, device=x.device) for w in ws_q]
+    for i, o in enumerate(outs):
+        _as_bf16(o, f"y[{i}]")
+    if mode == MODE_A8 and ws is None:
+        ws = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    arr_w = (ctypes.c_void_p * G)(*[w.data_ptr() for w in ws_q])
+    arr_n = (ctypes.c_int64 * G)(*[w.shape[0] for w in ws_q])
+    arr_s = (ctypes.c_void_p * G)(*[_scalar(s, f"s_w[{i}]").data_ptr() for i, s in enumerate(weight_scales)])
+    arr_y = (ctypes.c_void_p * G)(*[o.data_ptr() for o in outs])
+    s_in_p = _ptr(_scalar(s_in, "s_in")) if s_in is not None else ctypes.c_void_p(0)
+    _check(lib().qkv_shared_quant_gemm(mode, _ptr(x2), M, K, s_in_p, G, arr_w, arr_n, arr_s, arr_y,
+                                       _ptr(_as_u8(ws, "ws") if ws is not None else None), _stream(stream)))
+    return outs
+
+
+def fp8_linear_w8a8_group(qx, s_in, weights, weight_scales, outs=None, stream=None):
+    """G W8A8 projections over an activation already quantized to E4M3."""
+    q = _as_u8(qx, "qx")
+    q2 = _flat2(q)
+    M, K = q2.shape
+    G = len(weights)
+    ws_q = [_as_u8(w, f"w[{i}]") for i, w in enumerate(weights)]
+    if outs is None:
+        outs = [torch.empty(*qx.shape[:-1], w.shape[0], dtype=torch.bfloat16, device=qx.device) for w in ws_q]
+    for i, o in enumerate(outs):
+        _as_bf16(o, f"y[{i}]")
+    arr_w = (ctypes.c_void_p * G)(*[w.data_ptr() for w in ws_q])
+    arr_n = (ctypes.c_int64 * G)(*[w.shape[0] for w in ws_q])
+    arr_s = (ctypes.c_void_p * G)(*[_scalar(s, f"s_w[{i}]").data_ptr() for i, s in enumerate(weight_scales)])
+    arr_y = (ctypes.c_void_p * G)(*[o.data_ptr() for o in outs])
+    _check(lib().fp8_linear_w8a8_group(_ptr(q2), M, K, _ptr(_scalar(s_in, "s_in")), G, arr_w, arr_n,
+                                       arr_s, arr_y, _stream(stream)))
+    return outs
+
+
+def swiglu_2in_fp8(gate, up, s_out, out=None, stream=None):
+    g = _flat2(_as_bf16(gate, "gate"))
+    u = _flat2(_as_bf16(up, "up"))
+    if g.shape != u.shape:
+        raise W8Error(2, "gate and up shapes differ")
+    M, I = g.shape
+    if out is None:
+        out = torch.empty(gate.shape, dtype=torch.uint8, device=gate.device)
+    _check(lib().swiglu_2in_fp8(_ptr(g), _ptr(u), M, I, _ptr(_scalar(s_out, "s_out")),
+                                _ptr(_as_u8(out, "out")), _stream(stream)))
+    return out
+
+
+def swiglu_2in_bf16(gate, up, out=None, stream=None):
+    g = _flat2(_as_bf16(gate, "gate"))
+    u = _flat2(_as_bf16(up, "up"))
+    if g.shape != u.shape:
+        raise W8Error(2, "gate and up shapes differ")
+    M, I = g.shape
+    if out is None:
+        out = torch.empty(gate.shape, dtype=torch.bfloat16, device=gate.device)
+    _check(lib().swiglu_2in_bf16(_ptr(g), _ptr(u), M, I, _ptr(_as_bf16(out, "out")), _stream(stream)))
+    return out
+
+
+def step_policy_dispatch(policy, step, num_steps):
+    """MODE_A8 or MODE_A16 for a scheduler step; ``policy`` None = no policy."""
+    mode = ctypes.c_int32(-1)
+    p = ctypes.byref(policy) if policy is not None else None
+    _check(lib().step_policy_dispatch(p, step, num_steps, ctypes.byref(mode)))
+    return mode.value
+
+
+def check_group_scales(scales):
+    """Load-time check that a sharing group's input scales are identical."""
+    arr = (ctypes.c_void_p * len(scales))(*[_scalar(s, "s_in").data_ptr() for s in scales])
+    _check(lib().w8_check_group_scales(arr, len(scales)))

@@ -1,0 +1,358 @@
+// C-ABI entry points (include/w8lin.h): host-side argument validation, device
+// checks, and dispatch to the kernels.  Validation happens before any CUDA
+// call so that a bad argument never touches the GPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/w8lin.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+w8_status fail(w8_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+w8_status ok() {
+  g_last_error[0] = '\0';
+  return W8_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];      // 0 = not yet queried
+int g_arch_ok[kMaxDevices];  // 0 = unknown, 1 = sm_103, -1 = other
+std::mutex g_dev_mu;
+
+// Checks that the current device is sm_103 and returns its SM count.
+w8_status device_info(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(W8_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(W8_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0, n = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail(W8_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    g_sms[dev] = n;
+    if (g_arch_ok[dev] < 0)
+      return fail(W8_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                  major, minor);
+  }
+  if (g_arch_ok[dev] < 0) return fail(W8_ERR_ARCH, "device %d is not sm_103", dev);
+  *sms = g_sms[dev];
+  return W8_OK;
+}
+
+w8_status cuda_status(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(W8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+namespace w8 {
+
+EncodeTiledFn get_encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace w8
+
+extern "C" {
+
+int w8_abi_version(void) { return 1; }
+
+const char* w8_last_error(void) { return g_last_error; }
+
+w8_status w8_device_check(void) {
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  return st == W8_OK ? ok() : st;
+}
+
+w8_status w8_poll_device_error(void* stream) {
+  uint32_t err = 0;
+  cudaError_t e = w8::gemm_read_error(static_cast<cudaStream_t>(stream), &err);
+  if (e != cudaSuccess) return fail(W8_ERR_CUDA, "reading device error word: %s", cudaGetErrorString(e));
+  if (err & w8::kErrTimeout) return fail(W8_ERR_TIMEOUT, "a GEMM pipeline wait timed out");
+  return ok();
+}
+
+w8_status fp8_quant_static(const uint16_t* x, int64_t M, int64_t K, const float* s_in, uint8_t* q,
+                           void* stream) {
+  if (M < 0 || K <= 0) return fail(W8_ERR_SHAPE, "fp8_quant_static: M=%lld K=%lld", (long long)M, (long long)K);
+  if (K % 16) return fail(W8_ERR_SHAPE, "fp8_quant_static: K=%lld is not a multiple of 16", (long long)K);
+  if (M == 0) return ok();
+  if (!x || !s_in || !q) return fail(W8_ERR_NULL, "fp8_quant_static: NULL pointer");
+  if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(s_in) & 3u))
+    return fail(W8_ERR_ALIGN, "fp8_quant_static: x and q must be 16-byte aligned");
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  if (st != W8_OK) return st;
+  return cuda_status(w8::launch_quant_static(x, M * K, s_in, q, sms, static_cast<cudaStream_t>(stream)),
+                     "fp8_quant_static launch");
+}
+
+static w8_status check_linear_common(const char* fn, const void* x, int64_t M, int64_t K,
+                                     const uint8_t* w, int64_t N, const float* s_w, const uint16_t* y) {
+  if (M < 0 || K <= 0 || N <= 0)
+    return fail(W8_ERR_SHAPE, "%s: M=%lld K=%lld N=%lld", fn, (long long)M, (long long)K, (long long)N);
+  if (K % 16 || N % 16)
+    return fail(W8_ERR_SHAPE, "%s: K=%lld and N=%lld must be multiples of 16", fn, (long long)K, (long long)N);
+  if (M > INT32_MAX / 2 || K > INT32_MAX / 2 || N > INT32_MAX / 2)
+    return fail(W8_ERR_SHAPE, "%s: dimension too large", fn);
+  if (M == 0) return W8_OK;
+  if (!x || !w || !s_w || !y) return fail(W8_ERR_NULL, "%s: NULL pointer", fn);
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (reinterpret_cast<uintptr_t>(s_w) & 3u))
+    return fail(W8_ERR_ALIGN, "%s: x, w and y must be 16-byte aligned", fn);
+  return W8_OK;
+}
+
+w8_status fp8_linear_w8a8(const void* x, int32_t x_dtype, int64_t M, int64_t K, const uint8_t* w,
+                          int64_t N, const float* s_in, const float* s_w, uint16_t* y, uint8_t* ws,
+                          void* stream) {
+  if (x_dtype != W8_DTYPE_BF16 && x_dtype != W8_DTYPE_E4M3)
+    return fail(W8_ERR_DTYPE, "fp8_linear_w8a8: unknown activation dtype %d", x_dtype);
+  w8_status st = check_linear_common("fp8_linear_w8a8", x, M, K, w, N, s_w, y);
+  if (st != W8_OK) return st;
+  if (M == 0) return ok();
+  if (!s_in) return fail(W8_ERR_NULL, "fp8_linear_w8a8: NULL s_in");
+  if (x_dtype == W8_DTYPE_BF16) {
+    if (!ws) return fail(W8_ERR_NULL, "fp8_linear_w8a8: bf16 input needs the [M,K] E4M3 workspace");
+    if (!aligned16(ws)) return fail(W8_ERR_ALIGN, "fp8_linear_w8a8: ws must be 16-byte aligned");
+  }
+  int sms = 0;
+  if ((st = device_info(&sms)) != W8_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* qx = static_cast<const uint8_t*>(x);
+  if (x_dtype == W8_DTYPE_BF16) {
+    cudaError_t e = w8::launch_quant_static(static_cast<const uint16_t*>(x), M * K, s_in, ws, sms, s);
+    if (e != cudaSuccess) return cuda_status(e, "fp8_linear_w8a8: quant launch");
+    qx = ws;
+  }
+  w8::GemmProblem p{};
+  p.M = M;
+  p.K = K;
+  p.G = 1;
+  p.x = qx;
+  p.w[0] = w;
+  p.N[0] = N;
+  p.s_in = s_in;
+  p.s_w[0] = s_w;
+  p.y[0] = y;
+  int terr = 0;
+  cudaError_t e = w8::launch_gemm_w8a8(p, sms, s, &terr);
+  if (terr) return fail(W8_ERR_ALIGN, "fp8_linear_w8a8: tensor map encoding rejected the operands");
+  return cuda_status(e, "fp8_linear_w8a8: GEMM launch");
+}
+
+w8_status fp8_linear_w8a16(const void* x, int32_t x_dtype, int64_t M, int64_t K, const uint8_t* w,
+                           int64_t N, const float* s_w, uint16_t* y, void* stream) {
+  if (x_dtype != W8_DTYPE_BF16)
+    return fail(W8_ERR_DTYPE,
+                "fp8_linear_w8a16: activation must be bf16; an already-quantized input is refused");
+  w8_status st = check_linear_common("fp8_linear_w8a16", x, M, K, w, N, s_w, y);
+  if (st != W8_OK) return st;
+  if (M == 0) return ok();
+  int sms = 0;
+  if ((st = device_info(&sms)) != W8_OK) return st;
+  w8::GemmProblem p{};
+  p.M = M;
+  p.K = K;
+  p.G = 1;
+  p.x = x;
+  p.w[0] = w;
+  p.N[0] = N;
+  p.s_w[0] = s_w;
+  p.y[0] = y;
+  int terr = 0;
+  cudaError_t e = w8::launch_gemm_w8a16(p, sms, static_cast<cudaStream_t>(stream), &terr);
+  if (terr) return fail(W8_ERR_ALIGN, "fp8_linear_w8a16: tensor map encoding rejected the operands");
+  return cuda_status(e, "fp8_linear_w8a16: GEMM launch");
+}
+
+w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int64_t K,
+                                const float* s_in, int32_t G, const uint8_t* const* w,
+                                const int64_t* N, const float* const* s_w, uint16_t* const* y,
+                                uint8_t* ws, void* stream) {
+  if (mode != W8_MODE_A8 && mode != W8_MODE_A16)
+    return fail(W8_ERR_SHAPE, "qkv_shared_quant_gemm: unknown mode %d", mode);
+  if (G < 1 || G > w8::kMaxGroup)
+    return fail(W8_ERR_SHAPE, "qkv_shared_quant_gemm: group size %d outside 1..3", G);
+  if (!w || !N || !s_w || !y) return fail(W8_ERR_NULL, "qkv_shared_quant_gemm: NULL host array");
+  for (int g = 0; g < G; ++g) {
+    w8_status st = check_linear_common("qkv_shared_quant_gemm", x, M, K, w[g], N[g], s_w[g], y[g]);
+    if (st != W8_OK) return st;
+  }
+  if (M == 0) return ok();
+  if (mode == W8_MODE_A8) {
+    if (!s_in) return fail(W8_ERR_NULL, "qkv_shared_quant_gemm: NULL s_in");
+    if (!ws) return fail(W8_ERR_NULL, "qkv_shared_quant_gemm: A8 needs the [M,K] E4M3 workspace");
+    if (!aligned16(ws)) return fail(W8_ERR_ALIGN, "qkv_shared_quant_gemm: ws must be 16-byte aligned");
+  }
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  if (st != W8_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  w8::GemmProblem p{};
+  p.M = M;
+  p.K = K;
+  p.G = G;
+  for (int g = 0; g < G; ++g) {
+    p.w[g] = w[g];
+    p.N[g] = N[g];
+    p.s_w[g] = s_w[g];
+    p.y[g] = y[g];
+  }
+  int terr = 0;
+  cudaError_t e;
+  if (mode == W8_MODE_A8) {
+    e = w8::launch_quant_static(x, M * K, s_in, ws, sms, s);
+    if (e != cudaSuccess) return cuda_status(e, "qkv_shared_quant_gemm: quant launch");
+    p.x = ws;
+    p.s_in = s_in;
+    e = w8::launch_gemm_w8a8(p, sms, s, &terr);
+  } else {
+    p.x = x;
+    e = w8::launch_gemm_w8a16(p, sms, s, &terr);
+  }
+  if (terr) return fail(W8_ERR_ALIGN, "qkv_shared_quant_gemm: tensor map encoding rejected the operands");
+  return cuda_status(e, "qkv_shared_quant_gemm: GEMM launch");
+}
+
+w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const float* s_in,
+                                int32_t G, const uint8_t* const* w, const int64_t* N,
+                                const float* const* s_w, uint16_t* const* y, void* stream) {
+  if (G < 1 || G > w8::kMaxGroup)
+    return fail(W8_ERR_SHAPE, "fp8_linear_w8a8_group: group size %d outside 1..3", G);
+  if (!w || !N || !s_w || !y) return fail(W8_ERR_NULL, "fp8_linear_w8a8_group: NULL host array");
+  for (int g = 0; g < G; ++g) {
+    w8_status st = check_linear_common("fp8_linear_w8a8_group", qx, M, K, w[g], N[g], s_w[g], y[g]);
+    if (st != W8_OK) return st;
+  }
+  if (M == 0) return ok();
+  if (!s_in) return fail(W8_ERR_NULL, "fp8_linear_w8a8_group: NULL s_in");
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  if (st != W8_OK) return st;
+  w8::GemmProblem p{};
+  p.M = M;
+  p.K = K;
+  p.G = G;
+  p.x = qx;
+  p.s_in = s_in;
+  for (int g = 0; g < G; ++g) {
+    p.w[g] = w[g];
+    p.N[g] = N[g];
+    p.s_w[g] = s_w[g];
+    p.y[g] = y[g];
+  }
+  int terr = 0;
+  cudaError_t e = w8::launch_gemm_w8a8(p, sms, static_cast<cudaStream_t>(stream), &terr);
+  if (terr) return fail(W8_ERR_ALIGN, "fp8_linear_w8a8_group: tensor map encoding rejected the operands");
+  return cuda_status(e, "fp8_linear_w8a8_group: GEMM launch");
+}
+
+static w8_status check_swiglu(const char* fn, const uint16_t* g, const uint16_t* u, int64_t M,
+                              int64_t I, const void* out) {
+  if (M < 0 || I <= 0) return fail(W8_ERR_SHAPE, "%s: M=%lld I=%lld", fn, (long long)M, (long long)I);
+  if (I % 16) return fail(W8_ERR_SHAPE, "%s: I=%lld is not a multiple of 16", fn, (long long)I);
+  if (M == 0) return W8_OK;
+  if (!g || !u || !out) return fail(W8_ERR_NULL, "%s: NULL pointer", fn);
+  if (!aligned16(g) || !aligned16(u) || !aligned16(out))
+    return fail(W8_ERR_ALIGN, "%s: gate, up and out must be 16-byte aligned", fn);
+  return W8_OK;
+}
+
+w8_status swiglu_2in_fp8(const uint16_t* gate, const uint16_t* up, int64_t M, int64_t I,
+                         const float* s_out, uint8_t* out, void* stream) {
+  w8_status st = check_swiglu("swiglu_2in_fp8", gate, up, M, I, out);
+  if (st != W8_OK) return st;
+  if (M == 0) return ok();
+  if (!s_out) return fail(W8_ERR_NULL, "swiglu_2in_fp8: NULL s_out");
+  int sms = 0;
+  if ((st = device_info(&sms)) != W8_OK) return st;
+  return cuda_status(w8::launch_swiglu_fp8(gate, up, M * I, s_out, out, sms,
+                                           static_cast<cudaStream_t>(stream)),
+                     "swiglu_2in_fp8 launch");
+}
+
+w8_status swiglu_2in_bf16(const uint16_t* gate, const uint16_t* up, int64_t M, int64_t I,
+                          uint16_t* out, void* stream) {
+  w8_status st = check_swiglu("swiglu_2in_bf16", gate, up, M, I, out);
+  if (st != W8_OK) return st;
+  if (M == 0) return ok();
+  int sms = 0;
+  if ((st = device_info(&sms)) != W8_OK) return st;
+  return cuda_status(w8::launch_swiglu_bf16(gate, up, M * I, out, sms, static_cast<cudaStream_t>(stream)),
+                     "swiglu_2in_bf16 launch");
+}
+
+w8_status step_policy_dispatch(const w8_step_policy* policy, int32_t step, int32_t num_steps,
+                               int32_t* mode_out) {
+  if (!mode_out) return fail(W8_ERR_NULL, "step_policy_dispatch: NULL mode_out");
+  if (num_steps < 1 || step < 0 || step >= num_steps)
+    return fail(W8_ERR_POLICY, "step_policy_dispatch: step %d outside [0, %d)", step, num_steps);
+  if (!policy || !policy->enabled) {
+    *mode_out = W8_MODE_A8;
+    return ok();
+  }
+  if (policy->schema_version != 1)
+    return fail(W8_ERR_POLICY, "step_policy_dispatch: schema_version %d is not 1", policy->schema_version);
+  if (policy->first_steps < 0 || policy->last_steps < 0)
+    return fail(W8_ERR_POLICY, "step_policy_dispatch: negative step window");
+  if (num_steps == 1) {
+    *mode_out = W8_MODE_A8;
+    return ok();
+  }
+  const bool edge = step < policy->first_steps || step >= num_steps - policy->last_steps;
+  *mode_out = edge ? W8_MODE_A16 : W8_MODE_A8;
+  return ok();
+}
+
+w8_status w8_check_group_scales(const float* const* s_in, int32_t G) {
+  if (G < 1) return fail(W8_ERR_SHAPE, "w8_check_group_scales: G=%d", G);
+  if (!s_in) return fail(W8_ERR_NULL, "w8_check_group_scales: NULL array");
+  for (int g = 0; g < G; ++g)
+    if (!s_in[g]) return fail(W8_ERR_NULL, "w8_check_group_scales: NULL scale %d", g);
+  uint32_t first = 0;
+  for (int g = 0; g < G; ++g) {
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpy(&v, s_in[g], sizeof(float), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e, "w8_check_group_scales: read scale");
+    if (g == 0) first = v;
+    else if (v != first)
+      return fail(W8_ERR_SCALE, "w8_check_group_scales: input scale %d differs from scale 0", g);
+  }
+  return ok();
+}
+
+}  // extern "C"

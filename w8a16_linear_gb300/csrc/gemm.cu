@@ -1,0 +1,512 @@
+// Persistent tcgen05 GEMMs of the static per-tensor FP8 linear layer.
+//
+//  W8A8  (kind::f8f6f4): y = bf16( s_in * s_w * sum_k qx[m,k] * qw[n,k] ),
+//        E4M3 activations and weights, F32 accumulation in TMEM
+//        (cosmos-framework PR #157, "feat: load ModelOpt static-FP8
+//        checkpoints via TorchAO", section Verification: _scaled_mm on the
+//        two per-tensor scales).
+//  W8A16 (kind::f16):    y = bf16( sum_k x[m,k] * Wd[n,k] ),
+//        Wd = bf16( fl32(dec(qw) * s_w) ) formed in shared memory by a
+//        transform stage; the static input scale is not used and no
+//        dequantized weight is ever written to global memory (TensorRT-LLM
+//        PR #17476, "Load static FP8 Cosmos3 Nano/Super checkpoints without
+//        re-quantizing them", section Denoising-step activation precision;
+//        diffusers PR #14664, "[Cosmos3] Mixed W8A8/W8A16 denoising for
+//        ModelOpt FP8 checkpoints", section Behavior).
+//
+// One launch serves a group of up to three projections that share the same
+// activation (split Q/K/V or gate/up, each with its own weight and weight
+// scale and its own contiguous output; TensorRT-LLM PR #17476, sections
+// Description and What changed).
+//
+// Structure (one CTA per SM, static round-robin over output tiles):
+//   warp 0      TMA producer: activation and weight tiles into a smem ring
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> swizzled smem
+//               -> TMA store, double-buffered TMEM accumulators
+//   warps 6-13  (W8A16 only) E4M3 -> bf16 weight transform into the
+//               128-byte-swizzled K-major operand buffer
+// Every mbarrier wait is bounded: on a timeout the kernel records an error
+// bit, the other roles stop at their next wait, in-flight copies and MMAs
+// are drained with bounded waits, TMEM is freed and the kernel returns.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace w8 {
+
+__device__ uint32_t g_gemm_err;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr uint32_t kTmemCols = 512;             // two BN-column F32 accumulators
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBufBytes = 32 * 128;          // 32 rows x 64 bf16 columns
+constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+
+enum class Mode { W8A8, W8A16 };
+
+template <Mode MODE>
+struct Cfg;
+
+template <>
+struct Cfg<Mode::W8A8> {
+  static constexpr int kStages = 4;
+  static constexpr int kBK = 128;                    // K elements per stage (1 byte each)
+  static constexpr int kABytes = BM * 128;           // 16 KB
+  static constexpr int kBBytes = BN * 128;           // 32 KB (MMA operand)
+  static constexpr int kRawBytes = 0;
+  static constexpr uint32_t kTx = kABytes + kBBytes;
+  static constexpr int kTransformWarps = 0;
+  static constexpr uint32_t kIdesc = make_idesc(0, 0, BM, BN);  // E4M3 x E4M3
+};
+
+template <>
+struct Cfg<Mode::W8A16> {
+  static constexpr int kStages = 3;
+  static constexpr int kBK = 64;                     // K elements per stage (2 bytes each)
+  static constexpr int kABytes = BM * 128;           // 16 KB bf16 activation
+  static constexpr int kBBytes = BN * 128;           // 32 KB bf16 weight operand
+  static constexpr int kRawBytes = BN * 64;          // 16 KB raw E4M3 weight
+  static constexpr uint32_t kTx = kABytes + kRawBytes;
+  static constexpr int kTransformWarps = 8;
+  static constexpr uint32_t kIdesc = make_idesc(1, 1, BM, BN);  // BF16 x BF16
+};
+
+template <Mode MODE>
+struct Layout {
+  using C = Cfg<MODE>;
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + C::kStages * C::kABytes;
+  static constexpr int kRaw = kB + C::kStages * C::kBBytes;
+  static constexpr int kEpi = kRaw + C::kStages * C::kRawBytes;
+  static constexpr int kBar = kEpi + kEpiBytes;
+  // barriers: full[S], empty[S], ready[S], tfull[2], tempty[2], drain
+  static constexpr int kNumBars = 3 * C::kStages + 5;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kEnd = kAbort + 4;
+  static constexpr int kAlloc = kEnd + 1024;  // slack for 1024-byte alignment
+  static constexpr int kThreads = (2 + kEpiWarps + C::kTransformWarps) * 32;
+};
+
+struct Maps {
+  CUtensorMap a;
+  CUtensorMap b[kMaxGroup];
+  CUtensorMap y[kMaxGroup];
+};
+
+struct Args {
+  int G;
+  int M, K;
+  int N[kMaxGroup];
+  int tiles_n[kMaxGroup];
+  int tiles_per_m;
+  int num_tiles;
+  int num_kb;
+  const float* s_in;
+  const float* s_w[kMaxGroup];
+};
+
+__device__ __forceinline__ void decode_tile(const Args& a, int t, int& m0, int& g, int& n0) {
+  const int mb = t / a.tiles_per_m;
+  int r = t - mb * a.tiles_per_m;
+  g = 0;
+  while (g < a.G - 1 && r >= a.tiles_n[g]) {
+    r -= a.tiles_n[g];
+    ++g;
+  }
+  m0 = mb * BM;
+  n0 = r * BN;
+}
+
+__device__ __forceinline__ const CUtensorMap* map_b(const Maps& m, int g) {
+  return g == 0 ? &m.b[0] : (g == 1 ? &m.b[1] : &m.b[2]);
+}
+__device__ __forceinline__ const CUtensorMap* map_y(const Maps& m, int g) {
+  return g == 0 ? &m.y[0] : (g == 1 ? &m.y[1] : &m.y[2]);
+}
+__device__ __forceinline__ const float* scale_w(const Args& a, int g) {
+  return g == 0 ? a.s_w[0] : (g == 1 ? a.s_w[1] : a.s_w[2]);
+}
+
+__device__ __forceinline__ void record_timeout(volatile int* abort) {
+  *abort = 1;
+  atomicOr(&g_gemm_err, kErrTimeout);
+}
+
+template <Mode MODE>
+__global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args args) {
+  using C = Cfg<MODE>;
+  using L = Layout<MODE>;
+  constexpr int S = C::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::kBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto ready_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(ready_bar(s), C::kTransformWarps > 0 ? C::kTransformWarps : 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&maps.a);
+    for (int g = 0; g < args.G; ++g) {
+      prefetch_tensormap(map_b(maps, g));
+      prefetch_tensormap(map_y(maps, g));
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+        int m0, g, n0;
+        decode_tile(args, t, m0, g, n0);
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1, abort, kWaitLimitNs)) {
+            record_timeout(abort);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(s), C::kTx);
+          tma_load_2d(sbase + L::kA + s * C::kABytes, &maps.a, full_bar(s), kb * C::kBK, m0);
+          const uint32_t bdst = (MODE == Mode::W8A8) ? sbase + L::kB + s * C::kBBytes
+                                                     : sbase + L::kRaw + s * C::kRawBytes;
+          tma_load_2d(bdst, map_b(maps, g), full_bar(s), kb * C::kBK, n0);
+          ++issued;
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // Drain: every stage's most recent load must have landed before exit.
+      for (int j = 0; j < S && (uint32_t)j < issued; ++j) {
+        const uint32_t l = issued - 1 - j;  // the last S issues
+        const int st = (int)(l % S);
+        const uint32_t par = (l / S) & 1;
+        volatile int never = 0;
+        if (!mbar_wait(full_bar(st), par, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1, abort, kWaitLimitNs)) {
+          record_timeout(abort);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          const uint32_t wait_bar = (MODE == Mode::W8A8) ? full_bar(s) : ready_bar(s);
+          if (!mbar_wait(wait_bar, ph, abort, kWaitLimitNs)) {
+            record_timeout(abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + L::kA + s * C::kABytes;
+          const uint32_t b_addr = sbase + L::kB + s * C::kBBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
+            const uint64_t ad = sw128_kmajor_desc(a_addr + 32 * k);
+            const uint64_t bd = sw128_kmajor_desc(b_addr + 32 * k);
+            if (MODE == Mode::W8A8)
+              mma_f8f6f4(d, ad, bd, C::kIdesc, (kb | k) != 0);
+            else
+              mma_f16(d, ad, bd, C::kIdesc, (kb | k) != 0);
+          }
+          mma_commit(empty_bar(s));
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_ph ^= 1;
+        }
+      }
+      // Drain: all MMAs issued by this thread complete before TMEM is freed.
+      mma_commit(drain_bar);
+      volatile int never = 0;
+      if (!mbar_wait(drain_bar, 0, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
+    }
+  } else if (warp < 2 + kEpiWarps) {
+    // ---------------------------------------------------------------- epilogue
+    const int wq = warp & 3;  // TMEM lane quadrant this warp may access
+    const uint32_t buf0 = sbase + L::kEpi + (uint32_t)((warp - 2) * 2 * kEpiBufBytes);
+    uint8_t* buf0_ptr = smem + L::kEpi + (warp - 2) * 2 * kEpiBufBytes;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    int nbuf = 0;
+    for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+      int m0, g, n0;
+      decode_tile(args, t, m0, g, n0);
+      float alpha = 1.0f;
+      if (MODE == Mode::W8A8) alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, g)));
+      // Warp-uniform wait: the TMEM loads below are .sync.aligned.
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_ph, abort, kWaitLimitNs))) {
+        if (lane == 0) record_timeout(abort);
+        break;
+      }
+      tc_fence_after();
+      const int row0 = m0 + wq * 32;
+      const int ng = args.N[g];
+      const uint32_t tbase = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(tbase + c * 64, r0);
+        tmem_ld_32x32b_x32(tbase + c * 64 + 32, r1);
+        tmem_ld_wait();
+        if (c == BN / 64 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        uint32_t packed[32];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          packed[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r0[2 * j]), alpha),
+                                 __fmul_rn(__uint_as_float(r0[2 * j + 1]), alpha));
+          packed[16 + j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r1[2 * j]), alpha),
+                                      __fmul_rn(__uint_as_float(r1[2 * j + 1]), alpha));
+        }
+        const int col0 = n0 + c * 64;
+        if (col0 >= ng || row0 >= args.M) continue;  // nothing of this chunk is in range
+        // The store issued two chunks ago from this buffer must have read it.
+        if (lane == 0) tma_store_wait_read<1>();
+        __syncwarp();
+        uint8_t* bp = buf0_ptr + nbuf * kEpiBufBytes + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int pj = j ^ (lane & 7);  // 128-byte swizzle within the 1024-byte atom
+          *reinterpret_cast<uint4*>(bp + pj * 16) =
+              make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(map_y(maps, g), buf0 + nbuf * kEpiBufBytes, col0, row0);
+          tma_store_commit();
+        }
+        nbuf ^= 1;
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_ph ^= 1;
+      }
+    }
+    if (lane == 0) tma_store_wait_all();
+  } else {
+    // ---------------------------------------------------------------- weight transform
+    if constexpr (MODE == Mode::W8A16) {
+      const int r = threadIdx.x - (2 + kEpiWarps) * 32;  // weight row of the tile, 0..255
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+        int m0, g, n0;
+        decode_tile(args, t, m0, g, n0);
+        const float sw = __ldg(scale_w(args, g));
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait(full_bar(s), ph, abort, kWaitLimitNs))) {
+            if (lane == 0) record_timeout(abort);
+            ok = false;
+            break;
+          }
+          // Raw row: 64 bytes, 64-byte swizzle (16-byte chunk j at j ^ ((r >> 1) & 3)).
+          const uint8_t* raw = smem + L::kRaw + s * C::kRawBytes + r * 64;
+          uint8_t* dst = smem + L::kB + s * C::kBBytes + r * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + ((j ^ ((r >> 1) & 3)) * 16));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(w4[h] & 0xFFFF));
+              const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(w4[h] >> 16));
+              const float a0 = __half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFF)));
+              const float a1 = __half2float(__ushort_as_half((unsigned short)(f01 >> 16)));
+              const float a2 = __half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFF)));
+              const float a3 = __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
+              o[2 * h] = cvt_bf16x2(__fmul_rn(a0, sw), __fmul_rn(a1, sw));
+              o[2 * h + 1] = cvt_bf16x2(__fmul_rn(a2, sw), __fmul_rn(a3, sw));
+            }
+            // 16 raw bytes -> 32 bf16 bytes = chunks 2j and 2j+1 of the operand row.
+            const int c0 = (2 * j) ^ (r & 7);
+            const int c1 = (2 * j + 1) ^ (r & 7);
+            *reinterpret_cast<uint4*>(dst + c0 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + c1 * 16) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ready_bar(s));
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = get_encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <Mode MODE>
+cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  using C = Cfg<MODE>;
+  using L = Layout<MODE>;
+  *tmap_err = 0;
+  Maps maps;
+  Args args;
+  std::memset(&maps, 0, sizeof(maps));
+  std::memset(&args, 0, sizeof(args));
+  args.G = p.G;
+  args.M = (int)p.M;
+  args.K = (int)p.K;
+  args.num_kb = (int)((p.K + C::kBK - 1) / C::kBK);
+  args.s_in = p.s_in;
+  const int tiles_m = (int)((p.M + BM - 1) / BM);
+  args.tiles_per_m = 0;
+  bool ok = true;
+  if (MODE == Mode::W8A8) {
+    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.x, p.K, p.M, p.K, 128, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, p.K, p.M, p.K * 2, 64, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  for (int g = 0; g < p.G; ++g) {
+    args.N[g] = (int)p.N[g];
+    args.s_w[g] = p.s_w[g];
+    args.tiles_n[g] = (int)((p.N[g] + BN - 1) / BN);
+    args.tiles_per_m += args.tiles_n[g];
+    if (MODE == Mode::W8A8) {
+      ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 128,
+                      BN, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+      ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 64, BN,
+                      CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+    ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y[g], p.N[g], p.M, p.N[g] * 2,
+                    64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  for (int g = p.G; g < kMaxGroup; ++g) args.s_w[g] = p.s_w[0];
+  if (!ok) {
+    *tmap_err = 1;
+    return cudaSuccess;
+  }
+  args.num_tiles = tiles_m * args.tiles_per_m;
+  const int grid = args.num_tiles < sms ? args.num_tiles : sms;
+  auto kern = gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, L::kThreads, L::kAlloc, st>>>(maps, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  return launch<Mode::W8A8>(p, sms, st, tmap_err);
+}
+
+cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  return launch<Mode::W8A16>(p, sms, st, tmap_err);
+}
+
+cudaError_t gemm_read_error(cudaStream_t st, uint32_t* err) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(err, g_gemm_err, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  if (*err) {
+    e = cudaMemcpyToSymbolAsync(g_gemm_err, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(st);
+  }
+  return e;
+}
+
+}  // namespace w8

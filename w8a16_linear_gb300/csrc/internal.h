@@ -1,0 +1,53 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public header.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace w8 {
+
+// Error word bits set by kernels that wait on mbarriers.
+enum : uint32_t {
+  kErrTimeout = 1u,   // an mbarrier wait ran past its deadline
+};
+
+// ---- elementwise (elementwise.cu)
+cudaError_t launch_quant_static(const uint16_t* x, int64_t n, const float* s_in, uint8_t* q,
+                                int sms, cudaStream_t st);
+cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, const float* s_out,
+                              uint8_t* out, int sms, cudaStream_t st);
+cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* out,
+                               int sms, cudaStream_t st);
+
+// ---- GEMMs (gemm.cu)
+constexpr int kMaxGroup = 3;
+
+struct GemmProblem {
+  int64_t M, K;
+  int G;                         // projections sharing the activation (1..3)
+  const void* x;                 // E4M3 [M,K] (W8A8) or bf16 [M,K] (W8A16)
+  const uint8_t* w[kMaxGroup];   // E4M3 [N_g, K]
+  int64_t N[kMaxGroup];
+  const float* s_in;             // W8A8 only
+  const float* s_w[kMaxGroup];
+  uint16_t* y[kMaxGroup];        // bf16 [M, N_g]
+};
+
+// Returns cudaSuccess or the CUDA error; *tmap_err is set non-zero when a
+// tensor map could not be encoded.
+cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
+cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
+
+// Reads and clears the GEMM kernels' device error word (synchronises `st`).
+cudaError_t gemm_read_error(cudaStream_t st, uint32_t* err);
+
+// Driver entry point for tensor-map encoding (resolved once).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+
+}  // namespace w8
