@@ -305,6 +305,49 @@ def run_reference(args, rank, world):
     return 0
 
 
+# ---------------------------------------------------------------- profiling cases
+
+def run_case(args):
+    """Small fixed cases for ncu captures (not a bench line): the kernels of
+    the path at M=8192 tokens, inputs larger than L2."""
+    import __graft_entry__ as g
+    g.build()
+    import w8a16_linear_gb300 as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    W.device_check()
+    gen = torch.Generator(device=dev).manual_seed(0)
+    M = 8192
+    x = (torch.randn((M, HID), generator=gen, device=dev) * 0.25).to(torch.bfloat16)
+    s = torch.tensor([0.25 * 4 / 448], device=dev)
+    qs = [(torch.randn((HID, HID), generator=gen, device=dev) * 200).clamp(-448, 448)
+          .to(torch.float8_e4m3fn).view(torch.uint8) for _ in range(3)]
+    ss = [torch.tensor([0.02 * 4 / 448], device=dev) for _ in range(3)]
+    ys = [torch.empty((M, HID), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    qx = torch.empty((M, HID), dtype=torch.uint8, device=dev)
+    if args.case == "qkv8k":
+        fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A8, x, s, qs, ss, outs=ys, ws=qx)  # noqa: E731
+    elif args.case == "w8a16_8k":
+        fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, qs, ss, outs=ys)  # noqa: E731
+    elif args.case == "swiglu8k":
+        gg = (torch.randn((M, INTER), generator=gen, device=dev) * 2).to(torch.bfloat16)
+        uu = torch.randn((M, INTER), generator=gen, device=dev).to(torch.bfloat16)
+        h8 = torch.empty((M, INTER), dtype=torch.uint8, device=dev)
+        h16 = torch.empty((M, INTER), dtype=torch.bfloat16, device=dev)
+
+        def fn():
+            W.swiglu_2in_fp8(gg, uu, s, out=h8)
+            W.swiglu_2in_bf16(gg, uu, out=h16)
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    W.poll_device_error()
+    print(json.dumps({"case": args.case, "ok": True}))
+    return 0
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -314,8 +357,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="run a small profiling case (qkv8k, w8a16_8k, swiglu8k) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.case:
+        return run_case(args)
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
