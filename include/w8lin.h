@@ -174,6 +174,31 @@ w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const f
                                 const float* const* s_w, uint16_t* const* y, void* stream);
 
 /*
+ * fp8_linear_w8a8_noalloc — fp8_linear_w8a8 on a bf16 activation for callers
+ * that cannot allocate device memory (the web pages have no counterpart: this
+ * entry point exists for integration, not for the method).  Some callers can
+ * neither allocate nor be handed a workspace: operator or plugin interfaces
+ * that pass only inputs and outputs, runtimes whose memory belongs to a fixed
+ * pool, or code that may not call cudaMalloc because it can synchronise the
+ * device or because a stream capture is in progress.  The E4M3 copy of the
+ * activation goes instead into a fixed 32 MiB device array inside the
+ * library, so this call allocates nothing.
+ *   x bf16 [M, K]; w E4M3 [N, K]; s_in, s_w device float scalars; y bf16 [M, N].
+ *   Limit: M*K <= 33,554,432 (32 MiB of E4M3 codes); larger activations are
+ *   refused with W8_ERR_SHAPE (use fp8_linear_w8a8 with a workspace).
+ *   Every GPU that loads the library keeps the 32 MiB array until exit.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls on a device share the one array: calls that overlap on the GPU
+ *   race; calls ordered on one stream do not.  Nothing in the array needs to
+ *   start zeroed (every byte read was written by the same call).
+ * Errors: NULL, SHAPE, ALIGN, ARCH, CUDA.
+ */
+w8_status fp8_linear_w8a8_noalloc(const uint16_t* x, int64_t M, int64_t K, const uint8_t* w,
+                                  int64_t N, const float* s_in, const float* s_w, uint16_t* y,
+                                  void* stream);
+
+/*
  * swiglu_2in_fp8 — out = E4M3_satRNE( fl32( h / s_out ) ) with
  * h = fl32( fl32(g * u) / fl32(1 + exp_spec(-g)) ), SiLU(gate) * up from two
  * separate tensors written straight to FP8 for the down projection

@@ -44,6 +44,8 @@ SIGNATURES = {
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_i64),
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
                                              _c_void_p]),
+    "fp8_linear_w8a8_noalloc": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i64, _c_void_p,
+                                               _c_void_p, _c_void_p, _c_void_p]),
     "swiglu_2in_fp8": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p,
                                       _c_void_p]),
     "swiglu_2in_bf16": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
@@ -235,6 +237,23 @@ def fp8_linear_w8a8_group(qx, s_in, weights, weight_scales, outs=None, stream=No
     _check(lib().fp8_linear_w8a8_group(_ptr(q2), M, K, _ptr(_scalar(s_in, "s_in")), G, arr_w, arr_n,
                                        arr_s, arr_y, _stream(stream)))
     return outs
+
+
+def fp8_linear_w8a8_noalloc(x, w, s_in, s_w, out=None, stream=None):
+    """W8A8 linear on a bf16 activation using the library's fixed scratch
+    array instead of a workspace (for callers that cannot allocate).  ``out``
+    must be given by such callers; M*K is limited to 32 MiB."""
+    xd = _as_bf16(x, "x")
+    x2 = _flat2(xd)
+    M, K = x2.shape
+    wq = _as_u8(w, "w")
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty(*x.shape[:-1], N, dtype=torch.bfloat16, device=x.device)
+    _as_bf16(out, "out")
+    _check(lib().fp8_linear_w8a8_noalloc(_ptr(x2), M, K, _ptr(wq), N, _ptr(_scalar(s_in, "s_in")),
+                                         _ptr(_scalar(s_w, "s_w")), _ptr(out), _stream(stream)))
+    return out
 
 
 def swiglu_2in_fp8(gate, up, s_out, out=None, stream=None):

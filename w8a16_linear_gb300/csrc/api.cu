@@ -84,6 +84,12 @@ EncodeTiledFn get_encode_tiled() {
   return fn;
 }
 
+void set_last_error(const char* msg) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
+int query_device(int* sms) { return device_info(sms); }
+
 }  // namespace w8
 
 extern "C" {

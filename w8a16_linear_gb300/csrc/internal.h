@@ -43,6 +43,12 @@ cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, in
 // Reads and clears the GEMM kernels' device error word (synchronises `st`).
 cudaError_t gemm_read_error(cudaStream_t st, uint32_t* err);
 
+// Thread-local error text shared with the C-ABI layer, and the device check
+// (sm_103 and SM count of the current device) for entry points defined
+// outside api.cu.
+void set_last_error(const char* msg);
+int query_device(int* sms);  // returns a w8_status
+
 // Driver entry point for tensor-map encoding (resolved once).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
