@@ -348,6 +348,23 @@ def run_case(args):
     return 0
 
 
+# ---------------------------------------------------------------- multi-rank
+
+def max_over_ranks(value, device):
+    """Maximum of a per-rank float over all ranks (the slowest replica sets
+    the job's time)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, steps, max_total_ms):
+    """Whole-job throughput: every replica runs `steps` full steps."""
+    return world * GEMM_FLOPS * steps / (max_total_ms / 1e3) / 1e12
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -384,13 +401,9 @@ def main():
     g.build()
 
     r = run_ours(args, rank, world, dev)
-    total_ms = r["total_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(r["total_ms"], dev)
     ms_per_step = total_ms / args.steps
-    value = world * GEMM_FLOPS * args.steps / (total_ms / 1e3) / 1e12
+    value = job_tflops(world, args.steps, total_ms)
 
     if rank == 0:
         peaks = load_peaks()

@@ -89,6 +89,13 @@ w8_status w8_device_check(void);
  * timeout, else W8_OK. */
 w8_status w8_poll_device_error(void* stream);
 
+/* Self-test of the failure path (no counterpart on the pages): enqueues a
+ * one-thread kernel that waits on a pipeline barrier nothing arrives on; the
+ * wait gives up after 0.2 s and records the same timeout bit a stalled GEMM
+ * would, so that the next w8_poll_device_error() returns W8_ERR_TIMEOUT and
+ * clears it.  The CUDA context stays usable.  Errors: ARCH, CUDA. */
+w8_status w8_selftest_timeout(void* stream);
+
 /*
  * fp8_quant_static — static per-tensor activation quantization.
  * q[i] = E4M3_satRNE( fl32( x[i] / s_in ) ) for all M*K elements: one

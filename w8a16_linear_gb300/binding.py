@@ -31,6 +31,7 @@ SIGNATURES = {
     "w8_last_error": (ctypes.c_char_p, []),
     "w8_device_check": (ctypes.c_int, []),
     "w8_poll_device_error": (ctypes.c_int, [_c_void_p]),
+    "w8_selftest_timeout": (ctypes.c_int, [_c_void_p]),
     "fp8_quant_static": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
     "fp8_linear_w8a8": (ctypes.c_int, [_c_void_p, _i32, _i64, _i64, _c_void_p, _i64, _c_void_p,
                                        _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
@@ -145,6 +146,12 @@ def device_check():
 
 def poll_device_error(stream=None):
     _check(lib().w8_poll_device_error(_stream(stream)))
+
+
+def selftest_timeout(stream=None):
+    """Enqueue the bounded-wait self-test (its timeout shows up in the next
+    poll_device_error)."""
+    _check(lib().w8_selftest_timeout(_stream(stream)))
 
 
 def fp8_quant_static(x, s_in, out=None, stream=None):

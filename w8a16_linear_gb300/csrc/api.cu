@@ -112,6 +112,14 @@ w8_status w8_poll_device_error(void* stream) {
   return ok();
 }
 
+w8_status w8_selftest_timeout(void* stream) {
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  if (st != W8_OK) return st;
+  return cuda_status(w8::launch_selftest_timeout(static_cast<cudaStream_t>(stream)),
+                     "w8_selftest_timeout launch");
+}
+
 w8_status fp8_quant_static(const uint16_t* x, int64_t M, int64_t K, const float* s_in, uint8_t* q,
                            void* stream) {
   if (M < 0 || K <= 0) return fail(W8_ERR_SHAPE, "fp8_quant_static: M=%lld K=%lld", (long long)M, (long long)K);

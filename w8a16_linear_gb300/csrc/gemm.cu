@@ -19,9 +19,18 @@
 // scale and its own contiguous output; TensorRT-LLM PR #17476, sections
 // Description and What changed).
 //
-// Structure (one CTA per SM, static round-robin over output tiles):
+// Two shapes of the same kernel (template parameter CG):
+//   CG = 1  one CTA per SM computes a 128 x 256 output tile.
+//   CG = 2  a cluster of two CTAs on two SMs computes a 256 x 256 tile with
+//           CTA-pair MMAs (tcgen05 cta_group::2): each CTA stages its 128
+//           activation rows and half (128 rows) of the weight tile, the even
+//           CTA issues the MMAs, each CTA's TMEM receives its 128 output rows.
+//           Per SM this halves the weight bytes staged per FLOP (and, for
+//           W8A16, the weight rows each SM dequantizes).
+//
+// Roles (per CTA, one CTA per SM, static round-robin over output tiles):
 //   warp 0      TMA producer: activation and weight tiles into a smem ring
-//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warp 1      TMEM allocator; MMA issuer (one thread of the even CTA)
 //   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> swizzled smem
 //               -> TMA store, double-buffered TMEM accumulators
 //   warps 6-13  (W8A16 only) E4M3 -> bf16 weight transform into the
@@ -45,58 +54,49 @@ __device__ uint32_t g_gemm_err;
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr uint32_t kTmemCols = 512;             // two BN-column F32 accumulators
+constexpr int BM = 128;                          // output rows per CTA
+constexpr int BN = 256;                          // output columns per tile
+constexpr uint32_t kTmemCols = 512;              // two BN-column F32 accumulators
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kEpiWarps = 4;
-constexpr int kEpiBufBytes = 32 * 128;          // 32 rows x 64 bf16 columns
+constexpr int kEpiBufBytes = 32 * 128;           // 32 rows x 64 bf16 columns
 constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+constexpr int kTransformWarps = 8;
 
 enum class Mode { W8A8, W8A16 };
 
-template <Mode MODE>
-struct Cfg;
-
-template <>
-struct Cfg<Mode::W8A8> {
-  static constexpr int kStages = 4;
-  static constexpr int kBK = 128;                    // K elements per stage (1 byte each)
-  static constexpr int kABytes = BM * 128;           // 16 KB
-  static constexpr int kBBytes = BN * 128;           // 32 KB (MMA operand)
-  static constexpr int kRawBytes = 0;
-  static constexpr uint32_t kTx = kABytes + kBBytes;
-  static constexpr int kTransformWarps = 0;
-  static constexpr uint32_t kIdesc = make_idesc(0, 0, BM, BN);  // E4M3 x E4M3
+template <Mode MODE, int CG>
+struct Cfg {
+  static constexpr bool kA16 = (MODE == Mode::W8A16);
+  static constexpr int kBRows = BN / CG;                       // weight rows staged per CTA
+  static constexpr int kBK = kA16 ? 64 : 128;                  // K elements per stage
+  static constexpr int kABytes = BM * 128;                     // 128-byte rows
+  static constexpr int kBBytes = kBRows * 128;                 // MMA operand (E4M3 or bf16)
+  static constexpr int kRawBytes = kA16 ? kBRows * 64 : 0;     // raw E4M3 rows (W8A16)
+  static constexpr int kStages = kA16 ? (CG == 1 ? 3 : 4) : (CG == 1 ? 4 : 6);
+  static constexpr int kTW = kA16 ? kTransformWarps : 0;
+  static constexpr int kThreadsPerRow = kA16 ? (kTW * 32) / kBRows : 1;  // 1 or 2
+  static constexpr uint32_t kIdesc =
+      kA16 ? make_idesc(1, 1, BM * CG, BN) : make_idesc(0, 0, BM * CG, BN);
 };
 
-template <>
-struct Cfg<Mode::W8A16> {
-  static constexpr int kStages = 3;
-  static constexpr int kBK = 64;                     // K elements per stage (2 bytes each)
-  static constexpr int kABytes = BM * 128;           // 16 KB bf16 activation
-  static constexpr int kBBytes = BN * 128;           // 32 KB bf16 weight operand
-  static constexpr int kRawBytes = BN * 64;          // 16 KB raw E4M3 weight
-  static constexpr uint32_t kTx = kABytes + kRawBytes;
-  static constexpr int kTransformWarps = 8;
-  static constexpr uint32_t kIdesc = make_idesc(1, 1, BM, BN);  // BF16 x BF16
-};
-
-template <Mode MODE>
+template <Mode MODE, int CG>
 struct Layout {
-  using C = Cfg<MODE>;
+  using C = Cfg<MODE, CG>;
   static constexpr int kA = 0;
   static constexpr int kB = kA + C::kStages * C::kABytes;
   static constexpr int kRaw = kB + C::kStages * C::kBBytes;
   static constexpr int kEpi = kRaw + C::kStages * C::kRawBytes;
   static constexpr int kBar = kEpi + kEpiBytes;
-  // barriers: full[S], empty[S], ready[S], tfull[2], tempty[2], drain
-  static constexpr int kNumBars = 3 * C::kStages + 5;
+  // barriers: full[S], empty[S], ready[S], rawfull[S], peer_ready[S], tfull[2],
+  // tempty[2], drain
+  static constexpr int kNumBars = 5 * C::kStages + 5;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kAlloc = kEnd + 1024;  // slack for 1024-byte alignment
-  static constexpr int kThreads = (2 + kEpiWarps + C::kTransformWarps) * 32;
+  static constexpr int kThreads = (2 + kEpiWarps + C::kTW) * 32;
+  static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
 struct Maps {
@@ -117,6 +117,8 @@ struct Args {
   const float* s_w[kMaxGroup];
 };
 
+// Tile t -> first output row of the (cluster) tile, projection, first column.
+template <int CG>
 __device__ __forceinline__ void decode_tile(const Args& a, int t, int& m0, int& g, int& n0) {
   const int mb = t / a.tiles_per_m;
   int r = t - mb * a.tiles_per_m;
@@ -125,7 +127,7 @@ __device__ __forceinline__ void decode_tile(const Args& a, int t, int& m0, int& 
     r -= a.tiles_n[g];
     ++g;
   }
-  m0 = mb * BM;
+  m0 = mb * BM * CG;
   n0 = r * BN;
 }
 
@@ -144,12 +146,13 @@ __device__ __forceinline__ void record_timeout(volatile int* abort) {
   atomicOr(&g_gemm_err, kErrTimeout);
 }
 
-template <Mode MODE>
-__global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
+template <Mode MODE, int CG>
+__global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args args) {
-  using C = Cfg<MODE>;
-  using L = Layout<MODE>;
+  using C = Cfg<MODE, CG>;
+  using L = Layout<MODE, CG>;
   constexpr int S = C::kStages;
+  constexpr bool kA16 = C::kA16;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -159,24 +162,34 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto ready_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+  auto rawfull_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
+  auto peer_ready_bar = [&](int s) { return bar0 + 8u * (4 * S + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (5 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (5 * S + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (5 * S + 4);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const bool leader = (rank == 0);
+  const int cluster_id = blockIdx.x / CG;
+  const int num_clusters = gridDim.x / CG;
+  // Barriers that live in the even CTA, as shared::cluster addresses.
+  auto leader_addr = [&](uint32_t a) { return (CG == 2) ? mapa_shared(a, 0) : a; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-      mbar_init(ready_bar(s), C::kTransformWarps > 0 ? C::kTransformWarps : 1);
+      mbar_init(ready_bar(s), kA16 ? C::kTW : 1);  // this CTA's transform warps
+      mbar_init(rawfull_bar(s), 1);
+      mbar_init(peer_ready_bar(s), 1);              // forwarded by the odd CTA
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiWarps);
+      mbar_init(tempty_bar(b), kEpiWarps * CG);
     }
     mbar_init(drain_bar, 1);
     *abort = 0;
@@ -188,11 +201,17 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(sbase + L::kTmemSlot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // peer barriers initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -203,20 +222,40 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
         int m0, g, n0;
-        decode_tile(args, t, m0, g, n0);
+        decode_tile<CG>(args, t, m0, g, n0);
+        const int a_row = m0 + (int)rank * BM;
+        const int b_row = n0 + (int)rank * C::kBRows;
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1, abort, kWaitLimitNs)) {
             record_timeout(abort);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), C::kTx);
-          tma_load_2d(sbase + L::kA + s * C::kABytes, &maps.a, full_bar(s), kb * C::kBK, m0);
-          const uint32_t bdst = (MODE == Mode::W8A8) ? sbase + L::kB + s * C::kBBytes
-                                                     : sbase + L::kRaw + s * C::kRawBytes;
-          tma_load_2d(bdst, map_b(maps, g), full_bar(s), kb * C::kBK, n0);
+          const uint32_t a_dst = sbase + L::kA + s * C::kABytes;
+          const int kc = kb * C::kBK;
+          if constexpr (!kA16) {
+            const uint32_t b_dst = sbase + L::kB + s * C::kBBytes;
+            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * (C::kABytes + C::kBBytes));
+            if constexpr (CG == 2) {
+              const uint32_t fb = leader_addr(full_bar(s));
+              tma_load_2d_pair(a_dst, &maps.a, fb, kc, a_row);
+              tma_load_2d_pair(b_dst, map_b(maps, g), fb, kc, b_row);
+            } else {
+              tma_load_2d(a_dst, &maps.a, full_bar(s), kc, a_row);
+              tma_load_2d(b_dst, map_b(maps, g), full_bar(s), kc, b_row);
+            }
+          } else {
+            const uint32_t r_dst = sbase + L::kRaw + s * C::kRawBytes;
+            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * C::kABytes);
+            mbar_arrive_expect_tx(rawfull_bar(s), C::kRawBytes);
+            if constexpr (CG == 2)
+              tma_load_2d_pair(a_dst, &maps.a, leader_addr(full_bar(s)), kc, a_row);
+            else
+              tma_load_2d(a_dst, &maps.a, full_bar(s), kc, a_row);
+            tma_load_2d(r_dst, map_b(maps, g), rawfull_bar(s), kc, b_row);
+          }
           ++issued;
           if (++s == S) {
             s = 0;
@@ -224,24 +263,29 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
           }
         }
       }
-      // Drain: every stage's most recent load must have landed before exit.
+      // Drain: every stage's most recent loads must have landed before exit.
+      // (The full barriers of the odd CTA of a pair are not used; its loads
+      // are covered by the even CTA's MMA drain and the closing cluster sync.)
       for (int j = 0; j < S && (uint32_t)j < issued; ++j) {
-        const uint32_t l = issued - 1 - j;  // the last S issues
+        const uint32_t l = issued - 1 - j;
         const int st = (int)(l % S);
         const uint32_t par = (l / S) & 1;
         volatile int never = 0;
-        if (!mbar_wait(full_bar(st), par, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
+        if (leader && !mbar_wait(full_bar(st), par, &never, kWaitLimitNs))
+          atomicOr(&g_gemm_err, kErrTimeout);
+        if (kA16 && !mbar_wait(rawfull_bar(st), par, &never, kWaitLimitNs))
+          atomicOr(&g_gemm_err, kErrTimeout);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
         if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1, abort, kWaitLimitNs)) {
           record_timeout(abort);
           break;
@@ -249,8 +293,10 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < args.num_kb; ++kb) {
-          const uint32_t wait_bar = (MODE == Mode::W8A8) ? full_bar(s) : ready_bar(s);
-          if (!mbar_wait(wait_bar, ph, abort, kWaitLimitNs)) {
+          bool got = mbar_wait(full_bar(s), ph, abort, kWaitLimitNs);
+          if (kA16 && got) got = mbar_wait(ready_bar(s), ph, abort, kWaitLimitNs);
+          if (kA16 && CG == 2 && got) got = mbar_wait(peer_ready_bar(s), ph, abort, kWaitLimitNs);
+          if (!got) {
             record_timeout(abort);
             ok = false;
             break;
@@ -262,28 +308,56 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
           for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
             const uint64_t ad = sw128_kmajor_desc(a_addr + 32 * k);
             const uint64_t bd = sw128_kmajor_desc(b_addr + 32 * k);
-            if (MODE == Mode::W8A8)
-              mma_f8f6f4(d, ad, bd, C::kIdesc, (kb | k) != 0);
-            else
-              mma_f16(d, ad, bd, C::kIdesc, (kb | k) != 0);
+            const uint32_t accum = (kb | k) != 0;
+            if constexpr (CG == 2) {
+              if constexpr (kA16) mma_f16_pair(d, ad, bd, C::kIdesc, accum);
+              else mma_f8f6f4_pair(d, ad, bd, C::kIdesc, accum);
+            } else {
+              if constexpr (kA16) mma_f16(d, ad, bd, C::kIdesc, accum);
+              else mma_f8f6f4(d, ad, bd, C::kIdesc, accum);
+            }
           }
-          mma_commit(empty_bar(s));
+          if constexpr (CG == 2) mma_commit_pair_mc(empty_bar(s), 0x3);
+          else mma_commit(empty_bar(s));
           if (++s == S) {
             s = 0;
             ph ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
+        if constexpr (CG == 2) mma_commit_pair_mc(tfull_bar(acc), 0x3);
+        else mma_commit(tfull_bar(acc));
         if (++acc == 2) {
           acc = 0;
           acc_ph ^= 1;
         }
       }
       // Drain: all MMAs issued by this thread complete before TMEM is freed.
-      mma_commit(drain_bar);
+      if constexpr (CG == 2) mma_commit_pair(drain_bar);
+      else mma_commit(drain_bar);
       volatile int never = 0;
       if (!mbar_wait(drain_bar, 0, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
+    } else if (kA16 && CG == 2 && lane == 0) {
+      // Odd CTA of a W8A16 pair: forward "this CTA's weight half is
+      // transformed" to the even CTA once per stage, so that the transform
+      // warps only arrive locally and never pay for a cluster-scope release.
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(ready_bar(s), ph, abort, kWaitLimitNs)) {
+            record_timeout(abort);
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(leader_addr(peer_ready_bar(s)));
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
     }
   } else if (warp < 2 + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
@@ -293,18 +367,18 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
     int acc = 0;
     uint32_t acc_ph = 0;
     int nbuf = 0;
-    for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+    for (int t = cluster_id; t < args.num_tiles; t += num_clusters) {
       int m0, g, n0;
-      decode_tile(args, t, m0, g, n0);
+      decode_tile<CG>(args, t, m0, g, n0);
       float alpha = 1.0f;
-      if (MODE == Mode::W8A8) alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, g)));
+      if constexpr (!kA16) alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, g)));
       // Warp-uniform wait: the TMEM loads below are .sync.aligned.
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_ph, abort, kWaitLimitNs))) {
         if (lane == 0) record_timeout(abort);
         break;
       }
       tc_fence_after();
-      const int row0 = m0 + wq * 32;
+      const int row0 = m0 + (int)rank * BM + wq * 32;
       const int ng = args.N[g];
       const uint32_t tbase = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
@@ -316,7 +390,10 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
         if (c == BN / 64 - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          if (lane == 0) {
+            if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
+            else mbar_arrive(tempty_bar(acc));
+          }
         }
         uint32_t packed[32];
 #pragma unroll
@@ -354,17 +431,21 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
     if (lane == 0) tma_store_wait_all();
   } else {
     // ---------------------------------------------------------------- weight transform
-    if constexpr (MODE == Mode::W8A16) {
-      const int r = threadIdx.x - (2 + kEpiWarps) * 32;  // weight row of the tile, 0..255
+    if constexpr (kA16) {
+      constexpr int TPR = C::kThreadsPerRow;     // threads sharing one weight row
+      constexpr int kChunks = 4 / TPR;           // 16-byte raw chunks per thread
+      const int tt = threadIdx.x - (2 + kEpiWarps) * 32;
+      const int r = tt / TPR;                    // weight row of this CTA's tile
+      const int part = tt % TPR;
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
         int m0, g, n0;
-        decode_tile(args, t, m0, g, n0);
+        decode_tile<CG>(args, t, m0, g, n0);
         const float sw = __ldg(scale_w(args, g));
         for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!__all_sync(0xffffffffu, mbar_wait(full_bar(s), ph, abort, kWaitLimitNs))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(rawfull_bar(s), ph, abort, kWaitLimitNs))) {
             if (lane == 0) record_timeout(abort);
             ok = false;
             break;
@@ -373,7 +454,8 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
           const uint8_t* raw = smem + L::kRaw + s * C::kRawBytes + r * 64;
           uint8_t* dst = smem + L::kB + s * C::kBBytes + r * 128;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int jj = 0; jj < kChunks; ++jj) {
+            const int j = part * kChunks + jj;
             const uint4 v = *reinterpret_cast<const uint4*>(raw + ((j ^ ((r >> 1) & 3)) * 16));
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
             uint32_t o[8];
@@ -408,9 +490,12 @@ __global__ void __launch_bounds__(Layout<MODE>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // A pair leaves together: no remote arrive or MMA may target an exited CTA.
+  if constexpr (CG == 2) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (CG == 2) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -431,10 +516,10 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
   return r == CUDA_SUCCESS;
 }
 
-template <Mode MODE>
+template <Mode MODE, int CG>
 cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  using C = Cfg<MODE>;
-  using L = Layout<MODE>;
+  using C = Cfg<MODE, CG>;
+  using L = Layout<MODE, CG>;
   *tmap_err = 0;
   Maps maps;
   Args args;
@@ -445,7 +530,7 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   args.K = (int)p.K;
   args.num_kb = (int)((p.K + C::kBK - 1) / C::kBK);
   args.s_in = p.s_in;
-  const int tiles_m = (int)((p.M + BM - 1) / BM);
+  const int tiles_m = (int)((p.M + BM * CG - 1) / (BM * CG));
   args.tiles_per_m = 0;
   bool ok = true;
   if (MODE == Mode::W8A8) {
@@ -462,10 +547,10 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
     args.tiles_per_m += args.tiles_n[g];
     if (MODE == Mode::W8A8) {
       ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 128,
-                      BN, CU_TENSOR_MAP_SWIZZLE_128B);
+                      C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
     } else {
-      ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 64, BN,
-                      CU_TENSOR_MAP_SWIZZLE_64B);
+      ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 64,
+                      C::kBRows, CU_TENSOR_MAP_SWIZZLE_64B);
     }
     ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y[g], p.N[g], p.M, p.N[g] * 2,
                     64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -476,22 +561,69 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
     return cudaSuccess;
   }
   args.num_tiles = tiles_m * args.tiles_per_m;
-  const int grid = args.num_tiles < sms ? args.num_tiles : sms;
-  auto kern = gemm_kernel<MODE>;
+  const int max_clusters = sms / CG;
+  const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
+  auto kern = gemm_kernel<MODE, CG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, L::kThreads, L::kAlloc, st>>>(maps, args);
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(clusters * CG, 1, 1);
+  cfg.blockDim = dim3(L::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, maps, args);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives on, gives up after `limit_ns` and records the timeout bit exactly as
+// the GEMM roles do.  No other memory is touched.
+__global__ void selftest_timeout_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile int* ab = &abort_flag;
+    if (!mbar_wait(smem_u32(&bar), 0, ab, limit_ns)) record_timeout(ab);
+  }
+  __syncthreads();
+}
+
+// The CTA pair needs M above one 128-row tile to pay off.
+bool use_pair(const GemmProblem& p) { return p.M > BM; }
 
 }  // namespace
 
 cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  return launch<Mode::W8A8>(p, sms, st, tmap_err);
+  return use_pair(p) ? launch<Mode::W8A8, 2>(p, sms, st, tmap_err)
+                     : launch<Mode::W8A8, 1>(p, sms, st, tmap_err);
 }
 
+// W8A16 stays on one CTA per tile: in the CTA pair each 64-K stage would wait
+// for the odd CTA's transform to be signalled across the SM pair, and that
+// cluster-scope hand-off costs more than the halved per-SM transform saves
+// (measured 766 vs 1054 TFLOP/s on the 20670 x 3 x 4096 x 4096 group).
 cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  return launch<Mode::W8A16>(p, sms, st, tmap_err);
+  return launch<Mode::W8A16, 1>(p, sms, st, tmap_err);
+}
+
+cudaError_t launch_selftest_timeout(cudaStream_t st) {
+  selftest_timeout_kernel<<<1, 32, 0, st>>>(200000000ull);  // 0.2 s
+  return cudaGetLastError();
 }
 
 cudaError_t gemm_read_error(cudaStream_t st, uint32_t* err) {

@@ -40,6 +40,9 @@ struct GemmProblem {
 cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 
+// Launches a one-thread kernel whose mbarrier wait times out (0.2 s).
+cudaError_t launch_selftest_timeout(cudaStream_t st);
+
 // Reads and clears the GEMM kernels' device error word (synchronises `st`).
 cudaError_t gemm_read_error(cudaStream_t st, uint32_t* err);
 
