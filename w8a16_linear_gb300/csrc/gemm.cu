@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       float alpha = 1.0f;
       if constexpr (!kA16) alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, g)));
       // Warp-uniform wait: the TMEM loads below are .sync.aligned.
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_ph, abort, kWaitLimitNs))) {
+      if (!mbar_wait_warp(tfull_bar(acc), acc_ph, abort, kWaitLimitNs)) {
         if (lane == 0) record_timeout(abort);
         break;
       }
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
         decode_tile<CG>(args, t, m0, g, n0);
         const float sw = __ldg(scale_w(args, g));
         for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!__all_sync(0xffffffffu, mbar_wait(rawfull_bar(s), ph, abort, kWaitLimitNs))) {
+          if (!mbar_wait_warp(rawfull_bar(s), ph, abort, kWaitLimitNs)) {
             if (lane == 0) record_timeout(abort);
             ok = false;
             break;
@@ -496,6 +496,287 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     tc_fence_after();
     if constexpr (CG == 2) tmem_dealloc_pair(tmem_base, kTmemCols);
     else tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ W8A16, weights in TMEM
+//
+// The W8A16 product computed transposed, D[n, m] = sum_k Wd[n, k] * x[m, k]:
+// the dequantized weight is the MMA's A operand and lives in TMEM, written
+// there by the transform warps with tcgen05.st (it never passes through
+// shared memory); the activation tile is the B operand, staged by TMA into a
+// 128-byte-swizzled K-major shared-memory buffer.  D has the 128 weight rows
+// of the tile across the TMEM lanes and the 192 tokens across columns; the
+// epilogue turns each 32-token x 32-feature block into row-major y through a
+// small staging buffer and a TMA store.
+//
+// TMEM columns: D[0] 0-191, D[1] 192-383 (double-buffered accumulators),
+// A stages 384 + 32 s (64 K-values of 128 rows, two bf16 per column).
+namespace a16t {
+constexpr int BT = 192;                      // tokens per tile (MMA N)
+constexpr int BW = 128;                      // weight rows per tile (MMA M)
+constexpr int BK = 64;                       // K per stage
+constexpr int S = 4;                         // stages
+constexpr int kXBytes = BT * 128;            // bf16 activation tile, 128-byte rows
+constexpr int kRawBytes = BW * 64;           // raw E4M3 weight rows
+constexpr int kEpiBuf = 32 * 64;             // 32 tokens x 32 features bf16
+constexpr int kOffX = 0;
+constexpr int kOffRaw = kOffX + S * kXBytes;
+constexpr int kOffEpi = kOffRaw + S * kRawBytes;
+constexpr int kOffBar = kOffEpi + 4 * 2 * kEpiBuf;
+constexpr int kNumBars = 3 * S + 5;          // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kAlloc = kOffAbort + 4 + 1024;
+constexpr int kTransformWarps = 16;         // 4 per TMEM lane quadrant, 16 K-values each
+constexpr int kThreads = (2 + 4 + kTransformWarps) * 32;
+constexpr uint32_t kTmemA = 2 * BT;          // first A-stage column
+constexpr uint32_t kIdesc = make_idesc(1, 1, BW, BT);
+static_assert(kTmemA + S * 32 <= kTmemCols, "TMEM budget");
+static_assert(kAlloc <= 232448, "shared memory budget");
+}  // namespace a16t
+
+__device__ __forceinline__ void decode_tile_a16t(const Args& a, int t, int& m0, int& g, int& n0) {
+  const int mb = t / a.tiles_per_m;
+  int r = t - mb * a.tiles_per_m;
+  g = 0;
+  while (g < a.G - 1 && r >= a.tiles_n[g]) {
+    r -= a.tiles_n[g];
+    ++g;
+  }
+  m0 = mb * a16t::BT;
+  n0 = r * a16t::BW;
+}
+
+__global__ void __launch_bounds__(a16t::kThreads, 1)
+    gemm_a16t_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args args) {
+  using namespace a16t;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + kOffBar;
+  auto full_bar = [&](int st) { return bar0 + 8u * st; };
+  auto empty_bar = [&](int st) { return bar0 + 8u * (S + st); };
+  auto ready_bar = [&](int st) { return bar0 + 8u * (2 * S + st); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < S; ++st) {
+      mbar_init(full_bar(st), 1);
+      mbar_init(empty_bar(st), 1);
+      mbar_init(ready_bar(st), a16t::kTransformWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&maps.a);
+    for (int g = 0; g < args.G; ++g) {
+      prefetch_tensormap(map_b(maps, g));
+      prefetch_tensormap(map_y(maps, g));
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0, issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+        int m0, g, n0;
+        decode_tile_a16t(args, t, m0, g, n0);
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(st), ph ^ 1, abort, kWaitLimitNs)) {
+            record_timeout(abort);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(st), kXBytes + kRawBytes);
+          tma_load_2d(sbase + kOffX + st * kXBytes, &maps.a, full_bar(st), kb * BK, m0);
+          tma_load_2d(sbase + kOffRaw + st * kRawBytes, map_b(maps, g), full_bar(st), kb * BK, n0);
+          ++issued;
+          if (++st == S) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      for (int j = 0; j < S && (uint32_t)j < issued; ++j) {
+        const uint32_t l = issued - 1 - j;
+        volatile int never = 0;
+        if (!mbar_wait(full_bar((int)(l % S)), (l / S) & 1, &never, kWaitLimitNs))
+          atomicOr(&g_gemm_err, kErrTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1, abort, kWaitLimitNs)) {
+          record_timeout(abort);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BT);
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(ready_bar(st), ph, abort, kWaitLimitNs)) {
+            record_timeout(abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t x_addr = sbase + kOffX + st * kXBytes;
+          const uint32_t a_col = tmem_base + kTmemA + (uint32_t)(st * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)  // K = 16 per MMA: 8 TMEM columns, 32 smem bytes
+            mma_f16_tmem_a(d, a_col + 8 * k, sw128_kmajor_desc(x_addr + 32 * k), kIdesc,
+                           (kb | k) != 0);
+          mma_commit(empty_bar(st));
+          if (++st == S) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_ph ^= 1;
+        }
+      }
+      mma_commit(drain_bar);
+      volatile int never = 0;
+      if (!mbar_wait(drain_bar, 0, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant: weight rows (features) q*32 .. q*32+31
+    uint8_t* bufp = smem + kOffEpi + (warp - 2) * 2 * kEpiBuf;
+    const uint32_t bufs = sbase + kOffEpi + (uint32_t)((warp - 2) * 2 * kEpiBuf);
+    int acc = 0, nbuf = 0;
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
+      int m0, g, n0;
+      decode_tile_a16t(args, t, m0, g, n0);
+      if (!mbar_wait_warp(tfull_bar(acc), acc_ph, abort, kWaitLimitNs)) {
+        if (lane == 0) record_timeout(abort);
+        break;
+      }
+      tc_fence_after();
+      const int f0 = n0 + q * 32;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
+#pragma unroll 1
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c * 32, r);  // feature f0+lane, tokens m0+c*32 .. +31
+        tmem_ld_wait();
+        if (c == BT / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        const int tok0 = m0 + c * 32;
+        if (tok0 >= args.M || f0 >= args.N[g]) continue;
+        if (lane == 0) tma_store_wait_read<1>();
+        __syncwarp();
+        uint16_t* bp = reinterpret_cast<uint16_t*>(bufp + nbuf * kEpiBuf);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const uint32_t pk = cvt_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+          bp[j * 32 + lane] = (uint16_t)(pk & 0xFFFF);        // token j, feature lane
+          bp[(j + 1) * 32 + lane] = (uint16_t)(pk >> 16);     // token j+1
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(map_y(maps, g), bufs + nbuf * kEpiBuf, f0, tok0);
+          tma_store_commit();
+        }
+        nbuf ^= 1;
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_ph ^= 1;
+      }
+    }
+    if (lane == 0) tma_store_wait_all();
+  } else {
+    // ---------------------------------------------------------------- weight transform
+    const int q = warp & 3;              // TMEM lane quadrant of this warp
+    const int kq = (warp - 6) >> 2;      // which 16 of the stage's 64 K-values
+    const int r = q * 32 + lane;         // weight row of the tile = TMEM lane
+    int st = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+      int m0, g, n0;
+      decode_tile_a16t(args, t, m0, g, n0);
+      const float sw = __ldg(scale_w(args, g));
+      for (int kb = 0; kb < args.num_kb; ++kb) {
+        if (!mbar_wait_warp(full_bar(st), ph, abort, kWaitLimitNs)) {
+          if (lane == 0) record_timeout(abort);
+          ok = false;
+          break;
+        }
+        // Raw row: 64 bytes with the 64-byte swizzle (chunk j at j ^ ((r >> 1) & 3));
+        // this thread converts chunk kq = K-values 16 kq .. 16 kq + 15.
+        const uint8_t* raw = smem + kOffRaw + st * kRawBytes + r * 64;
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + ((kq ^ ((r >> 1) & 3)) * 16));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(w4[e] & 0xFFFF));
+          const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(w4[e] >> 16));
+          const float a0 = __half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFF)));
+          const float a1 = __half2float(__ushort_as_half((unsigned short)(f01 >> 16)));
+          const float a2 = __half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFF)));
+          const float a3 = __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
+          o[2 * e] = cvt_bf16x2(__fmul_rn(a0, sw), __fmul_rn(a1, sw));
+          o[2 * e + 1] = cvt_bf16x2(__fmul_rn(a2, sw), __fmul_rn(a3, sw));
+        }
+        tmem_st_32x32b_x8(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(st * 32 + kq * 8), o);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready_bar(st));
+        if (++st == S) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -584,6 +865,44 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   return cudaGetLastError();
 }
 
+cudaError_t launch_a16t(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  using namespace a16t;
+  *tmap_err = 0;
+  Maps maps;
+  Args args;
+  std::memset(&maps, 0, sizeof(maps));
+  std::memset(&args, 0, sizeof(args));
+  args.G = p.G;
+  args.M = (int)p.M;
+  args.K = (int)p.K;
+  args.num_kb = (int)((p.K + BK - 1) / BK);
+  const int tiles_m = (int)((p.M + BT - 1) / BT);
+  bool ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, p.K, p.M, p.K * 2, 64, BT,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  for (int g = 0; g < p.G; ++g) {
+    args.N[g] = (int)p.N[g];
+    args.s_w[g] = p.s_w[g];
+    args.tiles_n[g] = (int)((p.N[g] + BW - 1) / BW);
+    args.tiles_per_m += args.tiles_n[g];
+    ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 64, BW,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+    ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y[g], p.N[g], p.M, p.N[g] * 2,
+                    32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  for (int g = p.G; g < kMaxGroup; ++g) args.s_w[g] = p.s_w[0];
+  if (!ok) {
+    *tmap_err = 1;
+    return cudaSuccess;
+  }
+  args.num_tiles = tiles_m * args.tiles_per_m;
+  const int grid = args.num_tiles < sms ? args.num_tiles : sms;
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_a16t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+  if (e != cudaSuccess) return e;
+  gemm_a16t_kernel<<<grid, kThreads, kAlloc, st>>>(maps, args);
+  return cudaGetLastError();
+}
+
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
 // arrives on, gives up after `limit_ns` and records the timeout bit exactly as
 // the GEMM roles do.  No other memory is touched.
@@ -618,7 +937,7 @@ cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int
 // cluster-scope hand-off costs more than the halved per-SM transform saves
 // (measured 766 vs 1054 TFLOP/s on the 20670 x 3 x 4096 x 4096 group).
 cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  return launch<Mode::W8A16, 1>(p, sms, st, tmap_err);
+  return launch_a16t(p, sms, st, tmap_err);
 }
 
 cudaError_t launch_selftest_timeout(cudaStream_t st) {
