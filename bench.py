@@ -1,14 +1,20 @@
 """Benchmark of the static per-tensor FP8 linear path on GB300.
 
-Workload (the headline): split Q/K/V with one shared activation
-quantization, 20670 tokens (a 13x30x53 latent grid), hidden 4096, three
-4096x4096 E4M3 weights with distinct weight scales and one static input
-scale.  One step = ``qkv_shared_quant_gemm`` in W8A8 mode: one quantization
-kernel plus one persistent tcgen05 GEMM launch over the three projections.
-Metric: W8A8 FP8 linear TFLOPS (3 * 2 * M * N * K per step / step time).
+Workload: one denoising-block pass of a 4096-wide diffusion transformer at
+20670 tokens (a 13x30x53 latent grid) on a W8A8 step of the 8-step policy.
+One step runs every row of the path through the public C ABI:
 
-Other kernels of the path (W8A16 group, SwiGLU FP8/bf16, the gated-MLP
-projections) are timed after the headline and reported under "breakdown".
+  step_policy_dispatch(step 3 of 8)                       -> W8A8
+  qkv_shared_quant_gemm  Q/K/V, one shared quantization, 3 x 4096x4096
+  fp8_linear_w8a8        out-projection 4096x4096 (quantizes its input)
+  qkv_shared_quant_gemm  gate/up, one shared quantization, 2 x 4096->16384
+  swiglu_2in_fp8         SiLU(gate)*up straight to E4M3 for the down projection
+  fp8_linear_w8a8        down projection 16384->4096 on the E4M3 codes
+
+Metric: W8A8 FP8 linear TFLOPS = the block's linear FLOPs (32 * M * 4096^2)
+per step / step time (quantization and SwiGLU kernels included in the time).
+The W8A16 rows (16-bit steps), the 8-step schedule, the split-QKV group
+alone and each kernel are timed after the headline under "breakdown".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 run under torchrun; every rank runs an independent replica (the
@@ -30,10 +36,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 M_TOK, HID, INTER = 20670, 4096, 16384
-GEMM_FLOPS = 3 * 2.0 * M_TOK * HID * HID
+BLOCK_FLOPS = 32.0 * M_TOK * HID * HID           # QKV 6 + out 2 + gate/up 16 + down 8
+QKV_FLOPS = 6.0 * M_TOK * HID * HID
 METRIC = "W8A8 FP8 linear TFLOPS (M≈20k, K=N=4096) and % of GB300 dense FP8 peak"
-WORKLOAD = "split QKV, shared static-FP8 activation quant, M=20670 (13x30x53), 3 x 4096x4096"
+WORKLOAD = ("A8 denoising-block step, M=20670 tokens (13x30x53), hidden 4096: split-QKV shared "
+            "quant 3x4096x4096, out-proj 4096x4096, split gate/up shared quant 2x4096->16384, "
+            "swiglu_2in FP8, down 16384->4096")
 L2_FLUSH_BYTES = 512 << 20
+POLICY_STEP, POLICY_STEPS = 3, 8
 
 
 def load_peaks():
@@ -64,7 +74,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:  # noqa: BLE001
             self.proc = None
@@ -100,113 +110,93 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- inputs
 
-def make_inputs(dev, seed=0):
-    """Synthetic device-resident inputs (drawn on the GPU with torch's seeded
-    generator; E4M3 weights from scaled normal draws with amax calibration)."""
-    g = torch.Generator(device=dev).manual_seed(seed)
-    x = torch.randn((M_TOK, HID), generator=g, device=dev) * 0.25
-    k = int(x.numel() * 0.001)
-    idx = torch.randint(0, x.numel(), (k,), generator=g, device=dev)
-    x.view(-1)[idx] *= 8.0
-    x = x.to(torch.bfloat16)
-    s_in = (x.float().abs().amax() / 448.0).reshape(1).contiguous()
+class Block:
+    """Device-resident synthetic inputs and outputs of one block.
 
-    def weight(n, kk, mult):
-        w = torch.randn((n, kk), generator=g, device=dev) * (0.02 * mult)
-        s = (w.abs().amax() / 448.0).reshape(1).contiguous()
-        q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
-        return q.contiguous(), s
+    Activations ~ N(0, 0.25^2) with 0.1% outliers x8 (drawn on the GPU with a
+    seeded torch generator); weights N(0, 0.02^2) scaled per projection by
+    c ~ U[0.5, 1], E4M3 with amax/448 weight scales; static input scales from
+    a separately drawn calibration batch (amax/448), so the live batch may
+    saturate."""
 
-    c = (torch.rand(3, generator=g, device=dev) * 0.5 + 0.5).tolist()
-    qkv = [weight(HID, HID, c[i]) for i in range(3)]
-    return x, s_in, qkv, weight
+    def __init__(self, dev, seed=0):
+        g = torch.Generator(device=dev).manual_seed(seed)
+        self.dev = dev
+
+        def act(n_rows, n_cols):
+            t = torch.randn((n_rows, n_cols), generator=g, device=dev) * 0.25
+            k = int(t.numel() * 0.001)
+            idx = torch.randint(0, t.numel(), (k,), generator=g, device=dev)
+            t.view(-1)[idx] *= 8.0
+            return t.to(torch.bfloat16)
+
+        def scale(t):
+            return (t.float().abs().amax() / 448.0).reshape(1).contiguous()
+
+        def weight(n, k):
+            c = float(torch.rand((), generator=g, device=dev)) * 0.5 + 0.5
+            w = torch.randn((n, k), generator=g, device=dev) * (0.02 * c)
+            s = scale(w)
+            q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+            return q, s
+
+        self.x_qkv, self.x_out, self.x_mlp = act(M_TOK, HID), act(M_TOK, HID), act(M_TOK, HID)
+        self.s_qkv = scale(act(4096, HID))
+        self.s_out = scale(act(4096, HID))
+        self.s_mlp = scale(act(4096, HID))
+        self.w_qkv = [weight(HID, HID) for _ in range(3)]
+        self.w_out = weight(HID, HID)
+        self.w_gu = [weight(INTER, HID) for _ in range(2)]
+        self.w_down = weight(HID, INTER)
+        self.s_h = torch.tensor([0.02], device=dev)        # down projection's input scale
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.y_qkv = [torch.empty((M_TOK, HID), **bf) for _ in range(3)]
+        self.y_out = torch.empty((M_TOK, HID), **bf)
+        self.y_gu = [torch.empty((M_TOK, INTER), **bf) for _ in range(2)]
+        self.h8 = torch.empty((M_TOK, INTER), dtype=torch.uint8, device=dev)
+        self.h16 = torch.empty((M_TOK, INTER), **bf)
+        self.y_down = torch.empty((M_TOK, HID), **bf)
+        self.ws = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
+
+    def outputs(self):
+        return self.y_qkv + [self.y_out, self.y_down]
+
+    def step(self, W, policy, step_index, num_steps, x_qkv=None, x_out=None, x_mlp=None):
+        """One block pass in the precision the policy selects for this step;
+        returns the number of kernel launches."""
+        x_qkv = self.x_qkv if x_qkv is None else x_qkv
+        x_out = self.x_out if x_out is None else x_out
+        x_mlp = self.x_mlp if x_mlp is None else x_mlp
+        mode = W.step_policy_dispatch(policy, step_index, num_steps)
+        wq = [q for q, _ in self.w_qkv]
+        sq = [s for _, s in self.w_qkv]
+        wgu = [q for q, _ in self.w_gu]
+        sgu = [s for _, s in self.w_gu]
+        if mode == W.MODE_A8:
+            W.qkv_shared_quant_gemm(W.MODE_A8, x_qkv, self.s_qkv, wq, sq, outs=self.y_qkv, ws=self.ws)
+            W.fp8_linear_w8a8(x_out, self.w_out[0], self.s_out, self.w_out[1], out=self.y_out, ws=self.ws)
+            W.qkv_shared_quant_gemm(W.MODE_A8, x_mlp, self.s_mlp, wgu, sgu, outs=self.y_gu, ws=self.ws)
+            W.swiglu_2in_fp8(self.y_gu[0], self.y_gu[1], self.s_h, out=self.h8)
+            W.fp8_linear_w8a8(self.h8, self.w_down[0], self.s_h, self.w_down[1], out=self.y_down)
+            return 8
+        W.qkv_shared_quant_gemm(W.MODE_A16, x_qkv, None, wq, sq, outs=self.y_qkv)
+        W.fp8_linear_w8a16(x_out, self.w_out[0], self.w_out[1], out=self.y_out)
+        W.qkv_shared_quant_gemm(W.MODE_A16, x_mlp, None, wgu, sgu, outs=self.y_gu)
+        W.swiglu_2in_bf16(self.y_gu[0], self.y_gu[1], out=self.h16)
+        W.fp8_linear_w8a16(self.h16, self.w_down[0], self.w_down[1], out=self.y_down)
+        return 5
 
 
 def flush_l2(buf):
     buf.add_(1.0)
 
 
-# ---------------------------------------------------------------- our arm
-
-def run_ours(args, rank, world, dev):
-    import w8a16_linear_gb300 as W
-    W.device_check()
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
-    x, s_in, qkv, weight = make_inputs(dev)
-    ws_q = [q for q, _ in qkv]
-    ws_s = [s for _, s in qkv]
-    ys = [torch.empty((M_TOK, HID), dtype=torch.bfloat16, device=dev) for _ in range(3)]
-    qx = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        W.qkv_shared_quant_gemm(W.MODE_A8, x, s_in, ws_q, ws_s, outs=ys, ws=qx)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    W.poll_device_error()
-
-    # ---- timed region: K steps, L2 flushed between steps (outside the events)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    for i in range(args.steps):
-        flush_l2(flush)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    W.poll_device_error()
-
-    # ---- dominant kernel: the 3-projection GEMM launch alone, same stream
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush_l2(flush)
-        gev[i][0].record(stream)
-        W.fp8_linear_w8a8_group(qx, s_in, ws_q, ws_s, outs=ys)
-        gev[i][1].record(stream)
-    torch.cuda.synchronize()
-    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in gev)
-
-    # ---- end to end through the public API with host buffers
-    xh = x.cpu().pin_memory()
-    yh = [torch.empty((M_TOK, HID), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
-    xd = torch.empty_like(x)
-    e2e_steps = max(3, min(args.steps, 10))
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(e2e_steps)]
-    for i in range(e2e_steps):
-        flush_l2(flush)
-        eev[i][0].record(stream)
-        xd.copy_(xh, non_blocking=True)
-        W.qkv_shared_quant_gemm(W.MODE_A8, xd, s_in, ws_q, ws_s, outs=ys, ws=qx)
-        for y, h in zip(ys, yh):
-            h.copy_(y, non_blocking=True)
-        eev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
-
-    breakdown = breakdown_ours(W, dev, stream, x, s_in, ws_q, ws_s, ys, qx, weight, flush, args)
-
-    return {"total_ms": total_ms, "step_ms": step_ms, "gemm_ms": gemm_ms, "e2e_ms": e2e_ms,
-            "h2d": x.numel() * 2, "d2h": 3 * M_TOK * HID * 2, "clocks": clk,
-            "breakdown": breakdown}
+def _events(n):
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
 
 
 def _time(fn, flush, stream, n):
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    ev = _events(n)
     fn()
     for i in range(n):
         flush_l2(flush)
@@ -217,59 +207,165 @@ def _time(fn, flush, stream, n):
     return statistics.median(a.elapsed_time(b) for a, b in ev)
 
 
-def breakdown_ours(W, dev, stream, x, s_in, ws_q, ws_s, ys, qx, weight, flush, args):
-    n = max(3, min(args.steps, 10))
-    out = {}
-    ms = _time(lambda: W.fp8_quant_static(x, s_in, out=qx), flush, stream, n)
-    out["fp8_quant_static"] = {"us": ms * 1e3, "GB_s": 3 * x.numel() / ms / 1e6}
-    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, ws_q, ws_s, outs=ys), flush, stream, n)
-    out["qkv_w8a16_group"] = {"us": ms * 1e3, "TFLOPS": GEMM_FLOPS / ms / 1e9}
-    ms = _time(lambda: W.fp8_linear_w8a8_group(qx, s_in, ws_q[:1], ws_s[:1], outs=ys[:1]), flush, stream, n)
-    out["w8a8_single_4096"] = {"us": ms * 1e3, "TFLOPS": GEMM_FLOPS / 3 / ms / 1e9}
-    del ys
-    g = torch.randn((M_TOK, INTER), device=dev).to(torch.bfloat16)
-    u = torch.randn((M_TOK, INTER), device=dev).to(torch.bfloat16)
-    h8 = torch.empty((M_TOK, INTER), dtype=torch.uint8, device=dev)
-    h16 = torch.empty((M_TOK, INTER), dtype=torch.bfloat16, device=dev)
-    s_out = torch.tensor([0.02], device=dev)
-    ms = _time(lambda: W.swiglu_2in_fp8(g, u, s_out, out=h8), flush, stream, n)
-    out["swiglu_2in_fp8"] = {"us": ms * 1e3, "GB_s": 5 * g.numel() / ms / 1e6}
-    ms = _time(lambda: W.swiglu_2in_bf16(g, u, out=h16), flush, stream, n)
-    out["swiglu_2in_bf16"] = {"us": ms * 1e3, "GB_s": 6 * g.numel() / ms / 1e6}
-    del h16
-    qg, sg = weight(INTER, HID, 0.8)
-    qd, sd = weight(HID, INTER, 0.9)
-    yg = torch.empty((M_TOK, INTER), dtype=torch.bfloat16, device=dev)
-    ms = _time(lambda: W.fp8_linear_w8a8_group(qx, s_in, [qg], [sg], outs=[yg]), flush, stream, n)
-    out["w8a8_gate_4096x16384"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
-    yd = torch.empty((M_TOK, HID), dtype=torch.bfloat16, device=dev)
-    ms = _time(lambda: W.fp8_linear_w8a8_group(h8, s_out, [qd], [sd], outs=[yd]), flush, stream, n)
-    out["w8a8_down_16384x4096"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, dev):
+    import w8a16_linear_gb300 as W
+    W.device_check()
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    blk = Block(dev)
+    policy = W.StepPolicy(1, 1, 3, 3)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        blk.step(W, policy, POLICY_STEP, POLICY_STEPS)
     torch.cuda.synchronize()
     W.poll_device_error()
+
+    # ---- timed region: K block steps, L2 flushed between steps (outside the events)
+    ev = _events(args.steps)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches = 0
+    for i in range(args.steps):
+        flush_l2(flush)
+        ev[i][0].record(stream)
+        launches += blk.step(W, policy, POLICY_STEP, POLICY_STEPS)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    W.poll_device_error()
+
+    # ---- dominant kernel: the block's four W8A8 GEMM launches alone, same
+    # shapes, on pre-quantized activations, same stream
+    q_qkv = W.fp8_quant_static(blk.x_qkv, blk.s_qkv)
+    q_out = W.fp8_quant_static(blk.x_out, blk.s_out)
+    q_mlp = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
+
+    def gemms():
+        W.fp8_linear_w8a8_group(q_qkv, blk.s_qkv, [q for q, _ in blk.w_qkv], [s for _, s in blk.w_qkv],
+                                outs=blk.y_qkv)
+        W.fp8_linear_w8a8_group(q_out, blk.s_out, [blk.w_out[0]], [blk.w_out[1]], outs=[blk.y_out])
+        W.fp8_linear_w8a8_group(q_mlp, blk.s_mlp, [q for q, _ in blk.w_gu], [s for _, s in blk.w_gu],
+                                outs=blk.y_gu)
+        W.fp8_linear_w8a8_group(blk.h8, blk.s_h, [blk.w_down[0]], [blk.w_down[1]], outs=[blk.y_down])
+
+    gemm_ms = _time(gemms, flush, stream, args.steps)
+    del q_qkv, q_out, q_mlp
+
+    # ---- end to end through the public API with host buffers
+    xh = [t.cpu().pin_memory() for t in (blk.x_qkv, blk.x_out, blk.x_mlp)]
+    yh = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in blk.outputs()]
+    xd = [torch.empty_like(t) for t in (blk.x_qkv, blk.x_out, blk.x_mlp)]
+    e2e_steps = max(3, min(args.steps, 10))
+    eev = _events(e2e_steps)
+    for i in range(e2e_steps):
+        flush_l2(flush)
+        eev[i][0].record(stream)
+        for d, h in zip(xd, xh):
+            d.copy_(h, non_blocking=True)
+        blk.step(W, policy, POLICY_STEP, POLICY_STEPS, *xd)
+        for d, h in zip(blk.outputs(), yh):
+            h.copy_(d, non_blocking=True)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in eev)
+    h2d = sum(t.numel() * t.element_size() for t in xd)
+    d2h = sum(t.numel() * t.element_size() for t in yh)
+    del xh, yh, xd
+
+    breakdown = breakdown_ours(W, blk, policy, flush, stream, args)
+    W.poll_device_error()
+    return {"total_ms": sum(step_ms), "step_ms": step_ms, "gemm_ms": gemm_ms, "e2e_ms": e2e_ms,
+            "h2d": h2d, "d2h": d2h, "clocks": clk, "launches": launches, "breakdown": breakdown}
+
+
+def breakdown_ours(W, blk, policy, flush, stream, args):
+    n = max(3, min(args.steps, 10))
+    out = {}
+    wq = [q for q, _ in blk.w_qkv]
+    sq = [s for _, s in blk.w_qkv]
+    ms = _time(lambda: blk.step(W, policy, 0, POLICY_STEPS), flush, stream, n)
+    out["block_a16_step"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
+                             "note": "W8A16 rows: QKV/gate-up groups in A16, out/down W8A16, swiglu bf16"}
+    ev = _events(1)
+    flush_l2(flush)
+    ev[0][0].record(stream)
+    for s in range(POLICY_STEPS):
+        blk.step(W, policy, s, POLICY_STEPS)
+    ev[0][1].record(stream)
+    torch.cuda.synchronize()
+    ms = ev[0][0].elapsed_time(ev[0][1])
+    out["schedule_8_steps_one_block"] = {"ms": ms, "TFLOPS": 8 * BLOCK_FLOPS / ms / 1e9,
+                                         "modes": "A16 x3, A8 x2, A16 x3"}
+    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A8, blk.x_qkv, blk.s_qkv, wq, sq, outs=blk.y_qkv,
+                                               ws=blk.ws), flush, stream, n)
+    out["qkv_group_a8"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
+                           "note": "quant + one 3-projection W8A8 launch, M=20670, 3x4096x4096"}
+    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, blk.x_qkv, None, wq, sq, outs=blk.y_qkv),
+               flush, stream, n)
+    out["qkv_group_a16"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9}
+    ms = _time(lambda: W.fp8_quant_static(blk.x_qkv, blk.s_qkv, out=blk.ws), flush, stream, n)
+    out["fp8_quant_static"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6}
+    ms = _time(lambda: W.swiglu_2in_fp8(blk.y_gu[0], blk.y_gu[1], blk.s_h, out=blk.h8), flush, stream, n)
+    out["swiglu_2in_fp8"] = {"us": ms * 1e3, "GB_s": 5 * blk.h8.numel() / ms / 1e6}
+    ms = _time(lambda: W.swiglu_2in_bf16(blk.y_gu[0], blk.y_gu[1], out=blk.h16), flush, stream, n)
+    out["swiglu_2in_bf16"] = {"us": ms * 1e3, "GB_s": 6 * blk.h16.numel() / ms / 1e6}
+    q = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
+    ms = _time(lambda: W.fp8_linear_w8a8_group(q, blk.s_mlp, [blk.w_gu[0][0]], [blk.w_gu[0][1]],
+                                               outs=[blk.y_gu[0]]), flush, stream, n)
+    out["w8a8_gate_4096x16384"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
+    ms = _time(lambda: W.fp8_linear_w8a8_group(blk.h8, blk.s_h, [blk.w_down[0]], [blk.w_down[1]],
+                                               outs=[blk.y_down]), flush, stream, n)
+    out["w8a8_down_16384x4096"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
+    ms = _time(lambda: W.fp8_linear_w8a16(blk.h16, blk.w_down[0], blk.w_down[1], out=blk.y_down),
+               flush, stream, n)
+    out["w8a16_down_16384x4096"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
+    torch.cuda.synchronize()
     return out
 
 
 # ---------------------------------------------------------------- oracle arm
 
-def run_oracle_sample(rows=512, seed=0):
-    """The CPU oracle on a bounded sample of the workload: ``rows`` tokens of
-    the split-QKV step (quantization plus the three W8A8 projections)."""
-    import oracle as O
-    from w8a16_linear_gb300 import synth
-    x = synth.activations_bf16(seed, (rows, HID), 0.25, outlier_frac=0.001)
-    s_in = np.float32(np.abs(O.bf16_decode(x)).max() / 448)
-    qws, s_ws = [], []
-    for i in range(3):
-        w = synth.normal_f32(10 + i, (HID, HID), 0.02)
-        s = np.float32(np.abs(w).max() / 448)
-        qws.append(O.e4m3_encode(w / s))
-        s_ws.append(s)
-    t0 = time.perf_counter()
-    O.qkv_shared_quant_gemm("A8", x, s_in, qws, s_ws)
-    dt = time.perf_counter() - t0
-    flops = 3 * 2.0 * rows * HID * HID
-    return flops / dt / 1e12, dt, rows
+class OracleBlock:
+    """The same block for the CPU oracle on a sample of tokens (set-up draws
+    E4M3 weights of the same shapes; scales as in `Block`)."""
+
+    def __init__(self, rows, seed=0):
+        import oracle as O
+        from w8a16_linear_gb300 import synth
+        self.O = O
+        self.rows = rows
+        self.x = [synth.activations_bf16(seed + i, (rows, HID), 0.25, outlier_frac=0.001) for i in range(3)]
+        self.s_in = [np.float32(np.abs(O.bf16_decode(x)).max() / 448) for x in self.x]
+
+        def weight(sd, n, k):
+            w = torch.randn((n, k), generator=torch.Generator().manual_seed(sd)) * 0.02
+            s = float(w.abs().max()) / 448.0
+            q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            return q, np.float32(s)
+
+        self.w_qkv = [weight(10 + i, HID, HID) for i in range(3)]
+        self.w_out = weight(13, HID, HID)
+        self.w_gu = [weight(20 + i, INTER, HID) for i in range(2)]
+        self.w_down = weight(30, HID, INTER)
+
+    def step(self):
+        O = self.O
+        O.qkv_shared_quant_gemm("A8", self.x[0], self.s_in[0], [q for q, _ in self.w_qkv],
+                                [s for _, s in self.w_qkv])
+        O.linear_w8a8(O.quant_static(self.x[1], self.s_in[1]), self.w_out[0], self.s_in[1], self.w_out[1])
+        g, u = O.qkv_shared_quant_gemm("A8", self.x[2], self.s_in[2], [q for q, _ in self.w_gu],
+                                       [s for _, s in self.w_gu])
+        h = O.swiglu_2in_fp8(g[1], u[1], np.float32(0.02))
+        O.linear_w8a8(h, self.w_down[0], np.float32(0.02), self.w_down[1])
 
 
 def cpu_cores():
@@ -279,26 +375,36 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def oracle_sample(rows=64, reps=1):
+    ob = OracleBlock(rows)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        ob.step()
+    dt = (time.perf_counter() - t0) / reps
+    return 32.0 * rows * HID * HID / dt / 1e12, dt
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
+    rows = 32
+    ob = OracleBlock(rows)
     for _ in range(args.warmup):
-        run_oracle_sample(rows=64)
-    vals, secs = [], []
-    rows = 512
+        ob.step()
+    secs = []
     for _ in range(args.steps):
-        v, dt, _ = run_oracle_sample(rows=rows)
-        vals.append(v)
-        secs.append(dt)
-    value = statistics.mean(vals)
+        t0 = time.perf_counter()
+        ob.step()
+        secs.append(time.perf_counter() - t0)
     ms = statistics.mean(secs) * 1e3
+    value = 32.0 * rows * HID * HID / (ms / 1e3) / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample_rows": rows, "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{rows} of {M_TOK} tokens of the split-QKV step per bench step"},
+                         "sample": f"{rows} of {M_TOK} tokens of the block per step"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -361,8 +467,8 @@ def max_over_ranks(value, device):
 
 
 def job_tflops(world, steps, max_total_ms):
-    """Whole-job throughput: every replica runs `steps` full steps."""
-    return world * GEMM_FLOPS * steps / (max_total_ms / 1e3) / 1e12
+    """Whole-job throughput: every replica runs `steps` full block steps."""
+    return world * BLOCK_FLOPS * steps / (max_total_ms / 1e3) / 1e12
 
 
 # ---------------------------------------------------------------- main
@@ -408,27 +514,28 @@ def main():
     if rank == 0:
         peaks = load_peaks()
         fp8_peak = peaks["bf16_tflops"] * 2.0          # nominal FP8:BF16 dense ratio 4.5:2.25
-        achieved = GEMM_FLOPS / (r["gemm_ms"] / 1e3) / 1e12
+        achieved = BLOCK_FLOPS / (r["gemm_ms"] / 1e3) / 1e12
         cpu = None
         if not args.no_cpu_baseline:
-            v, dt, rows = run_oracle_sample(rows=512)
+            v, dt = oracle_sample(rows=64)
             cpu = {"value": v, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-                   "sample": f"{rows} of {M_TOK} tokens of the split-QKV step ({dt:.1f} s)"}
+                   "sample": f"64 of {M_TOK} tokens of the block step ({dt:.1f} s)"}
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M_TOK, "K": HID, "N": HID, "projections": 3,
+            "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "intermediate": INTER,
+                       "policy_step": f"{POLICY_STEP} of {POLICY_STEPS} (W8A8)",
                        "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "tensor", "kernel": "gemm_kernel<W8A8> (3-projection launch)",
+            "roofline": {"bound": "tensor", "kernel": "gemm_kernel<W8A8, CTA pair> (the block's 4 launches)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                          "frac": achieved / fp8_peak, "traffic": None,
                          "peak_note": f"{peaks['source']} bf16 burst x 2 (nominal FP8/BF16 ratio)"},
             "pct_of_5pf_fp8": value / 5000.0,
             "cpu_baseline": cpu,
-            "e2e": {"value": GEMM_FLOPS / (r["e2e_ms"] / 1e3) / 1e12, "unit": "TFLOPS",
+            "e2e": {"value": BLOCK_FLOPS / (r["e2e_ms"] / 1e3) / 1e12, "unit": "TFLOPS",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": r["launches"],
             "clocks": r["clocks"],
             "breakdown": r["breakdown"],
         }
