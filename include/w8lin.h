@@ -181,6 +181,27 @@ w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const f
                                 const float* const* s_w, uint16_t* const* y, void* stream);
 
 /*
+ * gate_up_swiglu_fp8 — the split gated MLP's gate and up projections and the
+ * two-input SwiGLU in one pass, writing the down projection's E4M3 input:
+ *   g = bf16_RNE( fl32(s_in * s_w_gate) * qx . w_gate^T )
+ *   u = bf16_RNE( fl32(s_in * s_w_up)   * qx . w_up^T )
+ *   out = swiglu_2in_fp8(g, u, s_out)   (same specification, same codes)
+ * The gate and up accumulators live side by side in TMEM and never go to
+ * global memory; each projection keeps its own weight scale ([P4] What
+ * changed: split gate/up, one shared activation quantization, SiLU(G) * U
+ * quantized directly for the FP8 down projection).
+ *   x      activation [M, K]: bf16 if x_dtype == W8_DTYPE_BF16 (quantized
+ *          first with s_in into `ws`), or E4M3 codes quantized with s_in
+ *   w_gate, w_up  E4M3 [I, K];  s_in, s_w_gate, s_w_up, s_out device floats
+ *   out    E4M3 [M, I], written;  ws E4M3 [M, K] scratch (bf16 input only)
+ * Errors: NULL, SHAPE (K%16, I%16), DTYPE, ALIGN, ARCH, CUDA.
+ */
+w8_status gate_up_swiglu_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t K,
+                             const float* s_in, const uint8_t* w_gate, const uint8_t* w_up,
+                             int64_t I, const float* s_w_gate, const float* s_w_up,
+                             const float* s_out, uint8_t* out, uint8_t* ws, void* stream);
+
+/*
  * fp8_linear_w8a8_noalloc — fp8_linear_w8a8 on a bf16 activation for callers
  * that cannot allocate device memory (the web pages have no counterpart: this
  * entry point exists for integration, not for the method).  Some callers can

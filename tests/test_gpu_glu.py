@@ -1,0 +1,77 @@
+"""GPU parity of gate_up_swiglu_fp8, the fused gate/up GEMMs with the SwiGLU
+epilogue: the same E4M3 codes as the separate path (group GEMM -> bf16 gate
+and up -> swiglu_2in_fp8), bit-exact against the oracle where every partial
+sum is exact, and against the oracle chain elsewhere."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_util import W, dev_bf16, dev_f32, dev_u8, host_bits, host_u8, amax_scale  # noqa: F401
+from w8a16_linear_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(M, K, I, seed=0):
+    x = synth.activations_bf16(seed, (M, K), 0.25, outlier_frac=0.001)
+    xc = synth.activations_bf16(seed + 1, (min(M, 2048), K), 0.25, outlier_frac=0.001)
+    s_in = amax_scale(O.bf16_decode(xc))
+    ws, ss = [], []
+    for i, c in enumerate((0.7, 1.0)):
+        w = synth.normal_f32(seed + 10 + i, (I, K), 0.02) * np.float32(c)
+        s = amax_scale(w)
+        ws.append(O.e4m3_encode(w / s))
+        ss.append(s)
+    return x, s_in, ws, ss
+
+
+@pytest.mark.parametrize("M,K,I", [(64, 256, 256), (1, 16, 16), (129, 144, 272), (300, 512, 1024),
+                                   (2048, 4096, 4096)])
+def test_fused_equals_separate_path(W, M, K, I):
+    x, s_in, ws, ss = _problem(M, K, I, seed=M)
+    xd, si = dev_bf16(x), dev_f32(s_in)
+    wd, sd = [dev_u8(w) for w in ws], [dev_f32(s) for s in ss]
+    # calibrate the down projection's input scale on this batch's SwiGLU output
+    g, u = W.qkv_shared_quant_gemm(W.MODE_A8, xd, si, wd, sd)
+    h = O.swiglu_h(host_bits(g), host_bits(u))
+    s_out = dev_f32(amax_scale(h) if h.size else 1.0)
+    sep = W.swiglu_2in_fp8(g, u, s_out)
+    fused = W.gate_up_swiglu_fp8(xd, si, wd[0], wd[1], sd[0], sd[1], s_out)
+    torch.cuda.synchronize()
+    W.poll_device_error()
+    assert torch.equal(fused, sep)
+
+
+def test_fused_exact_sums_bit_exact_vs_oracle(W):
+    rng = np.random.default_rng(3)
+    M, K, I = 300, 2048, 512
+    vals = np.array([0.0, 0.5, -0.5, 1.0, -1.0, 1.5, -2.0], np.float32)
+    qx = O.e4m3_encode(rng.choice(vals, size=(M, K)))
+    wg = O.e4m3_encode(rng.choice(vals, size=(I, K)))
+    wu = O.e4m3_encode(rng.choice(vals, size=(I, K)))
+    s_in, s_g, s_u, s_out = (np.float32(2.0 ** -3), np.float32(2.0 ** -5), np.float32(2.0 ** -4),
+                             np.float32(0.0123))
+    out = W.gate_up_swiglu_fp8(dev_u8(qx), dev_f32(s_in), dev_u8(wg), dev_u8(wu), dev_f32(s_g),
+                               dev_f32(s_u), dev_f32(s_out))
+    _, gb = O.linear_w8a8(qx, wg, s_in, s_g)
+    _, ub = O.linear_w8a8(qx, wu, s_in, s_u)
+    assert np.array_equal(host_u8(out), O.swiglu_2in_fp8(gb, ub, s_out))
+
+
+def test_fused_vs_oracle_chain(W):
+    M, K, I = 512, 1024, 2048
+    x, s_in, ws, ss = _problem(M, K, I, seed=7)
+    s_out = np.float32(0.004)
+    out = host_u8(W.gate_up_swiglu_fp8(dev_bf16(x), dev_f32(s_in), dev_u8(ws[0]), dev_u8(ws[1]),
+                                       dev_f32(ss[0]), dev_f32(ss[1]), dev_f32(s_out)))
+    (_, gb), (_, ub) = O.qkv_shared_quant_gemm("A8", x, s_in, ws, ss)
+    want = O.swiglu_2in_fp8(gb, ub, s_out)
+    # codes can differ only where the GPU's bf16 gate/up differ from the
+    # correctly rounded ones (accumulation order); then by one E4M3 step
+    diff = out != want
+    assert diff.mean() < 2e-3
+    dv = np.abs(O.e4m3_decode(out[diff]).astype(np.float64) - O.e4m3_decode(want[diff]))
+    step = np.maximum(np.abs(O.e4m3_decode(want[diff])).astype(np.float64), 2.0 ** -6) / 8
+    assert np.all(dv <= step * 1.0001)

@@ -45,6 +45,9 @@ SIGNATURES = {
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_i64),
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
                                              _c_void_p]),
+    "gate_up_swiglu_fp8": (ctypes.c_int, [_c_void_p, _i32, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
+                                          _i64, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                          _c_void_p]),
     "fp8_linear_w8a8_noalloc": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i64, _c_void_p,
                                                _c_void_p, _c_void_p, _c_void_p]),
     "swiglu_2in_fp8": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p,
@@ -244,6 +247,30 @@ def fp8_linear_w8a8_group(qx, s_in, weights, weight_scales, outs=None, stream=No
     _check(lib().fp8_linear_w8a8_group(_ptr(q2), M, K, _ptr(_scalar(s_in, "s_in")), G, arr_w, arr_n,
                                        arr_s, arr_y, _stream(stream)))
     return outs
+
+
+def gate_up_swiglu_fp8(x, s_in, w_gate, w_up, s_w_gate, s_w_up, s_out, out=None, ws=None, stream=None):
+    """Fused gate/up W8A8 GEMMs + SwiGLU -> E4M3 [M, I] for the down projection."""
+    if x.dtype == torch.bfloat16:
+        xd, dt = _as_bf16(x, "x"), DTYPE_BF16
+    else:
+        xd, dt = _as_u8(x, "x"), DTYPE_E4M3
+    x2 = _flat2(xd)
+    M, K = x2.shape
+    wg, wu = _as_u8(w_gate, "w_gate"), _as_u8(w_up, "w_up")
+    if wg.shape != wu.shape:
+        raise W8Error(2, "gate and up weights differ in shape")
+    I = wg.shape[0]
+    if out is None:
+        out = torch.empty(*x.shape[:-1], I, dtype=torch.uint8, device=x.device)
+    o = _as_u8(out, "out")
+    if dt == DTYPE_BF16 and ws is None:
+        ws = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    _check(lib().gate_up_swiglu_fp8(_ptr(x2), dt, M, K, _ptr(_scalar(s_in, "s_in")), _ptr(wg), _ptr(wu), I,
+                                    _ptr(_scalar(s_w_gate, "s_w_gate")), _ptr(_scalar(s_w_up, "s_w_up")),
+                                    _ptr(_scalar(s_out, "s_out")), _ptr(o),
+                                    _ptr(_as_u8(ws, "ws") if ws is not None else None), _stream(stream)))
+    return out
 
 
 def fp8_linear_w8a8_noalloc(x, w, s_in, s_w, out=None, stream=None):

@@ -295,6 +295,50 @@ w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const f
   return cuda_status(e, "fp8_linear_w8a8_group: GEMM launch");
 }
 
+w8_status gate_up_swiglu_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t K,
+                             const float* s_in, const uint8_t* w_gate, const uint8_t* w_up,
+                             int64_t I, const float* s_w_gate, const float* s_w_up,
+                             const float* s_out, uint8_t* out, uint8_t* ws, void* stream) {
+  if (x_dtype != W8_DTYPE_BF16 && x_dtype != W8_DTYPE_E4M3)
+    return fail(W8_ERR_DTYPE, "gate_up_swiglu_fp8: unknown activation dtype %d", x_dtype);
+  w8_status st = check_linear_common("gate_up_swiglu_fp8", x, M, K, w_gate, I, s_w_gate,
+                                     reinterpret_cast<const uint16_t*>(out));
+  if (st != W8_OK) return st;
+  if (M == 0) return ok();
+  if (!w_up || !s_w_up || !s_in || !s_out) return fail(W8_ERR_NULL, "gate_up_swiglu_fp8: NULL pointer");
+  if (!aligned16(w_up)) return fail(W8_ERR_ALIGN, "gate_up_swiglu_fp8: w_up must be 16-byte aligned");
+  if (x_dtype == W8_DTYPE_BF16) {
+    if (!ws) return fail(W8_ERR_NULL, "gate_up_swiglu_fp8: bf16 input needs the [M,K] E4M3 workspace");
+    if (!aligned16(ws)) return fail(W8_ERR_ALIGN, "gate_up_swiglu_fp8: ws must be 16-byte aligned");
+  }
+  int sms = 0;
+  if ((st = device_info(&sms)) != W8_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* qx = static_cast<const uint8_t*>(x);
+  if (x_dtype == W8_DTYPE_BF16) {
+    cudaError_t e = w8::launch_quant_static(static_cast<const uint16_t*>(x), M * K, s_in, ws, sms, s);
+    if (e != cudaSuccess) return cuda_status(e, "gate_up_swiglu_fp8: quant launch");
+    qx = ws;
+  }
+  w8::GemmProblem p{};
+  p.M = M;
+  p.K = K;
+  p.G = 1;
+  p.x = qx;
+  p.w[0] = w_gate;
+  p.w[1] = w_up;
+  p.N[0] = I;
+  p.s_in = s_in;
+  p.s_w[0] = s_w_gate;
+  p.s_w[1] = s_w_up;
+  p.y[0] = out;
+  p.s_out = s_out;
+  int terr = 0;
+  cudaError_t e = w8::launch_gemm_glu(p, sms, s, &terr);
+  if (terr) return fail(W8_ERR_ALIGN, "gate_up_swiglu_fp8: tensor map encoding rejected the operands");
+  return cuda_status(e, "gate_up_swiglu_fp8: GEMM launch");
+}
+
 static w8_status check_swiglu(const char* fn, const uint16_t* g, const uint16_t* u, int64_t M,
                               int64_t I, const void* out) {
   if (M < 0 || I <= 0) return fail(W8_ERR_SHAPE, "%s: M=%lld I=%lld", fn, (long long)M, (long long)I);

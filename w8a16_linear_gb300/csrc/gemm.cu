@@ -4,37 +4,41 @@
 //        E4M3 activations and weights, F32 accumulation in TMEM
 //        (cosmos-framework PR #157, "feat: load ModelOpt static-FP8
 //        checkpoints via TorchAO", section Verification: _scaled_mm on the
-//        two per-tensor scales).
-//  W8A16 (kind::f16):    y = bf16( sum_k x[m,k] * Wd[n,k] ),
-//        Wd = bf16( fl32(dec(qw) * s_w) ) formed in shared memory by a
-//        transform stage; the static input scale is not used and no
-//        dequantized weight is ever written to global memory (TensorRT-LLM
-//        PR #17476, "Load static FP8 Cosmos3 Nano/Super checkpoints without
-//        re-quantizing them", section Denoising-step activation precision;
-//        diffusers PR #14664, "[Cosmos3] Mixed W8A8/W8A16 denoising for
-//        ModelOpt FP8 checkpoints", section Behavior).
+//        two per-tensor scales).  One launch serves a group of up to three
+//        projections that share the same activation (split Q/K/V or gate/up,
+//        each with its own weight and weight scale and its own contiguous
+//        output; TensorRT-LLM PR #17476, "Load static FP8 Cosmos3 Nano/Super
+//        checkpoints without re-quantizing them", sections Description and
+//        What changed).
+//  GLU   (kind::f8f6f4): the gate and up projections of a split gated MLP in
+//        one pass, followed in the epilogue by the two-input SwiGLU written
+//        straight to E4M3 for the down projection: out = E4M3(SwiGLU(g, u) /
+//        s_out) with g = bf16(s_in s_wg acc_g), u = bf16(s_in s_wu acc_u) --
+//        the same bf16 values the separate GEMMs would write, so the codes are
+//        those of swiglu_2in_fp8 applied to them; each projection keeps its
+//        own weight scale (TensorRT-LLM PR #17476, section What changed).
+//  W8A16 (kind::f16, below): y = bf16( sum_k x[m,k] * Wd[n,k] ),
+//        Wd = bf16( fl32(dec(qw) * s_w) ), the dequantized weight formed in
+//        TMEM; the static input scale is not used and no dequantized weight
+//        is written to global memory (TensorRT-LLM PR #17476, section
+//        Denoising-step activation precision; diffusers PR #14664,
+//        "[Cosmos3] Mixed W8A8/W8A16 denoising for ModelOpt FP8 checkpoints",
+//        section Behavior).
 //
-// One launch serves a group of up to three projections that share the same
-// activation (split Q/K/V or gate/up, each with its own weight and weight
-// scale and its own contiguous output; TensorRT-LLM PR #17476, sections
-// Description and What changed).
-//
-// Two shapes of the same kernel (template parameter CG):
-//   CG = 1  one CTA per SM computes a 128 x 256 output tile.
-//   CG = 2  a cluster of two CTAs on two SMs computes a 256 x 256 tile with
+// W8A8 / GLU kernel shapes (template parameter CG):
+//   CG = 1  one CTA per SM computes a 128-row output tile.
+//   CG = 2  a cluster of two CTAs on two SMs computes a 256-row tile with
 //           CTA-pair MMAs (tcgen05 cta_group::2): each CTA stages its 128
-//           activation rows and half (128 rows) of the weight tile, the even
+//           activation rows and half of the weight rows of the tile, the even
 //           CTA issues the MMAs, each CTA's TMEM receives its 128 output rows.
-//           Per SM this halves the weight bytes staged per FLOP (and, for
-//           W8A16, the weight rows each SM dequantizes).
+//           Per SM this halves the weight bytes staged per FLOP.
 //
 // Roles (per CTA, one CTA per SM, static round-robin over output tiles):
 //   warp 0      TMA producer: activation and weight tiles into a smem ring
 //   warp 1      TMEM allocator; MMA issuer (one thread of the even CTA)
-//   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> swizzled smem
-//               -> TMA store, double-buffered TMEM accumulators
-//   warps 6-13  (W8A16 only) E4M3 -> bf16 weight transform into the
-//               128-byte-swizzled K-major operand buffer
+//   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 (or SwiGLU ->
+//               E4M3) -> swizzled smem -> TMA store; double-buffered TMEM
+//               accumulators let it overlap the next tile's main loop
 // Every mbarrier wait is bounded: on a timeout the kernel records an error
 // bit, the other roles stop at their next wait, in-flight copies and MMAs
 // are drained with bounded waits, TMEM is freed and the kernel returns.
@@ -47,6 +51,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "swiglu_spec.cuh"
 
 namespace w8 {
 
@@ -54,30 +59,27 @@ __device__ uint32_t g_gemm_err;
 
 namespace {
 
-constexpr int BM = 128;                          // output rows per CTA
-constexpr int BN = 256;                          // output columns per tile
-constexpr uint32_t kTmemCols = 512;              // two BN-column F32 accumulators
+constexpr int BM = 128;                           // output rows per CTA
+constexpr uint32_t kTmemCols = 512;               // two 256-column F32 accumulator buffers
+constexpr uint32_t kAccCols = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kEpiWarps = 4;
-constexpr int kEpiBufBytes = 32 * 128;           // 32 rows x 64 bf16 columns
+constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x 128 bytes
 constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
-constexpr int kTransformWarps = 8;
 
-enum class Mode { W8A8, W8A16 };
+enum class Mode { W8A8, GLU };
 
 template <Mode MODE, int CG>
 struct Cfg {
-  static constexpr bool kA16 = (MODE == Mode::W8A16);
-  static constexpr int kBRows = BN / CG;                       // weight rows staged per CTA
-  static constexpr int kBK = kA16 ? 64 : 128;                  // K elements per stage
-  static constexpr int kABytes = BM * 128;                     // 128-byte rows
-  static constexpr int kBBytes = kBRows * 128;                 // MMA operand (E4M3 or bf16)
-  static constexpr int kRawBytes = kA16 ? kBRows * 64 : 0;     // raw E4M3 rows (W8A16)
-  static constexpr int kStages = kA16 ? (CG == 1 ? 3 : 4) : (CG == 1 ? 4 : 6);
-  static constexpr int kTW = kA16 ? kTransformWarps : 0;
-  static constexpr int kThreadsPerRow = kA16 ? (kTW * 32) / kBRows : 1;  // 1 or 2
-  static constexpr uint32_t kIdesc =
-      kA16 ? make_idesc(1, 1, BM * CG, BN) : make_idesc(0, 0, BM * CG, BN);
+  static constexpr bool kGlu = (MODE == Mode::GLU);
+  static constexpr int kBN = kGlu ? 128 : 256;              // output columns per tile
+  static constexpr int kBRows = kBN / CG;                   // weight rows per projection per CTA
+  static constexpr int kBK = 128;                           // K per stage (bytes = elements)
+  static constexpr int kABytes = BM * 128;
+  static constexpr int kBHalf = kBRows * 128;               // one projection's weight tile
+  static constexpr int kBBytes = (kGlu ? 2 : 1) * kBHalf;
+  static constexpr int kStages = CG == 1 ? 4 : 6;
+  static constexpr uint32_t kIdesc = make_idesc(0, 0, BM * CG, kBN);  // E4M3 x E4M3 -> F32
 };
 
 template <Mode MODE, int CG>
@@ -85,17 +87,15 @@ struct Layout {
   using C = Cfg<MODE, CG>;
   static constexpr int kA = 0;
   static constexpr int kB = kA + C::kStages * C::kABytes;
-  static constexpr int kRaw = kB + C::kStages * C::kBBytes;
-  static constexpr int kEpi = kRaw + C::kStages * C::kRawBytes;
+  static constexpr int kEpi = kB + C::kStages * C::kBBytes;
   static constexpr int kBar = kEpi + kEpiBytes;
-  // barriers: full[S], empty[S], ready[S], rawfull[S], peer_ready[S], tfull[2],
-  // tempty[2], drain
-  static constexpr int kNumBars = 5 * C::kStages + 5;
+  // barriers: full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int kNumBars = 2 * C::kStages + 5;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kAlloc = kEnd + 1024;  // slack for 1024-byte alignment
-  static constexpr int kThreads = (2 + kEpiWarps + C::kTW) * 32;
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -115,11 +115,12 @@ struct Args {
   int num_kb;
   const float* s_in;
   const float* s_w[kMaxGroup];
+  const float* s_out;  // GLU: the down projection's input scale
 };
 
 // Tile t -> first output row of the (cluster) tile, projection, first column.
-template <int CG>
-__device__ __forceinline__ void decode_tile(const Args& a, int t, int& m0, int& g, int& n0) {
+__device__ __forceinline__ void decode_tile(const Args& a, int t, int rows_per_tile, int cols_per_tile,
+                                            int& m0, int& g, int& n0) {
   const int mb = t / a.tiles_per_m;
   int r = t - mb * a.tiles_per_m;
   g = 0;
@@ -127,8 +128,8 @@ __device__ __forceinline__ void decode_tile(const Args& a, int t, int& m0, int& 
     r -= a.tiles_n[g];
     ++g;
   }
-  m0 = mb * BM * CG;
-  n0 = r * BN;
+  m0 = mb * rows_per_tile;
+  n0 = r * cols_per_tile;
 }
 
 __device__ __forceinline__ const CUtensorMap* map_b(const Maps& m, int g) {
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
   using C = Cfg<MODE, CG>;
   using L = Layout<MODE, CG>;
   constexpr int S = C::kStages;
-  constexpr bool kA16 = C::kA16;
+  constexpr bool kGlu = C::kGlu;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -161,12 +162,9 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
   const uint32_t bar0 = sbase + L::kBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-  auto ready_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  auto rawfull_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
-  auto peer_ready_bar = [&](int s) { return bar0 + 8u * (4 * S + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (5 * S + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (5 * S + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (5 * S + 4);
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
@@ -183,9 +181,6 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-      mbar_init(ready_bar(s), kA16 ? C::kTW : 1);  // this CTA's transform warps
-      mbar_init(rawfull_bar(s), 1);
-      mbar_init(peer_ready_bar(s), 1);              // forwarded by the odd CTA
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -195,10 +190,8 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     *abort = 0;
     fence_mbar_init();
     prefetch_tensormap(&maps.a);
-    for (int g = 0; g < args.G; ++g) {
-      prefetch_tensormap(map_b(maps, g));
-      prefetch_tensormap(map_y(maps, g));
-    }
+    for (int g = 0; g < (kGlu ? 2 : args.G); ++g) prefetch_tensormap(map_b(maps, g));
+    for (int g = 0; g < args.G; ++g) prefetch_tensormap(map_y(maps, g));
   }
   if (warp == 1) {
     if constexpr (CG == 2) {
@@ -224,7 +217,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       bool ok = true;
       for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
         int m0, g, n0;
-        decode_tile<CG>(args, t, m0, g, n0);
+        decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
         const int a_row = m0 + (int)rank * BM;
         const int b_row = n0 + (int)rank * C::kBRows;
         for (int kb = 0; kb < args.num_kb; ++kb) {
@@ -234,27 +227,20 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
             break;
           }
           const uint32_t a_dst = sbase + L::kA + s * C::kABytes;
+          const uint32_t b_dst = sbase + L::kB + s * C::kBBytes;
           const int kc = kb * C::kBK;
-          if constexpr (!kA16) {
-            const uint32_t b_dst = sbase + L::kB + s * C::kBBytes;
-            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * (C::kABytes + C::kBBytes));
-            if constexpr (CG == 2) {
-              const uint32_t fb = leader_addr(full_bar(s));
-              tma_load_2d_pair(a_dst, &maps.a, fb, kc, a_row);
-              tma_load_2d_pair(b_dst, map_b(maps, g), fb, kc, b_row);
-            } else {
-              tma_load_2d(a_dst, &maps.a, full_bar(s), kc, a_row);
-              tma_load_2d(b_dst, map_b(maps, g), full_bar(s), kc, b_row);
-            }
+          if (leader) mbar_arrive_expect_tx(full_bar(s), CG * (C::kABytes + C::kBBytes));
+          const uint32_t fb = leader_addr(full_bar(s));
+          // GLU: gate rows, then up rows, in one stage.
+          const CUtensorMap* mb0 = kGlu ? &maps.b[0] : map_b(maps, g);
+          if constexpr (CG == 2) {
+            tma_load_2d_pair(a_dst, &maps.a, fb, kc, a_row);
+            tma_load_2d_pair(b_dst, mb0, fb, kc, b_row);
+            if constexpr (kGlu) tma_load_2d_pair(b_dst + C::kBHalf, &maps.b[1], fb, kc, b_row);
           } else {
-            const uint32_t r_dst = sbase + L::kRaw + s * C::kRawBytes;
-            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * C::kABytes);
-            mbar_arrive_expect_tx(rawfull_bar(s), C::kRawBytes);
-            if constexpr (CG == 2)
-              tma_load_2d_pair(a_dst, &maps.a, leader_addr(full_bar(s)), kc, a_row);
-            else
-              tma_load_2d(a_dst, &maps.a, full_bar(s), kc, a_row);
-            tma_load_2d(r_dst, map_b(maps, g), rawfull_bar(s), kc, b_row);
+            tma_load_2d(a_dst, &maps.a, fb, kc, a_row);
+            tma_load_2d(b_dst, mb0, fb, kc, b_row);
+            if constexpr (kGlu) tma_load_2d(b_dst + C::kBHalf, &maps.b[1], fb, kc, b_row);
           }
           ++issued;
           if (++s == S) {
@@ -264,17 +250,15 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
         }
       }
       // Drain: every stage's most recent loads must have landed before exit.
-      // (The full barriers of the odd CTA of a pair are not used; its loads
-      // are covered by the even CTA's MMA drain and the closing cluster sync.)
-      for (int j = 0; j < S && (uint32_t)j < issued; ++j) {
-        const uint32_t l = issued - 1 - j;
-        const int st = (int)(l % S);
-        const uint32_t par = (l / S) & 1;
-        volatile int never = 0;
-        if (leader && !mbar_wait(full_bar(st), par, &never, kWaitLimitNs))
-          atomicOr(&g_gemm_err, kErrTimeout);
-        if (kA16 && !mbar_wait(rawfull_bar(st), par, &never, kWaitLimitNs))
-          atomicOr(&g_gemm_err, kErrTimeout);
+      // (The odd CTA of a pair has no armed full barriers; its loads are
+      // covered by the even CTA's MMA drain and the closing cluster sync.)
+      if (leader) {
+        for (int j = 0; j < S && (uint32_t)j < issued; ++j) {
+          const uint32_t l = issued - 1 - j;
+          volatile int never = 0;
+          if (!mbar_wait(full_bar((int)(l % S)), (l / S) & 1, &never, kWaitLimitNs))
+            atomicOr(&g_gemm_err, kErrTimeout);
+        }
       }
     }
   } else if (warp == 1) {
@@ -291,12 +275,9 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
         for (int kb = 0; kb < args.num_kb; ++kb) {
-          bool got = mbar_wait(full_bar(s), ph, abort, kWaitLimitNs);
-          if (kA16 && got) got = mbar_wait(ready_bar(s), ph, abort, kWaitLimitNs);
-          if (kA16 && CG == 2 && got) got = mbar_wait(peer_ready_bar(s), ph, abort, kWaitLimitNs);
-          if (!got) {
+          if (!mbar_wait(full_bar(s), ph, abort, kWaitLimitNs)) {
             record_timeout(abort);
             ok = false;
             break;
@@ -307,14 +288,13 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
             const uint64_t ad = sw128_kmajor_desc(a_addr + 32 * k);
-            const uint64_t bd = sw128_kmajor_desc(b_addr + 32 * k);
             const uint32_t accum = (kb | k) != 0;
-            if constexpr (CG == 2) {
-              if constexpr (kA16) mma_f16_pair(d, ad, bd, C::kIdesc, accum);
-              else mma_f8f6f4_pair(d, ad, bd, C::kIdesc, accum);
-            } else {
-              if constexpr (kA16) mma_f16(d, ad, bd, C::kIdesc, accum);
-              else mma_f8f6f4(d, ad, bd, C::kIdesc, accum);
+#pragma unroll
+            for (int h = 0; h < (kGlu ? 2 : 1); ++h) {  // GLU: gate into d, up into d + 128
+              const uint64_t bd = sw128_kmajor_desc(b_addr + h * C::kBHalf + 32 * k);
+              const uint32_t dh = d + (uint32_t)(h * C::kBN);
+              if constexpr (CG == 2) mma_f8f6f4_pair(dh, ad, bd, C::kIdesc, accum);
+              else mma_f8f6f4(dh, ad, bd, C::kIdesc, accum);
             }
           }
           if constexpr (CG == 2) mma_commit_pair_mc(empty_bar(s), 0x3);
@@ -337,29 +317,8 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       else mma_commit(drain_bar);
       volatile int never = 0;
       if (!mbar_wait(drain_bar, 0, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
-    } else if (kA16 && CG == 2 && lane == 0) {
-      // Odd CTA of a W8A16 pair: forward "this CTA's weight half is
-      // transformed" to the even CTA once per stage, so that the transform
-      // warps only arrive locally and never pay for a cluster-scope release.
-      int s = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
-        for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!mbar_wait(ready_bar(s), ph, abort, kWaitLimitNs)) {
-            record_timeout(abort);
-            ok = false;
-            break;
-          }
-          mbar_arrive_cluster(leader_addr(peer_ready_bar(s)));
-          if (++s == S) {
-            s = 0;
-            ph ^= 1;
-          }
-        }
-      }
     }
-  } else if (warp < 2 + kEpiWarps) {
+  } else {
     // ---------------------------------------------------------------- epilogue
     const int wq = warp & 3;  // TMEM lane quadrant this warp may access
     const uint32_t buf0 = sbase + L::kEpi + (uint32_t)((warp - 2) * 2 * kEpiBufBytes);
@@ -367,11 +326,19 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     int acc = 0;
     uint32_t acc_ph = 0;
     int nbuf = 0;
+    float s_out = 1.0f, rs_out = 1.0f;
+    bool exact_only = false;
+    if constexpr (kGlu) {
+      s_out = __ldg(args.s_out);
+      rs_out = __frcp_rn(s_out);
+      exact_only = !scale_is_fast(s_out, rs_out);
+    }
     for (int t = cluster_id; t < args.num_tiles; t += num_clusters) {
       int m0, g, n0;
-      decode_tile<CG>(args, t, m0, g, n0);
-      float alpha = 1.0f;
-      if constexpr (!kA16) alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, g)));
+      decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
+      float alpha = 1.0f, alpha_u = 1.0f;
+      alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, kGlu ? 0 : g)));
+      if constexpr (kGlu) alpha_u = __fmul_rn(__ldg(args.s_in), __ldg(args.s_w[1]));
       // Warp-uniform wait: the TMEM loads below are .sync.aligned.
       if (!mbar_wait_warp(tfull_bar(acc), acc_ph, abort, kWaitLimitNs)) {
         if (lane == 0) record_timeout(abort);
@@ -380,45 +347,91 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       tc_fence_after();
       const int row0 = m0 + (int)rank * BM + wq * 32;
       const int ng = args.N[g];
-      const uint32_t tbase = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t tbase = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * kAccCols);
+      if constexpr (!kGlu) {
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tbase + c * 64, r0);
-        tmem_ld_32x32b_x32(tbase + c * 64 + 32, r1);
-        tmem_ld_wait();
-        if (c == BN / 64 - 1) {
-          tc_fence_before();
+        for (int c = 0; c < C::kBN / 64; ++c) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(tbase + c * 64, r0);
+          tmem_ld_32x32b_x32(tbase + c * 64 + 32, r1);
+          tmem_ld_wait();
+          if (c == C::kBN / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
+              else mbar_arrive(tempty_bar(acc));
+            }
+          }
+          uint32_t packed[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            packed[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r0[2 * j]), alpha),
+                                   __fmul_rn(__uint_as_float(r0[2 * j + 1]), alpha));
+            packed[16 + j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r1[2 * j]), alpha),
+                                        __fmul_rn(__uint_as_float(r1[2 * j + 1]), alpha));
+          }
+          const int col0 = n0 + c * 64;
+          if (col0 >= ng || row0 >= args.M) continue;  // nothing of this chunk is in range
+          // The store issued two chunks ago from this buffer must have read it.
+          if (lane == 0) tma_store_wait_read<1>();
+          __syncwarp();
+          uint8_t* bp = buf0_ptr + nbuf * kEpiBufBytes + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int pj = j ^ (lane & 7);  // 128-byte swizzle within the 1024-byte atom
+            *reinterpret_cast<uint4*>(bp + pj * 16) =
+                make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
-            else mbar_arrive(tempty_bar(acc));
+            tma_store_2d(map_y(maps, g), buf0 + nbuf * kEpiBufBytes, col0, row0);
+            tma_store_commit();
           }
+          nbuf ^= 1;
         }
-        uint32_t packed[32];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          packed[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r0[2 * j]), alpha),
-                                 __fmul_rn(__uint_as_float(r0[2 * j + 1]), alpha));
-          packed[16 + j] = cvt_bf16x2(__fmul_rn(__uint_as_float(r1[2 * j]), alpha),
-                                      __fmul_rn(__uint_as_float(r1[2 * j + 1]), alpha));
-        }
-        const int col0 = n0 + c * 64;
-        if (col0 >= ng || row0 >= args.M) continue;  // nothing of this chunk is in range
-        // The store issued two chunks ago from this buffer must have read it.
+      } else {
+        // 128 intermediate columns per row: gate at tbase, up at tbase + 128.
+        // Each 32-column chunk gives 32 E4M3 codes (two 16-byte chunks of the
+        // row's 128-byte staging line).
         if (lane == 0) tma_store_wait_read<1>();
         __syncwarp();
         uint8_t* bp = buf0_ptr + nbuf * kEpiBufBytes + lane * 128;
+#pragma unroll 1
+        for (int c = 0; c < C::kBN / 32; ++c) {
+          uint32_t rg[32], ru[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, rg);
+          tmem_ld_32x32b_x32(tbase + C::kBN + c * 32, ru);
+          tmem_ld_wait();
+          if (c == C::kBN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
+              else mbar_arrive(tempty_bar(acc));
+            }
+          }
+          uint32_t codes[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int pj = j ^ (lane & 7);  // 128-byte swizzle within the 1024-byte atom
-          *reinterpret_cast<uint4*>(bp + pj * 16) =
-              make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+          for (int j = 0; j < 16; ++j) {
+            // the bf16 values the separate gate / up GEMMs would have written
+            const uint32_t gw = cvt_bf16x2(__fmul_rn(__uint_as_float(rg[2 * j]), alpha),
+                                           __fmul_rn(__uint_as_float(rg[2 * j + 1]), alpha));
+            const uint32_t uw = cvt_bf16x2(__fmul_rn(__uint_as_float(ru[2 * j]), alpha_u),
+                                           __fmul_rn(__uint_as_float(ru[2 * j + 1]), alpha_u));
+            const uint32_t pair = swiglu_fp8_pair(gw, uw, s_out, rs_out, exact_only);
+            if (j & 1) codes[j >> 1] |= pair << 16;
+            else codes[j >> 1] = pair;
+          }
+          const int pj0 = (2 * c) ^ (lane & 7), pj1 = (2 * c + 1) ^ (lane & 7);
+          *reinterpret_cast<uint4*>(bp + pj0 * 16) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          *reinterpret_cast<uint4*>(bp + pj1 * 16) = make_uint4(codes[4], codes[5], codes[6], codes[7]);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(map_y(maps, g), buf0 + nbuf * kEpiBufBytes, col0, row0);
+        if (lane == 0 && n0 < ng && row0 < args.M) {
+          tma_store_2d(map_y(maps, 0), buf0 + nbuf * kEpiBufBytes, n0, row0);
           tma_store_commit();
         }
         nbuf ^= 1;
@@ -429,63 +442,6 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       }
     }
     if (lane == 0) tma_store_wait_all();
-  } else {
-    // ---------------------------------------------------------------- weight transform
-    if constexpr (kA16) {
-      constexpr int TPR = C::kThreadsPerRow;     // threads sharing one weight row
-      constexpr int kChunks = 4 / TPR;           // 16-byte raw chunks per thread
-      const int tt = threadIdx.x - (2 + kEpiWarps) * 32;
-      const int r = tt / TPR;                    // weight row of this CTA's tile
-      const int part = tt % TPR;
-      int s = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
-        int m0, g, n0;
-        decode_tile<CG>(args, t, m0, g, n0);
-        const float sw = __ldg(scale_w(args, g));
-        for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!mbar_wait_warp(rawfull_bar(s), ph, abort, kWaitLimitNs)) {
-            if (lane == 0) record_timeout(abort);
-            ok = false;
-            break;
-          }
-          // Raw row: 64 bytes, 64-byte swizzle (16-byte chunk j at j ^ ((r >> 1) & 3)).
-          const uint8_t* raw = smem + L::kRaw + s * C::kRawBytes + r * 64;
-          uint8_t* dst = smem + L::kB + s * C::kBBytes + r * 128;
-#pragma unroll
-          for (int jj = 0; jj < kChunks; ++jj) {
-            const int j = part * kChunks + jj;
-            const uint4 v = *reinterpret_cast<const uint4*>(raw + ((j ^ ((r >> 1) & 3)) * 16));
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[8];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(w4[h] & 0xFFFF));
-              const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(w4[h] >> 16));
-              const float a0 = __half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFF)));
-              const float a1 = __half2float(__ushort_as_half((unsigned short)(f01 >> 16)));
-              const float a2 = __half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFF)));
-              const float a3 = __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
-              o[2 * h] = cvt_bf16x2(__fmul_rn(a0, sw), __fmul_rn(a1, sw));
-              o[2 * h + 1] = cvt_bf16x2(__fmul_rn(a2, sw), __fmul_rn(a3, sw));
-            }
-            // 16 raw bytes -> 32 bf16 bytes = chunks 2j and 2j+1 of the operand row.
-            const int c0 = (2 * j) ^ (r & 7);
-            const int c1 = (2 * j + 1) ^ (r & 7);
-            *reinterpret_cast<uint4*>(dst + c0 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(dst + c1 * 16) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ready_bar(s));
-          if (++s == S) {
-            s = 0;
-            ph ^= 1;
-          }
-        }
-      }
-    }
   }
 
   tc_fence_before();
@@ -505,48 +461,40 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
 // the dequantized weight is the MMA's A operand and lives in TMEM, written
 // there by the transform warps with tcgen05.st (it never passes through
 // shared memory); the activation tile is the B operand, staged by TMA into a
-// 128-byte-swizzled K-major shared-memory buffer.  D has the 128 weight rows
-// of the tile across the TMEM lanes and the 192 tokens across columns; the
-// epilogue turns each 32-token x 32-feature block into row-major y through a
-// small staging buffer and a TMA store.
+// 128-byte-swizzled K-major shared-memory buffer.  A tile is 128 weight rows
+// x 384 tokens, computed as two N = 192 MMAs that share each dequantized
+// weight stage, so every weight element is converted once per 384 tokens.
+// D has the weight rows across the TMEM lanes and the tokens across columns;
+// the epilogue turns each 32-token x 32-feature block into row-major y
+// through a small staging buffer and a TMA store.
 //
-// TMEM columns: D[0] 0-191, D[1] 192-383 (double-buffered accumulators),
-// A stages 384 + 32 s (64 K-values of 128 rows, two bf16 per column).
+// TMEM columns: D (tokens 0-191) 0-191, D (tokens 192-383) 192-383, A stages
+// 384 + 32 s (64 K-values of 128 rows, two bf16 per column).
 namespace a16t {
-constexpr int BT = 192;                      // tokens per tile (MMA N)
+constexpr int NH = 192;                      // tokens per MMA (MMA N)
+constexpr int BT = 2 * NH;                   // tokens per tile
 constexpr int BW = 128;                      // weight rows per tile (MMA M)
 constexpr int BK = 64;                       // K per stage
-constexpr int S = 4;                         // stages
-constexpr int kXBytes = BT * 128;            // bf16 activation tile, 128-byte rows
+constexpr int S = 3;                         // stages
+constexpr int kXHalf = NH * 128;             // bf16 activation rows of one MMA, 128-byte rows
+constexpr int kXBytes = 2 * kXHalf;
 constexpr int kRawBytes = BW * 64;           // raw E4M3 weight rows
 constexpr int kEpiBuf = 32 * 64;             // 32 tokens x 32 features bf16
 constexpr int kOffX = 0;
 constexpr int kOffRaw = kOffX + S * kXBytes;
 constexpr int kOffEpi = kOffRaw + S * kRawBytes;
 constexpr int kOffBar = kOffEpi + 4 * 2 * kEpiBuf;
-constexpr int kNumBars = 3 * S + 5;          // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
+constexpr int kNumBars = 3 * S + 3;          // full[S], empty[S], ready[S], tfull, tempty, drain
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kAlloc = kOffAbort + 4 + 1024;
-constexpr int kTransformWarps = 16;         // 4 per TMEM lane quadrant, 16 K-values each
+constexpr int kTransformWarps = 8;           // 2 per TMEM lane quadrant, 32 K-values each
 constexpr int kThreads = (2 + 4 + kTransformWarps) * 32;
-constexpr uint32_t kTmemA = 2 * BT;          // first A-stage column
-constexpr uint32_t kIdesc = make_idesc(1, 1, BW, BT);
+constexpr uint32_t kTmemA = 2 * NH;          // first A-stage column
+constexpr uint32_t kIdesc = make_idesc(1, 1, BW, NH);
 static_assert(kTmemA + S * 32 <= kTmemCols, "TMEM budget");
 static_assert(kAlloc <= 232448, "shared memory budget");
 }  // namespace a16t
-
-__device__ __forceinline__ void decode_tile_a16t(const Args& a, int t, int& m0, int& g, int& n0) {
-  const int mb = t / a.tiles_per_m;
-  int r = t - mb * a.tiles_per_m;
-  g = 0;
-  while (g < a.G - 1 && r >= a.tiles_n[g]) {
-    r -= a.tiles_n[g];
-    ++g;
-  }
-  m0 = mb * a16t::BT;
-  n0 = r * a16t::BW;
-}
 
 __global__ void __launch_bounds__(a16t::kThreads, 1)
     gemm_a16t_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args args) {
@@ -559,9 +507,9 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
   auto full_bar = [&](int st) { return bar0 + 8u * st; };
   auto empty_bar = [&](int st) { return bar0 + 8u * (S + st); };
   auto ready_bar = [&](int st) { return bar0 + 8u * (2 * S + st); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+  const uint32_t tfull_bar = bar0 + 8u * (3 * S);
+  const uint32_t tempty_bar = bar0 + 8u * (3 * S + 1);
+  const uint32_t drain_bar = bar0 + 8u * (3 * S + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
   const int warp = threadIdx.x >> 5;
@@ -571,12 +519,10 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
     for (int st = 0; st < S; ++st) {
       mbar_init(full_bar(st), 1);
       mbar_init(empty_bar(st), 1);
-      mbar_init(ready_bar(st), a16t::kTransformWarps);
+      mbar_init(ready_bar(st), kTransformWarps);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
-    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 4);
     mbar_init(drain_bar, 1);
     *abort = 0;
     fence_mbar_init();
@@ -603,7 +549,7 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
         int m0, g, n0;
-        decode_tile_a16t(args, t, m0, g, n0);
+        decode_tile(args, t, BT, BW, m0, g, n0);
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(st), ph ^ 1, abort, kWaitLimitNs)) {
             record_timeout(abort);
@@ -611,7 +557,9 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(st), kXBytes + kRawBytes);
-          tma_load_2d(sbase + kOffX + st * kXBytes, &maps.a, full_bar(st), kb * BK, m0);
+          const uint32_t xd = sbase + kOffX + st * kXBytes;
+          tma_load_2d(xd, &maps.a, full_bar(st), kb * BK, m0);
+          tma_load_2d(xd + kXHalf, &maps.a, full_bar(st), kb * BK, m0 + NH);
           tma_load_2d(sbase + kOffRaw + st * kRawBytes, map_b(maps, g), full_bar(st), kb * BK, n0);
           ++issued;
           if (++st == S) {
@@ -631,17 +579,14 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       int st = 0;
-      uint32_t ph = 0;
-      int acc = 0;
-      uint32_t acc_ph = 0;
+      uint32_t ph = 0, acc_ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
-        if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1, abort, kWaitLimitNs)) {
+        if (!mbar_wait(tempty_bar, acc_ph ^ 1, abort, kWaitLimitNs)) {
           record_timeout(abort);
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * BT);
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(ready_bar(st), ph, abort, kWaitLimitNs)) {
             record_timeout(abort);
@@ -652,9 +597,12 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
           const uint32_t x_addr = sbase + kOffX + st * kXBytes;
           const uint32_t a_col = tmem_base + kTmemA + (uint32_t)(st * 32);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // K = 16 per MMA: 8 TMEM columns, 32 smem bytes
-            mma_f16_tmem_a(d, a_col + 8 * k, sw128_kmajor_desc(x_addr + 32 * k), kIdesc,
-                           (kb | k) != 0);
+          for (int k = 0; k < 4; ++k) {  // K = 16 per MMA: 8 TMEM columns, 32 smem bytes
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              mma_f16_tmem_a(tmem_base + (uint32_t)(h * NH), a_col + 8 * k,
+                             sw128_kmajor_desc(x_addr + h * kXHalf + 32 * k), kIdesc, (kb | k) != 0);
+          }
           mma_commit(empty_bar(st));
           if (++st == S) {
             st = 0;
@@ -662,11 +610,8 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
-        if (++acc == 2) {
-          acc = 0;
-          acc_ph ^= 1;
-        }
+        mma_commit(tfull_bar);
+        acc_ph ^= 1;
       }
       mma_commit(drain_bar);
       volatile int never = 0;
@@ -677,18 +622,18 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
     const int q = warp & 3;  // TMEM lane quadrant: weight rows (features) q*32 .. q*32+31
     uint8_t* bufp = smem + kOffEpi + (warp - 2) * 2 * kEpiBuf;
     const uint32_t bufs = sbase + kOffEpi + (uint32_t)((warp - 2) * 2 * kEpiBuf);
-    int acc = 0, nbuf = 0;
+    int nbuf = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
       int m0, g, n0;
-      decode_tile_a16t(args, t, m0, g, n0);
-      if (!mbar_wait_warp(tfull_bar(acc), acc_ph, abort, kWaitLimitNs)) {
+      decode_tile(args, t, BT, BW, m0, g, n0);
+      if (!mbar_wait_warp(tfull_bar, acc_ph, abort, kWaitLimitNs)) {
         if (lane == 0) record_timeout(abort);
         break;
       }
       tc_fence_after();
       const int f0 = n0 + q * 32;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < BT / 32; ++c) {
         uint32_t r[32];
@@ -697,7 +642,7 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
         if (c == BT / 32 - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          if (lane == 0) mbar_arrive(tempty_bar);
         }
         const int tok0 = m0 + c * 32;
         if (tok0 >= args.M || f0 >= args.N[g]) continue;
@@ -718,23 +663,20 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
         }
         nbuf ^= 1;
       }
-      if (++acc == 2) {
-        acc = 0;
-        acc_ph ^= 1;
-      }
+      acc_ph ^= 1;
     }
     if (lane == 0) tma_store_wait_all();
   } else {
     // ---------------------------------------------------------------- weight transform
     const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int kq = (warp - 6) >> 2;      // which 16 of the stage's 64 K-values
+    const int h = (warp - 6) >> 2;       // which 32 of the stage's 64 K-values
     const int r = q * 32 + lane;         // weight row of the tile = TMEM lane
     int st = 0;
     uint32_t ph = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
       int m0, g, n0;
-      decode_tile_a16t(args, t, m0, g, n0);
+      decode_tile(args, t, BT, BW, m0, g, n0);
       const float sw = __ldg(scale_w(args, g));
       for (int kb = 0; kb < args.num_kb; ++kb) {
         if (!mbar_wait_warp(full_bar(st), ph, abort, kWaitLimitNs)) {
@@ -742,24 +684,26 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
           ok = false;
           break;
         }
-        // Raw row: 64 bytes with the 64-byte swizzle (chunk j at j ^ ((r >> 1) & 3));
-        // this thread converts chunk kq = K-values 16 kq .. 16 kq + 15.
+        // Raw row: 64 bytes with the 64-byte swizzle (chunk j at j ^ ((r >> 1) & 3)).
         const uint8_t* raw = smem + kOffRaw + st * kRawBytes + r * 64;
-        const uint4 v = *reinterpret_cast<const uint4*>(raw + ((kq ^ ((r >> 1) & 3)) * 16));
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[8];
+        const uint4 v0 = *reinterpret_cast<const uint4*>(raw + (((2 * h) ^ ((r >> 1) & 3)) * 16));
+        const uint4 v1 = *reinterpret_cast<const uint4*>(raw + (((2 * h + 1) ^ ((r >> 1) & 3)) * 16));
+        const uint32_t w8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t o[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(w4[e] & 0xFFFF));
-          const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(w4[e] >> 16));
-          const float a0 = __half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFF)));
-          const float a1 = __half2float(__ushort_as_half((unsigned short)(f01 >> 16)));
-          const float a2 = __half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFF)));
-          const float a3 = __half2float(__ushort_as_half((unsigned short)(f23 >> 16)));
-          o[2 * e] = cvt_bf16x2(__fmul_rn(a0, sw), __fmul_rn(a1, sw));
-          o[2 * e + 1] = cvt_bf16x2(__fmul_rn(a2, sw), __fmul_rn(a3, sw));
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(w8[e] & 0xFFFF));
+          const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(w8[e] >> 16));
+          const F2 lo = mul2(F2{__half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFF))),
+                                __half2float(__ushort_as_half((unsigned short)(f01 >> 16)))},
+                             splat(sw));
+          const F2 hi = mul2(F2{__half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFF))),
+                                __half2float(__ushort_as_half((unsigned short)(f23 >> 16)))},
+                             splat(sw));
+          o[2 * e] = cvt_bf16x2(lo.x, lo.y);
+          o[2 * e + 1] = cvt_bf16x2(hi.x, hi.y);
         }
-        tmem_st_32x32b_x8(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(st * 32 + kq * 8), o);
+        tmem_st_32x32b_x16(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(st * 32 + h * 16), o);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -797,65 +741,19 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
   return r == CUDA_SUCCESS;
 }
 
-template <Mode MODE, int CG>
-cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  using C = Cfg<MODE, CG>;
-  using L = Layout<MODE, CG>;
-  *tmap_err = 0;
-  Maps maps;
-  Args args;
-  std::memset(&maps, 0, sizeof(maps));
-  std::memset(&args, 0, sizeof(args));
-  args.G = p.G;
-  args.M = (int)p.M;
-  args.K = (int)p.K;
-  args.num_kb = (int)((p.K + C::kBK - 1) / C::kBK);
-  args.s_in = p.s_in;
-  const int tiles_m = (int)((p.M + BM * CG - 1) / (BM * CG));
-  args.tiles_per_m = 0;
-  bool ok = true;
-  if (MODE == Mode::W8A8) {
-    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.x, p.K, p.M, p.K, 128, BM,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
-  } else {
-    ok &= encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, p.K, p.M, p.K * 2, 64, BM,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
-  }
-  for (int g = 0; g < p.G; ++g) {
-    args.N[g] = (int)p.N[g];
-    args.s_w[g] = p.s_w[g];
-    args.tiles_n[g] = (int)((p.N[g] + BN - 1) / BN);
-    args.tiles_per_m += args.tiles_n[g];
-    if (MODE == Mode::W8A8) {
-      ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 128,
-                      C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
-    } else {
-      ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 64,
-                      C::kBRows, CU_TENSOR_MAP_SWIZZLE_64B);
-    }
-    ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y[g], p.N[g], p.M, p.N[g] * 2,
-                    64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-  }
-  for (int g = p.G; g < kMaxGroup; ++g) args.s_w[g] = p.s_w[0];
-  if (!ok) {
-    *tmap_err = 1;
-    return cudaSuccess;
-  }
-  args.num_tiles = tiles_m * args.tiles_per_m;
-  const int max_clusters = sms / CG;
-  const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
-  auto kern = gemm_kernel<MODE, CG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+cudaError_t launch_cluster(void (*kern)(Maps, Args), int grid, int threads, int smem, int cg,
+                           cudaStream_t st, const Maps& maps, const Args& args) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(clusters * CG, 1, 1);
-  cfg.blockDim = dim3(L::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.x = cg;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -864,6 +762,57 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+template <Mode MODE, int CG>
+cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  using C = Cfg<MODE, CG>;
+  using L = Layout<MODE, CG>;
+  constexpr bool kGlu = C::kGlu;
+  *tmap_err = 0;
+  Maps maps;
+  Args args;
+  std::memset(&maps, 0, sizeof(maps));
+  std::memset(&args, 0, sizeof(args));
+  args.G = kGlu ? 1 : p.G;
+  args.M = (int)p.M;
+  args.K = (int)p.K;
+  args.num_kb = (int)((p.K + C::kBK - 1) / C::kBK);
+  args.s_in = p.s_in;
+  args.s_out = p.s_out;
+  const int tiles_m = (int)((p.M + BM * CG - 1) / (BM * CG));
+  bool ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.x, p.K, p.M, p.K, 128, BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  const int nb = kGlu ? 2 : p.G;  // weight maps: GLU gate and up
+  for (int g = 0; g < nb; ++g) {
+    args.s_w[g] = p.s_w[g];
+    ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[kGlu ? 0 : g], p.K,
+                    128, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  for (int g = 0; g < args.G; ++g) {
+    args.N[g] = (int)p.N[g];
+    args.tiles_n[g] = (int)((p.N[g] + C::kBN - 1) / C::kBN);
+    args.tiles_per_m += args.tiles_n[g];
+    if (kGlu)  // E4M3 output [M, I], 128-byte rows of the staging buffer
+      ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.y[g], p.N[g], p.M, p.N[g], 128,
+                      32, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y[g], p.N[g], p.M, p.N[g] * 2,
+                      64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  for (int g = nb; g < kMaxGroup; ++g) args.s_w[g] = p.s_w[0];
+  if (!ok) {
+    *tmap_err = 1;
+    return cudaSuccess;
+  }
+  args.num_tiles = tiles_m * args.tiles_per_m;
+  const int max_clusters = sms / CG;
+  const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
+  return launch_cluster(gemm_kernel<MODE, CG>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
+                        args);
+}
+
+// The CTA pair needs M above one 128-row tile to pay off.
+bool use_pair(const GemmProblem& p) { return p.M > BM; }
 
 cudaError_t launch_a16t(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
   using namespace a16t;
@@ -877,7 +826,7 @@ cudaError_t launch_a16t(const GemmProblem& p, int sms, cudaStream_t st, int* tma
   args.K = (int)p.K;
   args.num_kb = (int)((p.K + BK - 1) / BK);
   const int tiles_m = (int)((p.M + BT - 1) / BT);
-  bool ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, p.K, p.M, p.K * 2, 64, BT,
+  bool ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, p.K, p.M, p.K * 2, 64, NH,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   for (int g = 0; g < p.G; ++g) {
     args.N[g] = (int)p.N[g];
@@ -922,8 +871,6 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
   __syncthreads();
 }
 
-// The CTA pair needs M above one 128-row tile to pay off.
-bool use_pair(const GemmProblem& p) { return p.M > BM; }
 
 }  // namespace
 
@@ -932,10 +879,15 @@ cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int
                      : launch<Mode::W8A8, 1>(p, sms, st, tmap_err);
 }
 
-// W8A16 stays on one CTA per tile: in the CTA pair each 64-K stage would wait
-// for the odd CTA's transform to be signalled across the SM pair, and that
-// cluster-scope hand-off costs more than the halved per-SM transform saves
-// (measured 766 vs 1054 TFLOP/s on the 20670 x 3 x 4096 x 4096 group).
+cudaError_t launch_gemm_glu(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  return use_pair(p) ? launch<Mode::GLU, 2>(p, sms, st, tmap_err)
+                     : launch<Mode::GLU, 1>(p, sms, st, tmap_err);
+}
+
+// W8A16 runs one CTA per tile with the dequantized weight in TMEM: a CTA pair
+// would have to signal every 64-K stage of the odd CTA's dequantization
+// across the SM pair, and that cluster-scope hand-off measured slower than
+// the work it halves.
 cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
   return launch_a16t(p, sms, st, tmap_err);
 }

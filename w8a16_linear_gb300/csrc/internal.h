@@ -32,13 +32,17 @@ struct GemmProblem {
   int64_t N[kMaxGroup];
   const float* s_in;             // W8A8 only
   const float* s_w[kMaxGroup];
-  uint16_t* y[kMaxGroup];        // bf16 [M, N_g]
+  void* y[kMaxGroup];            // bf16 [M, N_g] (GLU: E4M3 [M, I])
+  const float* s_out;            // GLU: input scale of the down projection
 };
 
 // Returns cudaSuccess or the CUDA error; *tmap_err is set non-zero when a
 // tensor map could not be encoded.
 cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
+// Gate/up W8A8 GEMMs with the SwiGLU-to-E4M3 epilogue: x E4M3 [M,K], w[0] gate
+// and w[1] up [I,K] with s_w[0], s_w[1]; N[0] = I; y[0] E4M3 [M,I]; s_out.
+cudaError_t launch_gemm_glu(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 
 // Launches a one-thread kernel whose mbarrier wait times out (0.2 s).
 cudaError_t launch_selftest_timeout(cudaStream_t st);
