@@ -7,8 +7,9 @@ One step runs every row of the path through the public C ABI:
   step_policy_dispatch(step 3 of 8)                       -> W8A8
   qkv_shared_quant_gemm  Q/K/V, one shared quantization, 3 x 4096x4096
   fp8_linear_w8a8        out-projection 4096x4096 (quantizes its input)
-  qkv_shared_quant_gemm  gate/up, one shared quantization, 2 x 4096->16384
-  swiglu_2in_fp8         SiLU(gate)*up straight to E4M3 for the down projection
+  gate_up_swiglu_fp8     gate/up (one shared quantization, 2 x 4096->16384) with
+                         SiLU(gate)*up written straight to E4M3 in the GEMM
+                         epilogue (same codes as the group GEMM + swiglu_2in_fp8)
   fp8_linear_w8a8        down projection 16384->4096 on the E4M3 codes
 
 Metric: W8A8 FP8 linear TFLOPS = the block's linear FLOPs (32 * M * 4096^2)
@@ -40,8 +41,8 @@ BLOCK_FLOPS = 32.0 * M_TOK * HID * HID           # QKV 6 + out 2 + gate/up 16 + 
 QKV_FLOPS = 6.0 * M_TOK * HID * HID
 METRIC = "W8A8 FP8 linear TFLOPS (M≈20k, K=N=4096) and % of GB300 dense FP8 peak"
 WORKLOAD = ("A8 denoising-block step, M=20670 tokens (13x30x53), hidden 4096: split-QKV shared "
-            "quant 3x4096x4096, out-proj 4096x4096, split gate/up shared quant 2x4096->16384, "
-            "swiglu_2in FP8, down 16384->4096")
+            "quant 3x4096x4096, out-proj 4096x4096, split gate/up shared quant 2x4096->16384 fused "
+            "with swiglu_2in FP8, down 16384->4096")
 L2_FLUSH_BYTES = 512 << 20
 POLICY_STEP, POLICY_STEPS = 3, 8
 
@@ -161,9 +162,10 @@ class Block:
     def outputs(self):
         return self.y_qkv + [self.y_out, self.y_down]
 
-    def step(self, W, policy, step_index, num_steps, x_qkv=None, x_out=None, x_mlp=None):
+    def step(self, W, policy, step_index, num_steps, x_qkv=None, x_out=None, x_mlp=None, fused=True):
         """One block pass in the precision the policy selects for this step;
-        returns the number of kernel launches."""
+        returns the number of kernel launches.  `fused` selects the fused
+        gate/up + SwiGLU kernel on W8A8 steps (else group GEMM + SwiGLU)."""
         x_qkv = self.x_qkv if x_qkv is None else x_qkv
         x_out = self.x_out if x_out is None else x_out
         x_mlp = self.x_mlp if x_mlp is None else x_mlp
@@ -175,10 +177,14 @@ class Block:
         if mode == W.MODE_A8:
             W.qkv_shared_quant_gemm(W.MODE_A8, x_qkv, self.s_qkv, wq, sq, outs=self.y_qkv, ws=self.ws)
             W.fp8_linear_w8a8(x_out, self.w_out[0], self.s_out, self.w_out[1], out=self.y_out, ws=self.ws)
-            W.qkv_shared_quant_gemm(W.MODE_A8, x_mlp, self.s_mlp, wgu, sgu, outs=self.y_gu, ws=self.ws)
-            W.swiglu_2in_fp8(self.y_gu[0], self.y_gu[1], self.s_h, out=self.h8)
+            if fused:
+                W.gate_up_swiglu_fp8(x_mlp, self.s_mlp, wgu[0], wgu[1], sgu[0], sgu[1], self.s_h,
+                                     out=self.h8, ws=self.ws)
+            else:
+                W.qkv_shared_quant_gemm(W.MODE_A8, x_mlp, self.s_mlp, wgu, sgu, outs=self.y_gu, ws=self.ws)
+                W.swiglu_2in_fp8(self.y_gu[0], self.y_gu[1], self.s_h, out=self.h8)
             W.fp8_linear_w8a8(self.h8, self.w_down[0], self.s_h, self.w_down[1], out=self.y_down)
-            return 8
+            return 7 if fused else 8
         W.qkv_shared_quant_gemm(W.MODE_A16, x_qkv, None, wq, sq, outs=self.y_qkv)
         W.fp8_linear_w8a16(x_out, self.w_out[0], self.w_out[1], out=self.y_out)
         W.qkv_shared_quant_gemm(W.MODE_A16, x_mlp, None, wgu, sgu, outs=self.y_gu)
@@ -253,8 +259,8 @@ def run_ours(args, rank, world, dev):
         W.fp8_linear_w8a8_group(q_qkv, blk.s_qkv, [q for q, _ in blk.w_qkv], [s for _, s in blk.w_qkv],
                                 outs=blk.y_qkv)
         W.fp8_linear_w8a8_group(q_out, blk.s_out, [blk.w_out[0]], [blk.w_out[1]], outs=[blk.y_out])
-        W.fp8_linear_w8a8_group(q_mlp, blk.s_mlp, [q for q, _ in blk.w_gu], [s for _, s in blk.w_gu],
-                                outs=blk.y_gu)
+        W.gate_up_swiglu_fp8(q_mlp, blk.s_mlp, blk.w_gu[0][0], blk.w_gu[1][0], blk.w_gu[0][1],
+                             blk.w_gu[1][1], blk.s_h, out=blk.h8)
         W.fp8_linear_w8a8_group(blk.h8, blk.s_h, [blk.w_down[0]], [blk.w_down[1]], outs=[blk.y_down])
 
     gemm_ms = _time(gemms, flush, stream, args.steps)
@@ -292,6 +298,9 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     out = {}
     wq = [q for q, _ in blk.w_qkv]
     sq = [s for _, s in blk.w_qkv]
+    ms = _time(lambda: blk.step(W, policy, POLICY_STEP, POLICY_STEPS, fused=False), flush, stream, n)
+    out["block_a8_step_unfused_mlp"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
+                                        "note": "gate/up group GEMM -> bf16 -> swiglu_2in_fp8 instead of the fused kernel"}
     ms = _time(lambda: blk.step(W, policy, 0, POLICY_STEPS), flush, stream, n)
     out["block_a16_step"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
                              "note": "W8A16 rows: QKV/gate-up groups in A16, out/down W8A16, swiglu bf16"}
@@ -319,6 +328,10 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     ms = _time(lambda: W.swiglu_2in_bf16(blk.y_gu[0], blk.y_gu[1], out=blk.h16), flush, stream, n)
     out["swiglu_2in_bf16"] = {"us": ms * 1e3, "GB_s": 6 * blk.h16.numel() / ms / 1e6}
     q = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
+    ms = _time(lambda: W.gate_up_swiglu_fp8(q, blk.s_mlp, blk.w_gu[0][0], blk.w_gu[1][0], blk.w_gu[0][1],
+                                            blk.w_gu[1][1], blk.s_h, out=blk.h8), flush, stream, n)
+    out["glu_gate_up_swiglu_fp8"] = {"us": ms * 1e3, "TFLOPS": 4.0 * M_TOK * HID * INTER / ms / 1e9,
+                                     "note": "fused gate+up GEMMs (E4M3 input) with SwiGLU->E4M3 epilogue"}
     ms = _time(lambda: W.fp8_linear_w8a8_group(q, blk.s_mlp, [blk.w_gu[0][0]], [blk.w_gu[0][1]],
                                                outs=[blk.y_gu[0]]), flush, stream, n)
     out["w8a8_gate_4096x16384"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
@@ -435,6 +448,13 @@ def run_case(args):
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A8, x, s, qs, ss, outs=ys, ws=qx)  # noqa: E731
     elif args.case == "w8a16_8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, qs, ss, outs=ys)  # noqa: E731
+    elif args.case == "glu8k":
+        wg = (torch.randn((INTER, HID), generator=gen, device=dev) * 200).clamp(-448, 448) \
+            .to(torch.float8_e4m3fn).view(torch.uint8)
+        wu = (torch.randn((INTER, HID), generator=gen, device=dev) * 200).clamp(-448, 448) \
+            .to(torch.float8_e4m3fn).view(torch.uint8)
+        h8 = torch.empty((M, INTER), dtype=torch.uint8, device=dev)
+        fn = lambda: W.gate_up_swiglu_fp8(x, s, wg, wu, ss[0], ss[1], s, out=h8, ws=qx)  # noqa: E731
     elif args.case == "swiglu8k":
         gg = (torch.randn((M, INTER), generator=gen, device=dev) * 2).to(torch.bfloat16)
         uu = torch.randn((M, INTER), generator=gen, device=dev).to(torch.bfloat16)
@@ -481,7 +501,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="run a small profiling case (qkv8k, w8a16_8k, swiglu8k) instead of the bench")
+                    help="run a small profiling case (qkv8k, w8a16_8k, glu8k, swiglu8k) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.case:
