@@ -449,12 +449,18 @@ def run_case(args):
     elif args.case == "w8a16_8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, qs, ss, outs=ys)  # noqa: E731
     elif args.case == "glu8k":
-        wg = (torch.randn((INTER, HID), generator=gen, device=dev) * 200).clamp(-448, 448) \
-            .to(torch.float8_e4m3fn).view(torch.uint8)
-        wu = (torch.randn((INTER, HID), generator=gen, device=dev) * 200).clamp(-448, 448) \
-            .to(torch.float8_e4m3fn).view(torch.uint8)
+        # weights as in the bench: N(0, 0.02^2) with amax/448 scales, so the
+        # SwiGLU inputs have a realistic spread (the exact-division fallback of
+        # the epilogue is data dependent)
+        def weight():
+            w = torch.randn((INTER, HID), generator=gen, device=dev) * 0.02
+            sc = (w.abs().amax() / 448).reshape(1).contiguous()
+            return (w / sc).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8), sc
+        (wg, sg), (wu, su) = weight(), weight()
+        s_x = (x.float().abs().amax() / 448).reshape(1).contiguous()
+        s_h = torch.tensor([0.02], device=dev)
         h8 = torch.empty((M, INTER), dtype=torch.uint8, device=dev)
-        fn = lambda: W.gate_up_swiglu_fp8(x, s, wg, wu, ss[0], ss[1], s, out=h8, ws=qx)  # noqa: E731
+        fn = lambda: W.gate_up_swiglu_fp8(x, s_x, wg, wu, sg, su, s_h, out=h8, ws=qx)  # noqa: E731
     elif args.case == "swiglu8k":
         gg = (torch.randn((M, INTER), generator=gen, device=dev) * 2).to(torch.bfloat16)
         uu = torch.randn((M, INTER), generator=gen, device=dev).to(torch.bfloat16)

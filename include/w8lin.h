@@ -260,6 +260,29 @@ w8_status step_policy_dispatch(const w8_step_policy* policy, int32_t step, int32
                                int32_t* mode_out);
 
 /*
+ * w8_step_policy_parse — host-only, fail-closed parse of a checkpoint's
+ * quantization_config.runtime.diffusion_step_policy JSON text into a
+ * w8_step_policy ([P4] Denoising-step activation precision: unknown or
+ * missing fields, schema_version other than 1, and any other type,
+ * index_space, default_mode or overlap value are refused rather than
+ * partially honoured; overlap is validated, not acted on; [P3] Behavior:
+ * "runtime: null" means no policy).
+ *   json   NUL-terminated text: `null`, or an object with exactly the keys
+ *          schema_version (1), type ("first_last_n"), index_space
+ *          ("scheduler_step"), default_mode ("w8a8"), overlap ("w8a16"),
+ *          first_steps and last_steps (integers >= 0), reasoner ("a16" or
+ *          "a8").  The pages name the fields but not the value spellings;
+ *          these spellings are this library's reading.
+ *   policy_out        filled on success (`null` gives enabled = 0)
+ *   reasoner_mode_out W8_MODE_A16 / W8_MODE_A8 as stated, -1 for `null`
+ *                     (the reasoner is not step-gated; its precision is
+ *                     stated by the policy)
+ * Errors: NULL, POLICY (with the reason in w8_last_error()).
+ */
+w8_status w8_step_policy_parse(const char* json, w8_step_policy* policy_out,
+                               int32_t* reasoner_mode_out);
+
+/*
  * w8_check_group_scales — load-time check that the G projections of a
  * sharing group carry bit-identical input scales ([P4] What changed: the
  * invariant the sharing rests on, validated in post_load_weights(), never

@@ -34,7 +34,7 @@ from .linear import (quant_static, linear_w8a8, linear_w8a16,
                      dequant_weight_bf16, requant_onto_max_scale,
                      qkv_shared_quant_gemm)
 from .swiglu import exp_spec, swiglu_2in_fp8, swiglu_2in_bf16, swiglu_h
-from .policy import StepPolicy, PolicyError, step_mode, A8, A16
+from .policy import StepPolicy, PolicyError, step_mode, parse_policy, A8, A16
 
 __all__ = [
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_all_values",
@@ -42,5 +42,5 @@ __all__ = [
     "quant_static", "linear_w8a8", "linear_w8a16", "dequant_weight_bf16",
     "requant_onto_max_scale", "qkv_shared_quant_gemm",
     "exp_spec", "swiglu_2in_fp8", "swiglu_2in_bf16", "swiglu_h",
-    "StepPolicy", "PolicyError", "step_mode", "A8", "A16",
+    "StepPolicy", "PolicyError", "step_mode", "parse_policy", "A8", "A16",
 ]

@@ -75,3 +75,34 @@ def test_fused_vs_oracle_chain(W):
     dv = np.abs(O.e4m3_decode(out[diff]).astype(np.float64) - O.e4m3_decode(want[diff]))
     step = np.maximum(np.abs(O.e4m3_decode(want[diff])).astype(np.float64), 2.0 ** -6) / 8
     assert np.all(dv <= step * 1.0001)
+
+
+def test_fused_full_size(W):
+    """20670 tokens, 4096 -> 2 x 16384: the fused kernel equals the separate
+    path everywhere, and the oracle chain on sampled rows plus the tail."""
+    M, K, I = 20670, 4096, 16384
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    x = (torch.randn((M, K), generator=gen, device="cuda") * 0.25).to(torch.bfloat16)
+    wq, sw = [], []
+    for c in (0.6, 1.0):
+        w = torch.randn((I, K), generator=gen, device="cuda") * (0.02 * c)
+        s = (w.abs().amax() / 448).reshape(1)
+        wq.append((w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
+        sw.append(s.contiguous())
+    s_in = (x.float().abs().amax() / 448).reshape(1).contiguous()
+    s_out = dev_f32(0.02)
+    fused = W.gate_up_swiglu_fp8(x, s_in, wq[0], wq[1], sw[0], sw[1], s_out)
+    g, u = W.qkv_shared_quant_gemm(W.MODE_A8, x, s_in, wq, sw)
+    sep = W.swiglu_2in_fp8(g, u, s_out)
+    torch.cuda.synchronize()
+    W.poll_device_error()
+    assert torch.equal(fused, sep)
+    rows = np.concatenate([synth.random_rows(9, M, 48), np.arange(M - 62, M)])
+    ri = torch.from_numpy(rows).cuda()
+    xs = host_bits(x[ri])
+    qws = [host_u8(w) for w in wq]
+    sws = [np.float32(s.item()) for s in sw]
+    (_, gb), (_, ub) = O.qkv_shared_quant_gemm("A8", xs, np.float32(s_in.item()), qws, sws)
+    want = O.swiglu_2in_fp8(gb, ub, np.float32(0.02))
+    got = host_u8(fused[ri])
+    assert (got != want).mean() < 2e-3

@@ -26,6 +26,14 @@ MODE_A8, MODE_A16 = 0, 1
 _c_void_p = ctypes.c_void_p
 _i64 = ctypes.c_int64
 _i32 = ctypes.c_int32
+
+
+class StepPolicy(ctypes.Structure):
+    """Mirror of ``w8_step_policy``."""
+    _fields_ = [("schema_version", _i32), ("enabled", _i32),
+                ("first_steps", _i32), ("last_steps", _i32)]
+
+
 SIGNATURES = {
     "w8_abi_version": (ctypes.c_int, []),
     "w8_last_error": (ctypes.c_char_p, []),
@@ -55,6 +63,8 @@ SIGNATURES = {
     "swiglu_2in_bf16": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
     "step_policy_dispatch": (ctypes.c_int, [_c_void_p, _i32, _i32, ctypes.POINTER(_i32)]),
     "w8_check_group_scales": (ctypes.c_int, [ctypes.POINTER(_c_void_p), _i32]),
+    "w8_step_policy_parse": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(StepPolicy),
+                                            ctypes.POINTER(_i32)]),
 }
 
 
@@ -62,12 +72,6 @@ class W8Error(RuntimeError):
     def __init__(self, status, detail):
         self.status = status
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {detail}")
-
-
-class StepPolicy(ctypes.Structure):
-    """Mirror of ``w8_step_policy``."""
-    _fields_ = [("schema_version", _i32), ("enabled", _i32),
-                ("first_steps", _i32), ("last_steps", _i32)]
 
 
 _lib = None
@@ -321,6 +325,16 @@ def step_policy_dispatch(policy, step, num_steps):
     p = ctypes.byref(policy) if policy is not None else None
     _check(lib().step_policy_dispatch(p, step, num_steps, ctypes.byref(mode)))
     return mode.value
+
+
+def step_policy_parse(text):
+    """Parse a diffusion_step_policy JSON text: returns (StepPolicy, reasoner
+    mode or None).  Raises W8Error (W8_ERR_POLICY) on any refused shape."""
+    pol = StepPolicy()
+    reasoner = ctypes.c_int32(-2)
+    _check(lib().w8_step_policy_parse(text.encode() if isinstance(text, str) else text,
+                                      ctypes.byref(pol), ctypes.byref(reasoner)))
+    return pol, (None if reasoner.value < 0 else reasoner.value)
 
 
 def check_group_scales(scales):

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libw8lin.so")
-SOURCES = ["api.cu", "elementwise.cu", "gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "elementwise.cu", "gemm.cu", "noalloc.cu", "policy.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

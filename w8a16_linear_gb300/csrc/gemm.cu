@@ -63,9 +63,7 @@ constexpr int BM = 128;                           // output rows per CTA
 constexpr uint32_t kTmemCols = 512;               // two 256-column F32 accumulator buffers
 constexpr uint32_t kAccCols = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
-constexpr int kEpiWarps = 4;
-constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x 128 bytes
-constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+constexpr int kEpiBufBytes = 32 * 128;            // W8A8 staging: 32 rows x 64 bf16
 
 enum class Mode { W8A8, GLU };
 
@@ -80,6 +78,11 @@ struct Cfg {
   static constexpr int kBBytes = (kGlu ? 2 : 1) * kBHalf;
   static constexpr int kStages = CG == 1 ? 4 : 6;
   static constexpr uint32_t kIdesc = make_idesc(0, 0, BM * CG, kBN);  // E4M3 x E4M3 -> F32
+  // GLU: four warps per TMEM lane quadrant (32 columns each) to keep the
+  // SwiGLU epilogue ahead of the tensor cores; staging 32 rows x 32 codes.
+  static constexpr int kEpiWarps = kGlu ? 16 : 4;
+  static constexpr int kEpiBuf = kGlu ? 32 * 32 : kEpiBufBytes;
+  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBuf;
 };
 
 template <Mode MODE, int CG>
@@ -88,14 +91,14 @@ struct Layout {
   static constexpr int kA = 0;
   static constexpr int kB = kA + C::kStages * C::kABytes;
   static constexpr int kEpi = kB + C::kStages * C::kBBytes;
-  static constexpr int kBar = kEpi + kEpiBytes;
+  static constexpr int kBar = kEpi + C::kEpiBytes;
   // barriers: full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int kNumBars = 2 * C::kStages + 5;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kEnd = kAbort + 4;
   static constexpr int kAlloc = kEnd + 1024;  // slack for 1024-byte alignment
-  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kThreads = (2 + C::kEpiWarps) * 32;
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiWarps * CG);
+      mbar_init(tempty_bar(b), C::kEpiWarps * CG);
     }
     mbar_init(drain_bar, 1);
     *abort = 0;
@@ -320,9 +323,11 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int wq = warp & 3;  // TMEM lane quadrant this warp may access
-    const uint32_t buf0 = sbase + L::kEpi + (uint32_t)((warp - 2) * 2 * kEpiBufBytes);
-    uint8_t* buf0_ptr = smem + L::kEpi + (warp - 2) * 2 * kEpiBufBytes;
+    const int wq = warp & 3;              // TMEM lane quadrant this warp may access
+    const int cp = (warp - 2) >> 2;       // GLU: which 32 of the tile's 128 columns
+    constexpr int EB = C::kEpiBuf;
+    const uint32_t buf0 = sbase + L::kEpi + (uint32_t)((warp - 2) * 2 * EB);
+    uint8_t* buf0_ptr = smem + L::kEpi + (warp - 2) * 2 * EB;
     int acc = 0;
     uint32_t acc_ph = 0;
     int nbuf = 0;
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           // The store issued two chunks ago from this buffer must have read it.
           if (lane == 0) tma_store_wait_read<1>();
           __syncwarp();
-          uint8_t* bp = buf0_ptr + nbuf * kEpiBufBytes + lane * 128;
+          uint8_t* bp = buf0_ptr + nbuf * EB + lane * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int pj = j ^ (lane & 7);  // 128-byte swizzle within the 1024-byte atom
@@ -386,52 +391,49 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(map_y(maps, g), buf0 + nbuf * kEpiBufBytes, col0, row0);
+            tma_store_2d(map_y(maps, g), buf0 + nbuf * EB, col0, row0);
             tma_store_commit();
           }
           nbuf ^= 1;
         }
       } else {
-        // 128 intermediate columns per row: gate at tbase, up at tbase + 128.
-        // Each 32-column chunk gives 32 E4M3 codes (two 16-byte chunks of the
-        // row's 128-byte staging line).
+        // 128 intermediate columns per tile: gate at tbase, up at tbase + 128.
+        // This warp takes columns cp*32 .. cp*32+31: 32 E4M3 codes per lane,
+        // staged as one 32-byte row per lane with the 32-byte swizzle (16-byte
+        // chunk j at j ^ ((row >> 2) & 1)).
+        uint32_t rg[32], ru[32];
+        tmem_ld_32x32b_x32(tbase + cp * 32, rg);
+        tmem_ld_32x32b_x32(tbase + C::kBN + cp * 32, ru);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
+          else mbar_arrive(tempty_bar(acc));
+        }
+        uint32_t codes[8];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          // the bf16 values the separate gate / up GEMMs would have written
+          const uint32_t gw = cvt_bf16x2(__fmul_rn(__uint_as_float(rg[2 * j]), alpha),
+                                         __fmul_rn(__uint_as_float(rg[2 * j + 1]), alpha));
+          const uint32_t uw = cvt_bf16x2(__fmul_rn(__uint_as_float(ru[2 * j]), alpha_u),
+                                         __fmul_rn(__uint_as_float(ru[2 * j + 1]), alpha_u));
+          const uint32_t pair = swiglu_fp8_pair(gw, uw, s_out, rs_out, exact_only);
+          if (j & 1) codes[j >> 1] |= pair << 16;
+          else codes[j >> 1] = pair;
+        }
         if (lane == 0) tma_store_wait_read<1>();
         __syncwarp();
-        uint8_t* bp = buf0_ptr + nbuf * kEpiBufBytes + lane * 128;
-#pragma unroll 1
-        for (int c = 0; c < C::kBN / 32; ++c) {
-          uint32_t rg[32], ru[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, rg);
-          tmem_ld_32x32b_x32(tbase + C::kBN + c * 32, ru);
-          tmem_ld_wait();
-          if (c == C::kBN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
-              else mbar_arrive(tempty_bar(acc));
-            }
-          }
-          uint32_t codes[8];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            // the bf16 values the separate gate / up GEMMs would have written
-            const uint32_t gw = cvt_bf16x2(__fmul_rn(__uint_as_float(rg[2 * j]), alpha),
-                                           __fmul_rn(__uint_as_float(rg[2 * j + 1]), alpha));
-            const uint32_t uw = cvt_bf16x2(__fmul_rn(__uint_as_float(ru[2 * j]), alpha_u),
-                                           __fmul_rn(__uint_as_float(ru[2 * j + 1]), alpha_u));
-            const uint32_t pair = swiglu_fp8_pair(gw, uw, s_out, rs_out, exact_only);
-            if (j & 1) codes[j >> 1] |= pair << 16;
-            else codes[j >> 1] = pair;
-          }
-          const int pj0 = (2 * c) ^ (lane & 7), pj1 = (2 * c + 1) ^ (lane & 7);
-          *reinterpret_cast<uint4*>(bp + pj0 * 16) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          *reinterpret_cast<uint4*>(bp + pj1 * 16) = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-        }
+        uint8_t* bp = buf0_ptr + nbuf * EB + lane * 32;
+        const int sw = (lane >> 2) & 1;
+        *reinterpret_cast<uint4*>(bp + ((0 ^ sw) * 16)) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        *reinterpret_cast<uint4*>(bp + ((1 ^ sw) * 16)) = make_uint4(codes[4], codes[5], codes[6], codes[7]);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && n0 < ng && row0 < args.M) {
-          tma_store_2d(map_y(maps, 0), buf0 + nbuf * kEpiBufBytes, n0, row0);
+        const int col0 = n0 + cp * 32;
+        if (lane == 0 && col0 < ng && row0 < args.M) {
+          tma_store_2d(map_y(maps, 0), buf0 + nbuf * EB, col0, row0);
           tma_store_commit();
         }
         nbuf ^= 1;
@@ -792,9 +794,9 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
     args.N[g] = (int)p.N[g];
     args.tiles_n[g] = (int)((p.N[g] + C::kBN - 1) / C::kBN);
     args.tiles_per_m += args.tiles_n[g];
-    if (kGlu)  // E4M3 output [M, I], 128-byte rows of the staging buffer
-      ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.y[g], p.N[g], p.M, p.N[g], 128,
-                      32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (kGlu)  // E4M3 output [M, I]: 32 rows x 32 codes per epilogue warp
+      ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.y[g], p.N[g], p.M, p.N[g], 32,
+                      32, CU_TENSOR_MAP_SWIZZLE_32B);
     else
       ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y[g], p.N[g], p.M, p.N[g] * 2,
                       64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
