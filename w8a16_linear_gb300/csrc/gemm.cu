@@ -78,10 +78,10 @@ struct Cfg {
   static constexpr int kBBytes = (kGlu ? 2 : 1) * kBHalf;
   static constexpr int kStages = CG == 1 ? 4 : 6;
   static constexpr uint32_t kIdesc = make_idesc(0, 0, BM * CG, kBN);  // E4M3 x E4M3 -> F32
-  // GLU: four warps per TMEM lane quadrant (32 columns each) to keep the
-  // SwiGLU epilogue ahead of the tensor cores; staging 32 rows x 32 codes.
-  static constexpr int kEpiWarps = kGlu ? 16 : 4;
-  static constexpr int kEpiBuf = kGlu ? 32 * 32 : kEpiBufBytes;
+  // GLU: two warps per TMEM lane quadrant (64 columns each) to keep the
+  // SwiGLU epilogue ahead of the tensor cores; staging 32 rows x 64 codes.
+  static constexpr int kEpiWarps = kGlu ? 8 : 4;
+  static constexpr int kEpiBuf = kGlu ? 32 * 64 : kEpiBufBytes;
   static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBuf;
 };
 
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     const int wq = warp & 3;              // TMEM lane quadrant this warp may access
-    const int cp = (warp - 2) >> 2;       // GLU: which 32 of the tile's 128 columns
+    const int cp = (warp - 2) >> 2;       // GLU: which 64 of the tile's 128 columns
     constexpr int EB = C::kEpiBuf;
     const uint32_t buf0 = sbase + L::kEpi + (uint32_t)((warp - 2) * 2 * EB);
     uint8_t* buf0_ptr = smem + L::kEpi + (warp - 2) * 2 * EB;
@@ -398,40 +398,54 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
         }
       } else {
         // 128 intermediate columns per tile: gate at tbase, up at tbase + 128.
-        // This warp takes columns cp*32 .. cp*32+31: 32 E4M3 codes per lane,
-        // staged as one 32-byte row per lane with the 32-byte swizzle (16-byte
-        // chunk j at j ^ ((row >> 2) & 1)).
-        uint32_t rg[32], ru[32];
-        tmem_ld_32x32b_x32(tbase + cp * 32, rg);
-        tmem_ld_32x32b_x32(tbase + C::kBN + cp * 32, ru);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
-          else mbar_arrive(tempty_bar(acc));
-        }
-        uint32_t codes[8];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          // the bf16 values the separate gate / up GEMMs would have written
-          const uint32_t gw = cvt_bf16x2(__fmul_rn(__uint_as_float(rg[2 * j]), alpha),
-                                         __fmul_rn(__uint_as_float(rg[2 * j + 1]), alpha));
-          const uint32_t uw = cvt_bf16x2(__fmul_rn(__uint_as_float(ru[2 * j]), alpha_u),
-                                         __fmul_rn(__uint_as_float(ru[2 * j + 1]), alpha_u));
-          const uint32_t pair = swiglu_fp8_pair(gw, uw, s_out, rs_out, exact_only);
-          if (j & 1) codes[j >> 1] |= pair << 16;
-          else codes[j >> 1] = pair;
-        }
+        // This warp takes columns cp*64 .. cp*64+63: two 32-column chunks of
+        // 32 E4M3 codes each, staged as one 64-byte row per lane with the
+        // 64-byte swizzle (16-byte chunk j at j ^ ((row >> 1) & 3)).
         if (lane == 0) tma_store_wait_read<1>();
         __syncwarp();
-        uint8_t* bp = buf0_ptr + nbuf * EB + lane * 32;
-        const int sw = (lane >> 2) & 1;
-        *reinterpret_cast<uint4*>(bp + ((0 ^ sw) * 16)) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-        *reinterpret_cast<uint4*>(bp + ((1 ^ sw) * 16)) = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        uint8_t* bp = buf0_ptr + nbuf * EB + lane * 64;
+        const int sw = (lane >> 1) & 3;
+#pragma unroll 1
+        for (int lc = 0; lc < 2; ++lc) {
+          const int c = 2 * cp + lc;
+          uint32_t rg[32], ru[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, rg);
+          tmem_ld_32x32b_x32(tbase + C::kBN + c * 32, ru);
+          tmem_ld_wait();
+          if (lc == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
+              else mbar_arrive(tempty_bar(acc));
+            }
+          }
+          uint32_t codes[8];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            // the bf16 values the separate gate / up GEMMs would have written
+            uint32_t gw[8], uw[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int e = 16 * hh + 2 * j;
+              gw[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(rg[e]), alpha),
+                                 __fmul_rn(__uint_as_float(rg[e + 1]), alpha));
+              uw[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(ru[e]), alpha_u),
+                                 __fmul_rn(__uint_as_float(ru[e + 1]), alpha_u));
+            }
+            uint32_t c4[4];
+            swiglu_fp8_x16(gw, uw, s_out, rs_out, exact_only, c4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) codes[4 * hh + j] = c4[j];
+          }
+          *reinterpret_cast<uint4*>(bp + (((2 * lc) ^ sw) * 16)) =
+              make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          *reinterpret_cast<uint4*>(bp + (((2 * lc + 1) ^ sw) * 16)) =
+              make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        }
         fence_proxy_async_smem();
         __syncwarp();
-        const int col0 = n0 + cp * 32;
+        const int col0 = n0 + cp * 64;
         if (lane == 0 && col0 < ng && row0 < args.M) {
           tma_store_2d(map_y(maps, 0), buf0 + nbuf * EB, col0, row0);
           tma_store_commit();
@@ -794,9 +808,9 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
     args.N[g] = (int)p.N[g];
     args.tiles_n[g] = (int)((p.N[g] + C::kBN - 1) / C::kBN);
     args.tiles_per_m += args.tiles_n[g];
-    if (kGlu)  // E4M3 output [M, I]: 32 rows x 32 codes per epilogue warp
-      ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.y[g], p.N[g], p.M, p.N[g], 32,
-                      32, CU_TENSOR_MAP_SWIZZLE_32B);
+    if (kGlu)  // E4M3 output [M, I]: 32 rows x 64 codes per epilogue warp
+      ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.y[g], p.N[g], p.M, p.N[g], 64,
+                      32, CU_TENSOR_MAP_SWIZZLE_64B);
     else
       ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y[g], p.N[g], p.M, p.N[g] * 2,
                       64, 32, CU_TENSOR_MAP_SWIZZLE_128B);

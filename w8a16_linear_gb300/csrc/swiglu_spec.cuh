@@ -186,4 +186,71 @@ __device__ __forceinline__ uint32_t swiglu_bf16_pair(uint32_t gw, uint32_t uw) {
   return cvt_bf16x2(h.x, h.y);
 }
 
+// ---- 16 elements at once: the fast values of all 16 are computed
+// straight-line (independent pairs interleave), one flag records whether any
+// element needs the exact path, and a single, rarely taken branch repairs
+// those elements.  gw/uw: 8 words of two bf16 each.
+
+__device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const uint32_t (&uw)[8],
+                                               float s, float rs, bool exact_only,
+                                               uint32_t (&codes)[4]) {
+  float q[16];
+  bool any = exact_only;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    F2 p, d;
+    swiglu_pd(gw[j], uw[j], p, d);
+    const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
+    const F2 qf = mul2(hf, splat(rs));
+    q[2 * j] = qf.x;
+    q[2 * j + 1] = qf.y;
+    any |= h_needs_exact(p.x, d.x, hf.x) | h_needs_exact(p.y, d.y, hf.y) |
+           maybe_near_e4m3_midpoint<32>(qf.x) | maybe_near_e4m3_midpoint<32>(qf.y);
+  }
+  if (any) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      F2 p, d;
+      swiglu_pd(gw[j], uw[j], p, d);
+      const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
+      if (exact_only || h_needs_exact(p.x, d.x, hf.x) || near_e4m3_midpoint<32>(q[2 * j]))
+        q[2 * j] = __fdiv_rn(__fdiv_rn(p.x, d.x), s);
+      if (exact_only || h_needs_exact(p.y, d.y, hf.y) || near_e4m3_midpoint<32>(q[2 * j + 1]))
+        q[2 * j + 1] = __fdiv_rn(__fdiv_rn(p.y, d.y), s);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    codes[j] = cvt_e4m3x2(q[4 * j], q[4 * j + 1]) | (cvt_e4m3x2(q[4 * j + 2], q[4 * j + 3]) << 16);
+}
+
+__device__ __forceinline__ void swiglu_bf16_x16(const uint32_t (&gw)[8], const uint32_t (&uw)[8],
+                                                uint32_t (&out)[8]) {
+  float h[16];
+  bool any = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    F2 p, d;
+    swiglu_pd(gw[j], uw[j], p, d);
+    const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
+    h[2 * j] = hf.x;
+    h[2 * j + 1] = hf.y;
+    any |= h_needs_exact(p.x, d.x, hf.x) | h_needs_exact(p.y, d.y, hf.y) |
+           near_bf16_midpoint<8>(hf.x) | near_bf16_midpoint<8>(hf.y);
+  }
+  if (any) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      F2 p, d;
+      swiglu_pd(gw[j], uw[j], p, d);
+      if (h_needs_exact(p.x, d.x, h[2 * j]) || near_bf16_midpoint<8>(h[2 * j]))
+        h[2 * j] = __fdiv_rn(p.x, d.x);
+      if (h_needs_exact(p.y, d.y, h[2 * j + 1]) || near_bf16_midpoint<8>(h[2 * j + 1]))
+        h[2 * j + 1] = __fdiv_rn(p.y, d.y);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[j] = cvt_bf16x2(h[2 * j], h[2 * j + 1]);
+}
+
 }  // namespace w8
