@@ -39,6 +39,8 @@ namespace {
 __device__ __forceinline__ uint32_t quant_pair(uint32_t w, float s, float r, bool exact_only) {
   const float v0 = bf16_lo(w), v1 = bf16_hi(w);
   F2 f = mul2(F2{v0, v1}, splat(r));
+  // Activations rarely fall in the E4M3 subnormal range, so the cheap
+  // pre-test (which admits that whole range) keeps the branch rare here.
   if (exact_only | maybe_near_e4m3_midpoint<4>(f.x) | maybe_near_e4m3_midpoint<4>(f.y)) {
     if (exact_only || near_e4m3_midpoint<4>(f.x)) f.x = __fdiv_rn(v0, s);
     if (exact_only || near_e4m3_midpoint<4>(f.y)) f.y = __fdiv_rn(v1, s);
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(256, 8) quant_static_kernel(const uint16_t* __
   }
 }
 
-__global__ void __launch_bounds__(256, 4) swiglu_fp8_kernel(const uint16_t* __restrict__ g,
+__global__ void __launch_bounds__(256, 6) swiglu_fp8_kernel(const uint16_t* __restrict__ g,
                                                             const uint16_t* __restrict__ u,
                                                             int64_t n16,
                                                             const float* __restrict__ s_out,
@@ -78,15 +80,20 @@ __global__ void __launch_bounds__(256, 4) swiglu_fp8_kernel(const uint16_t* __re
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
     const uint4 ga = ldg16(g + i * 16), gb = ldg16(g + i * 16 + 8);
     const uint4 ua = ldg16(u + i * 16), ub = ldg16(u + i * 16 + 8);
-    const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-    const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
-    uint32_t c[4];
-    swiglu_fp8_x16(gw, uw, s, rs, exact_only, c);
-    *reinterpret_cast<uint4*>(out + i * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+    uint4 o;
+    o.x = swiglu_fp8_pair(ga.x, ua.x, s, rs, exact_only) |
+          (swiglu_fp8_pair(ga.y, ua.y, s, rs, exact_only) << 16);
+    o.y = swiglu_fp8_pair(ga.z, ua.z, s, rs, exact_only) |
+          (swiglu_fp8_pair(ga.w, ua.w, s, rs, exact_only) << 16);
+    o.z = swiglu_fp8_pair(gb.x, ub.x, s, rs, exact_only) |
+          (swiglu_fp8_pair(gb.y, ub.y, s, rs, exact_only) << 16);
+    o.w = swiglu_fp8_pair(gb.z, ub.z, s, rs, exact_only) |
+          (swiglu_fp8_pair(gb.w, ub.w, s, rs, exact_only) << 16);
+    *reinterpret_cast<uint4*>(out + i * 16) = o;
   }
 }
 
-__global__ void __launch_bounds__(256, 4) swiglu_bf16_kernel(const uint16_t* __restrict__ g,
+__global__ void __launch_bounds__(256, 6) swiglu_bf16_kernel(const uint16_t* __restrict__ g,
                                                              const uint16_t* __restrict__ u,
                                                              int64_t n16,
                                                              uint16_t* __restrict__ out) {
@@ -94,13 +101,11 @@ __global__ void __launch_bounds__(256, 4) swiglu_bf16_kernel(const uint16_t* __r
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
     const uint4 ga = ldg16(g + i * 16), gb = ldg16(g + i * 16 + 8);
     const uint4 ua = ldg16(u + i * 16), ub = ldg16(u + i * 16 + 8);
-    const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-    const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
-    uint32_t o[8];
-    swiglu_bf16_x16(gw, uw, o);
     uint4* dst = reinterpret_cast<uint4*>(out + i * 16);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    dst[0] = make_uint4(swiglu_bf16_pair(ga.x, ua.x), swiglu_bf16_pair(ga.y, ua.y),
+                        swiglu_bf16_pair(ga.z, ua.z), swiglu_bf16_pair(ga.w, ua.w));
+    dst[1] = make_uint4(swiglu_bf16_pair(gb.x, ub.x), swiglu_bf16_pair(gb.y, ub.y),
+                        swiglu_bf16_pair(gb.z, ub.z), swiglu_bf16_pair(gb.w, ub.w));
   }
 }
 

@@ -70,14 +70,19 @@ enum class Mode { W8A8, GLU };
 template <Mode MODE, int CG>
 struct Cfg {
   static constexpr bool kGlu = (MODE == Mode::GLU);
+  // W8A8: 256 output columns per tile.  GLU: 128 intermediate columns per
+  // tile, computed by one N = 256 MMA whose B operand is [128 gate rows | 128
+  // up rows] of the slice: D columns 0-127 hold gate, 128-255 hold up, and
+  // the activation operand is read once for both.  In the CTA pair the even
+  // CTA stages the gate rows and the odd CTA the up rows.
   static constexpr int kBN = kGlu ? 128 : 256;              // output columns per tile
-  static constexpr int kBRows = kBN / CG;                   // weight rows per projection per CTA
+  static constexpr int kMmaN = 256;
+  static constexpr int kBRows = kMmaN / CG;                 // weight rows staged per CTA
   static constexpr int kBK = 128;                           // K per stage (bytes = elements)
   static constexpr int kABytes = BM * 128;
-  static constexpr int kBHalf = kBRows * 128;               // one projection's weight tile
-  static constexpr int kBBytes = (kGlu ? 2 : 1) * kBHalf;
+  static constexpr int kBBytes = kBRows * 128;
   static constexpr int kStages = CG == 1 ? 4 : 6;
-  static constexpr uint32_t kIdesc = make_idesc(0, 0, BM * CG, kBN);  // E4M3 x E4M3 -> F32
+  static constexpr uint32_t kIdesc = make_idesc(0, 0, BM * CG, kMmaN);  // E4M3 x E4M3 -> F32
   // GLU: two warps per TMEM lane quadrant (64 columns each) to keep the
   // SwiGLU epilogue ahead of the tensor cores; staging 32 rows x 64 codes.
   static constexpr int kEpiWarps = kGlu ? 8 : 4;
@@ -222,7 +227,10 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
         int m0, g, n0;
         decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
         const int a_row = m0 + (int)rank * BM;
-        const int b_row = n0 + (int)rank * C::kBRows;
+        // W8A8: this CTA's half (pair) or all of the tile's weight rows.
+        // GLU: the slice's rows n0 .. n0+127 of gate (even CTA / first half)
+        // and of up (odd CTA / second half).
+        const int b_row = kGlu ? n0 : n0 + (int)rank * C::kBRows;
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1, abort, kWaitLimitNs)) {
             record_timeout(abort);
@@ -234,16 +242,14 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           const int kc = kb * C::kBK;
           if (leader) mbar_arrive_expect_tx(full_bar(s), CG * (C::kABytes + C::kBBytes));
           const uint32_t fb = leader_addr(full_bar(s));
-          // GLU: gate rows, then up rows, in one stage.
-          const CUtensorMap* mb0 = kGlu ? &maps.b[0] : map_b(maps, g);
+          const CUtensorMap* mb0 = kGlu ? (rank == 0 ? &maps.b[0] : &maps.b[1]) : map_b(maps, g);
           if constexpr (CG == 2) {
             tma_load_2d_pair(a_dst, &maps.a, fb, kc, a_row);
             tma_load_2d_pair(b_dst, mb0, fb, kc, b_row);
-            if constexpr (kGlu) tma_load_2d_pair(b_dst + C::kBHalf, &maps.b[1], fb, kc, b_row);
           } else {
             tma_load_2d(a_dst, &maps.a, fb, kc, a_row);
             tma_load_2d(b_dst, mb0, fb, kc, b_row);
-            if constexpr (kGlu) tma_load_2d(b_dst + C::kBHalf, &maps.b[1], fb, kc, b_row);
+            if constexpr (kGlu) tma_load_2d(b_dst + 128 * 128, &maps.b[1], fb, kc, b_row);
           }
           ++issued;
           if (++s == S) {
@@ -291,14 +297,10 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
             const uint64_t ad = sw128_kmajor_desc(a_addr + 32 * k);
+            const uint64_t bd = sw128_kmajor_desc(b_addr + 32 * k);
             const uint32_t accum = (kb | k) != 0;
-#pragma unroll
-            for (int h = 0; h < (kGlu ? 2 : 1); ++h) {  // GLU: gate into d, up into d + 128
-              const uint64_t bd = sw128_kmajor_desc(b_addr + h * C::kBHalf + 32 * k);
-              const uint32_t dh = d + (uint32_t)(h * C::kBN);
-              if constexpr (CG == 2) mma_f8f6f4_pair(dh, ad, bd, C::kIdesc, accum);
-              else mma_f8f6f4(dh, ad, bd, C::kIdesc, accum);
-            }
+            if constexpr (CG == 2) mma_f8f6f4_pair(d, ad, bd, C::kIdesc, accum);
+            else mma_f8f6f4(d, ad, bd, C::kIdesc, accum);
           }
           if constexpr (CG == 2) mma_commit_pair_mc(empty_bar(s), 0x3);
           else mma_commit(empty_bar(s));
@@ -496,16 +498,17 @@ constexpr int kXHalf = NH * 128;             // bf16 activation rows of one MMA,
 constexpr int kXBytes = 2 * kXHalf;
 constexpr int kRawBytes = BW * 64;           // raw E4M3 weight rows
 constexpr int kEpiBuf = 32 * 64;             // 32 tokens x 32 features bf16
+constexpr int kEpiWarps = 8;                 // 2 per TMEM lane quadrant, 6 token chunks each
 constexpr int kOffX = 0;
 constexpr int kOffRaw = kOffX + S * kXBytes;
 constexpr int kOffEpi = kOffRaw + S * kRawBytes;
-constexpr int kOffBar = kOffEpi + 4 * 2 * kEpiBuf;
+constexpr int kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
 constexpr int kNumBars = 3 * S + 3;          // full[S], empty[S], ready[S], tfull, tempty, drain
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kAlloc = kOffAbort + 4 + 1024;
 constexpr int kTransformWarps = 8;           // 2 per TMEM lane quadrant, 32 K-values each
-constexpr int kThreads = (2 + 4 + kTransformWarps) * 32;
+constexpr int kThreads = (2 + kEpiWarps + kTransformWarps) * 32;
 constexpr uint32_t kTmemA = 2 * NH;          // first A-stage column
 constexpr uint32_t kIdesc = make_idesc(1, 1, BW, NH);
 static_assert(kTmemA + S * 32 <= kTmemCols, "TMEM budget");
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
       mbar_init(ready_bar(st), kTransformWarps);
     }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, 4);
+    mbar_init(tempty_bar, kEpiWarps);
     mbar_init(drain_bar, 1);
     *abort = 0;
     fence_mbar_init();
@@ -633,9 +636,10 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
       volatile int never = 0;
       if (!mbar_wait(drain_bar, 0, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant: weight rows (features) q*32 .. q*32+31
+    const int eh = (warp - 2) >> 2;  // which half of the tile's 384 tokens
     uint8_t* bufp = smem + kOffEpi + (warp - 2) * 2 * kEpiBuf;
     const uint32_t bufs = sbase + kOffEpi + (uint32_t)((warp - 2) * 2 * kEpiBuf);
     int nbuf = 0;
@@ -651,11 +655,11 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
       const int f0 = n0 + q * 32;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BT / 32; ++c) {
+      for (int c = eh * (NH / 32); c < (eh + 1) * (NH / 32); ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c * 32, r);  // feature f0+lane, tokens m0+c*32 .. +31
         tmem_ld_wait();
-        if (c == BT / 32 - 1) {
+        if (c == (eh + 1) * (NH / 32) - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar);
@@ -685,7 +689,7 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
   } else {
     // ---------------------------------------------------------------- weight transform
     const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int h = (warp - 6) >> 2;       // which 32 of the stage's 64 K-values
+    const int h = (warp - 2 - kEpiWarps) >> 2;  // which 32 of the stage's 64 K-values
     const int r = q * 32 + lane;         // weight row of the tile = TMEM lane
     int st = 0;
     uint32_t ph = 0;
@@ -802,7 +806,7 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   for (int g = 0; g < nb; ++g) {
     args.s_w[g] = p.s_w[g];
     ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[kGlu ? 0 : g], p.K,
-                    128, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
+                    128, kGlu ? 128 : C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   for (int g = 0; g < args.G; ++g) {
     args.N[g] = (int)p.N[g];

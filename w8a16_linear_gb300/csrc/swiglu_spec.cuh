@@ -99,6 +99,8 @@ __device__ __forceinline__ float rcp_approx(float d) {
 // range (|f| < 2^-6) the midpoints are the odd multiples of 2^-10: there f
 // needs the exact path only when f * 2^9 is within 2^-14 of a half-integer
 // (far more than W binary32 ulps of f at that scale).
+// Cheap pre-test: true near a midpoint of the normal E4M3 range and for every
+// value in the subnormal range (a superset of near_e4m3_midpoint).
 template <int W>
 __device__ __forceinline__ bool maybe_near_e4m3_midpoint(float f) {
   const uint32_t b = __float_as_uint(f);
@@ -108,16 +110,14 @@ __device__ __forceinline__ bool maybe_near_e4m3_midpoint(float f) {
   return sub | mid;
 }
 
-// Precise version, evaluated only where the cheap test above fired.
 template <int W>
 __device__ __forceinline__ bool near_e4m3_midpoint(float f) {
   const float a = fabsf(f);
-  if (a != 0.0f && a < 0.015625f) {
-    const float t = a * 512.0f;                                   // exact scaling
-    return fabsf((t - floorf(t)) - 0.5f) < 6.103515625e-05f;      // 2^-14
-  }
+  const float t = a * 512.0f;                                       // exact scaling
+  const bool near_sub = fabsf((t - floorf(t)) - 0.5f) < 6.103515625e-05f;   // 2^-14
   const uint32_t b = __float_as_uint(f);
-  return ((b & 0xFFFFFu) + (uint32_t)W - 0x80000u) <= (uint32_t)(2 * W);
+  const bool mid = ((b & 0xFFFFFu) + (uint32_t)W - 0x80000u) <= (uint32_t)(2 * W);
+  return (a < 0.015625f) ? near_sub : mid;                          // |f| < 2^-6: subnormal E4M3
 }
 
 template <int W>
@@ -164,12 +164,11 @@ __device__ __forceinline__ uint32_t swiglu_fp8_pair(uint32_t gw, uint32_t uw, fl
   swiglu_pd(gw, uw, p, d);
   const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
   F2 q = mul2(hf, splat(rs));
-  if (exact_only | h_needs_exact(p.x, d.x, hf.x) | h_needs_exact(p.y, d.y, hf.y) |
-      maybe_near_e4m3_midpoint<32>(q.x) | maybe_near_e4m3_midpoint<32>(q.y)) {
-    if (exact_only || h_needs_exact(p.x, d.x, hf.x) || near_e4m3_midpoint<32>(q.x))
-      q.x = __fdiv_rn(__fdiv_rn(p.x, d.x), s);
-    if (exact_only || h_needs_exact(p.y, d.y, hf.y) || near_e4m3_midpoint<32>(q.y))
-      q.y = __fdiv_rn(__fdiv_rn(p.y, d.y), s);
+  const bool fx = exact_only | h_needs_exact(p.x, d.x, hf.x) | near_e4m3_midpoint<32>(q.x);
+  const bool fy = exact_only | h_needs_exact(p.y, d.y, hf.y) | near_e4m3_midpoint<32>(q.y);
+  if (fx | fy) {                       // rare: a rounding decision the fast value cannot settle
+    if (fx) q.x = __fdiv_rn(__fdiv_rn(p.x, d.x), s);
+    if (fy) q.y = __fdiv_rn(__fdiv_rn(p.y, d.y), s);
   }
   return cvt_e4m3x2(q.x, q.y);
 }
@@ -186,16 +185,17 @@ __device__ __forceinline__ uint32_t swiglu_bf16_pair(uint32_t gw, uint32_t uw) {
   return cvt_bf16x2(h.x, h.y);
 }
 
-// ---- 16 elements at once: the fast values of all 16 are computed
-// straight-line (independent pairs interleave), one flag records whether any
-// element needs the exact path, and a single, rarely taken branch repairs
-// those elements.  gw/uw: 8 words of two bf16 each.
+// ---- 16 elements at once (the fused gate/up epilogue): the fast values of all
+// 16 are computed straight-line so that independent pairs interleave, a
+// bitmask records the elements whose rounding decision the fast value cannot
+// settle, and a single, rarely taken branch recomputes those exactly.
+// gw/uw: 8 words of two bf16 each.
 
 __device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const uint32_t (&uw)[8],
                                                float s, float rs, bool exact_only,
                                                uint32_t (&codes)[4]) {
-  float q[16];
-  bool any = exact_only;
+  float q[16], pp[16], dd[16];
+  uint32_t fix = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     F2 p, d;
@@ -204,53 +204,21 @@ __device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const ui
     const F2 qf = mul2(hf, splat(rs));
     q[2 * j] = qf.x;
     q[2 * j + 1] = qf.y;
-    any |= h_needs_exact(p.x, d.x, hf.x) | h_needs_exact(p.y, d.y, hf.y) |
-           maybe_near_e4m3_midpoint<32>(qf.x) | maybe_near_e4m3_midpoint<32>(qf.y);
+    pp[2 * j] = p.x;
+    pp[2 * j + 1] = p.y;
+    dd[2 * j] = d.x;
+    dd[2 * j + 1] = d.y;
+    fix |= (uint32_t)(exact_only | h_needs_exact(p.x, d.x, hf.x) | near_e4m3_midpoint<32>(qf.x)) << (2 * j);
+    fix |= (uint32_t)(exact_only | h_needs_exact(p.y, d.y, hf.y) | near_e4m3_midpoint<32>(qf.y)) << (2 * j + 1);
   }
-  if (any) {
+  if (fix) {                           // rare: decisions the fast values cannot settle
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      F2 p, d;
-      swiglu_pd(gw[j], uw[j], p, d);
-      const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
-      if (exact_only || h_needs_exact(p.x, d.x, hf.x) || near_e4m3_midpoint<32>(q[2 * j]))
-        q[2 * j] = __fdiv_rn(__fdiv_rn(p.x, d.x), s);
-      if (exact_only || h_needs_exact(p.y, d.y, hf.y) || near_e4m3_midpoint<32>(q[2 * j + 1]))
-        q[2 * j + 1] = __fdiv_rn(__fdiv_rn(p.y, d.y), s);
-    }
+    for (int e = 0; e < 16; ++e)
+      if (fix & (1u << e)) q[e] = __fdiv_rn(__fdiv_rn(pp[e], dd[e]), s);
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j)
     codes[j] = cvt_e4m3x2(q[4 * j], q[4 * j + 1]) | (cvt_e4m3x2(q[4 * j + 2], q[4 * j + 3]) << 16);
-}
-
-__device__ __forceinline__ void swiglu_bf16_x16(const uint32_t (&gw)[8], const uint32_t (&uw)[8],
-                                                uint32_t (&out)[8]) {
-  float h[16];
-  bool any = false;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    F2 p, d;
-    swiglu_pd(gw[j], uw[j], p, d);
-    const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
-    h[2 * j] = hf.x;
-    h[2 * j + 1] = hf.y;
-    any |= h_needs_exact(p.x, d.x, hf.x) | h_needs_exact(p.y, d.y, hf.y) |
-           near_bf16_midpoint<8>(hf.x) | near_bf16_midpoint<8>(hf.y);
-  }
-  if (any) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      F2 p, d;
-      swiglu_pd(gw[j], uw[j], p, d);
-      if (h_needs_exact(p.x, d.x, h[2 * j]) || near_bf16_midpoint<8>(h[2 * j]))
-        h[2 * j] = __fdiv_rn(p.x, d.x);
-      if (h_needs_exact(p.y, d.y, h[2 * j + 1]) || near_bf16_midpoint<8>(h[2 * j + 1]))
-        h[2 * j + 1] = __fdiv_rn(p.y, d.y);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) out[j] = cvt_bf16x2(h[2 * j], h[2 * j + 1]);
 }
 
 }  // namespace w8
