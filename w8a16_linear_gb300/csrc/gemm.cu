@@ -480,20 +480,20 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
 // there by the transform warps with tcgen05.st (it never passes through
 // shared memory); the activation tile is the B operand, staged by TMA into a
 // 128-byte-swizzled K-major shared-memory buffer.  A tile is 128 weight rows
-// x 384 tokens, computed as two N = 192 MMAs that share each dequantized
-// weight stage, so every weight element is converted once per 384 tokens.
+// x 320 tokens, computed as two N = 160 MMAs that share each dequantized
+// weight stage, so every weight element is converted once per 320 tokens.
 // D has the weight rows across the TMEM lanes and the tokens across columns;
 // the epilogue turns each 32-token x 32-feature block into row-major y
 // through a small staging buffer and a TMA store.
 //
-// TMEM columns: D (tokens 0-191) 0-191, D (tokens 192-383) 192-383, A stages
-// 384 + 32 s (64 K-values of 128 rows, two bf16 per column).
+// TMEM columns: D (tokens 0-159) 0-159, D (tokens 160-319) 160-319, A stages
+// 320 + 32 s (64 K-values of 128 rows, two bf16 per column).
 namespace a16t {
-constexpr int NH = 192;                      // tokens per MMA (MMA N)
+constexpr int NH = 160;                      // tokens per MMA (MMA N)
 constexpr int BT = 2 * NH;                   // tokens per tile
 constexpr int BW = 128;                      // weight rows per tile (MMA M)
 constexpr int BK = 64;                       // K per stage
-constexpr int S = 3;                         // stages
+constexpr int S = 4;                         // stages
 constexpr int kXHalf = NH * 128;             // bf16 activation rows of one MMA, 128-byte rows
 constexpr int kXBytes = 2 * kXHalf;
 constexpr int kRawBytes = BW * 64;           // raw E4M3 weight rows
