@@ -191,11 +191,19 @@ __device__ __forceinline__ uint32_t swiglu_bf16_pair(uint32_t gw, uint32_t uw) {
 // settle, and a single, rarely taken branch recomputes those exactly.
 // gw/uw: 8 words of two bf16 each.
 
+// Cheap integer form of h_needs_exact for the straight-line pass:
+// d >= 2^126 (or NaN), or |hf| < 2^-100 while p != 0.
+__device__ __forceinline__ bool h_maybe_bad(float p, float d, float hf) {
+  const uint32_t db = __float_as_uint(d);
+  const uint32_t hb = __float_as_uint(hf) & 0x7FFFFFFFu;
+  return (db >= 0x7E800000u) | ((hb < 0x0D800000u) & ((__float_as_uint(p) << 1) != 0u));
+}
+
 __device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const uint32_t (&uw)[8],
                                                float s, float rs, bool exact_only,
                                                uint32_t (&codes)[4]) {
   float q[16], pp[16], dd[16];
-  uint32_t fix = 0;
+  uint32_t maybe = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     F2 p, d;
@@ -208,13 +216,19 @@ __device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const ui
     pp[2 * j + 1] = p.y;
     dd[2 * j] = d.x;
     dd[2 * j + 1] = d.y;
-    fix |= (uint32_t)(exact_only | h_needs_exact(p.x, d.x, hf.x) | near_e4m3_midpoint<32>(qf.x)) << (2 * j);
-    fix |= (uint32_t)(exact_only | h_needs_exact(p.y, d.y, hf.y) | near_e4m3_midpoint<32>(qf.y)) << (2 * j + 1);
+    maybe |= (uint32_t)(h_maybe_bad(p.x, d.x, hf.x) | maybe_near_e4m3_midpoint<32>(qf.x)) << (2 * j);
+    maybe |= (uint32_t)(h_maybe_bad(p.y, d.y, hf.y) | maybe_near_e4m3_midpoint<32>(qf.y)) << (2 * j + 1);
   }
-  if (fix) {                           // rare: decisions the fast values cannot settle
+  if (exact_only) maybe = 0xFFFFu;
+  if (maybe) {                         // the precise tests, then the rare exact divisions
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-      if (fix & (1u << e)) q[e] = __fdiv_rn(__fdiv_rn(pp[e], dd[e]), s);
+    for (int e = 0; e < 16; ++e) {
+      if (maybe & (1u << e)) {
+        const float hf = __fmul_rn(pp[e], rcp_approx(dd[e]));
+        if (exact_only || h_needs_exact(pp[e], dd[e], hf) || near_e4m3_midpoint<32>(q[e]))
+          q[e] = __fdiv_rn(__fdiv_rn(pp[e], dd[e]), s);
+      }
+    }
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j)
