@@ -119,6 +119,8 @@ struct Args {
   int N[kMaxGroup];
   int tiles_n[kMaxGroup];
   int tiles_per_m;
+  int tiles_m;
+  int group_m;   // m-blocks swept together down each column of tiles
   int num_tiles;
   int num_kb;
   const float* s_in;
@@ -127,10 +129,19 @@ struct Args {
 };
 
 // Tile t -> first output row of the (cluster) tile, projection, first column.
+// Tiles are rasterised in groups of `group_m` m-blocks: within a group the
+// m-block varies fastest, then the column of tiles (projection, n-block), so
+// the CTAs running at the same time share each weight tile through L2 and
+// the group's activation rows stay L2-resident while it sweeps the columns.
 __device__ __forceinline__ void decode_tile(const Args& a, int t, int rows_per_tile, int cols_per_tile,
                                             int& m0, int& g, int& n0) {
-  const int mb = t / a.tiles_per_m;
-  int r = t - mb * a.tiles_per_m;
+  const int per_group = a.group_m * a.tiles_per_m;
+  const int grp = t / per_group;
+  const int mb0 = grp * a.group_m;
+  const int gm = min(a.group_m, a.tiles_m - mb0);
+  const int rr = t - grp * per_group;
+  int r = rr / gm;                       // column of tiles
+  const int mb = mb0 + (rr - r * gm);
   g = 0;
   while (g < a.G - 1 && r >= a.tiles_n[g]) {
     r -= a.tiles_n[g];
@@ -746,6 +757,15 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
+// m-blocks per rasterisation group: as many as keep the group's activation
+// rows within ~32 MB of L2, between 1 and 16.
+int group_rows(int rows_per_tile, int64_t K, int elem_bytes, int tiles_m) {
+  const int64_t per_block = (int64_t)rows_per_tile * K * elem_bytes;
+  int gm = (int)((32ll << 20) / (per_block > 0 ? per_block : 1));
+  gm = gm < 1 ? 1 : (gm > 16 ? 16 : gm);
+  return gm < tiles_m ? gm : tiles_m;
+}
+
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle sw) {
@@ -825,6 +845,8 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
     return cudaSuccess;
   }
   args.num_tiles = tiles_m * args.tiles_per_m;
+  args.tiles_m = tiles_m;
+  args.group_m = group_rows(BM * CG, p.K, 1, tiles_m);
   const int max_clusters = sms / CG;
   const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   return launch_cluster(gemm_kernel<MODE, CG>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
@@ -864,6 +886,8 @@ cudaError_t launch_a16t(const GemmProblem& p, int sms, cudaStream_t st, int* tma
     return cudaSuccess;
   }
   args.num_tiles = tiles_m * args.tiles_per_m;
+  args.tiles_m = tiles_m;
+  args.group_m = group_rows(BT, p.K, 2, tiles_m);
   const int grid = args.num_tiles < sms ? args.num_tiles : sms;
   cudaError_t e =
       cudaFuncSetAttribute(gemm_a16t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
