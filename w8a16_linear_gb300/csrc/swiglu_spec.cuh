@@ -84,6 +84,35 @@ __device__ __forceinline__ F2 exp_spec2(F2 t) {
   return res;
 }
 
+// d = 1 + exp_spec(t) on the fast path.  For every binary32 t <= -17 the
+// specification's exp_spec(t) is below 2^-24, so 1 + e rounds to exactly 1:
+// clamping t at -17 leaves d unchanged.  For t in [-17, 88] the specified
+// result q * 2^(n>>1) * 2^(n-(n>>1)) is a normal binary32 number, so both
+// power-of-two multiplications are exact and equal one add of n to the
+// exponent field.  Arguments above 88 are clamped too; they give d >= 2^126,
+// which the guards send to the exact path (h_needs_exact / h_maybe_bad).
+__device__ __forceinline__ F2 dplus1_fast(F2 t) {
+  const float kL2E = __uint_as_float(0x3FB8AA3Bu);
+  const float kLn2Hi = __uint_as_float(0x3F317000u);
+  const float kLn2Lo = __uint_as_float(0x3805FDF4u);
+  const F2 tc{fminf(fmaxf(t.x, -17.0f), 88.0f), fminf(fmaxf(t.y, -17.0f), 88.0f)};
+  const F2 nl = mul2(tc, splat(kL2E));
+  const F2 n{rintf(nl.x), rintf(nl.y)};
+  F2 r = add2(tc, neg(mul2(n, splat(kLn2Hi))));
+  r = add2(r, neg(mul2(n, splat(kLn2Lo))));
+  F2 q = splat(__uint_as_float(0x39500D01u));
+  q = add2(mul2(q, r), splat(__uint_as_float(0x3AB60B61u)));
+  q = add2(mul2(q, r), splat(__uint_as_float(0x3C088889u)));
+  q = add2(mul2(q, r), splat(__uint_as_float(0x3D2AAAABu)));
+  q = add2(mul2(q, r), splat(__uint_as_float(0x3E2AAAABu)));
+  q = add2(mul2(q, r), splat(0.5f));
+  q = add2(mul2(q, r), splat(1.0f));
+  q = add2(mul2(q, r), splat(1.0f));
+  const F2 e{__int_as_float(__float_as_int(q.x) + (__float2int_rn(n.x) << 23)),
+             __int_as_float(__float_as_int(q.y) + (__float2int_rn(n.y) << 23))};
+  return add2(splat(1.0f), e);
+}
+
 __device__ __forceinline__ float rcp_approx(float d) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
@@ -151,11 +180,18 @@ __device__ __forceinline__ bool h_needs_exact(float p, float d, float hf) {
          | ((ah < 7.888609e-31f) & ((ah != 0.0f) | (p != 0.0f)));  // |hf| < 2^-100
 }
 
-// Two elements: gate word and up word each hold a bf16 pair.
+// Two elements: gate word and up word each hold a bf16 pair.  p exact, d the
+// fast form of 1 + exp_spec(-g) (exact except where the guards catch it).
 __device__ __forceinline__ void swiglu_pd(uint32_t gw, uint32_t uw, F2& p, F2& d) {
   const F2 g{bf16_lo(gw), bf16_hi(gw)};
   p = mul2(g, F2{bf16_lo(uw), bf16_hi(uw)});
-  d = add2(splat(1.0f), exp_spec2(neg(g)));
+  d = dplus1_fast(neg(g));
+}
+
+// 1 + exp_spec(-g) exactly as specified (every argument), for the exact path.
+__device__ __forceinline__ F2 swiglu_d_exact(uint32_t gw) {
+  const F2 g{bf16_lo(gw), bf16_hi(gw)};
+  return add2(splat(1.0f), exp_spec2(neg(g)));
 }
 
 __device__ __forceinline__ uint32_t swiglu_fp8_pair(uint32_t gw, uint32_t uw, float s, float rs,
@@ -167,8 +203,9 @@ __device__ __forceinline__ uint32_t swiglu_fp8_pair(uint32_t gw, uint32_t uw, fl
   const bool fx = exact_only | h_needs_exact(p.x, d.x, hf.x) | near_e4m3_midpoint<32>(q.x);
   const bool fy = exact_only | h_needs_exact(p.y, d.y, hf.y) | near_e4m3_midpoint<32>(q.y);
   if (fx | fy) {                       // rare: a rounding decision the fast value cannot settle
-    if (fx) q.x = __fdiv_rn(__fdiv_rn(p.x, d.x), s);
-    if (fy) q.y = __fdiv_rn(__fdiv_rn(p.y, d.y), s);
+    const F2 de = swiglu_d_exact(gw);
+    if (fx) q.x = __fdiv_rn(__fdiv_rn(p.x, de.x), s);
+    if (fy) q.y = __fdiv_rn(__fdiv_rn(p.y, de.y), s);
   }
   return cvt_e4m3x2(q.x, q.y);
 }
@@ -179,8 +216,9 @@ __device__ __forceinline__ uint32_t swiglu_bf16_pair(uint32_t gw, uint32_t uw) {
   F2 h = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
   if (h_needs_exact(p.x, d.x, h.x) | h_needs_exact(p.y, d.y, h.y) | near_bf16_midpoint<8>(h.x) |
       near_bf16_midpoint<8>(h.y)) {
-    if (h_needs_exact(p.x, d.x, h.x) || near_bf16_midpoint<8>(h.x)) h.x = __fdiv_rn(p.x, d.x);
-    if (h_needs_exact(p.y, d.y, h.y) || near_bf16_midpoint<8>(h.y)) h.y = __fdiv_rn(p.y, d.y);
+    const F2 de = swiglu_d_exact(gw);
+    if (h_needs_exact(p.x, d.x, h.x) || near_bf16_midpoint<8>(h.x)) h.x = __fdiv_rn(p.x, de.x);
+    if (h_needs_exact(p.y, d.y, h.y) || near_bf16_midpoint<8>(h.y)) h.y = __fdiv_rn(p.y, de.y);
   }
   return cvt_bf16x2(h.x, h.y);
 }
@@ -225,8 +263,10 @@ __device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const ui
     for (int e = 0; e < 16; ++e) {
       if (maybe & (1u << e)) {
         const float hf = __fmul_rn(pp[e], rcp_approx(dd[e]));
-        if (exact_only || h_needs_exact(pp[e], dd[e], hf) || near_e4m3_midpoint<32>(q[e]))
-          q[e] = __fdiv_rn(__fdiv_rn(pp[e], dd[e]), s);
+        if (exact_only || h_needs_exact(pp[e], dd[e], hf) || near_e4m3_midpoint<32>(q[e])) {
+          const F2 de = swiglu_d_exact(gw[e >> 1]);
+          q[e] = __fdiv_rn(__fdiv_rn(pp[e], (e & 1) ? de.y : de.x), s);
+        }
       }
     }
   }
