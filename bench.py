@@ -6,7 +6,9 @@ One step runs every row of the path through the public C ABI:
 
   step_policy_dispatch(step 3 of 8)                       -> W8A8
   qkv_shared_quant_gemm  Q/K/V, one shared quantization, 3 x 4096x4096
-  fp8_linear_w8a8        out-projection 4096x4096 (quantizes its input)
+  fp8_linear_w8a8        out-projection 4096x4096
+  (the out-projection's and the MLP's fp8_quant_static run on a second
+  stream, overlapped with the Q/K/V GEMM)
   gate_up_swiglu_fp8     gate/up (one shared quantization, 2 x 4096->16384) with
                          SiLU(gate)*up written straight to E4M3 in the GEMM
                          epilogue (same codes as the group GEMM + swiglu_2in_fp8)
@@ -158,6 +160,9 @@ class Block:
         self.h16 = torch.empty((M_TOK, INTER), **bf)
         self.y_down = torch.empty((M_TOK, HID), **bf)
         self.ws = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
+        self.q_out = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
+        self.q_mlp = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
+        self.side = torch.cuda.Stream(device=dev)
 
     def outputs(self):
         return self.y_qkv + [self.y_out, self.y_down]
@@ -174,6 +179,22 @@ class Block:
         sq = [s for _, s in self.w_qkv]
         wgu = [q for q, _ in self.w_gu]
         sgu = [s for _, s in self.w_gu]
+        if mode == W.MODE_A8 and fused:
+            # The out-projection's and the MLP's activation quantizations do
+            # not depend on the Q/K/V GEMM: run them on a second stream while
+            # it occupies the tensor cores, then feed the E4M3 codes in.
+            main = torch.cuda.current_stream()
+            self.side.wait_stream(main)
+            with torch.cuda.stream(self.side):
+                W.fp8_quant_static(x_out, self.s_out, out=self.q_out)
+                W.fp8_quant_static(x_mlp, self.s_mlp, out=self.q_mlp)
+            W.qkv_shared_quant_gemm(W.MODE_A8, x_qkv, self.s_qkv, wq, sq, outs=self.y_qkv, ws=self.ws)
+            main.wait_stream(self.side)
+            W.fp8_linear_w8a8(self.q_out, self.w_out[0], self.s_out, self.w_out[1], out=self.y_out)
+            W.gate_up_swiglu_fp8(self.q_mlp, self.s_mlp, wgu[0], wgu[1], sgu[0], sgu[1], self.s_h,
+                                 out=self.h8)
+            W.fp8_linear_w8a8(self.h8, self.w_down[0], self.s_h, self.w_down[1], out=self.y_down)
+            return 7
         if mode == W.MODE_A8:
             W.qkv_shared_quant_gemm(W.MODE_A8, x_qkv, self.s_qkv, wq, sq, outs=self.y_qkv, ws=self.ws)
             W.fp8_linear_w8a8(x_out, self.w_out[0], self.s_out, self.w_out[1], out=self.y_out, ws=self.ws)
