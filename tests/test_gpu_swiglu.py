@@ -47,6 +47,50 @@ def test_swiglu_all_gate_values(W):
     _bf16_equal(got16, O.swiglu_2in_bf16(g2, u2))
 
 
+@pytest.mark.parametrize("s", [2.0 ** -20, 2.0 ** -22, 2e38])
+def test_swiglu_scales_at_and_outside_the_fast_range(W, s):
+    """|1/s| = 2^20 is the last scale of the fast path; 2^-22 (|1/s| > 2^20)
+    and 2e38 (1/s not normal) send every element to the exact divisions."""
+    g = np.arange(1 << 16, dtype=np.uint16)
+    g = g[_finite(g)]
+    n = (g.size // 16) * 16
+    g = g[:n].reshape(-1, 16)
+    u = synth.activations_bf16(2, g.shape, 1.5)
+    got = host_u8(W.swiglu_2in_fp8(dev_bf16(g), dev_bf16(u), dev_f32(s)))
+    _fp8_equal(got, O.swiglu_2in_fp8(g, u, np.float32(s)))
+
+
+def _rel_to_e4m3_midpoint(q):
+    """Relative distance of binary32 q (normal E4M3 range) to the nearest
+    rounding midpoint of E4M3 (three fraction bits)."""
+    m, e = np.frexp(np.abs(q).astype(np.float64))       # |q| = m * 2^e, m in [0.5, 1)
+    f = m * 16.0                                        # 8..16: the grid step is 1
+    return np.abs(f - np.floor(f) - 0.5) / f
+
+
+def test_swiglu_near_midpoint_cases(W):
+    """Pairs (g, u) whose specified h / s lies within 2^-16 (relative) of an
+    E4M3 rounding midpoint: the fast value cannot settle them alone, so this
+    exercises the bracket and the exact path on the cases that matter."""
+    s = np.float32(0.02)
+    gb = np.arange(1 << 16, dtype=np.uint16)
+    gv = O.bf16_decode(gb)
+    gb = gb[np.isfinite(gv) & (np.abs(gv) <= 16.0) & (np.abs(gv) >= 2.0 ** -12)]
+    ub = synth.activations_bf16(9, (1024,), 3.0)
+    G = np.repeat(gb, ub.size)
+    U = np.tile(ub, gb.size)
+    h = O.swiglu_h(G, U)
+    q = h / s
+    aq = np.abs(q)
+    keep = (aq >= 2.0 ** -6) & (aq <= 400.0) & (_rel_to_e4m3_midpoint(q) < 2.0 ** -16)
+    G, U = G[keep], U[keep]
+    assert G.size >= 512, G.size
+    n = (G.size // 16) * 16
+    G, U = G[:n].reshape(-1, 16), U[:n].reshape(-1, 16)
+    got = host_u8(W.swiglu_2in_fp8(dev_bf16(G), dev_bf16(U), dev_f32(s)))
+    _fp8_equal(got, O.swiglu_2in_fp8(G, U, s))
+
+
 @pytest.mark.parametrize("M,I", [(64, 256), (333, 4096), (1, 16), (7, 16400)])
 def test_swiglu_shapes(W, M, I):
     g = synth.activations_bf16(3, (M, I), 2.0)

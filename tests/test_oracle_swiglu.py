@@ -18,6 +18,18 @@ def test_exp_spec_accuracy_dense_sweep():
     assert (np.abs(e - ref) / ulp)[normal].max() <= 2.0
 
 
+def test_denominator_within_1p5_ulp_on_every_bf16_argument():
+    """fl(1 + exp_spec(t)) against 1 + e^t for every finite bf16 t in [-88, 88]
+    (the arguments the SwiGLU meets): within 1.5 * 2^-24 relative.  The fast
+    FP8 SwiGLU's error budget counts on this figure."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    t = (bits << 16).view(np.float32)
+    t = t[np.isfinite(t) & (np.abs(t) <= 88.0)]
+    d = (np.float32(1.0) + O.exp_spec(t)).astype(np.float64)
+    ref = 1.0 + np.exp(t.astype(np.float64))
+    assert np.max(np.abs(d / ref - 1.0)) <= 1.5 * 2.0 ** -24
+
+
 def test_exp_spec_special_values():
     t = np.array([0.0, -0.0, 88.5, np.inf, -88.5, -np.inf], np.float32)
     e = O.exp_spec(t)

@@ -31,21 +31,23 @@ namespace {
 
 // ------------------------------------------------------------------ quant
 //
-// q = E4M3(fl32(x / s)).  Fast path: f = fl32(x * fl32(1/s)), within 2.5 ulp
-// of fl32(x / s) when s and 1/s are normal (two rounding errors of 2^-24 each
-// on the exact quotient, plus the final half ulp); a window of 4 ulp sends
-// every element whose code could differ to the correctly rounded division.
+// q = E4M3(fl32(x / s)).  Fast value f = fl32(x * fl32(1/s)): two roundings
+// of 2^-24 on the exact quotient against the specification's one, so
+// |f / fl32(x / s) - 1| <= 3 * 2^-24 when s and 1/s are normal (a binary32
+// subnormal f is below every E4M3 rounding boundary, as is the specified
+// value).  The bracket of 2^-21 (swiglu_spec.cuh) settles every pair whose
+// code cannot differ; the rest take the correctly rounded division.
+
+constexpr float kQuantBracketLo = 0.99999952316284180f;   // 1 - 2^-21
+constexpr float kQuantBracketHi = 1.00000047683715820f;   // 1 + 2^-21
 
 __device__ __forceinline__ uint32_t quant_pair(uint32_t w, float s, float r, bool exact_only) {
   const float v0 = bf16_lo(w), v1 = bf16_hi(w);
-  F2 f = mul2(F2{v0, v1}, splat(r));
-  // Activations rarely fall in the E4M3 subnormal range, so the cheap
-  // pre-test (which admits that whole range) keeps the branch rare here.
-  if (exact_only | maybe_near_e4m3_midpoint<4>(f.x) | maybe_near_e4m3_midpoint<4>(f.y)) {
-    if (exact_only || near_e4m3_midpoint<4>(f.x)) f.x = __fdiv_rn(v0, s);
-    if (exact_only || near_e4m3_midpoint<4>(f.y)) f.y = __fdiv_rn(v1, s);
-  }
-  return cvt_e4m3x2(f.x, f.y);
+  bool unsettled;
+  const uint32_t code = e4m3x2_bracket(mul2(F2{v0, v1}, splat(r)), kQuantBracketLo,
+                                       kQuantBracketHi, unsettled);
+  if (exact_only | unsettled) return cvt_e4m3x2(__fdiv_rn(v0, s), __fdiv_rn(v1, s));
+  return code;
 }
 
 __global__ void __launch_bounds__(256, 8) quant_static_kernel(const uint16_t* __restrict__ x,
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(256, 6) swiglu_fp8_kernel(const uint16_t* __re
                                                             uint8_t* __restrict__ out) {
   const float s = __ldg(s_out);
   const float rs = __frcp_rn(s);
-  const bool exact_only = !scale_is_fast(s, rs);
+  const bool exact_only = !swiglu_fp8_scale_is_fast(s, rs);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
     const uint4 ga = ldg16(g + i * 16), gb = ldg16(g + i * 16 + 8);

@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     if constexpr (kGlu) {
       s_out = __ldg(args.s_out);
       rs_out = __frcp_rn(s_out);
-      exact_only = !scale_is_fast(s_out, rs_out);
+      exact_only = !swiglu_fp8_scale_is_fast(s_out, rs_out);
     }
     for (int t = cluster_id; t < args.num_tiles; t += num_clusters) {
       int m0, g, n0;

@@ -90,7 +90,7 @@ __device__ __forceinline__ F2 exp_spec2(F2 t) {
 // result q * 2^(n>>1) * 2^(n-(n>>1)) is a normal binary32 number, so both
 // power-of-two multiplications are exact and equal one add of n to the
 // exponent field.  Arguments above 88 are clamped too; they give d >= 2^126,
-// which the guards send to the exact path (h_needs_exact / h_maybe_bad).
+// which the guard sends to the exact path (h_needs_exact).
 __device__ __forceinline__ F2 dplus1_fast(F2 t) {
   const float kL2E = __uint_as_float(0x3FB8AA3Bu);
   const float kLn2Hi = __uint_as_float(0x3F317000u);
@@ -119,36 +119,31 @@ __device__ __forceinline__ float rcp_approx(float d) {
   return r;
 }
 
-// ---- exactness guards.  A fast result f within a known number of binary32
-// ulps of the specified value v gives the same E4M3 code (bf16 bits) as v
-// unless a rounding midpoint of the narrow format lies between them.  In the
-// normal E4M3 range every midpoint has the low 20 significand bits equal to
-// 0x80000 (bf16: low 16 bits equal to 0x8000), so f needs the exact path only
-// when its low bits are within `W` of that pattern.  In the E4M3 subnormal
-// range (|f| < 2^-6) the midpoints are the odd multiples of 2^-10: there f
-// needs the exact path only when f * 2^9 is within 2^-14 of a half-integer
-// (far more than W binary32 ulps of f at that scale).
-// Cheap pre-test: true near a midpoint of the normal E4M3 range and for every
-// value in the subnormal range (a superset of near_e4m3_midpoint).
-template <int W>
-__device__ __forceinline__ bool maybe_near_e4m3_midpoint(float f) {
-  const uint32_t b = __float_as_uint(f);
-  const uint32_t a = b & 0x7FFFFFFFu;
-  const bool sub = (a != 0u) & (a < 0x3C800000u);                   // 0 < |f| < 2^-6
-  const bool mid = ((b & 0xFFFFFu) + (uint32_t)W - 0x80000u) <= (uint32_t)(2 * W);
-  return sub | mid;
+// ---- exactness guards.
+//
+// E4M3 (bracket test): a fast value f with |f / v - 1| <= E of the specified
+// value v, E < eps - 2^-24, gives the specified code unless a rounding
+// boundary of the saturating round-to-nearest-even conversion lies between
+// f (1 - eps) and f (1 + eps).  Conversion is monotonic, so converting both
+// ends (each rounded to binary32, hence the 2^-24) and comparing the codes
+// settles it: equal codes are the code of every value in between, v
+// included.  This holds in the normal and the subnormal E4M3 range, at
+// saturation, for zeros (sign kept) and NaN.  A pair of elements is settled
+// together (one packed conversion per end).
+__device__ __forceinline__ uint32_t e4m3x2_bracket(F2 f, float lo_factor, float hi_factor,
+                                                   bool& unsettled) {
+  const F2 lo = mul2(f, splat(lo_factor));
+  const F2 hi = mul2(f, splat(hi_factor));
+  const uint32_t clo = cvt_e4m3x2(lo.x, lo.y);
+  const uint32_t chi = cvt_e4m3x2(hi.x, hi.y);
+  unsettled = clo != chi;
+  return chi;
 }
 
-template <int W>
-__device__ __forceinline__ bool near_e4m3_midpoint(float f) {
-  const float a = fabsf(f);
-  const float t = a * 512.0f;                                       // exact scaling
-  const bool near_sub = fabsf((t - floorf(t)) - 0.5f) < 6.103515625e-05f;   // 2^-14
-  const uint32_t b = __float_as_uint(f);
-  const bool mid = ((b & 0xFFFFFu) + (uint32_t)W - 0x80000u) <= (uint32_t)(2 * W);
-  return (a < 0.015625f) ? near_sub : mid;                          // |f| < 2^-6: subnormal E4M3
-}
-
+// bf16 (window test): in the normal range every bf16 rounding midpoint has
+// the low 16 significand bits of the binary32 value equal to 0x8000, so a
+// fast value within W binary32 ulps of the specified one needs the exact path
+// only when its low bits are within W of that pattern.
 template <int W>
 __device__ __forceinline__ bool near_bf16_midpoint(float f) {
   const uint32_t b = __float_as_uint(f);
@@ -166,13 +161,36 @@ __device__ __forceinline__ bool scale_is_fast(float s, float r) {
 
 // ------------------------------------------------------------------ swiglu
 //
-// h = p / d with p = g * u and d = 1 + exp_spec(-g), both exact to the
-// specification.  Fast path: hf = fl32(p * rcp(d)) (rcp: the hardware
-// reciprocal approximation), within a few ulp of fl32(p / d) for d < 2^126;
-// FP8: qf = fl32(hf * fl32(1/s)).  Elements where the fast value is within the
-// guard window of a midpoint, where d >= 2^126 (the reciprocal flushes), or
-// where hf is tiny (binary32 subnormal range) take the correctly rounded
-// divisions.
+// FP8 output.  Fast value, elementwise: p = g * u (exact, as specified),
+// d' = fl(1 + __expf(-g)), q' = fl(fl(p * rcp.approx(d')) * fl(1/s)).
+// Error budget against the specified q = fl(fl(p / d) / s), relative, in
+// units of 2^-24, for gates g >= -8 (t = -g <= 8):
+//   __expf(t): documented within 2 + floor(|1.173 t|) ulp of e^t, at most 11
+//     ulp (22) for 0 < t <= 8; for t <= 0 its share of d = 1 + e is below
+//     2^-23 (2) because e / (1 + e) shrinks faster than the bound grows;
+//     plus the rounding of 1 + e (1)                                      <= 23
+//   the specified d against 1 + e^t (exp_spec checked exhaustively on
+//     every bf16 argument on the host: within 1.5)                       <= 1.5
+//   rcp.approx: documented within 1 ulp                                    <= 2
+//   roundings of p * r, of fl(1/s), of q' and the specification's two      <= 5
+// in all below 32 (2^-19), under the bracket's 2^-18 - 2^-24.  Gates below
+// -8 (and -inf) take the exact path.  A scale with |1/s| > 2^20 (or 1/s not
+// normal) sends every element to the exact path: with |1/s| <= 2^20 a
+// binary32-subnormal h' (absolute error 2^-149, not relative) maps to
+// |q| < 2^-106, code 0 either way, with the same sign.
+//
+// bf16 output.  d is the specification's own (dplus1_fast), hf = fl(p *
+// rcp.approx(d)) within a few ulp of fl(p / d) for d < 2^126; elements where
+// hf is within the window of a bf16 midpoint, where d >= 2^126 (the
+// reciprocal flushes) or where hf is tiny (binary32 subnormal range) take the
+// correctly rounded division.
+
+constexpr float kFp8BracketLo = 0.999996185302734375f;   // 1 - 2^-18
+constexpr float kFp8BracketHi = 1.000003814697265625f;   // 1 + 2^-18
+
+__device__ __forceinline__ bool swiglu_fp8_scale_is_fast(float s, float rs) {
+  return scale_is_fast(s, rs) && fabsf(rs) <= 1048576.0f;            // |1/s| <= 2^20
+}
 
 __device__ __forceinline__ bool h_needs_exact(float p, float d, float hf) {
   const float ah = fabsf(hf);
@@ -194,20 +212,32 @@ __device__ __forceinline__ F2 swiglu_d_exact(uint32_t gw) {
   return add2(splat(1.0f), exp_spec2(neg(g)));
 }
 
+// The specified E4M3 codes of a pair, by correctly rounded divisions.
+__device__ __forceinline__ uint32_t swiglu_fp8_exact_pair(uint32_t gw, uint32_t uw, float s) {
+  const F2 p = mul2(F2{bf16_lo(gw), bf16_hi(gw)}, F2{bf16_lo(uw), bf16_hi(uw)});
+  const F2 d = swiglu_d_exact(gw);
+  return cvt_e4m3x2(__fdiv_rn(__fdiv_rn(p.x, d.x), s), __fdiv_rn(__fdiv_rn(p.y, d.y), s));
+}
+
+// Fast codes of a pair; `unsettled` when the bracket does not settle them or
+// a gate is below -8.
+__device__ __forceinline__ uint32_t swiglu_fp8_fast_pair(uint32_t gw, uint32_t uw, float rs,
+                                                         bool& unsettled) {
+  const F2 g{bf16_lo(gw), bf16_hi(gw)};
+  const F2 p = mul2(g, F2{bf16_lo(uw), bf16_hi(uw)});
+  const F2 d = add2(splat(1.0f), F2{__expf(-g.x), __expf(-g.y)});
+  const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
+  const uint32_t code = e4m3x2_bracket(mul2(hf, splat(rs)), kFp8BracketLo, kFp8BracketHi, unsettled);
+  unsettled |= (g.x < -8.0f) | (g.y < -8.0f);
+  return code;
+}
+
 __device__ __forceinline__ uint32_t swiglu_fp8_pair(uint32_t gw, uint32_t uw, float s, float rs,
                                                     bool exact_only) {
-  F2 p, d;
-  swiglu_pd(gw, uw, p, d);
-  const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
-  F2 q = mul2(hf, splat(rs));
-  const bool fx = exact_only | h_needs_exact(p.x, d.x, hf.x) | near_e4m3_midpoint<32>(q.x);
-  const bool fy = exact_only | h_needs_exact(p.y, d.y, hf.y) | near_e4m3_midpoint<32>(q.y);
-  if (fx | fy) {                       // rare: a rounding decision the fast value cannot settle
-    const F2 de = swiglu_d_exact(gw);
-    if (fx) q.x = __fdiv_rn(__fdiv_rn(p.x, de.x), s);
-    if (fy) q.y = __fdiv_rn(__fdiv_rn(p.y, de.y), s);
-  }
-  return cvt_e4m3x2(q.x, q.y);
+  bool unsettled;
+  const uint32_t code = swiglu_fp8_fast_pair(gw, uw, rs, unsettled);
+  if (exact_only | unsettled) return swiglu_fp8_exact_pair(gw, uw, s);   // rare
+  return code;
 }
 
 __device__ __forceinline__ uint32_t swiglu_bf16_pair(uint32_t gw, uint32_t uw) {
@@ -223,56 +253,30 @@ __device__ __forceinline__ uint32_t swiglu_bf16_pair(uint32_t gw, uint32_t uw) {
   return cvt_bf16x2(h.x, h.y);
 }
 
-// ---- 16 elements at once (the fused gate/up epilogue): the fast values of all
-// 16 are computed straight-line so that independent pairs interleave, a
-// bitmask records the elements whose rounding decision the fast value cannot
-// settle, and a single, rarely taken branch recomputes those exactly.
-// gw/uw: 8 words of two bf16 each.
-
-// Cheap integer form of h_needs_exact for the straight-line pass:
-// d >= 2^126 (or NaN), or |hf| < 2^-100 while p != 0.
-__device__ __forceinline__ bool h_maybe_bad(float p, float d, float hf) {
-  const uint32_t db = __float_as_uint(d);
-  const uint32_t hb = __float_as_uint(hf) & 0x7FFFFFFFu;
-  return (db >= 0x7E800000u) | ((hb < 0x0D800000u) & ((__float_as_uint(p) << 1) != 0u));
-}
-
+// 16 elements at once (the fused gate/up epilogue): the fast codes of all 8
+// pairs are computed straight-line so that independent pairs interleave, a
+// bitmask records the unsettled pairs, and a single, rarely taken branch
+// recomputes those exactly.  gw/uw: 8 words of two bf16 each; codes: 16 E4M3
+// codes, element 0 in the low byte of codes[0].
 __device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const uint32_t (&uw)[8],
                                                float s, float rs, bool exact_only,
                                                uint32_t (&codes)[4]) {
-  float q[16], pp[16], dd[16];
-  uint32_t maybe = 0;
+  uint32_t c[8];
+  uint32_t bad = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    F2 p, d;
-    swiglu_pd(gw[j], uw[j], p, d);
-    const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
-    const F2 qf = mul2(hf, splat(rs));
-    q[2 * j] = qf.x;
-    q[2 * j + 1] = qf.y;
-    pp[2 * j] = p.x;
-    pp[2 * j + 1] = p.y;
-    dd[2 * j] = d.x;
-    dd[2 * j + 1] = d.y;
-    maybe |= (uint32_t)(h_maybe_bad(p.x, d.x, hf.x) | maybe_near_e4m3_midpoint<32>(qf.x)) << (2 * j);
-    maybe |= (uint32_t)(h_maybe_bad(p.y, d.y, hf.y) | maybe_near_e4m3_midpoint<32>(qf.y)) << (2 * j + 1);
+    bool unsettled;
+    c[j] = swiglu_fp8_fast_pair(gw[j], uw[j], rs, unsettled);
+    bad |= (uint32_t)unsettled << j;
   }
-  if (exact_only) maybe = 0xFFFFu;
-  if (maybe) {                         // the precise tests, then the rare exact divisions
+  if (exact_only) bad = 0xFFu;
+  if (bad) {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      if (maybe & (1u << e)) {
-        const float hf = __fmul_rn(pp[e], rcp_approx(dd[e]));
-        if (exact_only || h_needs_exact(pp[e], dd[e], hf) || near_e4m3_midpoint<32>(q[e])) {
-          const F2 de = swiglu_d_exact(gw[e >> 1]);
-          q[e] = __fdiv_rn(__fdiv_rn(pp[e], (e & 1) ? de.y : de.x), s);
-        }
-      }
-    }
+    for (int j = 0; j < 8; ++j)
+      if (bad & (1u << j)) c[j] = swiglu_fp8_exact_pair(gw[j], uw[j], s);
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    codes[j] = cvt_e4m3x2(q[4 * j], q[4 * j + 1]) | (cvt_e4m3x2(q[4 * j + 2], q[4 * j + 3]) << 16);
+  for (int j = 0; j < 4; ++j) codes[j] = c[2 * j] | (c[2 * j + 1] << 16);
 }
 
 }  // namespace w8
