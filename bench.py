@@ -574,7 +574,7 @@ def main():
             "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "intermediate": INTER,
                        "policy_step": f"{POLICY_STEP} of {POLICY_STEPS} (W8A8)",
                        "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "tensor", "kernel": "gemm_kernel<W8A8, CTA pair> (the block's 4 launches)",
+            "roofline": {"bound": "tensor", "kernel": "gemm_kernel<W8A8|GLU, CTA pair> (the block's 4 GEMM launches: QKV group, out-proj, gate/up+SwiGLU, down)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                          "frac": achieved / fp8_peak, "traffic": None,
                          "peak_note": f"{peaks['source']} bf16 burst x 2 (nominal FP8/BF16 ratio)"},
