@@ -167,6 +167,16 @@ class Block:
     def outputs(self):
         return self.y_qkv + [self.y_out, self.y_down]
 
+    def gemm_launches(self, W, q_qkv, q_out, q_mlp):
+        """The A8 block's four GEMM launches alone on E4M3 activations: Q/K/V
+        group, out-projection, fused gate/up + SwiGLU, down projection."""
+        W.fp8_linear_w8a8_group(q_qkv, self.s_qkv, [q for q, _ in self.w_qkv], [s for _, s in self.w_qkv],
+                                outs=self.y_qkv)
+        W.fp8_linear_w8a8_group(q_out, self.s_out, [self.w_out[0]], [self.w_out[1]], outs=[self.y_out])
+        W.gate_up_swiglu_fp8(q_mlp, self.s_mlp, self.w_gu[0][0], self.w_gu[1][0], self.w_gu[0][1],
+                             self.w_gu[1][1], self.s_h, out=self.h8)
+        W.fp8_linear_w8a8_group(self.h8, self.s_h, [self.w_down[0]], [self.w_down[1]], outs=[self.y_down])
+
     def step(self, W, policy, step_index, num_steps, x_qkv=None, x_out=None, x_mlp=None, fused=True):
         """One block pass in the precision the policy selects for this step;
         returns the number of kernel launches.  `fused` selects the fused
@@ -276,15 +286,7 @@ def run_ours(args, rank, world, dev):
     q_out = W.fp8_quant_static(blk.x_out, blk.s_out)
     q_mlp = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
 
-    def gemms():
-        W.fp8_linear_w8a8_group(q_qkv, blk.s_qkv, [q for q, _ in blk.w_qkv], [s for _, s in blk.w_qkv],
-                                outs=blk.y_qkv)
-        W.fp8_linear_w8a8_group(q_out, blk.s_out, [blk.w_out[0]], [blk.w_out[1]], outs=[blk.y_out])
-        W.gate_up_swiglu_fp8(q_mlp, blk.s_mlp, blk.w_gu[0][0], blk.w_gu[1][0], blk.w_gu[0][1],
-                             blk.w_gu[1][1], blk.s_h, out=blk.h8)
-        W.fp8_linear_w8a8_group(blk.h8, blk.s_h, [blk.w_down[0]], [blk.w_down[1]], outs=[blk.y_down])
-
-    gemm_ms = _time(gemms, flush, stream, args.steps)
+    gemm_ms = _time(lambda: blk.gemm_launches(W, q_qkv, q_out, q_mlp), flush, stream, args.steps)
     del q_qkv, q_out, q_mlp
 
     # ---- end to end through the public API with host buffers
@@ -465,7 +467,14 @@ def run_case(args):
     ss = [torch.tensor([0.02 * 4 / 448], device=dev) for _ in range(3)]
     ys = [torch.empty((M, HID), dtype=torch.bfloat16, device=dev) for _ in range(3)]
     qx = torch.empty((M, HID), dtype=torch.uint8, device=dev)
-    if args.case == "qkv8k":
+    if args.case == "block_gemms":
+        # the bench's four GEMM launches of one A8 block step at M=20670
+        # (for the DRAM-traffic capture of the dominant kernel)
+        blk = Block(dev)
+        qa = [W.fp8_quant_static(t, sc) for t, sc in ((blk.x_qkv, blk.s_qkv), (blk.x_out, blk.s_out),
+                                                         (blk.x_mlp, blk.s_mlp))]
+        fn = lambda: blk.gemm_launches(W, *qa)  # noqa: E731
+    elif args.case == "qkv8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A8, x, s, qs, ss, outs=ys, ws=qx)  # noqa: E731
     elif args.case == "w8a16_8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, qs, ss, outs=ys)  # noqa: E731
@@ -528,7 +537,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="run a small profiling case (qkv8k, w8a16_8k, glu8k, swiglu8k) instead of the bench")
+                    help="run a profiling case (qkv8k, w8a16_8k, glu8k, swiglu8k, block_gemms) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.case:
