@@ -224,6 +224,13 @@ class Block:
         return 5
 
 
+# DRAM bytes (read + write) of the A8 block step's four GEMM launches at
+# M=20670 from one ncu capture of the current gemm_kernel build (2961.0 MB read
+# + 1110.8 MB written; algorithmic 861 + 1185 MB).  Re-capture, or set to None,
+# whenever gemm_kernel changes.
+GEMM_TRAFFIC_BYTES = 4071.8e6
+
+
 def flush_l2(buf):
     buf.add_(1.0)
 
@@ -585,7 +592,9 @@ def main():
                        "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "kernel": "gemm_kernel<W8A8|GLU, CTA pair> (the block's 4 GEMM launches: QKV group, out-proj, gate/up+SwiGLU, down)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                         "frac": achieved / fp8_peak, "traffic": None,
+                         "frac": achieved / fp8_peak, "traffic": GEMM_TRAFFIC_BYTES,
+                         "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of the four launches "
+                                         "(one ncu capture at M=20670, caches flushed per launch)",
                          "peak_note": f"{peaks['source']} bf16 burst x 2 (nominal FP8/BF16 ratio)"},
             "pct_of_5pf_fp8": value / 5000.0,
             "cpu_baseline": cpu,
