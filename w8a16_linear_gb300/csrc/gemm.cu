@@ -491,38 +491,39 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
 // there by the transform warps with tcgen05.st (it never passes through
 // shared memory); the activation tile is the B operand, staged by TMA into a
 // 128-byte-swizzled K-major shared-memory buffer.  A tile is 128 weight rows
-// x 192 tokens (one M = 128, N = 192 MMA per 16 K-values).  D has the weight
-// rows across the TMEM lanes and the tokens across columns; two accumulators
-// let the epilogue of one tile overlap the MMAs of the next.  The epilogue
-// turns each 32-token x 32-feature block into row-major y through a small
-// staging buffer and a TMA store.
+// x 320 tokens, computed as two N = 160 MMAs that share each dequantized
+// weight stage, so every weight element is converted once per 320 tokens.
+// D has the weight rows across the TMEM lanes and the tokens across columns;
+// the epilogue turns each 32-token x 32-feature block into row-major y
+// through a small staging buffer and a TMA store.
 //
-// TMEM columns: D0 0-191, D1 192-383, A stages 384 + 32 s (64 K-values of
-// 128 rows, two bf16 per column).
+// TMEM columns: D (tokens 0-159) 0-159, D (tokens 160-319) 160-319, A stages
+// 320 + 32 s (64 K-values of 128 rows, two bf16 per column).
 namespace a16t {
-constexpr int BT = 192;                      // tokens per tile (MMA N)
+constexpr int NH = 160;                      // tokens per MMA (MMA N)
+constexpr int BT = 2 * NH;                   // tokens per tile
 constexpr int BW = 128;                      // weight rows per tile (MMA M)
 constexpr int BK = 64;                       // K per stage
 constexpr int S = 4;                         // stages
-constexpr int kXBytes = BT * 128;            // bf16 activation rows, 128-byte rows
+constexpr int kXHalf = NH * 128;             // bf16 activation rows of one MMA, 128-byte rows
+constexpr int kXBytes = 2 * kXHalf;
 constexpr int kRawBytes = BW * 64;           // raw E4M3 weight rows
 constexpr int kEpiBuf = 32 * 64;             // 32 tokens x 32 features bf16
-constexpr int kEpiWarps = 8;                 // 2 per TMEM lane quadrant, 3 token chunks each
+constexpr int kEpiWarps = 8;                 // 2 per TMEM lane quadrant, 6 token chunks each
 constexpr int kOffX = 0;
 constexpr int kOffRaw = kOffX + S * kXBytes;
 constexpr int kOffEpi = kOffRaw + S * kRawBytes;
 constexpr int kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
-constexpr int kNumBars = 3 * S + 5;          // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
+constexpr int kNumBars = 3 * S + 3;          // full[S], empty[S], ready[S], tfull, tempty, drain
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kAlloc = kOffAbort + 4 + 1024;
 constexpr int kTransformWarps = 8;           // 2 per TMEM lane quadrant, 32 K-values each
 constexpr int kThreads = (2 + kEpiWarps + kTransformWarps) * 32;
-constexpr uint32_t kTmemA = 2 * BT;          // first A-stage column (after two accumulators)
-constexpr uint32_t kIdesc = make_idesc(1, 1, BW, BT);
+constexpr uint32_t kTmemA = 2 * NH;          // first A-stage column
+constexpr uint32_t kIdesc = make_idesc(1, 1, BW, NH);
 static_assert(kTmemA + S * 32 <= kTmemCols, "TMEM budget");
 static_assert(kAlloc <= 232448, "shared memory budget");
-static_assert(BT % 64 == 0 && BT <= 256, "MMA N and the epilogue split");
 }  // namespace a16t
 
 __global__ void __launch_bounds__(a16t::kThreads, 1)
@@ -536,9 +537,9 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
   auto full_bar = [&](int st) { return bar0 + 8u * st; };
   auto empty_bar = [&](int st) { return bar0 + 8u * (S + st); };
   auto ready_bar = [&](int st) { return bar0 + 8u * (2 * S + st); };
-  auto tfull_bar = [&](int acc) { return bar0 + 8u * (3 * S + acc); };
-  auto tempty_bar = [&](int acc) { return bar0 + 8u * (3 * S + 2 + acc); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+  const uint32_t tfull_bar = bar0 + 8u * (3 * S);
+  const uint32_t tempty_bar = bar0 + 8u * (3 * S + 1);
+  const uint32_t drain_bar = bar0 + 8u * (3 * S + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
   const int warp = threadIdx.x >> 5;
@@ -550,10 +551,8 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
       mbar_init(empty_bar(st), 1);
       mbar_init(ready_bar(st), kTransformWarps);
     }
-    for (int acc = 0; acc < 2; ++acc) {
-      mbar_init(tfull_bar(acc), 1);
-      mbar_init(tempty_bar(acc), kEpiWarps);
-    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, kEpiWarps);
     mbar_init(drain_bar, 1);
     *abort = 0;
     fence_mbar_init();
@@ -588,7 +587,9 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(st), kXBytes + kRawBytes);
-          tma_load_2d(sbase + kOffX + st * kXBytes, &maps.a, full_bar(st), kb * BK, m0);
+          const uint32_t xd = sbase + kOffX + st * kXBytes;
+          tma_load_2d(xd, &maps.a, full_bar(st), kb * BK, m0);
+          tma_load_2d(xd + kXHalf, &maps.a, full_bar(st), kb * BK, m0 + NH);
           tma_load_2d(sbase + kOffRaw + st * kRawBytes, map_b(maps, g), full_bar(st), kb * BK, n0);
           ++issued;
           if (++st == S) {
@@ -607,16 +608,15 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int st = 0, acc = 0;
+      int st = 0;
       uint32_t ph = 0, acc_ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
-        if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1, abort, kWaitLimitNs)) {
+        if (!mbar_wait(tempty_bar, acc_ph ^ 1, abort, kWaitLimitNs)) {
           record_timeout(abort);
           break;
         }
         tc_fence_after();
-        const uint32_t d_col = tmem_base + (uint32_t)(acc * BT);
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(ready_bar(st), ph, abort, kWaitLimitNs)) {
             record_timeout(abort);
@@ -627,9 +627,12 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
           const uint32_t x_addr = sbase + kOffX + st * kXBytes;
           const uint32_t a_col = tmem_base + kTmemA + (uint32_t)(st * 32);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // K = 16 per MMA: 8 TMEM columns, 32 smem bytes
-            mma_f16_tmem_a(d_col, a_col + 8 * k, sw128_kmajor_desc(x_addr + 32 * k), kIdesc,
-                           (kb | k) != 0);
+          for (int k = 0; k < 4; ++k) {  // K = 16 per MMA: 8 TMEM columns, 32 smem bytes
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              mma_f16_tmem_a(tmem_base + (uint32_t)(h * NH), a_col + 8 * k,
+                             sw128_kmajor_desc(x_addr + h * kXHalf + 32 * k), kIdesc, (kb | k) != 0);
+          }
           mma_commit(empty_bar(st));
           if (++st == S) {
             st = 0;
@@ -637,11 +640,8 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
-        if (++acc == 2) {
-          acc = 0;
-          acc_ph ^= 1;
-        }
+        mma_commit(tfull_bar);
+        acc_ph ^= 1;
       }
       mma_commit(drain_bar);
       volatile int never = 0;
@@ -649,32 +649,31 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
     }
   } else if (warp < 2 + kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
-    constexpr int kChunks = BT / 64;  // 32-token chunks per epilogue warp
     const int q = warp & 3;  // TMEM lane quadrant: weight rows (features) q*32 .. q*32+31
-    const int eh = (warp - 2) >> 2;  // which half of the tile's tokens
+    const int eh = (warp - 2) >> 2;  // which half of the tile's 384 tokens
     uint8_t* bufp = smem + kOffEpi + (warp - 2) * 2 * kEpiBuf;
     const uint32_t bufs = sbase + kOffEpi + (uint32_t)((warp - 2) * 2 * kEpiBuf);
-    int nbuf = 0, acc = 0;
+    int nbuf = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < args.num_tiles; t += gridDim.x) {
       int m0, g, n0;
       decode_tile(args, t, BT, BW, m0, g, n0);
-      if (!mbar_wait_warp(tfull_bar(acc), acc_ph, abort, kWaitLimitNs)) {
+      if (!mbar_wait_warp(tfull_bar, acc_ph, abort, kWaitLimitNs)) {
         if (lane == 0) record_timeout(abort);
         break;
       }
       tc_fence_after();
       const int f0 = n0 + q * 32;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c = eh * kChunks; c < (eh + 1) * kChunks; ++c) {
+      for (int c = eh * (NH / 32); c < (eh + 1) * (NH / 32); ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c * 32, r);  // feature f0+lane, tokens m0+c*32 .. +31
         tmem_ld_wait();
-        if (c == (eh + 1) * kChunks - 1) {
+        if (c == (eh + 1) * (NH / 32) - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          if (lane == 0) mbar_arrive(tempty_bar);
         }
         const int tok0 = m0 + c * 32;
         if (tok0 >= args.M || f0 >= args.N[g]) continue;
@@ -695,10 +694,7 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
         }
         nbuf ^= 1;
       }
-      if (++acc == 2) {
-        acc = 0;
-        acc_ph ^= 1;
-      }
+      acc_ph ^= 1;
     }
     if (lane == 0) tma_store_wait_all();
   } else {
@@ -872,7 +868,7 @@ cudaError_t launch_a16t(const GemmProblem& p, int sms, cudaStream_t st, int* tma
   args.K = (int)p.K;
   args.num_kb = (int)((p.K + BK - 1) / BK);
   const int tiles_m = (int)((p.M + BT - 1) / BT);
-  bool ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, p.K, p.M, p.K * 2, 64, BT,
+  bool ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, p.K, p.M, p.K * 2, 64, NH,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   for (int g = 0; g < p.G; ++g) {
     args.N[g] = (int)p.N[g];
