@@ -58,10 +58,11 @@ typedef enum {
   W8_ERR_POLICY = 7,   /* step policy refused (schema, window, step range) */
   W8_ERR_TIMEOUT = 8,  /* a kernel's bounded pipeline wait expired */
   W8_ERR_CUDA = 9,     /* a CUDA runtime/driver call failed */
-  W8_ERR_SCALE = 10    /* projections of a sharing group carry different input scales */
+  W8_ERR_SCALE = 10,   /* projections of a sharing group carry different input scales */
+  W8_ERR_PARAM = 11    /* a scalar parameter is out of its range (not finite, limit <= 0) */
 } w8_status;
 
-typedef enum { W8_DTYPE_BF16 = 0, W8_DTYPE_E4M3 = 1 } w8_dtype;
+typedef enum { W8_DTYPE_BF16 = 0, W8_DTYPE_E4M3 = 1, W8_DTYPE_F16 = 2 } w8_dtype;
 
 /* Activation precision of one denoising step ([P3] Behavior). */
 typedef enum { W8_MODE_A8 = 0, W8_MODE_A16 = 1 } w8_mode;
@@ -244,6 +245,39 @@ w8_status swiglu_2in_fp8(const uint16_t* gate, const uint16_t* up, int64_t M, in
  * which the FP8 output stands down ([P4] Denoising-step activation precision). */
 w8_status swiglu_2in_bf16(const uint16_t* gate, const uint16_t* up, int64_t M, int64_t I,
                           uint16_t* out, void* stream);
+
+/* Options of the two-input SwiGLU ([P4] Test Coverage: swiglu_limit,
+ * swiglu_alpha + swiglu_beta).  The pages name the options and no formula; the
+ * reading is the clamped, shifted SwiGLU of the public gpt-oss MLP:
+ *   g = min(g, limit), u = clamp(u, -limit, limit)   (if has_limit)
+ *   h = fl32( fl32(g * fl32(u + beta)) / fl32(1 + exp_spec(-fl32(alpha * g))) )
+ * with the addition of beta skipped when beta == 0.  {0, 0, 1, 0} is the
+ * plain SwiGLU of swiglu_2in_fp8 / swiglu_2in_bf16, bit for bit. */
+typedef struct {
+  int32_t has_limit; /* nonzero: apply `limit` */
+  float limit;       /* finite, > 0 when has_limit */
+  float alpha;       /* finite; 1 = plain SiLU */
+  float beta;        /* finite; 0 = none */
+} w8_swiglu_params;
+
+/*
+ * swiglu_2in_ex_fp8 — the SwiGLU with options and bf16 or binary16 inputs
+ * ([P4] Test Coverage: BF16 / FP16 inputs, swiglu_limit, swiglu_alpha +
+ * swiglu_beta, FP8 output), written as E4M3_satRNE(fl32(h / s_out)).
+ *   gate, up   [M, I] of in_dtype (W8_DTYPE_BF16 or W8_DTYPE_F16), device;
+ *   prm        host struct, read during the call only;
+ *   s_out      device float scalar;  out E4M3 [M, I], device.
+ * Errors: NULL, SHAPE (I%16), ALIGN, DTYPE, PARAM, ARCH, CUDA.
+ */
+w8_status swiglu_2in_ex_fp8(const void* gate, const void* up, int32_t in_dtype, int64_t M, int64_t I,
+                            const w8_swiglu_params* prm, const float* s_out, uint8_t* out,
+                            void* stream);
+
+/* swiglu_2in_ex_16 — as swiglu_2in_ex_fp8 with a 16-bit output in the input's
+ * format (bf16_RNE(h) or binary16_RNE(h), overflow to infinity): the
+ * 16-bit-step form. */
+w8_status swiglu_2in_ex_16(const void* gate, const void* up, int32_t in_dtype, int64_t M, int64_t I,
+                           const w8_swiglu_params* prm, void* out, void* stream);
 
 /*
  * step_policy_dispatch — host-only, pure function of (policy, step, num_steps).

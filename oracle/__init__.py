@@ -30,17 +30,20 @@ of numpy float32 operations (no fused multiply-add anywhere).
 
 from .e4m3 import (E4M3_MAX, e4m3_decode, e4m3_encode, e4m3_all_values)
 from .bf16 import bf16_decode, bf16_round
+from .fp16 import fp16_decode, fp16_round
 from .linear import (quant_static, linear_w8a8, linear_w8a16,
                      dequant_weight_bf16, requant_onto_max_scale,
                      qkv_shared_quant_gemm)
-from .swiglu import exp_spec, swiglu_2in_fp8, swiglu_2in_bf16, swiglu_h
+from .swiglu import (exp_spec, swiglu_2in_fp8, swiglu_2in_bf16, swiglu_h, swiglu_h_ex,
+                     swiglu_2in_ex_fp8, swiglu_2in_ex_16)
 from .policy import StepPolicy, PolicyError, step_mode, parse_policy, A8, A16
 
 __all__ = [
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_all_values",
-    "bf16_decode", "bf16_round",
+    "bf16_decode", "bf16_round", "fp16_decode", "fp16_round",
     "quant_static", "linear_w8a8", "linear_w8a16", "dequant_weight_bf16",
     "requant_onto_max_scale", "qkv_shared_quant_gemm",
-    "exp_spec", "swiglu_2in_fp8", "swiglu_2in_bf16", "swiglu_h",
+    "exp_spec", "swiglu_2in_fp8", "swiglu_2in_bf16", "swiglu_h", "swiglu_h_ex",
+    "swiglu_2in_ex_fp8", "swiglu_2in_ex_16",
     "StepPolicy", "PolicyError", "step_mode", "parse_policy", "A8", "A16",
 ]

@@ -33,6 +33,24 @@ operation a separately rounded binary32 multiply or add (no FMA):
   powers of two, arithmetic shift).
 
 NaN inputs are outside the specification (``p`` is NaN and so is ``h``).
+
+Variants ([P4] *Test Coverage*: the op is tested "for BF16 / FP16 /
+swiglu_limit / swiglu_alpha+swiglu_beta / FP8 output").  The pages name the
+options and no formula.  Reading (the plainest one the names support, the
+clamped and shifted SwiGLU of the public gpt-oss MLP):
+
+* FP16 inputs: ``g``, ``u`` are binary16, widened exactly; the 16-bit output
+  is binary16 as well.
+* ``swiglu_limit = L``: ``g = min(g, L)``, ``u = clamp(u, -L, L)`` before
+  anything else (a NaN stays NaN).
+* ``swiglu_alpha = a``: the sigmoid's argument is ``t = fl32(a * g)``.
+* ``swiglu_beta = b``: ``u`` becomes ``fl32(u + b)``; the addition is
+  omitted when ``b == 0``, so that ``-0`` keeps its sign and the defaults
+  reproduce the base op bit for bit.
+
+Then ``p = fl32(g * u)``, ``e = exp_spec(-t)``, ``h = fl32(p / fl32(1 + e))``
+as above.  With ``a = 1``, ``b = 0`` and no limit, ``t = g`` and ``p`` is
+the exact product, i.e. the base specification.
 """
 
 import math
@@ -41,6 +59,7 @@ import numpy as np
 
 from .e4m3 import e4m3_encode
 from .bf16 import bf16_decode, bf16_round
+from .fp16 import fp16_decode, fp16_round
 
 
 def _bits_to_f32(u):
@@ -99,3 +118,41 @@ def swiglu_2in_fp8(g_bits, u_bits, s_out):
 def swiglu_2in_bf16(g_bits, u_bits):
     """bf16 output, used when a 16-bit step stands the FP8 output down."""
     return bf16_round(swiglu_h(g_bits, u_bits))
+
+
+def _decode16(bits, in_dtype):
+    if in_dtype == "bf16":
+        return bf16_decode(bits)
+    if in_dtype == "fp16":
+        return fp16_decode(bits)
+    raise ValueError(in_dtype)
+
+
+def swiglu_h_ex(g_bits, u_bits, in_dtype="bf16", limit=None, alpha=1.0, beta=0.0):
+    """``h`` of the variant specification (module doc): clamp, then
+    ``fl32(g * (u + b)) / fl32(1 + exp_spec(-fl32(a * g)))``."""
+    g = _decode16(g_bits, in_dtype)
+    u = _decode16(u_bits, in_dtype)
+    if limit is not None:
+        lim = np.float32(limit)
+        g = np.where(g > lim, lim, g).astype(np.float32)
+        u = np.where(u > lim, lim, np.where(u < -lim, -lim, u)).astype(np.float32)
+    t = np.float32(alpha) * g
+    v = u if beta == 0 else u + np.float32(beta)
+    p = g * v
+    d = np.float32(1) + exp_spec(-t)
+    h = p / d
+    assert h.dtype == np.float32
+    return h
+
+
+def swiglu_2in_ex_fp8(g_bits, u_bits, s_out, in_dtype="bf16", limit=None, alpha=1.0, beta=0.0):
+    """Variant with FP8 output: ``E4M3_satRNE(fl32(h / s_out))``."""
+    h = swiglu_h_ex(g_bits, u_bits, in_dtype, limit, alpha, beta)
+    return e4m3_encode(h / np.float32(s_out))
+
+
+def swiglu_2in_ex_16(g_bits, u_bits, in_dtype="bf16", limit=None, alpha=1.0, beta=0.0):
+    """Variant with 16-bit output in the input's format (bf16 or binary16)."""
+    h = swiglu_h_ex(g_bits, u_bits, in_dtype, limit, alpha, beta)
+    return bf16_round(h) if in_dtype == "bf16" else fp16_round(h)

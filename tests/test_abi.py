@@ -35,7 +35,7 @@ def test_header_symbols_exported(L):
     for n in names:
         assert hasattr(L, n), n
         assert n in binding.SIGNATURES, n
-    assert L.w8_abi_version() == 1
+    assert L.w8_abi_version() == 2
 
 
 def test_policy_matches_oracle_everywhere(L):
@@ -109,3 +109,28 @@ def test_zero_rows_is_a_noop(L):
     assert L.qkv_shared_quant_gemm(0, p16, 0, 16, p16, 3, arr, ns, arr, arr, None, None) == 0
     assert L.swiglu_2in_fp8(p16, p16, 0, 16, p16, p16, None) == 0
     assert L.swiglu_2in_bf16(p16, p16, 0, 16, p16, None) == 0
+
+
+def test_swiglu_variant_validation_before_any_cuda_call(L):
+    from w8a16_linear_gb300 import binding as b
+    p16 = _u(0x10000)
+    ok = b.SwigluParams(1, 7.0, 1.702, 1.0)
+    ref = ctypes.byref
+    # shape, NULL, alignment as the plain SwiGLU
+    assert L.swiglu_2in_ex_fp8(p16, p16, 0, 4, 24, ref(ok), p16, p16, None) == 2
+    assert L.swiglu_2in_ex_fp8(p16, p16, 0, 4, 16, ref(ok), None, p16, None) == 1
+    assert L.swiglu_2in_ex_16(p16, _u(0x10004), 0, 4, 16, ref(ok), p16, None) == 3
+    # input dtype: bf16 (0) or f16 (2) only
+    assert L.swiglu_2in_ex_16(p16, p16, 1, 4, 16, ref(ok), p16, None) == 5
+    # parameters
+    assert L.swiglu_2in_ex_16(p16, p16, 0, 4, 16, None, p16, None) == 1
+    for bad in (b.SwigluParams(1, 0.0, 1.0, 0.0), b.SwigluParams(1, -1.0, 1.0, 0.0),
+                b.SwigluParams(1, float("inf"), 1.0, 0.0), b.SwigluParams(0, 0.0, float("nan"), 0.0),
+                b.SwigluParams(0, 0.0, 1.0, float("inf"))):
+        assert L.swiglu_2in_ex_fp8(p16, p16, 2, 4, 16, ref(bad), p16, p16, None) == 11
+    assert b"swiglu_2in_ex_fp8" in L.w8_last_error()
+    # a limit that is not applied is not checked
+    assert L.swiglu_2in_ex_16(p16, p16, 2, 0, 16, ref(b.SwigluParams(0, -5.0, 1.0, 0.0)), p16, None) == 0
+    # zero rows: no launch
+    assert L.swiglu_2in_ex_fp8(p16, p16, 0, 0, 16, ref(ok), p16, p16, None) == 0
+    assert L.swiglu_2in_ex_16(p16, p16, 2, 0, 16, ref(ok), p16, None) == 0

@@ -103,3 +103,26 @@ def test_bf16_decode_exact():
     bits = np.arange(1 << 16, dtype=np.uint16)
     ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
     assert np.array_equal(O.bf16_decode(bits), ref, equal_nan=True)
+
+
+def test_fp16_decode_matches_numpy():
+    """Every binary16 pattern decodes to numpy's own widening (a library
+    routine independent of the oracle's field arithmetic)."""
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    assert np.array_equal(O.fp16_decode(bits), ref, equal_nan=True)
+
+
+def test_fp16_round_matches_numpy_and_format_edges():
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal(300_000) * 10.0 ** rng.integers(-9, 6, 300_000)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        ref = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(O.fp16_round(v), ref)
+    # format edges written from the definition
+    edges = {65504.0: 0x7BFF, 65519.0: 0x7BFF, 65520.0: 0x7C00, -1e9: 0xFC00,
+             2.0 ** -24: 0x0001, 2.0 ** -25: 0x0000, 3 * 2.0 ** -26: 0x0001, 3 * 2.0 ** -25: 0x0002,
+             2.0 ** -14: 0x0400, -0.0: 0x8000, 1.0 + 2.0 ** -11: 0x3C00, 1.0 + 3 * 2.0 ** -11: 0x3C02}
+    for val, code in edges.items():
+        assert int(O.fp16_round(np.float64(val))) == code, (val, code)
+    assert int(O.fp16_round(np.float32(np.inf))) == 0x7C00

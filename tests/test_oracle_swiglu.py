@@ -3,6 +3,7 @@ float64 exp, the activation against a float64 SiLU(g)*u, and the special
 cases that reduce to closed forms."""
 
 import numpy as np
+import pytest
 import torch
 
 import oracle as O
@@ -93,3 +94,71 @@ def test_swiglu_bf16_output_is_rounded_h():
     assert np.array_equal(O.swiglu_2in_bf16(g, u), O.bf16_round(O.swiglu_h(g, u)))
     ref = torch.from_numpy(O.swiglu_h(g, u)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(O.swiglu_2in_bf16(g, u), ref)
+
+
+# ---------------------------------------------------------------- variants
+
+def _bits_with_specials(seed, n, scale):
+    rng = np.random.default_rng(seed)
+    v = (rng.standard_normal(n) * scale).astype(np.float32)
+    v[:8] = [0.0, -0.0, np.inf, -np.inf, 1e30, -1e30, 7.0, -7.0]
+    return v
+
+
+def test_variant_defaults_reduce_to_the_base_specification():
+    g = O.bf16_round(_bits_with_specials(1, 20000, 4.0))
+    u = O.bf16_round(_bits_with_specials(2, 20000, 2.0))
+    a, b = O.swiglu_h_ex(g, u), O.swiglu_h(g, u)
+    assert np.array_equal(a.view(np.uint32)[~np.isnan(a)], b.view(np.uint32)[~np.isnan(b)])
+    assert np.array_equal(np.isnan(a), np.isnan(b))
+
+
+@pytest.mark.parametrize("in_dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("limit,alpha,beta", [(7.0, 1.702, 1.0), (None, 1.702, 0.0), (3.0, 1.0, 0.5),
+                                              (None, 0.75, -1.0)])
+def test_variant_against_float64_formula(in_dtype, limit, alpha, beta):
+    """h against g * sigmoid(alpha g) * (u + beta) in float64 with the clamps
+    written independently: relative error below 2^-19 wherever |h| is a
+    normal binary32 number (argument rounding of alpha*g at |alpha g| <= 16,
+    four roundings, the exponential's own 1.5 ulp)."""
+    rng = np.random.default_rng(3)
+    gv = (rng.standard_normal(50000) * 3.0).astype(np.float32)
+    uv = (rng.standard_normal(50000) * 3.0).astype(np.float32)
+    gv, uv = np.clip(gv, -9, 9), np.clip(uv, -9, 9)
+    enc = O.bf16_round if in_dtype == "bf16" else O.fp16_round
+    dec = O.bf16_decode if in_dtype == "bf16" else O.fp16_decode
+    g, u = enc(gv), enc(uv)
+    h = O.swiglu_h_ex(g, u, in_dtype, limit, alpha, beta).astype(np.float64)
+    g64, u64 = dec(g).astype(np.float64), dec(u).astype(np.float64)
+    if limit is not None:
+        g64 = np.minimum(g64, limit)
+        u64 = np.clip(u64, -limit, limit)
+    ref = g64 * (u64 + beta) / (1.0 + np.exp(-alpha * g64))
+    ok = np.abs(ref) > 1e-30
+    assert np.max(np.abs(h[ok] / ref[ok] - 1.0)) < 2.0 ** -19
+
+
+def test_variant_limit_closed_forms():
+    """With a limit L every gate above L acts as L (also +inf) and up is held
+    to [-L, L] (also +-inf); below the limit the clamp changes nothing."""
+    L = 7.0
+    g = O.bf16_round(np.array([7.0, 8.0, 1e30, np.inf, 3.0, 3.0, 3.0, 3.0], np.float32))
+    u = O.bf16_round(np.array([1.0, 1.0, 1.0, 1.0, 7.0, 100.0, np.inf, -np.inf], np.float32))
+    h = O.swiglu_h_ex(g, u, limit=L, alpha=1.702, beta=1.0)
+    assert h[0] == h[1] == h[2] == h[3] and np.isfinite(h[0])
+    assert h[4] == h[5] == h[6]
+    assert h[7] == O.swiglu_h_ex(g[7:], O.bf16_round(np.float32(-7.0)).reshape(1), limit=L, alpha=1.702,
+                                 beta=1.0)[0]
+    # -inf gate: the clamp is one-sided, so p = -inf and d = inf: NaN
+    assert np.isnan(O.swiglu_h_ex(O.bf16_round(np.float32(-np.inf)).reshape(1),
+                                  O.bf16_round(np.float32(1.0)).reshape(1), limit=L)[0])
+
+
+def test_variant_bf16_and_fp16_inputs_agree_where_both_represent_the_value():
+    v = np.array([0.5, -1.25, 3.0, -6.5, 0.0078125, 100.0, -0.375], np.float32)
+    gb, ub = O.bf16_round(v), O.bf16_round(v[::-1].copy())
+    gf, uf = O.fp16_round(v), O.fp16_round(v[::-1].copy())
+    for kw in ({}, {"limit": 7.0, "alpha": 1.702, "beta": 1.0}):
+        hb = O.swiglu_h_ex(gb, ub, "bf16", **kw)
+        hf = O.swiglu_h_ex(gf, uf, "fp16", **kw)
+        assert np.array_equal(hb, hf)

@@ -17,9 +17,9 @@ W8_OK = 0
 STATUS_NAMES = {
     0: "W8_OK", 1: "W8_ERR_NULL", 2: "W8_ERR_SHAPE", 3: "W8_ERR_ALIGN", 4: "W8_ERR_STRIDE",
     5: "W8_ERR_DTYPE", 6: "W8_ERR_ARCH", 7: "W8_ERR_POLICY", 8: "W8_ERR_TIMEOUT",
-    9: "W8_ERR_CUDA", 10: "W8_ERR_SCALE",
+    9: "W8_ERR_CUDA", 10: "W8_ERR_SCALE", 11: "W8_ERR_PARAM",
 }
-DTYPE_BF16, DTYPE_E4M3 = 0, 1
+DTYPE_BF16, DTYPE_E4M3, DTYPE_F16 = 0, 1, 2
 MODE_A8, MODE_A16 = 0, 1
 
 # Every symbol the header declares, with its ctypes signature.
@@ -32,6 +32,12 @@ class StepPolicy(ctypes.Structure):
     """Mirror of ``w8_step_policy``."""
     _fields_ = [("schema_version", _i32), ("enabled", _i32),
                 ("first_steps", _i32), ("last_steps", _i32)]
+
+
+class SwigluParams(ctypes.Structure):
+    """Mirror of ``w8_swiglu_params``."""
+    _fields_ = [("has_limit", _i32), ("limit", ctypes.c_float), ("alpha", ctypes.c_float),
+                ("beta", ctypes.c_float)]
 
 
 SIGNATURES = {
@@ -61,6 +67,10 @@ SIGNATURES = {
     "swiglu_2in_fp8": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p,
                                       _c_void_p]),
     "swiglu_2in_bf16": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
+    "swiglu_2in_ex_fp8": (ctypes.c_int, [_c_void_p, _c_void_p, _i32, _i64, _i64, ctypes.POINTER(SwigluParams),
+                                         _c_void_p, _c_void_p, _c_void_p]),
+    "swiglu_2in_ex_16": (ctypes.c_int, [_c_void_p, _c_void_p, _i32, _i64, _i64, ctypes.POINTER(SwigluParams),
+                                        _c_void_p, _c_void_p]),
     "step_policy_dispatch": (ctypes.c_int, [_c_void_p, _i32, _i32, ctypes.POINTER(_i32)]),
     "w8_check_group_scales": (ctypes.c_int, [ctypes.POINTER(_c_void_p), _i32]),
     "w8_step_policy_parse": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(StepPolicy),
@@ -316,6 +326,57 @@ def swiglu_2in_bf16(gate, up, out=None, stream=None):
     if out is None:
         out = torch.empty(gate.shape, dtype=torch.bfloat16, device=gate.device)
     _check(lib().swiglu_2in_bf16(_ptr(g), _ptr(u), M, I, _ptr(_as_bf16(out, "out")), _stream(stream)))
+    return out
+
+
+def _as_16(t, name):
+    _dense(t, name)
+    if t.dtype == torch.bfloat16:
+        return t, DTYPE_BF16
+    if t.dtype == torch.float16:
+        return t, DTYPE_F16
+    raise W8Error(5, f"{name}: expected bfloat16 or float16, got {t.dtype}")
+
+
+def _swiglu_params(limit, alpha, beta):
+    return SwigluParams(1 if limit is not None else 0, float(limit) if limit is not None else 0.0,
+                        float(alpha), float(beta))
+
+
+def _swiglu_ex_inputs(gate, up):
+    (g, dt), (u, du) = _as_16(gate, "gate"), _as_16(up, "up")
+    if dt != du:
+        raise W8Error(5, "gate and up dtypes differ")
+    g, u = _flat2(g), _flat2(u)
+    if g.shape != u.shape:
+        raise W8Error(2, "gate and up shapes differ")
+    return g, u, dt
+
+
+def swiglu_2in_ex_fp8(gate, up, s_out, limit=None, alpha=1.0, beta=0.0, out=None, stream=None):
+    """SwiGLU with options (``limit``: clamp, ``alpha``: sigmoid slope,
+    ``beta``: shift of up), bf16 or float16 inputs, E4M3 output."""
+    g, u, dt = _swiglu_ex_inputs(gate, up)
+    M, I = g.shape
+    if out is None:
+        out = torch.empty(gate.shape, dtype=torch.uint8, device=gate.device)
+    prm = _swiglu_params(limit, alpha, beta)
+    _check(lib().swiglu_2in_ex_fp8(_ptr(g), _ptr(u), dt, M, I, ctypes.byref(prm), _ptr(_scalar(s_out, "s_out")),
+                                   _ptr(_as_u8(out, "out")), _stream(stream)))
+    return out
+
+
+def swiglu_2in_ex_16(gate, up, limit=None, alpha=1.0, beta=0.0, out=None, stream=None):
+    """SwiGLU with options; output in the inputs' 16-bit format."""
+    g, u, dt = _swiglu_ex_inputs(gate, up)
+    M, I = g.shape
+    if out is None:
+        out = torch.empty(gate.shape, dtype=gate.dtype, device=gate.device)
+    o, do = _as_16(out, "out")
+    if do != dt:
+        raise W8Error(5, "out must have the inputs' dtype")
+    prm = _swiglu_params(limit, alpha, beta)
+    _check(lib().swiglu_2in_ex_16(_ptr(g), _ptr(u), dt, M, I, ctypes.byref(prm), _ptr(o), _stream(stream)))
     return out
 
 

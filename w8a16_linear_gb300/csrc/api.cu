@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -94,7 +95,7 @@ int query_device(int* sms) { return device_info(sms); }
 
 extern "C" {
 
-int w8_abi_version(void) { return 1; }
+int w8_abi_version(void) { return 2; }
 
 const char* w8_last_error(void) { return g_last_error; }
 
@@ -372,6 +373,56 @@ w8_status swiglu_2in_bf16(const uint16_t* gate, const uint16_t* up, int64_t M, i
   if ((st = device_info(&sms)) != W8_OK) return st;
   return cuda_status(w8::launch_swiglu_bf16(gate, up, M * I, out, sms, static_cast<cudaStream_t>(stream)),
                      "swiglu_2in_bf16 launch");
+}
+
+static w8_status check_swiglu_ex(const char* fn, const void* g, const void* u, int32_t in_dtype,
+                                 int64_t M, int64_t I, const w8_swiglu_params* prm, const void* out,
+                                 w8::SwigluExArgs* a) {
+  w8_status st = check_swiglu(fn, static_cast<const uint16_t*>(g), static_cast<const uint16_t*>(u), M, I,
+                              out);
+  if (st != W8_OK) return st;
+  if (in_dtype != W8_DTYPE_BF16 && in_dtype != W8_DTYPE_F16)
+    return fail(W8_ERR_DTYPE, "%s: in_dtype %d is neither bf16 nor f16", fn, in_dtype);
+  if (!prm) return fail(W8_ERR_NULL, "%s: NULL params", fn);
+  if (!std::isfinite(prm->alpha) || !std::isfinite(prm->beta))
+    return fail(W8_ERR_PARAM, "%s: alpha and beta must be finite", fn);
+  if (prm->has_limit && !(std::isfinite(prm->limit) && prm->limit > 0.0f))
+    return fail(W8_ERR_PARAM, "%s: limit must be finite and > 0", fn);
+  a->has_limit = prm->has_limit != 0;
+  a->limit = prm->limit;
+  a->alpha = prm->alpha;
+  a->beta = prm->beta;
+  return W8_OK;
+}
+
+w8_status swiglu_2in_ex_fp8(const void* gate, const void* up, int32_t in_dtype, int64_t M, int64_t I,
+                            const w8_swiglu_params* prm, const float* s_out, uint8_t* out,
+                            void* stream) {
+  w8::SwigluExArgs a{};
+  w8_status st = check_swiglu_ex("swiglu_2in_ex_fp8", gate, up, in_dtype, M, I, prm, out, &a);
+  if (st != W8_OK) return st;
+  if (M == 0) return ok();
+  if (!s_out) return fail(W8_ERR_NULL, "swiglu_2in_ex_fp8: NULL s_out");
+  int sms = 0;
+  if ((st = device_info(&sms)) != W8_OK) return st;
+  return cuda_status(w8::launch_swiglu_ex(static_cast<const uint16_t*>(gate), static_cast<const uint16_t*>(up),
+                                          M * I, in_dtype == W8_DTYPE_F16, true, a, s_out, out, sms,
+                                          static_cast<cudaStream_t>(stream)),
+                     "swiglu_2in_ex_fp8 launch");
+}
+
+w8_status swiglu_2in_ex_16(const void* gate, const void* up, int32_t in_dtype, int64_t M, int64_t I,
+                           const w8_swiglu_params* prm, void* out, void* stream) {
+  w8::SwigluExArgs a{};
+  w8_status st = check_swiglu_ex("swiglu_2in_ex_16", gate, up, in_dtype, M, I, prm, out, &a);
+  if (st != W8_OK) return st;
+  if (M == 0) return ok();
+  int sms = 0;
+  if ((st = device_info(&sms)) != W8_OK) return st;
+  return cuda_status(w8::launch_swiglu_ex(static_cast<const uint16_t*>(gate), static_cast<const uint16_t*>(up),
+                                          M * I, in_dtype == W8_DTYPE_F16, false, a, nullptr, out, sms,
+                                          static_cast<cudaStream_t>(stream)),
+                     "swiglu_2in_ex_16 launch");
 }
 
 w8_status step_policy_dispatch(const w8_step_policy* policy, int32_t step, int32_t num_steps,

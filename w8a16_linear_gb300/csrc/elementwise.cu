@@ -111,6 +111,44 @@ __global__ void __launch_bounds__(256, 6) swiglu_bf16_kernel(const uint16_t* __r
   }
 }
 
+// The SwiGLU variants (swiglu_spec.cuh): bf16 or binary16 inputs, FP8 output
+// or a 16-bit output in the input's format.
+template <bool kF16, bool kFp8>
+__global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __restrict__ g,
+                                                           const uint16_t* __restrict__ u,
+                                                           int64_t n16, SwigluParams pr,
+                                                           const float* __restrict__ s_out,
+                                                           void* __restrict__ out) {
+  float s = 1.0f, rs = 1.0f;
+  bool exact_only = false;
+  if constexpr (kFp8) {
+    s = __ldg(s_out);
+    rs = __frcp_rn(s);
+    exact_only = !swiglu_fp8_scale_is_fast(s, rs);
+  }
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    const uint4 ga = ldg16(g + i * 16), gb = ldg16(g + i * 16 + 8);
+    const uint4 ua = ldg16(u + i * 16), ub = ldg16(u + i * 16 + 8);
+    const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+    const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+    if constexpr (kFp8) {
+      uint32_t c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = swiglu_ex_fp8_pair<kF16>(gw[j], uw[j], pr, s, rs, exact_only);
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + i * 16) =
+          make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
+    } else {
+      uint32_t h[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[j] = swiglu_ex_16_pair<kF16>(gw[j], uw[j], pr);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + i * 16);
+      dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+      dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
 int grid_for(int64_t n16, int sms) {
   const int64_t want = (n16 + 255) / 256;
   const int64_t cap = (int64_t)sms * 8;   // 8 resident 256-thread blocks per SM
@@ -118,6 +156,22 @@ int grid_for(int64_t n16, int sms) {
 }
 
 }  // namespace
+
+cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bool in_f16, bool out_fp8,
+                             const SwigluExArgs& a, const float* s_out, void* out, int sms,
+                             cudaStream_t st) {
+  const int64_t n16 = n / 16;
+  const SwigluParams pr{a.limit, a.alpha, a.beta, a.has_limit ? 1 : 0, a.beta != 0.0f ? 1 : 0};
+  const int grid = grid_for(n16, sms);
+  if (in_f16) {
+    if (out_fp8) swiglu_ex_kernel<true, true><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
+    else swiglu_ex_kernel<true, false><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
+  } else {
+    if (out_fp8) swiglu_ex_kernel<false, true><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
+    else swiglu_ex_kernel<false, false><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_static(const uint16_t* x, int64_t n, const float* s_in, uint8_t* q,
                                 int sms, cudaStream_t st) {

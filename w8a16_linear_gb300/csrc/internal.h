@@ -21,6 +21,14 @@ cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, c
 cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* out,
                                int sms, cudaStream_t st);
 
+struct SwigluExArgs {            // validated by the caller
+  bool has_limit;
+  float limit, alpha, beta;
+};
+cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bool in_f16, bool out_fp8,
+                             const SwigluExArgs& a, const float* s_out, void* out, int sms,
+                             cudaStream_t st);
+
 // ---- GEMMs (gemm.cu)
 constexpr int kMaxGroup = 3;
 

@@ -387,6 +387,21 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Two binary32 values -> packed binary16 pair, round to nearest even (overflow
+// to infinity).  `lo` low half.
+__device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Packed binary16 pair -> two binary32 values (exact).
+__device__ __forceinline__ void f16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  asm("{.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
+}
+
 // Two E4M3 codes (low byte first) -> packed f16x2 (exact).
 __device__ __forceinline__ uint32_t cvt_e4m3x2_to_f16x2(uint16_t codes) {
   uint32_t r;

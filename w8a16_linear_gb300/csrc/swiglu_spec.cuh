@@ -279,4 +279,100 @@ __device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const ui
   for (int j = 0; j < 4; ++j) codes[j] = c[2 * j] | (c[2 * j + 1] << 16);
 }
 
+// ------------------------------------------------------------------ variants
+//
+// The options the two-input SwiGLU is tested with besides the plain form
+// (TensorRT-LLM PR #17476, section Test Coverage: BF16 / FP16 inputs,
+// swiglu_limit, swiglu_alpha + swiglu_beta, FP8 output).  The pages name them
+// only; the specification here is the clamped, shifted SwiGLU of the public
+// gpt-oss MLP:
+//   g = min(g, L), u = clamp(u, -L, L)            (limit L; a NaN stays NaN)
+//   t = fl32(a * g)                               (alpha a)
+//   u = fl32(u + b)                               (beta b; skipped when b == 0)
+//   p = fl32(g * u), h = fl32(p / fl32(1 + exp_spec(-t)))
+// With a = 1, b = 0 and no limit this is the base specification bit for bit.
+// The fast paths are the base ones with t in place of g: FP8 output through
+// __expf and the 2^-18 bracket (exact path for t < -8); 16-bit output with the
+// specification's denominator, p * rcp.approx(d) (within 4 * 2^-24 of the
+// specified h) and a 2^-21 bracket on the packed 16-bit conversion, plus the
+// d >= 2^126 and tiny-h guards.
+
+struct SwigluParams {
+  float limit;     // used when has_limit
+  float alpha;
+  float beta;      // added to up when has_beta
+  int has_limit;
+  int has_beta;
+};
+
+constexpr float k16BracketLo = 0.99999952316284180f;   // 1 - 2^-21
+constexpr float k16BracketHi = 1.00000047683715820f;   // 1 + 2^-21
+
+template <bool kF16>
+__device__ __forceinline__ F2 unpack16(uint32_t w) {
+  if constexpr (kF16) {
+    F2 r;
+    f16x2_to_f32(w, r.x, r.y);
+    return r;
+  } else {
+    return F2{bf16_lo(w), bf16_hi(w)};
+  }
+}
+
+__device__ __forceinline__ float clamp_hi(float v, float lim) { return v > lim ? lim : v; }
+__device__ __forceinline__ float clamp_sym(float v, float lim) {
+  return v > lim ? lim : (v < -lim ? -lim : v);
+}
+
+// t = fl32(a * g) and p = fl32(g * (u + b)) of a pair, after the clamps.
+template <bool kF16>
+__device__ __forceinline__ void swiglu_ex_operands(uint32_t gw, uint32_t uw, const SwigluParams& pr,
+                                                   F2& t, F2& p) {
+  F2 g = unpack16<kF16>(gw), u = unpack16<kF16>(uw);
+  if (pr.has_limit) {
+    g = F2{clamp_hi(g.x, pr.limit), clamp_hi(g.y, pr.limit)};
+    u = F2{clamp_sym(u.x, pr.limit), clamp_sym(u.y, pr.limit)};
+  }
+  t = mul2(g, splat(pr.alpha));
+  if (pr.has_beta) u = add2(u, splat(pr.beta));
+  p = mul2(g, u);
+}
+
+template <bool kF16>
+__device__ __forceinline__ uint32_t swiglu_ex_fp8_pair(uint32_t gw, uint32_t uw, const SwigluParams& pr,
+                                                       float s, float rs, bool exact_only) {
+  F2 t, p;
+  swiglu_ex_operands<kF16>(gw, uw, pr, t, p);
+  const F2 d = add2(splat(1.0f), F2{__expf(-t.x), __expf(-t.y)});
+  const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
+  bool unsettled;
+  const uint32_t code = e4m3x2_bracket(mul2(hf, splat(rs)), kFp8BracketLo, kFp8BracketHi, unsettled);
+  if (exact_only | unsettled | (t.x < -8.0f) | (t.y < -8.0f)) {   // rare
+    const F2 de = add2(splat(1.0f), exp_spec2(neg(t)));
+    return cvt_e4m3x2(__fdiv_rn(__fdiv_rn(p.x, de.x), s), __fdiv_rn(__fdiv_rn(p.y, de.y), s));
+  }
+  return code;
+}
+
+__device__ __forceinline__ uint32_t cvt16x2(bool f16, float lo, float hi) {
+  return f16 ? cvt_f16x2(lo, hi) : cvt_bf16x2(lo, hi);
+}
+
+template <bool kF16>
+__device__ __forceinline__ uint32_t swiglu_ex_16_pair(uint32_t gw, uint32_t uw, const SwigluParams& pr) {
+  F2 t, p;
+  swiglu_ex_operands<kF16>(gw, uw, pr, t, p);
+  const F2 d = dplus1_fast(neg(t));
+  const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
+  const F2 lo = mul2(hf, splat(k16BracketLo));
+  const F2 hi = mul2(hf, splat(k16BracketHi));
+  const uint32_t clo = cvt16x2(kF16, lo.x, lo.y);
+  const uint32_t chi = cvt16x2(kF16, hi.x, hi.y);
+  if ((clo != chi) | h_needs_exact(p.x, d.x, hf.x) | h_needs_exact(p.y, d.y, hf.y)) {   // rare
+    const F2 de = add2(splat(1.0f), exp_spec2(neg(t)));
+    return cvt16x2(kF16, __fdiv_rn(p.x, de.x), __fdiv_rn(p.y, de.y));
+  }
+  return chi;
+}
+
 }  // namespace w8

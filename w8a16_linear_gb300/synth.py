@@ -40,6 +40,12 @@ def activations_bf16(seed, shape, std, outlier_frac=0.0, outlier_mult=8.0):
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+def activations_f16(seed, shape, std):
+    """float16 activations ~ N(0, std^2); returns uint16 binary16 bits."""
+    t = torch.randn(*shape, generator=_gen(seed), dtype=torch.float32) * float(std)
+    return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+
+
 def uniform_f32(seed, shape, lo, hi):
     """float32 U[lo, hi) draw."""
     t = torch.rand(*shape, generator=_gen(seed), dtype=torch.float32)
