@@ -357,6 +357,15 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     out["swiglu_2in_fp8"] = {"us": ms * 1e3, "GB_s": 5 * blk.h8.numel() / ms / 1e6}
     ms = _time(lambda: W.swiglu_2in_bf16(blk.y_gu[0], blk.y_gu[1], out=blk.h16), flush, stream, n)
     out["swiglu_2in_bf16"] = {"us": ms * 1e3, "GB_s": 6 * blk.h16.numel() / ms / 1e6}
+    # the variant op with the limit / alpha / beta options on the same tensors
+    opts = dict(limit=7.0, alpha=1.702, beta=1.0)
+    ms = _time(lambda: W.swiglu_2in_ex_fp8(blk.y_gu[0], blk.y_gu[1], blk.s_h, out=blk.h8, **opts),
+               flush, stream, n)
+    out["swiglu_2in_ex_fp8"] = {"us": ms * 1e3, "GB_s": 5 * blk.h8.numel() / ms / 1e6,
+                                "note": "limit 7, alpha 1.702, beta 1, bf16 in"}
+    ms = _time(lambda: W.swiglu_2in_ex_16(blk.y_gu[0], blk.y_gu[1], out=blk.h16, **opts), flush, stream, n)
+    out["swiglu_2in_ex_16"] = {"us": ms * 1e3, "GB_s": 6 * blk.h16.numel() / ms / 1e6,
+                               "note": "limit 7, alpha 1.702, beta 1, bf16 in and out"}
     q = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
     ms = _time(lambda: W.gate_up_swiglu_fp8(q, blk.s_mlp, blk.w_gu[0][0], blk.w_gu[1][0], blk.w_gu[0][1],
                                             blk.w_gu[1][1], blk.s_h, out=blk.h8), flush, stream, n)
