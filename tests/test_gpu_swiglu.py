@@ -91,6 +91,40 @@ def test_swiglu_near_midpoint_cases(W):
     _fp8_equal(got, O.swiglu_2in_fp8(G, U, s))
 
 
+def _rel_to_bf16_midpoint(h):
+    m, _ = np.frexp(np.abs(h).astype(np.float64))
+    f = m * 256.0                                       # 128..256: one bf16 step is 1
+    return np.abs(f - np.floor(f) - 0.5) / f
+
+
+def test_swiglu_exact_path_near_ties(W):
+    """(g, u) pairs whose specified h lies within 2^-22 (relative) of a bf16
+    rounding midpoint, and whose h / s lies within 2^-20 of an E4M3 one:
+    only a denominator equal to the specification's, bit for bit, gives the
+    specified result there (a 1-ulp error in d flips these)."""
+    gb = np.arange(1 << 16, dtype=np.uint16)
+    gv = O.bf16_decode(gb)
+    gb = gb[np.isfinite(gv) & (np.abs(gv) <= 16.0) & (np.abs(gv) >= 2.0 ** -12)]
+    ub = synth.activations_bf16(11, (2048,), 3.0)
+    G, U = np.repeat(gb, ub.size), np.tile(ub, gb.size)
+    h = O.swiglu_h(G, U)
+    s = np.float32(0.02)
+    q = h / s
+    pick16 = (np.abs(h) >= 2.0 ** -100) & np.isfinite(h) & (_rel_to_bf16_midpoint(h) < 2.0 ** -22)
+    pick8 = (np.abs(q) >= 2.0 ** -6) & (np.abs(q) <= 400.0) & (_rel_to_e4m3_midpoint(q) < 2.0 ** -20)
+    for pick, fp8 in ((pick16, False), (pick8, True)):
+        Gs, Us = G[pick], U[pick]
+        assert Gs.size >= 64, Gs.size
+        n = (Gs.size // 16) * 16
+        Gs, Us = Gs[:n].reshape(-1, 16), Us[:n].reshape(-1, 16)
+        if fp8:
+            got = host_u8(W.swiglu_2in_fp8(dev_bf16(Gs), dev_bf16(Us), dev_f32(s)))
+            _fp8_equal(got, O.swiglu_2in_fp8(Gs, Us, s))
+        else:
+            got = host_bits(W.swiglu_2in_bf16(dev_bf16(Gs), dev_bf16(Us)))
+            _bf16_equal(got, O.swiglu_2in_bf16(Gs, Us))
+
+
 @pytest.mark.parametrize("M,I", [(64, 256), (333, 4096), (1, 16), (7, 16400)])
 def test_swiglu_shapes(W, M, I):
     g = synth.activations_bf16(3, (M, I), 2.0)

@@ -11,10 +11,10 @@
 //    activation precision).
 //
 // Each thread moves 16 elements per step with 128-bit loads and stores in a
-// grid-stride loop over a grid sized to the SM count.  All arithmetic is
-// IEEE binary32 with explicit round-to-nearest intrinsics, so that no
-// multiply-add is contracted and the result is the same bit pattern as the
-// specification below on any compiler setting.
+// grid-stride loop over a grid sized to the SM count.  Every output is the
+// specification's bit pattern: a fast value with a proven error bound is
+// kept only where it provably rounds to the same code, everything else is
+// recomputed with correctly rounded, never-fused scalar operations.
 //
 // The SwiGLU specification and its guarded fast evaluation live in
 // swiglu_spec.cuh.
