@@ -42,6 +42,8 @@ def test_linear_configs(W, M, K, N, kw):
 @pytest.mark.parametrize("M,K,N", [
     (1, 16, 16), (3, 48, 16), (127, 128, 256), (129, 144, 272), (200, 4112, 48),
     (333, 384, 512), (130, 64, 16 * 33),
+    # W8A16 CTA-pair tiles (256 weight rows x 384 tokens): ragged M, N and K
+    (1000, 256, 400), (777, 4112, 272), (385, 64, 16 * 17),
 ])
 def test_linear_ragged_shapes(W, M, K, N):
     x, qw, s_in, s_w = linear_problem(M, K, N, seed_x=M, seed_w=N)
@@ -67,9 +69,10 @@ def test_w8a8_exact_sums_bit_exact(W):
     assert np.array_equal(y, want)
 
 
-def test_w8a16_exact_sums_bit_exact(W):
+@pytest.mark.parametrize("M,N", [(260, 384), (900, 400)])
+def test_w8a16_exact_sums_bit_exact(W, M, N):
     rng = np.random.default_rng(1)
-    M, K, N = 260, 2048, 384
+    K = 2048
     xv = np.array([0.0, 0.25, -0.25, 0.5, -1.0, 1.5, 2.0, -3.0], np.float32)
     x = torch.from_numpy(rng.choice(xv, size=(M, K))).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     qw = O.e4m3_encode(rng.choice(np.array([0.0, 1.0, -1.0, 2.0, -0.5, 3.0], np.float32), size=(N, K)))
