@@ -755,292 +755,6 @@ __global__ void __launch_bounds__(a16t::kThreads, 1)
   }
 }
 
-// ------------------------------------------------------------------ W8A16, CTA pair
-//
-// The same transposed product on a CTA pair (cluster of 2): a tile is 256
-// weight rows x 384 tokens.  Each CTA converts its own 128 weight rows into
-// its own TMEM (A operand rows 0-127 / 128-255 of a cta_group::2 MMA) and
-// stages half of each MMA's tokens (B operand, split along N); the even CTA's
-// single MMA thread issues two M = 256, N = 192 kind::f16 MMAs per 16
-// K-values.  Against the 1-CTA kernel every weight element is converted once
-// per 384 tokens instead of 320, and each SM stages half the activation bytes
-// per FLOP.  The transform warps of both CTAs report a converted stage on the
-// even CTA's `ready` barrier (release/acquire at cluster scope, after
-// tcgen05.wait::st and tcgen05.fence::before_thread_sync); MMA completions are
-// multicast to both CTAs' `empty` and `tfull` barriers; both CTAs' epilogue
-// warps release the accumulator on the even CTA's `tempty` barrier.
-//
-// TMEM columns (each CTA): D 0-383 (tokens 0-191 of the first MMA, 192-383 of
-// the second), A stages 384 + 32 s.
-namespace a16p {
-constexpr int BTH = 96;                      // tokens of one MMA staged by each CTA
-constexpr int NH = 2 * BTH;                  // MMA N
-constexpr int BT = 2 * NH;                   // tokens per tile
-constexpr int BW = 128;                      // weight rows per CTA (256 per pair)
-constexpr int BK = 64;                       // K per stage
-constexpr int S = 4;                         // stages
-constexpr int kXHalf = BTH * 128;            // bf16 activation rows of one MMA half, 128-byte rows
-constexpr int kXBytes = 2 * kXHalf;
-constexpr int kRawBytes = BW * 64;           // raw E4M3 weight rows
-constexpr int kEpiBuf = 32 * 64;             // 32 tokens x 32 features bf16
-constexpr int kEpiWarps = 8;                 // 2 per TMEM lane quadrant, 6 token chunks each
-constexpr int kTransformWarps = 8;           // 2 per TMEM lane quadrant, 32 K-values each
-constexpr int kOffX = 0;
-constexpr int kOffRaw = kOffX + S * kXBytes;
-constexpr int kOffEpi = kOffRaw + S * kRawBytes;
-constexpr int kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
-constexpr int kNumBars = 3 * S + 3;          // full[S], empty[S], ready[S], tfull, tempty, drain
-constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kAlloc = kOffAbort + 4 + 1024;
-constexpr int kThreads = (2 + kEpiWarps + kTransformWarps) * 32;
-constexpr uint32_t kTmemA = BT;              // first A-stage column
-constexpr uint32_t kIdesc = make_idesc(1, 1, 2 * BW, NH);
-static_assert(kTmemA + S * 32 <= kTmemCols, "TMEM budget");
-static_assert(kAlloc <= 232448, "shared memory budget");
-static_assert(NH % 16 == 0 && NH <= 256 && BT % 64 == 0, "MMA N and the epilogue split");
-}  // namespace a16p
-
-__global__ void __launch_bounds__(a16p::kThreads, 1)
-    gemm_a16p_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args args) {
-  using namespace a16p;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + kOffBar;
-  auto full_bar = [&](int st) { return bar0 + 8u * st; };
-  auto empty_bar = [&](int st) { return bar0 + 8u * (S + st); };
-  auto ready_bar = [&](int st) { return bar0 + 8u * (2 * S + st); };
-  const uint32_t tfull_bar = bar0 + 8u * (3 * S);
-  const uint32_t tempty_bar = bar0 + 8u * (3 * S + 1);
-  const uint32_t drain_bar = bar0 + 8u * (3 * S + 2);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffAbort);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = (rank == 0);
-  const int cluster_id = blockIdx.x / 2;
-  const int num_clusters = gridDim.x / 2;
-
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < S; ++st) {
-      mbar_init(full_bar(st), 1);
-      mbar_init(empty_bar(st), 1);
-      mbar_init(ready_bar(st), 2 * kTransformWarps);
-    }
-    mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, 2 * kEpiWarps);
-    mbar_init(drain_bar, 1);
-    *abort = 0;
-    fence_mbar_init();
-    prefetch_tensormap(&maps.a);
-    for (int g = 0; g < args.G; ++g) {
-      prefetch_tensormap(map_b(maps, g));
-      prefetch_tensormap(map_y(maps, g));
-    }
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(sbase + kOffTmemSlot, kTmemCols);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // peer barriers initialised before any remote use
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer (each CTA)
-    if (lane == 0) {
-      int st = 0;
-      uint32_t ph = 0, issued = 0;
-      bool ok = true;
-      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
-        int m0, g, n0;
-        decode_tile(args, t, BT, 2 * BW, m0, g, n0);
-        for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!mbar_wait(empty_bar(st), ph ^ 1, abort, kWaitLimitNs)) {
-            record_timeout(abort);
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(st), kXBytes + kRawBytes);
-          const uint32_t xd = sbase + kOffX + st * kXBytes;
-          tma_load_2d(xd, &maps.a, full_bar(st), kb * BK, m0 + (int)rank * BTH);
-          tma_load_2d(xd + kXHalf, &maps.a, full_bar(st), kb * BK, m0 + NH + (int)rank * BTH);
-          tma_load_2d(sbase + kOffRaw + st * kRawBytes, map_b(maps, g), full_bar(st), kb * BK,
-                      n0 + (int)rank * BW);
-          ++issued;
-          if (++st == S) {
-            st = 0;
-            ph ^= 1;
-          }
-        }
-      }
-      for (int j = 0; j < S && (uint32_t)j < issued; ++j) {
-        const uint32_t l = issued - 1 - j;
-        volatile int never = 0;
-        if (!mbar_wait(full_bar((int)(l % S)), (l / S) & 1, &never, kWaitLimitNs))
-          atomicOr(&g_gemm_err, kErrTimeout);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer (even CTA)
-    if (lane == 0 && leader) {
-      int st = 0;
-      uint32_t ph = 0, acc_ph = 0;
-      bool ok = true;
-      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
-        if (!mbar_wait_cluster(tempty_bar, acc_ph ^ 1, abort, kWaitLimitNs)) {
-          record_timeout(abort);
-          break;
-        }
-        tc_fence_after();
-        for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!mbar_wait_cluster(ready_bar(st), ph, abort, kWaitLimitNs)) {
-            record_timeout(abort);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t x_addr = sbase + kOffX + st * kXBytes;
-          const uint32_t a_col = tmem_base + kTmemA + (uint32_t)(st * 32);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // K = 16 per MMA: 8 TMEM columns, 32 smem bytes
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              mma_f16_tmem_a_pair(tmem_base + (uint32_t)(h * NH), a_col + 8 * k,
-                                  sw128_kmajor_desc(x_addr + h * kXHalf + 32 * k), kIdesc, (kb | k) != 0);
-          }
-          mma_commit_pair_mc(empty_bar(st), 0x3);
-          if (++st == S) {
-            st = 0;
-            ph ^= 1;
-          }
-        }
-        if (!ok) break;
-        mma_commit_pair_mc(tfull_bar, 0x3);
-        acc_ph ^= 1;
-      }
-      mma_commit_pair(drain_bar);
-      volatile int never = 0;
-      if (!mbar_wait(drain_bar, 0, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
-    }
-  } else if (warp < 2 + kEpiWarps) {
-    // ---------------------------------------------------------------- epilogue (each CTA)
-    constexpr int kChunks = BT / 64;  // 32-token chunks per epilogue warp
-    const int q = warp & 3;  // TMEM lane quadrant: weight rows (features) q*32 .. q*32+31
-    const int eh = (warp - 2) >> 2;  // which half of the tile's tokens
-    uint8_t* bufp = smem + kOffEpi + (warp - 2) * 2 * kEpiBuf;
-    const uint32_t bufs = sbase + kOffEpi + (uint32_t)((warp - 2) * 2 * kEpiBuf);
-    const uint32_t tempty_leader = mapa_shared(tempty_bar, 0);
-    int nbuf = 0;
-    uint32_t acc_ph = 0;
-    for (int t = cluster_id; t < args.num_tiles; t += num_clusters) {
-      int m0, g, n0;
-      decode_tile(args, t, BT, 2 * BW, m0, g, n0);
-      if (!mbar_wait_warp(tfull_bar, acc_ph, abort, kWaitLimitNs)) {
-        if (lane == 0) record_timeout(abort);
-        break;
-      }
-      tc_fence_after();
-      const int f0 = n0 + (int)rank * BW + q * 32;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-      for (int c = eh * kChunks; c < (eh + 1) * kChunks; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + c * 32, r);  // feature f0+lane, tokens m0+c*32 .. +31
-        tmem_ld_wait();
-        if (c == (eh + 1) * kChunks - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(tempty_leader);
-        }
-        const int tok0 = m0 + c * 32;
-        if (tok0 >= args.M || f0 >= args.N[g]) continue;
-        if (lane == 0) tma_store_wait_read<1>();
-        __syncwarp();
-        uint16_t* bp = reinterpret_cast<uint16_t*>(bufp + nbuf * kEpiBuf);
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const uint32_t pk = cvt_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-          bp[j * 32 + lane] = (uint16_t)(pk & 0xFFFF);        // token j, feature lane
-          bp[(j + 1) * 32 + lane] = (uint16_t)(pk >> 16);     // token j+1
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(map_y(maps, g), bufs + nbuf * kEpiBuf, f0, tok0);
-          tma_store_commit();
-        }
-        nbuf ^= 1;
-      }
-      acc_ph ^= 1;
-    }
-    if (lane == 0) tma_store_wait_all();
-  } else {
-    // ---------------------------------------------------------------- weight transform (each CTA)
-    const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int h = (warp - 2 - kEpiWarps) >> 2;  // which 32 of the stage's 64 K-values
-    const int r = q * 32 + lane;         // weight row of this CTA's half = TMEM lane
-    const uint32_t ready_leader0 = mapa_shared(ready_bar(0), 0);
-    int st = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
-      int m0, g, n0;
-      decode_tile(args, t, BT, 2 * BW, m0, g, n0);
-      const float sw = __ldg(scale_w(args, g));
-      for (int kb = 0; kb < args.num_kb; ++kb) {
-        if (!mbar_wait_warp(full_bar(st), ph, abort, kWaitLimitNs)) {
-          if (lane == 0) record_timeout(abort);
-          ok = false;
-          break;
-        }
-        // Raw row: 64 bytes with the 64-byte swizzle (chunk j at j ^ ((r >> 1) & 3)).
-        const uint8_t* raw = smem + kOffRaw + st * kRawBytes + r * 64;
-        const uint4 v0 = *reinterpret_cast<const uint4*>(raw + (((2 * h) ^ ((r >> 1) & 3)) * 16));
-        const uint4 v1 = *reinterpret_cast<const uint4*>(raw + (((2 * h + 1) ^ ((r >> 1) & 3)) * 16));
-        const uint32_t w8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint32_t o[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(w8[e] & 0xFFFF));
-          const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(w8[e] >> 16));
-          const F2 lo = mul2(F2{__half2float(__ushort_as_half((unsigned short)(f01 & 0xFFFF))),
-                                __half2float(__ushort_as_half((unsigned short)(f01 >> 16)))},
-                             splat(sw));
-          const F2 hi = mul2(F2{__half2float(__ushort_as_half((unsigned short)(f23 & 0xFFFF))),
-                                __half2float(__ushort_as_half((unsigned short)(f23 >> 16)))},
-                             splat(sw));
-          o[2 * e] = cvt_bf16x2(lo.x, lo.y);
-          o[2 * e + 1] = cvt_bf16x2(hi.x, hi.y);
-        }
-        tmem_st_32x32b_x16(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(st * 32 + h * 16), o);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(ready_leader0 + 8u * st);
-        if (++st == S) {
-          st = 0;
-          ph ^= 1;
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  // A pair leaves together: no remote arrive or MMA may target an exited CTA.
-  cluster_sync();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
-  }
-}
-
 // ------------------------------------------------------------------ host side
 
 // m-blocks per rasterisation group: as many as keep the group's activation
@@ -1218,46 +932,7 @@ cudaError_t launch_gemm_glu(const GemmProblem& p, int sms, cudaStream_t st, int*
 // would have to signal every 64-K stage of the odd CTA's dequantization
 // across the SM pair, and that cluster-scope hand-off measured slower than
 // the work it halves.
-cudaError_t launch_a16p(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  using namespace a16p;
-  *tmap_err = 0;
-  Maps maps;
-  Args args;
-  std::memset(&maps, 0, sizeof(maps));
-  std::memset(&args, 0, sizeof(args));
-  args.G = p.G;
-  args.M = (int)p.M;
-  args.K = (int)p.K;
-  args.num_kb = (int)((p.K + BK - 1) / BK);
-  const int tiles_m = (int)((p.M + BT - 1) / BT);
-  bool ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, p.K, p.M, p.K * 2, 64, BTH,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  for (int g = 0; g < p.G; ++g) {
-    args.N[g] = (int)p.N[g];
-    args.s_w[g] = p.s_w[g];
-    args.tiles_n[g] = (int)((p.N[g] + 2 * BW - 1) / (2 * BW));
-    args.tiles_per_m += args.tiles_n[g];
-    ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[g], p.K, 64, BW,
-                    CU_TENSOR_MAP_SWIZZLE_64B);
-    ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.y[g], p.N[g], p.M, p.N[g] * 2,
-                    32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
-  for (int g = p.G; g < kMaxGroup; ++g) args.s_w[g] = p.s_w[0];
-  if (!ok) {
-    *tmap_err = 1;
-    return cudaSuccess;
-  }
-  args.num_tiles = tiles_m * args.tiles_per_m;
-  args.tiles_m = tiles_m;
-  args.group_m = group_rows(BT, p.K, 2, tiles_m);
-  const int pairs = sms / 2;
-  const int clusters = args.num_tiles < pairs ? args.num_tiles : pairs;
-  return launch_cluster(gemm_a16p_kernel, clusters * 2, kThreads, kAlloc, 2, st, maps, args);
-}
-
-// The pair's 384-token tiles pay off once M covers more than a 1-CTA tile.
 cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  if (p.M > a16t::BT) return launch_a16p(p, sms, st, tmap_err);
   return launch_a16t(p, sms, st, tmap_err);
 }
 
