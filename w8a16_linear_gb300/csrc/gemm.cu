@@ -122,12 +122,6 @@ struct Args {
   int tiles_m;
   int group_m;   // m-blocks swept together down each column of tiles
   int num_tiles;
-  // W8A8: the tiles from main_tiles on (the last, partial wave) are split
-  // into `split` slices of kBN / split columns each; num_work = main_tiles +
-  // (num_tiles - main_tiles) * split work items in all.
-  int main_tiles;
-  int split;
-  int num_work;
   int num_kb;
   const float* s_in;
   const float* s_w[kMaxGroup];
@@ -155,21 +149,6 @@ __device__ __forceinline__ void decode_tile(const Args& a, int t, int rows_per_t
   }
   m0 = mb * rows_per_tile;
   n0 = r * cols_per_tile;
-}
-
-// Work item w -> tile origin and width in output columns (a whole tile, or
-// a slice of one of the last wave's tiles).
-__device__ __forceinline__ void decode_work(const Args& a, int w, int rows_per_tile, int cols_per_tile,
-                                            int& m0, int& g, int& n0, int& ncols) {
-  if (w < a.main_tiles) {
-    decode_tile(a, w, rows_per_tile, cols_per_tile, m0, g, n0);
-    ncols = cols_per_tile;
-    return;
-  }
-  const int u = w - a.main_tiles;
-  ncols = cols_per_tile / a.split;
-  decode_tile(a, a.main_tiles + u / a.split, rows_per_tile, cols_per_tile, m0, g, n0);
-  n0 += (u % a.split) * ncols;
 }
 
 __device__ __forceinline__ const CUtensorMap* map_b(const Maps& m, int g) {
@@ -255,15 +234,14 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < args.num_work; t += num_clusters) {
-        int m0, g, n0, ncols;
-        decode_work(args, t, BM * CG, C::kBN, m0, g, n0, ncols);
+      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
+        int m0, g, n0;
+        decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
         const int a_row = m0 + (int)rank * BM;
-        // W8A8: this CTA's half (pair) or all of the tile's weight rows; a
-        // slice uses the first ncols / CG rows of the staged box.
+        // W8A8: this CTA's half (pair) or all of the tile's weight rows.
         // GLU: the slice's rows n0 .. n0+127 of gate (even CTA / first half)
         // and of up (odd CTA / second half).
-        const int b_row = kGlu ? n0 : n0 + (int)rank * (ncols / CG);
+        const int b_row = kGlu ? n0 : n0 + (int)rank * C::kBRows;
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1, abort, kWaitLimitNs)) {
             record_timeout(abort);
@@ -311,10 +289,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < args.num_work; t += num_clusters) {
-        int m0, g, n0, ncols;
-        decode_work(args, t, BM * CG, C::kBN, m0, g, n0, ncols);
-        const uint32_t idesc = (kGlu || ncols == C::kBN) ? C::kIdesc : make_idesc(0, 0, BM * CG, ncols);
+      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
         if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1, abort, kWaitLimitNs)) {
           record_timeout(abort);
           break;
@@ -335,8 +310,8 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
             const uint64_t ad = sw128_kmajor_desc(a_addr + 32 * k);
             const uint64_t bd = sw128_kmajor_desc(b_addr + 32 * k);
             const uint32_t accum = (kb | k) != 0;
-            if constexpr (CG == 2) mma_f8f6f4_pair(d, ad, bd, idesc, accum);
-            else mma_f8f6f4(d, ad, bd, idesc, accum);
+            if constexpr (CG == 2) mma_f8f6f4_pair(d, ad, bd, C::kIdesc, accum);
+            else mma_f8f6f4(d, ad, bd, C::kIdesc, accum);
           }
           if constexpr (CG == 2) mma_commit_pair_mc(empty_bar(s), 0x3);
           else mma_commit(empty_bar(s));
@@ -376,9 +351,9 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       rs_out = __frcp_rn(s_out);
       exact_only = !swiglu_fp8_scale_is_fast(s_out, rs_out);
     }
-    for (int t = cluster_id; t < args.num_work; t += num_clusters) {
-      int m0, g, n0, ncols;
-      decode_work(args, t, BM * CG, C::kBN, m0, g, n0, ncols);
+    for (int t = cluster_id; t < args.num_tiles; t += num_clusters) {
+      int m0, g, n0;
+      decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
       float alpha = 1.0f, alpha_u = 1.0f;
       alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, kGlu ? 0 : g)));
       if constexpr (kGlu) alpha_u = __fmul_rn(__ldg(args.s_in), __ldg(args.s_w[1]));
@@ -392,14 +367,13 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       const int ng = args.N[g];
       const uint32_t tbase = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * kAccCols);
       if constexpr (!kGlu) {
-        const int nchunks = ncols / 64;
 #pragma unroll 1
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = 0; c < C::kBN / 64; ++c) {
           uint32_t r0[32], r1[32];
           tmem_ld_32x32b_x32(tbase + c * 64, r0);
           tmem_ld_32x32b_x32(tbase + c * 64 + 32, r1);
           tmem_ld_wait();
-          if (c == nchunks - 1) {
+          if (c == C::kBN / 64 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -874,17 +848,7 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   args.tiles_m = tiles_m;
   args.group_m = group_rows(BM * CG, p.K, 1, tiles_m);
   const int max_clusters = sms / CG;
-  // The last wave: its R tiles would leave max_clusters - R clusters idle;
-  // slicing them 4 (or 2) ways along N spreads them over the idle clusters.
-  const int rem = args.num_tiles % max_clusters;
-  args.main_tiles = args.num_tiles - rem;
-  args.split = 1;
-  if (!kGlu && rem > 0) {
-    if (4 * rem <= max_clusters) args.split = 4;
-    else if (2 * rem <= max_clusters) args.split = 2;
-  }
-  args.num_work = args.main_tiles + rem * args.split;
-  const int clusters = args.num_work < max_clusters ? args.num_work : max_clusters;
+  const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   return launch_cluster(gemm_kernel<MODE, CG>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
                         args);
 }
