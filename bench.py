@@ -409,6 +409,30 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     ms = _time(lambda: W.swiglu_2in_ex_16(blk.y_gu[0], blk.y_gu[1], out=blk.h16, **opts), flush, stream, n)
     out["swiglu_2in_ex_16"] = {"us": ms * 1e3, "GB_s": 6 * blk.h16.numel() / ms / 1e6,
                                "note": "limit 7, alpha 1.702, beta 1, bf16 in and out"}
+    # library reference points on the Q/K/V shape (context only, not this path):
+    # cuBLASLt FP8 through torch._scaled_mm on the pre-quantized activation,
+    # cuBLAS bf16 through torch.matmul on weights dequantized beforehand
+    qx = W.fp8_quant_static(blk.x_qkv, blk.s_qkv).view(torch.float8_e4m3fn)
+    try:
+        wt = [q.view(torch.float8_e4m3fn).t() for q, _ in blk.w_qkv]
+
+        def lib_fp8():
+            for w_t, (_, sw) in zip(wt, blk.w_qkv):
+                torch._scaled_mm(qx, w_t, scale_a=blk.s_qkv, scale_b=sw, out_dtype=torch.bfloat16)
+        ms = _time(lib_fp8, flush, stream, n)
+        out["lib_scaled_mm_fp8_qkv"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
+                                        "note": "torch._scaled_mm (cuBLASLt) x3, E4M3 input; reference point"}
+    except Exception as e:  # noqa: BLE001
+        out["lib_scaled_mm_fp8_qkv"] = {"error": str(e).splitlines()[0][:160]}
+    wd = [(q.view(torch.float8_e4m3fn).float() * sw).to(torch.bfloat16) for q, sw in blk.w_qkv]
+
+    def lib_bf16():
+        for w in wd:
+            torch.matmul(blk.x_qkv, w.t())
+    ms = _time(lib_bf16, flush, stream, n)
+    out["lib_matmul_bf16_qkv"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
+                                  "note": "torch.matmul (cuBLAS) x3 on pre-dequantized bf16 weights; reference point"}
+    del qx, wd
     q = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
     ms = _time(lambda: W.gate_up_swiglu_fp8(q, blk.s_mlp, blk.w_gu[0][0], blk.w_gu[1][0], blk.w_gu[0][1],
                                             blk.w_gu[1][1], blk.s_h, out=blk.h8), flush, stream, n)
