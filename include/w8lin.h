@@ -154,19 +154,38 @@ w8_status fp8_linear_w8a16(const void* x, int32_t x_dtype, int64_t M, int64_t K,
  *                        persistent W8A8 launch over the tiles of all G
  *                        projections, all reading ws.
  *   mode == W8_MODE_A16: no quantization (sharing stands down on 16-bit
- *                        steps, [P4] Denoising-step activation precision);
- *                        one W8A16 launch over all G projections.
+ *                        steps, [P4] Denoising-step activation precision).
+ *                        With ws: each weight is dequantized into ws
+ *                        (Wd_g = bf16_RNE(fl32(dec(w_g) * s_w[g])), [P3]
+ *                        Behavior: dequant + F.linear; a transient copy,
+ *                        overwritten by the next call) and one bf16 GEMM
+ *                        launch covers all G projections.  Without ws: one
+ *                        launch that dequantizes inside the GEMM.  Both give
+ *                        the same operand bits; they may differ in the
+ *                        accumulation order only.
  *   x          bf16 [M, K], device
  *   s_in       device float scalar shared by the group (A8 only)
  *   w, N, s_w, y  HOST arrays of G entries: device weight [N_g, K], its row
  *              count, device weight scale, device output [M, N_g]
- *   ws         E4M3 scratch [M, K] (A8 only; may be NULL for A16)
+ *   ws         A8: E4M3 scratch [M, K], required.  A16: optional bf16
+ *              scratch of sum_g N_g * K values (2 bytes each), the
+ *              dequantized weights of the group in order; 16-byte aligned.
  * Errors: NULL, SHAPE (G outside 2..3 or 1, K%16, N_g%16), ALIGN, ARCH, CUDA.
  */
 w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int64_t K,
                                 const float* s_in, int32_t G, const uint8_t* const* w,
                                 const int64_t* N, const float* const* s_w, uint16_t* const* y,
                                 uint8_t* ws, void* stream);
+
+/*
+ * fp8_dequant_weight — the dequantization step of the W8A16 path on its own
+ * ([P3] Behavior: "dequant + F.linear"): Wd = bf16_RNE(fl32(dec(w) * s_w)).
+ *   w    E4M3 weight [N, K], device;  s_w device float scalar
+ *   wd   bf16 output [N, K], device (written)
+ * Errors: NULL, SHAPE (K%16, negative sizes), ALIGN, ARCH, CUDA.
+ */
+w8_status fp8_dequant_weight(const uint8_t* w, int64_t N, int64_t K, const float* s_w, uint16_t* wd,
+                             void* stream);
 
 /*
  * fp8_linear_w8a8_group — the GEMM half of qkv_shared_quant_gemm in A8 mode:

@@ -1,0 +1,95 @@
+"""GPU parity of the W8A16 "dequant + F.linear" path: fp8_dequant_weight
+(bit-exact dequantized weight) and qkv_shared_quant_gemm in A16 mode with a
+workspace (the group's weights dequantized there, then one bf16 GEMM launch)
+against the oracle and against the path that dequantizes inside the GEMM."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_util import W, GEMM_TOL, dev_bf16, dev_f32, dev_u8, host_bits, gemm_err, amax_scale  # noqa: F401
+from w8a16_linear_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("s_w", [0.5039 / 448, 2.0 ** -12, 1.0, 3.7e-3, 1e-30, 2e30])
+def test_dequant_every_code(W, s_w):
+    """All 256 codes (both NaN codes included) against the oracle's
+    bf16(fl32(dec(q) * s_w)); NaN codes may give any NaN pattern."""
+    q = np.tile(np.arange(256, dtype=np.uint8), 64).reshape(64, 256)
+    got = host_bits(W.fp8_dequant_weight(dev_u8(q), dev_f32(s_w)))
+    want = O.dequant_weight_bf16(q, np.float32(s_w))
+    nan = np.isnan(O.bf16_decode(want))
+    assert np.array_equal(np.isnan(O.bf16_decode(got)), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def _group(M, K, Ns, seed=0):
+    x = synth.activations_bf16(seed, (M, K), 0.25, outlier_frac=0.001)
+    c = synth.uniform_f32(3, (len(Ns),), 0.5, 1.0)
+    qws, s_ws = [], []
+    for i, N in enumerate(Ns):
+        w = synth.normal_f32(10 + i, (N, K), 0.02) * c[i]
+        s = amax_scale(w)
+        qws.append(O.e4m3_encode(w / s))
+        s_ws.append(s)
+    return x, qws, s_ws
+
+
+@pytest.mark.parametrize("M,K,Ns", [(1000, 512, (512, 512, 512)), (257, 256, (1024, 1024)),
+                                    (64, 256, (256,)), (129, 4112, (272,)), (777, 384, (400, 16 * 17))])
+def test_a16_workspace_vs_oracle_and_fused(W, M, K, Ns):
+    x, qws, s_ws = _group(M, K, Ns)
+    xd, wd, sd = dev_bf16(x), [dev_u8(q) for q in qws], [dev_f32(s) for s in s_ws]
+    ws = W.w8a16_workspace(wd)
+    ys = W.qkv_shared_quant_gemm(W.MODE_A16, xd, None, wd, sd, ws=ws)
+    yf = W.qkv_shared_quant_gemm(W.MODE_A16, xd, None, wd, sd)
+    torch.cuda.synchronize()
+    W.poll_device_error()
+    ref = O.qkv_shared_quant_gemm("A16", x, None, qws, s_ws)
+    off = 0
+    for y, f, (r64, _), q, s in zip(ys, yf, ref, qws, s_ws):
+        assert gemm_err(host_bits(y), r64) <= GEMM_TOL
+        assert gemm_err(host_bits(f), r64) <= GEMM_TOL
+        # the workspace holds the dequantized weight, bit for bit
+        n = q.size
+        assert np.array_equal(host_bits(ws[off:off + n]).reshape(q.shape), O.dequant_weight_bf16(q, s))
+        off += n
+
+
+def test_a16_workspace_exact_sums_bit_exact(W):
+    """Operands whose partial sums are exact in any order: the two-pass
+    result equals the oracle bit for bit (pair and single-CTA tiles)."""
+    rng = np.random.default_rng(1)
+    for M in (100, 900):
+        K, N = 2048, 400
+        xv = np.array([0.0, 0.25, -0.25, 0.5, -1.0, 1.5, 2.0, -3.0], np.float32)
+        x = torch.from_numpy(rng.choice(xv, size=(M, K))).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        qw = O.e4m3_encode(rng.choice(np.array([0.0, 1.0, -1.0, 2.0, -0.5, 3.0], np.float32), size=(N, K)))
+        s_w = np.float32(2.0 ** -4)
+        wd = [dev_u8(qw)]
+        y = W.qkv_shared_quant_gemm(W.MODE_A16, dev_bf16(x), None, wd, [dev_f32(s_w)], ws=W.w8a16_workspace(wd))
+        _, want = O.linear_w8a16(x, qw, s_w)
+        assert np.array_equal(host_bits(y[0]), want)
+
+
+def test_a16_workspace_full_size_sampled(W):
+    """20670 tokens, the Q/K/V group: sampled rows and the tail."""
+    M, K = 20670, 4096
+    x, qws, s_ws = _group(M, K, (4096, 4096, 4096))
+    xd, wd, sd = dev_bf16(x), [dev_u8(q) for q in qws], [dev_f32(s) for s in s_ws]
+    ys = W.qkv_shared_quant_gemm(W.MODE_A16, xd, None, wd, sd, ws=W.w8a16_workspace(wd))
+    rows = np.concatenate([synth.random_rows(8, M, 128), np.arange(M - 62, M)])
+    for y, q, s in zip(ys, qws, s_ws):
+        r16, _ = O.linear_w8a16(x, q, s, rows=rows)
+        assert gemm_err(host_bits(y)[rows], r16) <= GEMM_TOL
+
+
+def test_workspace_too_small_is_refused(W):
+    x = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    w = [torch.zeros((256, 256), dtype=torch.uint8, device="cuda")]
+    with pytest.raises(W.W8Error):
+        W.qkv_shared_quant_gemm(W.MODE_A16, x, None, w, [dev_f32(1.0)],
+                                ws=torch.empty((100,), dtype=torch.bfloat16, device="cuda"))

@@ -55,6 +55,7 @@ SIGNATURES = {
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_i64),
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
                                              _c_void_p, _c_void_p]),
+    "fp8_dequant_weight": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
     "fp8_linear_w8a8_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i32,
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_i64),
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
@@ -233,14 +234,40 @@ def qkv_shared_quant_gemm(mode, x, s_in, weights, weight_scales, outs=None, ws=N
         _as_bf16(o, f"y[{i}]")
     if mode == MODE_A8 and ws is None:
         ws = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if mode == MODE_A8 or ws is None:
+        ws_p = _ptr(_as_u8(ws, "ws") if ws is not None else None)
+    else:   # A16 with a workspace: room for the group's dequantized bf16 weights
+        _as_bf16(ws, "ws")
+        need = sum(int(w.shape[0]) * K for w in ws_q)
+        if ws.numel() < need:
+            raise W8Error(2, f"ws: {ws.numel()} bf16 values, the group needs {need}")
+        ws_p = _ptr(ws)
     arr_w = (ctypes.c_void_p * G)(*[w.data_ptr() for w in ws_q])
     arr_n = (ctypes.c_int64 * G)(*[w.shape[0] for w in ws_q])
     arr_s = (ctypes.c_void_p * G)(*[_scalar(s, f"s_w[{i}]").data_ptr() for i, s in enumerate(weight_scales)])
     arr_y = (ctypes.c_void_p * G)(*[o.data_ptr() for o in outs])
     s_in_p = _ptr(_scalar(s_in, "s_in")) if s_in is not None else ctypes.c_void_p(0)
     _check(lib().qkv_shared_quant_gemm(mode, _ptr(x2), M, K, s_in_p, G, arr_w, arr_n, arr_s, arr_y,
-                                       _ptr(_as_u8(ws, "ws") if ws is not None else None), _stream(stream)))
+                                       ws_p, _stream(stream)))
     return outs
+
+
+def fp8_dequant_weight(w, s_w, out=None, stream=None):
+    """bf16 [N, K] = bf16(fl32(dec(w) * s_w)): the W8A16 step's transient weight."""
+    wq = _as_u8(w, "w")
+    N, K = wq.shape
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.bfloat16, device=wq.device)
+    _check(lib().fp8_dequant_weight(_ptr(wq), N, K, _ptr(_scalar(s_w, "s_w")), _ptr(_as_bf16(out, "out")),
+                                    _stream(stream)))
+    return out
+
+
+def w8a16_workspace(weights):
+    """bf16 scratch for qkv_shared_quant_gemm(MODE_A16, ..., ws=...): room for
+    the group's dequantized weights (caller-side allocation)."""
+    n = sum(int(w.shape[0]) * int(w.shape[1]) for w in weights)
+    return torch.empty((n,), dtype=torch.bfloat16, device=weights[0].device)
 
 
 def fp8_linear_w8a8_group(qx, s_in, weights, weight_scales, outs=None, stream=None):

@@ -231,8 +231,8 @@ w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int6
   if (mode == W8_MODE_A8) {
     if (!s_in) return fail(W8_ERR_NULL, "qkv_shared_quant_gemm: NULL s_in");
     if (!ws) return fail(W8_ERR_NULL, "qkv_shared_quant_gemm: A8 needs the [M,K] E4M3 workspace");
-    if (!aligned16(ws)) return fail(W8_ERR_ALIGN, "qkv_shared_quant_gemm: ws must be 16-byte aligned");
   }
+  if (ws && !aligned16(ws)) return fail(W8_ERR_ALIGN, "qkv_shared_quant_gemm: ws must be 16-byte aligned");
   int sms = 0;
   w8_status st = device_info(&sms);
   if (st != W8_OK) return st;
@@ -255,12 +255,37 @@ w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int6
     p.x = ws;
     p.s_in = s_in;
     e = w8::launch_gemm_w8a8(p, sms, s, &terr);
+  } else if (ws) {
+    // dequant + F.linear: the group's weights into ws, then one bf16 launch
+    uint16_t* wd = reinterpret_cast<uint16_t*>(ws);
+    for (int g = 0; g < G; ++g) {
+      e = w8::launch_dequant_weight(w[g], N[g] * K, s_w[g], wd, sms, s);
+      if (e != cudaSuccess) return cuda_status(e, "qkv_shared_quant_gemm: dequantization launch");
+      p.w[g] = reinterpret_cast<const uint8_t*>(wd);
+      wd += N[g] * K;
+    }
+    p.x = x;
+    e = w8::launch_gemm_bf16(p, sms, s, &terr);
   } else {
     p.x = x;
     e = w8::launch_gemm_w8a16(p, sms, s, &terr);
   }
   if (terr) return fail(W8_ERR_ALIGN, "qkv_shared_quant_gemm: tensor map encoding rejected the operands");
   return cuda_status(e, "qkv_shared_quant_gemm: GEMM launch");
+}
+
+w8_status fp8_dequant_weight(const uint8_t* w, int64_t N, int64_t K, const float* s_w, uint16_t* wd,
+                             void* stream) {
+  if (N < 0 || K < 0) return fail(W8_ERR_SHAPE, "fp8_dequant_weight: N=%lld K=%lld", (long long)N, (long long)K);
+  if (K % 16) return fail(W8_ERR_SHAPE, "fp8_dequant_weight: K=%lld is not a multiple of 16", (long long)K);
+  if (N == 0 || K == 0) return ok();
+  if (!w || !s_w || !wd) return fail(W8_ERR_NULL, "fp8_dequant_weight: NULL pointer");
+  if (!aligned16(w) || !aligned16(wd)) return fail(W8_ERR_ALIGN, "fp8_dequant_weight: w and wd must be 16-byte aligned");
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  if (st != W8_OK) return st;
+  return cuda_status(w8::launch_dequant_weight(w, N * K, s_w, wd, sms, static_cast<cudaStream_t>(stream)),
+                     "fp8_dequant_weight launch");
 }
 
 w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const float* s_in,

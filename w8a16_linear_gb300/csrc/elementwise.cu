@@ -111,6 +111,39 @@ __global__ void __launch_bounds__(256, 6) swiglu_bf16_kernel(const uint16_t* __r
   }
 }
 
+// ------------------------------------------------------------------ weight dequantization
+//
+// Wd = bf16_RNE(fl32(dec(q) * s_w)): the W8A16 step's transient bf16 weight
+// ("dequant + F.linear").  E4M3 -> f16 is exact (cvt e4m3x2 -> f16x2), f16 ->
+// f32 exact, one correctly rounded binary32 multiply, one bf16 rounding.
+
+__global__ void __launch_bounds__(256, 8) dequant_weight_kernel(const uint8_t* __restrict__ q, int64_t n16,
+                                                                const float* __restrict__ s_w,
+                                                                uint16_t* __restrict__ wd) {
+  const float sw = __ldg(s_w);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    const uint4 c = ldg16(q + i * 16);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] & 0xFFFF));
+      const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] >> 16));
+      F2 a, b;
+      f16x2_to_f32(f01, a.x, a.y);
+      f16x2_to_f32(f23, b.x, b.y);
+      a = mul2(a, splat(sw));
+      b = mul2(b, splat(sw));
+      o[2 * e] = cvt_bf16x2(a.x, a.y);
+      o[2 * e + 1] = cvt_bf16x2(b.x, b.y);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(wd + i * 16);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // The SwiGLU variants (swiglu_spec.cuh): bf16 or binary16 inputs, FP8 output
 // or a 16-bit output in the input's format.
 template <bool kF16, bool kFp8>
@@ -170,6 +203,13 @@ cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bo
     if (out_fp8) swiglu_ex_kernel<false, true><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
     else swiglu_ex_kernel<false, false><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w, uint16_t* wd, int sms,
+                                  cudaStream_t st) {
+  const int64_t n16 = n / 16;
+  dequant_weight_kernel<<<grid_for(n16, sms), 256, 0, st>>>(q, n16, s_w, wd);
   return cudaGetLastError();
 }
 

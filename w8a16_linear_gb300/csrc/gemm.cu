@@ -65,11 +65,15 @@ constexpr uint32_t kAccCols = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kEpiBufBytes = 32 * 128;            // W8A8 staging: 32 rows x 64 bf16
 
-enum class Mode { W8A8, GLU };
+enum class Mode { W8A8, GLU, BF16 };
 
 template <Mode MODE, int CG>
 struct Cfg {
   static constexpr bool kGlu = (MODE == Mode::GLU);
+  // BF16: the W8A16 product on an already dequantized weight (bf16 x bf16,
+  // kind::f16): the same tiles and pipeline with 64 K-values (128 bytes) per
+  // stage and an unscaled epilogue.
+  static constexpr bool kBf16 = (MODE == Mode::BF16);
   // W8A8: 256 output columns per tile.  GLU: 128 intermediate columns per
   // tile, computed by one N = 256 MMA whose B operand is [128 gate rows | 128
   // up rows] of the slice: D columns 0-127 hold gate, 128-255 hold up, and
@@ -78,11 +82,12 @@ struct Cfg {
   static constexpr int kBN = kGlu ? 128 : 256;              // output columns per tile
   static constexpr int kMmaN = 256;
   static constexpr int kBRows = kMmaN / CG;                 // weight rows staged per CTA
-  static constexpr int kBK = 128;                           // K per stage (bytes = elements)
+  static constexpr int kBK = kBf16 ? 64 : 128;              // K per stage (128 bytes per row)
   static constexpr int kABytes = BM * 128;
   static constexpr int kBBytes = kBRows * 128;
   static constexpr int kStages = CG == 1 ? 4 : 6;
-  static constexpr uint32_t kIdesc = make_idesc(0, 0, BM * CG, kMmaN);  // E4M3 x E4M3 -> F32
+  static constexpr uint32_t kIdesc =                        // E4M3 x E4M3 or BF16 x BF16 -> F32
+      kBf16 ? make_idesc(1, 1, BM * CG, kMmaN) : make_idesc(0, 0, BM * CG, kMmaN);
   // GLU: two warps per TMEM lane quadrant (64 columns each) to keep the
   // SwiGLU epilogue ahead of the tensor cores; staging 32 rows x 64 codes.
   static constexpr int kEpiWarps = kGlu ? 8 : 4;
@@ -310,8 +315,13 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
             const uint64_t ad = sw128_kmajor_desc(a_addr + 32 * k);
             const uint64_t bd = sw128_kmajor_desc(b_addr + 32 * k);
             const uint32_t accum = (kb | k) != 0;
-            if constexpr (CG == 2) mma_f8f6f4_pair(d, ad, bd, C::kIdesc, accum);
-            else mma_f8f6f4(d, ad, bd, C::kIdesc, accum);
+            if constexpr (C::kBf16) {  // K = 16 per MMA: 32 bytes, as for E4M3
+              if constexpr (CG == 2) mma_f16_pair(d, ad, bd, C::kIdesc, accum);
+              else mma_f16(d, ad, bd, C::kIdesc, accum);
+            } else {
+              if constexpr (CG == 2) mma_f8f6f4_pair(d, ad, bd, C::kIdesc, accum);
+              else mma_f8f6f4(d, ad, bd, C::kIdesc, accum);
+            }
           }
           if constexpr (CG == 2) mma_commit_pair_mc(empty_bar(s), 0x3);
           else mma_commit(empty_bar(s));
@@ -355,7 +365,8 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       int m0, g, n0;
       decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
       float alpha = 1.0f, alpha_u = 1.0f;
-      alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, kGlu ? 0 : g)));
+      // BF16: the scale is already in the dequantized weight; y = bf16(acc).
+      if constexpr (!C::kBf16) alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, kGlu ? 0 : g)));
       if constexpr (kGlu) alpha_u = __fmul_rn(__ldg(args.s_in), __ldg(args.s_w[1]));
       // Warp-uniform wait: the TMEM loads below are .sync.aligned.
       if (!mbar_wait_warp(tfull_bar(acc), acc_ph, abort, kWaitLimitNs)) {
@@ -820,13 +831,14 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   args.s_in = p.s_in;
   args.s_out = p.s_out;
   const int tiles_m = (int)((p.M + BM * CG - 1) / (BM * CG));
-  bool ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.x, p.K, p.M, p.K, 128, BM,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+  constexpr int kEl = C::kBf16 ? 2 : 1;  // operand element bytes
+  const CUtensorMapDataType dt = C::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  bool ok = encode_2d(&maps.a, dt, p.x, p.K, p.M, p.K * kEl, C::kBK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   const int nb = kGlu ? 2 : p.G;  // weight maps: GLU gate and up
   for (int g = 0; g < nb; ++g) {
     args.s_w[g] = p.s_w[g];
-    ok &= encode_2d(&maps.b[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w[g], p.K, p.N[kGlu ? 0 : g], p.K,
-                    128, kGlu ? 128 : C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_2d(&maps.b[g], dt, p.w[g], p.K, p.N[kGlu ? 0 : g], p.K * kEl, C::kBK,
+                    kGlu ? 128 : C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   for (int g = 0; g < args.G; ++g) {
     args.N[g] = (int)p.N[g];
@@ -846,7 +858,7 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   }
   args.num_tiles = tiles_m * args.tiles_per_m;
   args.tiles_m = tiles_m;
-  args.group_m = group_rows(BM * CG, p.K, 1, tiles_m);
+  args.group_m = group_rows(BM * CG, p.K, kEl, tiles_m);
   const int max_clusters = sms / CG;
   const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   return launch_cluster(gemm_kernel<MODE, CG>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
@@ -921,6 +933,11 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
 cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
   return use_pair(p) ? launch<Mode::W8A8, 2>(p, sms, st, tmap_err)
                      : launch<Mode::W8A8, 1>(p, sms, st, tmap_err);
+}
+
+cudaError_t launch_gemm_bf16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  return use_pair(p) ? launch<Mode::BF16, 2>(p, sms, st, tmap_err)
+                     : launch<Mode::BF16, 1>(p, sms, st, tmap_err);
 }
 
 cudaError_t launch_gemm_glu(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {

@@ -21,6 +21,9 @@ cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, c
 cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* out,
                                int sms, cudaStream_t st);
 
+cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w, uint16_t* wd, int sms,
+                                  cudaStream_t st);
+
 struct SwigluExArgs {            // validated by the caller
   bool has_limit;
   float limit, alpha, beta;
@@ -50,6 +53,9 @@ cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int
 cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 // Gate/up W8A8 GEMMs with the SwiGLU-to-E4M3 epilogue: x E4M3 [M,K], w[0] gate
 // and w[1] up [I,K] with s_w[0], s_w[1]; N[0] = I; y[0] E4M3 [M,I]; s_out.
+// bf16 x bf16 GEMM of the W8A16 step on weights dequantized beforehand:
+// y_g = bf16(x . Wd_g^T), x bf16 [M,K], Wd_g bf16 [N_g,K] in w[g] (s_w unused).
+cudaError_t launch_gemm_bf16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 cudaError_t launch_gemm_glu(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 
 // Launches a one-thread kernel whose mbarrier wait times out (0.2 s).
