@@ -163,8 +163,19 @@ class Block:
         self.q_out = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
         self.q_mlp = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
         self.side = torch.cuda.Stream(device=dev)
-        # W8A16 steps: transient bf16 weights of the largest group (gate/up)
+        # W8A16 steps: transient bf16 weights of the largest group (gate/up) for
+        # the one-call form, and of every site of the block for the scheduled
+        # form (dequantized on a side stream ahead of the GEMMs that read them)
         self.wsd = torch.empty((2 * INTER * HID,), dtype=torch.bfloat16, device=dev)
+        wd_all = torch.empty((4 * HID * HID + 3 * INTER * HID,), dtype=torch.bfloat16, device=dev)
+        shapes = [(HID, HID)] * 4 + [(INTER, HID)] * 2 + [(HID, INTER)]
+        views, off = [], 0
+        for n_, k_ in shapes:
+            views.append(wd_all[off:off + n_ * k_].view(n_, k_))
+            off += n_ * k_
+        self.wd_qkv, self.wd_out, self.wd_gu, self.wd_down = views[:3], views[3], views[4:6], views[6]
+        self.dq = torch.cuda.Stream(device=dev)
+        self.dq_ev = [torch.cuda.Event() for _ in range(4)]
 
     def outputs(self):
         return self.y_qkv + [self.y_out, self.y_down]
@@ -218,15 +229,27 @@ class Block:
                 W.swiglu_2in_fp8(self.y_gu[0], self.y_gu[1], self.s_h, out=self.h8)
             W.fp8_linear_w8a8(self.h8, self.w_down[0], self.s_h, self.w_down[1], out=self.y_down)
             return 7 if fused else 8
-        # dequant + F.linear: each site's weights into the workspace, then one
-        # bf16 GEMM launch per site
-        W.qkv_shared_quant_gemm(W.MODE_A16, x_qkv, None, wq, sq, outs=self.y_qkv, ws=self.wsd)
-        W.qkv_shared_quant_gemm(W.MODE_A16, x_out, None, [self.w_out[0]], [self.w_out[1]], outs=[self.y_out],
-                                ws=self.wsd)
-        W.qkv_shared_quant_gemm(W.MODE_A16, x_mlp, None, wgu, sgu, outs=self.y_gu, ws=self.wsd)
+        # dequant + F.linear, scheduled: the weights do not depend on the
+        # activations, so all seven dequantizations run on a side stream in
+        # the order the GEMMs need them, overlapping the earlier GEMMs
+        main = torch.cuda.current_stream()
+        self.dq.wait_stream(main)          # the previous step's GEMMs are done with the buffers
+        sites = [(list(zip(wq, sq)), self.wd_qkv), ([self.w_out], [self.wd_out]),
+                 (list(zip(wgu, sgu)), self.wd_gu), ([self.w_down], [self.wd_down])]
+        with torch.cuda.stream(self.dq):
+            for (ws_, outs_), ev in zip(sites, self.dq_ev):
+                for (q, sc), o in zip(ws_, outs_):
+                    W.fp8_dequant_weight(q, sc, out=o)
+                ev.record(self.dq)
+        main.wait_event(self.dq_ev[0])
+        W.bf16_linear_group(x_qkv, self.wd_qkv, outs=self.y_qkv)
+        main.wait_event(self.dq_ev[1])
+        W.bf16_linear_group(x_out, [self.wd_out], outs=[self.y_out])
+        main.wait_event(self.dq_ev[2])
+        W.bf16_linear_group(x_mlp, self.wd_gu, outs=self.y_gu)
         W.swiglu_2in_bf16(self.y_gu[0], self.y_gu[1], out=self.h16)
-        W.qkv_shared_quant_gemm(W.MODE_A16, self.h16, None, [self.w_down[0]], [self.w_down[1]],
-                                outs=[self.y_down], ws=self.wsd)
+        main.wait_event(self.dq_ev[3])
+        W.bf16_linear_group(self.h16, [self.wd_down], outs=[self.y_down])
         return 12
 
 

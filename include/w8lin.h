@@ -188,6 +188,18 @@ w8_status fp8_dequant_weight(const uint8_t* w, int64_t N, int64_t K, const float
                              void* stream);
 
 /*
+ * bf16_linear_group — the "F.linear" half of the W8A16 path ([P3] Behavior:
+ * dequant + F.linear) on weights already dequantized by fp8_dequant_weight:
+ * G projections (1..3) of one bf16 activation in one launch,
+ * y_g = bf16_RNE( x . Wd_g^T ) with fp32 accumulation.
+ *   x    bf16 [M, K], device;  wd, N, y: HOST arrays of G entries: device
+ *   bf16 weight [N_g, K], its row count, device bf16 output [M, N_g]
+ * Errors: NULL, SHAPE (G outside 1..3, K%16, N_g%16), ALIGN, ARCH, CUDA.
+ */
+w8_status bf16_linear_group(const uint16_t* x, int64_t M, int64_t K, int32_t G, const uint16_t* const* wd,
+                            const int64_t* N, uint16_t* const* y, void* stream);
+
+/*
  * fp8_linear_w8a8_group — the GEMM half of qkv_shared_quant_gemm in A8 mode:
  * G projections (1..3) over an activation that is ALREADY E4M3, quantized
  * with s_in (for example by fp8_quant_static or swiglu_2in_fp8), in one

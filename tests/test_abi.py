@@ -94,6 +94,13 @@ def test_validation_before_any_cuda_call(L):
     assert L.swiglu_2in_fp8(p16, p16, 4, 24, p16, p16, None) == 2
     assert L.swiglu_2in_fp8(p16, p16, 4, 16, None, p16, None) == 1
     assert L.swiglu_2in_bf16(p16, _u(0x10004), 4, 16, p16, None) == 3
+    # dequantization and the bf16 group GEMM
+    assert L.fp8_dequant_weight(p16, 16, 24, p16, p16, None) == 2
+    assert L.fp8_dequant_weight(None, 16, 16, p16, p16, None) == 1
+    assert L.fp8_dequant_weight(p16, 0, 16, p16, p16, None) == 0
+    assert L.bf16_linear_group(p16, 4, 16, 4, arr, ns, arr, None) == 2
+    assert L.bf16_linear_group(p16, 4, 16, 3, None, ns, arr, None) == 1
+    assert L.bf16_linear_group(p16, 0, 16, 3, arr, ns, arr, None) == 0
     # group-scale check arguments
     assert L.w8_check_group_scales(None, 3) == 1
     assert L.w8_check_group_scales(arr, 0) == 2

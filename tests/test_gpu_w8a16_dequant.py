@@ -93,3 +93,17 @@ def test_workspace_too_small_is_refused(W):
     with pytest.raises(W.W8Error):
         W.qkv_shared_quant_gemm(W.MODE_A16, x, None, w, [dev_f32(1.0)],
                                 ws=torch.empty((100,), dtype=torch.bfloat16, device="cuda"))
+
+
+def test_bf16_linear_group_on_dequantized_weights(W):
+    """The F.linear half on its own: dequantize each weight, then one group
+    launch; equals qkv_shared_quant_gemm(A16, ws) bit for bit."""
+    x, qws, s_ws = _group(1000, 512, (512, 256, 768))
+    xd, wd, sd = dev_bf16(x), [dev_u8(q) for q in qws], [dev_f32(s) for s in s_ws]
+    wdq = [W.fp8_dequant_weight(w, s) for w, s in zip(wd, sd)]
+    ys = W.bf16_linear_group(xd, wdq)
+    yw = W.qkv_shared_quant_gemm(W.MODE_A16, xd, None, wd, sd, ws=W.w8a16_workspace(wd))
+    ref = O.qkv_shared_quant_gemm("A16", x, None, qws, s_ws)
+    for y, y2, (r64, _) in zip(ys, yw, ref):
+        assert gemm_err(host_bits(y), r64) <= GEMM_TOL
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))

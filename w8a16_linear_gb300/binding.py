@@ -56,6 +56,8 @@ SIGNATURES = {
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
                                              _c_void_p, _c_void_p]),
     "fp8_dequant_weight": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "bf16_linear_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _i32, ctypes.POINTER(_c_void_p),
+                                         ctypes.POINTER(_i64), ctypes.POINTER(_c_void_p), _c_void_p]),
     "fp8_linear_w8a8_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i32,
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_i64),
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
@@ -261,6 +263,24 @@ def fp8_dequant_weight(w, s_w, out=None, stream=None):
     _check(lib().fp8_dequant_weight(_ptr(wq), N, K, _ptr(_scalar(s_w, "s_w")), _ptr(_as_bf16(out, "out")),
                                     _stream(stream)))
     return out
+
+
+def bf16_linear_group(x, wds, outs=None, stream=None):
+    """y_g = bf16(x . Wd_g^T) for dequantized bf16 weights Wd_g (one launch)."""
+    x = _as_bf16(x, "x")
+    x2 = _flat2(x)
+    M, K = x2.shape
+    G = len(wds)
+    wq = [_as_bf16(w, f"wd[{i}]") for i, w in enumerate(wds)]
+    if outs is None:
+        outs = [torch.empty(*x.shape[:-1], w.shape[0], dtype=torch.bfloat16, device=x.device) for w in wq]
+    for i, o in enumerate(outs):
+        _as_bf16(o, f"y[{i}]")
+    arr_w = (ctypes.c_void_p * G)(*[w.data_ptr() for w in wq])
+    arr_n = (ctypes.c_int64 * G)(*[w.shape[0] for w in wq])
+    arr_y = (ctypes.c_void_p * G)(*[o.data_ptr() for o in outs])
+    _check(lib().bf16_linear_group(_ptr(x2), M, K, G, arr_w, arr_n, arr_y, _stream(stream)))
+    return outs
 
 
 def w8a16_workspace(weights):

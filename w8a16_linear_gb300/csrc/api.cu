@@ -288,6 +288,37 @@ w8_status fp8_dequant_weight(const uint8_t* w, int64_t N, int64_t K, const float
                      "fp8_dequant_weight launch");
 }
 
+w8_status bf16_linear_group(const uint16_t* x, int64_t M, int64_t K, int32_t G, const uint16_t* const* wd,
+                            const int64_t* N, uint16_t* const* y, void* stream) {
+  if (G < 1 || G > w8::kMaxGroup)
+    return fail(W8_ERR_SHAPE, "bf16_linear_group: group size %d outside 1..3", G);
+  if (!wd || !N || !y) return fail(W8_ERR_NULL, "bf16_linear_group: NULL host array");
+  static const float kOne = 1.0f;  // placeholder scale: the common check wants a pointer
+  for (int g = 0; g < G; ++g) {
+    w8_status st = check_linear_common("bf16_linear_group", x, M, K, reinterpret_cast<const uint8_t*>(wd[g]),
+                                       N[g], &kOne, y[g]);
+    if (st != W8_OK) return st;
+  }
+  if (M == 0) return ok();
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  if (st != W8_OK) return st;
+  w8::GemmProblem p{};
+  p.M = M;
+  p.K = K;
+  p.G = G;
+  p.x = x;
+  for (int g = 0; g < G; ++g) {
+    p.w[g] = reinterpret_cast<const uint8_t*>(wd[g]);
+    p.N[g] = N[g];
+    p.y[g] = y[g];
+  }
+  int terr = 0;
+  cudaError_t e = w8::launch_gemm_bf16(p, sms, static_cast<cudaStream_t>(stream), &terr);
+  if (terr) return fail(W8_ERR_ALIGN, "bf16_linear_group: tensor map encoding rejected the operands");
+  return cuda_status(e, "bf16_linear_group: GEMM launch");
+}
+
 w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const float* s_in,
                                 int32_t G, const uint8_t* const* w, const int64_t* N,
                                 const float* const* s_w, uint16_t* const* y, void* stream) {
