@@ -597,6 +597,20 @@ def run_case(args):
         fn = lambda: blk.gemm_launches(W, *qa)  # noqa: E731
     elif args.case == "qkv8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A8, x, s, qs, ss, outs=ys, ws=qx)  # noqa: E731
+    elif args.case == "w8a16_dq_8k":
+        # dequant + F.linear: the three weights into a workspace, one bf16 group GEMM
+        wsd = W.w8a16_workspace(qs)
+        fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, qs, ss, outs=ys, ws=wsd)  # noqa: E731
+    elif args.case == "swiglu_ex8k":
+        gg = (torch.randn((M, INTER), generator=gen, device=dev) * 2).to(torch.float16)
+        uu = torch.randn((M, INTER), generator=gen, device=dev).to(torch.float16)
+        h8 = torch.empty((M, INTER), dtype=torch.uint8, device=dev)
+        h16 = torch.empty((M, INTER), dtype=torch.float16, device=dev)
+        opts = dict(limit=7.0, alpha=1.702, beta=1.0)
+
+        def fn():
+            W.swiglu_2in_ex_fp8(gg, uu, s, out=h8, **opts)
+            W.swiglu_2in_ex_16(gg, uu, out=h16, **opts)
     elif args.case == "w8a16_8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, qs, ss, outs=ys)  # noqa: E731
     elif args.case == "glu8k":
@@ -658,7 +672,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="run a profiling case (qkv8k, w8a16_8k, glu8k, swiglu8k, block_gemms) instead of the bench")
+                    help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, swiglu8k, swiglu_ex8k, block_gemms) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.case:
