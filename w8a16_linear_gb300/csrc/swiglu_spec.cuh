@@ -178,17 +178,17 @@ __device__ __forceinline__ bool scale_is_fast(float s, float r) {
 // FP8 output.  Fast value, elementwise: p = g * u (exact, as specified),
 // d' = fl(1 + __expf(-g)), q' = fl(fl(p * rcp.approx(d')) * fl(1/s)).
 // Error budget against the specified q = fl(fl(p / d) / s), relative, in
-// units of 2^-24, for gates g >= -8 (t = -g <= 8):
-//   __expf(t): documented within 2 + floor(|1.173 t|) ulp of e^t, at most 11
-//     ulp (22) for 0 < t <= 8; for t <= 0 its share of d = 1 + e is below
+// units of 2^-24, for gates g >= -16 (x = -g <= 16):
+//   __expf(x): documented within 2 + floor(|1.173 x|) ulp of e^x, at most 20
+//     ulp (40) for 0 < x <= 16; for x <= 0 its share of d = 1 + e is below
 //     2^-23 (2) because e / (1 + e) shrinks faster than the bound grows;
-//     plus the rounding of 1 + e (1)                                      <= 23
-//   the specified d against 1 + e^t (exp_spec checked exhaustively on
+//     plus the rounding of 1 + e (1)                                      <= 41
+//   the specified d against 1 + e^x (exp_spec checked exhaustively on
 //     every bf16 argument on the host: within 1.5)                       <= 1.5
 //   rcp.approx: documented within 1 ulp                                    <= 2
 //   roundings of p * r, of fl(1/s), of q' and the specification's two      <= 5
-// in all below 32 (2^-19), under the bracket's 2^-18 - 2^-24.  Gates below
-// -8 (and -inf) take the exact path.  A scale with |1/s| > 2^20 (or 1/s not
+// in all below 50, under the bracket's 2^-18 - 2^-24 (63).  Gates below
+// -16 (and -inf) take the exact path.  A scale with |1/s| > 2^20 (or 1/s not
 // normal) sends every element to the exact path: with |1/s| <= 2^20 a
 // binary32-subnormal h' (absolute error 2^-149, not relative) maps to
 // |q| < 2^-106, code 0 either way, with the same sign.
@@ -237,7 +237,7 @@ __device__ __forceinline__ uint32_t swiglu_fp8_exact_pair(uint32_t gw, uint32_t 
 }
 
 // Fast codes of a pair; `unsettled` when the bracket does not settle them or
-// a gate is below -8.
+// a gate is below -16.
 __device__ __forceinline__ uint32_t swiglu_fp8_fast_pair(uint32_t gw, uint32_t uw, float rs,
                                                          bool& unsettled) {
   const F2 g{bf16_lo(gw), bf16_hi(gw)};
@@ -245,7 +245,7 @@ __device__ __forceinline__ uint32_t swiglu_fp8_fast_pair(uint32_t gw, uint32_t u
   const F2 d = add2(splat(1.0f), F2{__expf(-g.x), __expf(-g.y)});
   const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
   const uint32_t code = e4m3x2_bracket(mul2(hf, splat(rs)), kFp8BracketLo, kFp8BracketHi, unsettled);
-  unsettled |= (g.x < -8.0f) | (g.y < -8.0f);
+  unsettled |= (g.x < -16.0f) | (g.y < -16.0f);
   return code;
 }
 
@@ -309,7 +309,7 @@ __device__ __forceinline__ void swiglu_fp8_x16(const uint32_t (&gw)[8], const ui
 //   p = fl32(g * u), h = fl32(p / fl32(1 + exp_spec(-t)))
 // With a = 1, b = 0 and no limit this is the base specification bit for bit.
 // The fast paths are the base ones with t in place of g: FP8 output through
-// __expf and the 2^-18 bracket (exact path for t < -8); 16-bit output with
+// __expf and the 2^-18 bracket (exact path for t < -16); 16-bit output with
 // p * rcp.approx(d'), d' = dplus1_fast (within 8 * 2^-24 of the specified h,
 // as for the bf16 output above) and a 2^-20 bracket on the packed 16-bit
 // conversion, plus the d' >= 2^126 and tiny-h guards.
@@ -336,10 +336,19 @@ __device__ __forceinline__ F2 unpack16(uint32_t w) {
   }
 }
 
-__device__ __forceinline__ float clamp_hi(float v, float lim) { return v > lim ? lim : v; }
-__device__ __forceinline__ float clamp_sym(float v, float lim) {
-  return v > lim ? lim : (v < -lim ? -lim : v);
+// NaN-propagating min / max (a NaN input gives NaN, as the clamps specify).
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float clamp_hi(float v, float lim) { return min_nan(v, lim); }
+__device__ __forceinline__ float clamp_sym(float v, float lim) { return min_nan(max_nan(v, -lim), lim); }
 
 // t = fl32(a * g) and p = fl32(g * (u + b)) of a pair, after the clamps.
 template <bool kF16>
@@ -364,7 +373,7 @@ __device__ __forceinline__ uint32_t swiglu_ex_fp8_pair(uint32_t gw, uint32_t uw,
   const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
   bool unsettled;
   const uint32_t code = e4m3x2_bracket(mul2(hf, splat(rs)), kFp8BracketLo, kFp8BracketHi, unsettled);
-  if (exact_only | unsettled | (t.x < -8.0f) | (t.y < -8.0f)) {   // rare
+  if (exact_only | unsettled | (t.x < -16.0f) | (t.y < -16.0f)) {   // rare
     const F2 de = add2(splat(1.0f), exp_spec2(neg(t)));
     return cvt_e4m3x2(__fdiv_rn(__fdiv_rn(p.x, de.x), s), __fdiv_rn(__fdiv_rn(p.y, de.y), s));
   }
