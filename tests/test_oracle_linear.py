@@ -211,3 +211,38 @@ def test_requant_by_exact_half_is_lossless_above_subnormals():
     s1, s2 = np.float32(0.25), np.float32(0.5)
     fused, _ = O.requant_onto_max_scale([codes[fin], codes[fin]], [s1, s2])
     assert np.array_equal(O.e4m3_decode(fused[0]) * s2, vals[fin] * s1)
+
+
+def test_fused_requant_error_against_the_numerical_floor():
+    """Context, not a target ([P4] Description: re-quantizing onto max(s)
+    added error several times the numerical floor).  Reference: the float64
+    product on the exact checkpoint weights s_i * dec(qW_i) with the same
+    quantized activation; the split path's only error is then the bf16 output
+    rounding (the floor).  The fused variant re-rounds the weights of every
+    member whose scale is below max(s): its error is many times the floor,
+    while the max-scale member is unchanged (ratio exactly 1)."""
+    M, K, N = 256, 1024, 512
+    x = synth.activations_bf16(0, (M, K), 0.25, outlier_frac=0.001)
+    s_in = np.float32(np.abs(O.bf16_decode(x)).max() / 448)
+    qx = O.quant_static(x, s_in)
+    c = synth.uniform_f32(3, (3,), 0.5, 1.0)
+    qws, s_ws = [], []
+    for i in range(3):
+        w = synth.normal_f32(10 + i, (N, K), 0.02) * c[i]
+        s = np.float32(np.abs(w).max() / 448)
+        qws.append(O.e4m3_encode(w / s))
+        s_ws.append(s)
+    fused, s_max = O.requant_onto_max_scale(qws, s_ws)
+    ratios = []
+    for q, s, qf in zip(qws, s_ws, fused):
+        y64, yb = O.linear_w8a8(qx, q, s_in, s)
+        _, fb = O.linear_w8a8(qx, qf, s_in, s_max)
+        floor = np.linalg.norm(O.bf16_decode(yb).astype(np.float64) - y64)
+        err = np.linalg.norm(O.bf16_decode(fb).astype(np.float64) - y64)
+        ratios.append(err / floor)
+    print("fused-requant error / floor:", [round(r, 2) for r in ratios])
+    for r, s in zip(ratios, s_ws):
+        if s == s_max:
+            assert r == 1.0
+        else:
+            assert r > 3.0
