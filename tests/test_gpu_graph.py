@@ -1,6 +1,7 @@
 """The path's entry points only enqueue work on the caller's stream, so a
 whole W8A8 block (shared-quant Q/K/V group, out-projection, fused gate/up +
-SwiGLU, down projection) and a W8A16 block can be captured in a CUDA graph;
+SwiGLU, down projection) and a W8A16 block (fused, and through the
+dequantization workspace) can be captured in a CUDA graph;
 replaying the graph reproduces the eager results bit for bit."""
 
 import numpy as np
@@ -38,7 +39,10 @@ def test_block_in_cuda_graph(W):
         "gu16": [torch.empty((M, I), **bf) for _ in range(2)],
         "h16": torch.empty((M, I), **bf),
         "y16": torch.empty((M, H), **bf),
+        "qkv16w": [torch.empty((M, H), **bf) for _ in range(3)],
+        "y16w": torch.empty((M, H), **bf),
     }
+    wsd = W.w8a16_workspace([wg[0], wu[0]])
     ws = torch.empty((M, H), dtype=torch.uint8, device="cuda")
     ws2 = torch.empty((M, H), dtype=torch.uint8, device="cuda")
 
@@ -51,6 +55,10 @@ def test_block_in_cuda_graph(W):
         W.qkv_shared_quant_gemm(W.MODE_A16, x, None, [wg[0], wu[0]], [wg[1], wu[1]], outs=outs["gu16"])
         W.swiglu_2in_bf16(outs["gu16"][0], outs["gu16"][1], out=outs["h16"])
         W.fp8_linear_w8a16(outs["h16"], wd[0], wd[1], out=outs["y16"])
+        # W8A16 through the workspace (dequantization + bf16 group GEMM)
+        W.qkv_shared_quant_gemm(W.MODE_A16, x, None, [q for q, _ in wq], [s for _, s in wq], outs=outs["qkv16w"],
+                                ws=wsd)
+        W.qkv_shared_quant_gemm(W.MODE_A16, outs["h16"], None, [wd[0]], [wd[1]], outs=[outs["y16w"]], ws=wsd)
 
     def snapshot():
         flat = []
