@@ -141,3 +141,14 @@ def test_swiglu_variant_validation_before_any_cuda_call(L):
     # zero rows: no launch
     assert L.swiglu_2in_ex_fp8(p16, p16, 0, 0, 16, ref(ok), p16, p16, None) == 0
     assert L.swiglu_2in_ex_16(p16, p16, 2, 0, 16, ref(ok), p16, None) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: with the library absent every entry point raises."""
+    from w8a16_linear_gb300 import binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "libw8lin.so"))
+    with pytest.raises(ImportError):
+        b.abi_version()
+    with pytest.raises(ImportError):
+        b.step_policy_dispatch(None, 0, 8)
