@@ -193,7 +193,8 @@ class Block:
     def step(self, W, policy, step_index, num_steps, x_qkv=None, x_out=None, x_mlp=None, fused=True):
         """One block pass in the precision the policy selects for this step;
         returns the number of kernel launches.  `fused` selects the fused
-        gate/up + SwiGLU kernel on W8A8 steps (else group GEMM + SwiGLU)."""
+        gate/up + SwiGLU kernel (E4M3 out on W8A8 steps, bf16 out on W8A16
+        steps); else the group GEMM followed by the SwiGLU kernel."""
         x_qkv = self.x_qkv if x_qkv is None else x_qkv
         x_out = self.x_out if x_out is None else x_out
         x_mlp = self.x_mlp if x_mlp is None else x_mlp
@@ -246,11 +247,14 @@ class Block:
         main.wait_event(self.dq_ev[1])
         W.bf16_linear_group(x_out, [self.wd_out], outs=[self.y_out])
         main.wait_event(self.dq_ev[2])
-        W.bf16_linear_group(x_mlp, self.wd_gu, outs=self.y_gu)
-        W.swiglu_2in_bf16(self.y_gu[0], self.y_gu[1], out=self.h16)
+        if fused:       # gate/up GEMMs with the bf16 SwiGLU in their epilogue
+            W.bf16_gate_up_swiglu(x_mlp, self.wd_gu[0], self.wd_gu[1], out=self.h16)
+        else:
+            W.bf16_linear_group(x_mlp, self.wd_gu, outs=self.y_gu)
+            W.swiglu_2in_bf16(self.y_gu[0], self.y_gu[1], out=self.h16)
         main.wait_event(self.dq_ev[3])
         W.bf16_linear_group(self.h16, [self.wd_down], outs=[self.y_down])
-        return 12
+        return 11 if fused else 12
 
 
 # DRAM bytes (read + write) of the A8 block step's four GEMM launches at
@@ -405,7 +409,11 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
                                         "note": "gate/up group GEMM -> bf16 -> swiglu_2in_fp8 instead of the fused kernel"}
     ms = _time(lambda: blk.step(W, policy, 0, POLICY_STEPS), flush, stream, n)
     out["block_a16_step"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
-                             "note": "W8A16 rows: QKV/gate-up groups in A16, out/down W8A16, swiglu bf16"}
+                             "note": "W8A16: weights dequantized on a side stream; bf16 Q/K/V group, out, "
+                                     "gate/up + SwiGLU (bf16) fused, down"}
+    ms = _time(lambda: blk.step(W, policy, 0, POLICY_STEPS, fused=False), flush, stream, n)
+    out["block_a16_step_unfused_mlp"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
+                                         "note": "gate/up bf16 group GEMM -> bf16 -> swiglu_2in_bf16"}
     ev = _events(1)
     flush_l2(flush)
     ev[0][0].record(stream)

@@ -200,6 +200,21 @@ w8_status bf16_linear_group(const uint16_t* x, int64_t M, int64_t K, int32_t G, 
                             const int64_t* N, uint16_t* const* y, void* stream);
 
 /*
+ * bf16_gate_up_swiglu — the gate/up pair of a 16-bit step with its SwiGLU,
+ * on weights dequantized by fp8_dequant_weight, in one launch: out =
+ * bf16_RNE(h) with h the SwiGLU of swiglu_2in_bf16 applied to g =
+ * bf16_RNE(x . Wd_gate^T) and u = bf16_RNE(x . Wd_up^T) -- bit for bit the
+ * result of bf16_linear_group followed by swiglu_2in_bf16, without writing
+ * g and u ([P3] Behavior: dequant + F.linear; [P4] What changed: SiLU(G) * U
+ * from the split gate and up projections).
+ *   x        bf16 [M, K], device;  wd_gate, wd_up  bf16 [I, K], device
+ *   out      bf16 [M, I], device
+ * Errors: NULL, SHAPE (K%16, I%16), ALIGN, ARCH, CUDA.
+ */
+w8_status bf16_gate_up_swiglu(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wd_gate,
+                              const uint16_t* wd_up, int64_t I, uint16_t* out, void* stream);
+
+/*
  * fp8_linear_w8a8_group — the GEMM half of qkv_shared_quant_gemm in A8 mode:
  * G projections (1..3) over an activation that is ALREADY E4M3, quantized
  * with s_in (for example by fp8_quant_static or swiglu_2in_fp8), in one

@@ -107,3 +107,47 @@ def test_bf16_linear_group_on_dequantized_weights(W):
     for y, y2, (r64, _) in zip(ys, yw, ref):
         assert gemm_err(host_bits(y), r64) <= GEMM_TOL
         assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,K,I", [(1000, 512, 1024), (100, 256, 512), (257, 4112, 16 * 33),
+                                   (20670, 4096, 16384)])
+def test_bf16_gate_up_swiglu_equals_separate_path(W, M, K, I):
+    """The fused 16-bit gate/up + SwiGLU launch against bf16_linear_group ->
+    swiglu_2in_bf16 on the same dequantized weights: bit for bit (the
+    epilogue rounds gate and up to bf16 exactly as the GEMM would write
+    them)."""
+    gen = torch.Generator(device="cuda").manual_seed(M + I)
+    x = (torch.randn((M, K), generator=gen, device="cuda") * 0.25).to(torch.bfloat16)
+    wg = (torch.randn((I, K), generator=gen, device="cuda") * 0.02 * 448 / 0.1).clamp(-448, 448)
+    wu = (torch.randn((I, K), generator=gen, device="cuda") * 0.02 * 448 / 0.1).clamp(-448, 448)
+    qg = wg.to(torch.float8_e4m3fn).view(torch.uint8)
+    qu = wu.to(torch.float8_e4m3fn).view(torch.uint8)
+    sg, su = dev_f32(0.1 / 448), dev_f32(0.08 / 448)
+    dg, du = W.fp8_dequant_weight(qg, sg), W.fp8_dequant_weight(qu, su)
+    h = W.bf16_gate_up_swiglu(x, dg, du)
+    g, u = W.bf16_linear_group(x, [dg, du])
+    h_sep = W.swiglu_2in_bf16(g, u)
+    torch.cuda.synchronize()
+    W.poll_device_error()
+    assert torch.equal(h.view(torch.int16), h_sep.view(torch.int16))
+
+
+def test_bf16_gate_up_swiglu_exact_sums_vs_oracle(W):
+    """Operands whose partial sums are exact in any order: gate and up are
+    then the oracle's bit for bit, and so is the SwiGLU."""
+    rng = np.random.default_rng(3)
+    M, K, I = 300, 1024, 512
+    xv = np.array([0.0, 0.25, -0.25, 0.5, -1.0, 1.5, 2.0, -3.0], np.float32)
+    x = torch.from_numpy(rng.choice(xv, size=(M, K))).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    cv = np.array([0.0, 1.0, -1.0, 2.0, -0.5, 3.0], np.float32)
+    qg = O.e4m3_encode(rng.choice(cv, size=(I, K)))
+    qu = O.e4m3_encode(rng.choice(cv, size=(I, K)))
+    s_w = np.float32(2.0 ** -6)
+    dg, du = W.fp8_dequant_weight(dev_u8(qg), dev_f32(s_w)), W.fp8_dequant_weight(dev_u8(qu), dev_f32(s_w))
+    h = host_bits(W.bf16_gate_up_swiglu(dev_bf16(x), dg, du))
+    _, gb = O.linear_w8a16(x, qg, s_w)
+    _, ub = O.linear_w8a16(x, qu, s_w)
+    want = O.swiglu_2in_bf16(gb, ub)
+    nan = np.isnan(O.bf16_decode(want))
+    assert np.array_equal(np.isnan(O.bf16_decode(h)), nan)
+    assert np.array_equal(h[~nan], want[~nan])

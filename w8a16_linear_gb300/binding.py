@@ -56,6 +56,8 @@ SIGNATURES = {
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
                                              _c_void_p, _c_void_p]),
     "fp8_dequant_weight": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "bf16_gate_up_swiglu": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i64, _c_void_p,
+                                           _c_void_p]),
     "bf16_linear_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _i32, ctypes.POINTER(_c_void_p),
                                          ctypes.POINTER(_i64), ctypes.POINTER(_c_void_p), _c_void_p]),
     "fp8_linear_w8a8_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _i32,
@@ -281,6 +283,22 @@ def bf16_linear_group(x, wds, outs=None, stream=None):
     arr_y = (ctypes.c_void_p * G)(*[o.data_ptr() for o in outs])
     _check(lib().bf16_linear_group(_ptr(x2), M, K, G, arr_w, arr_n, arr_y, _stream(stream)))
     return outs
+
+
+def bf16_gate_up_swiglu(x, wd_gate, wd_up, out=None, stream=None):
+    """bf16 SwiGLU of the gate/up pair on dequantized bf16 weights, one launch."""
+    x = _as_bf16(x, "x")
+    x2 = _flat2(x)
+    M, K = x2.shape
+    wg, wu = _as_bf16(wd_gate, "wd_gate"), _as_bf16(wd_up, "wd_up")
+    if wg.shape != wu.shape:
+        raise W8Error(2, "gate and up weights differ in shape")
+    I = wg.shape[0]
+    if out is None:
+        out = torch.empty(*x.shape[:-1], I, dtype=torch.bfloat16, device=x.device)
+    _check(lib().bf16_gate_up_swiglu(_ptr(x2), M, K, _ptr(wg), _ptr(wu), I, _ptr(_as_bf16(out, "out")),
+                                     _stream(stream)))
+    return out
 
 
 def w8a16_workspace(weights):

@@ -319,6 +319,33 @@ w8_status bf16_linear_group(const uint16_t* x, int64_t M, int64_t K, int32_t G, 
   return cuda_status(e, "bf16_linear_group: GEMM launch");
 }
 
+w8_status bf16_gate_up_swiglu(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wd_gate,
+                              const uint16_t* wd_up, int64_t I, uint16_t* out, void* stream) {
+  static const float kOne = 1.0f;  // placeholder scale: the common check wants a pointer
+  const uint8_t* wg = reinterpret_cast<const uint8_t*>(wd_gate);
+  const uint8_t* wu = reinterpret_cast<const uint8_t*>(wd_up);
+  w8_status st = check_linear_common("bf16_gate_up_swiglu", x, M, K, wg, I, &kOne, out);
+  if (st != W8_OK) return st;
+  if ((st = check_linear_common("bf16_gate_up_swiglu", x, M, K, wu, I, &kOne, out)) != W8_OK) return st;
+  if (M == 0) return ok();
+  int sms = 0;
+  if ((st = device_info(&sms)) != W8_OK) return st;
+  w8::GemmProblem p{};
+  p.M = M;
+  p.K = K;
+  p.G = 1;
+  p.x = x;
+  p.w[0] = wg;
+  p.w[1] = wu;
+  p.N[0] = I;
+  p.N[1] = I;
+  p.y[0] = out;
+  int terr = 0;
+  cudaError_t e = w8::launch_gemm_glu16(p, sms, static_cast<cudaStream_t>(stream), &terr);
+  if (terr) return fail(W8_ERR_ALIGN, "bf16_gate_up_swiglu: tensor map encoding rejected the operands");
+  return cuda_status(e, "bf16_gate_up_swiglu: GEMM launch");
+}
+
 w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const float* s_in,
                                 int32_t G, const uint8_t* const* w, const int64_t* N,
                                 const float* const* s_w, uint16_t* const* y, void* stream) {

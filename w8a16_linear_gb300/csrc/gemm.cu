@@ -65,15 +65,17 @@ constexpr uint32_t kAccCols = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kEpiBufBytes = 32 * 128;            // W8A8 staging: 32 rows x 64 bf16
 
-enum class Mode { W8A8, GLU, BF16 };
+enum class Mode { W8A8, GLU, BF16, GLU16 };
 
 template <Mode MODE, int CG>
 struct Cfg {
-  static constexpr bool kGlu = (MODE == Mode::GLU);
+  static constexpr bool kGlu = (MODE == Mode::GLU || MODE == Mode::GLU16);
   // BF16: the W8A16 product on an already dequantized weight (bf16 x bf16,
   // kind::f16): the same tiles and pipeline with 64 K-values (128 bytes) per
-  // stage and an unscaled epilogue.
-  static constexpr bool kBf16 = (MODE == Mode::BF16);
+  // stage and an unscaled epilogue.  GLU16: the gate/up pair of a 16-bit
+  // step on dequantized weights, with the SwiGLU written as bf16.
+  static constexpr bool kBf16 = (MODE == Mode::BF16 || MODE == Mode::GLU16);
+  static constexpr bool kOut16 = (MODE == Mode::GLU16);
   // W8A8: 256 output columns per tile.  GLU: 128 intermediate columns per
   // tile, computed by one N = 256 MMA whose B operand is [128 gate rows | 128
   // up rows] of the slice: D columns 0-127 hold gate, 128-255 hold up, and
@@ -91,8 +93,10 @@ struct Cfg {
   // GLU: two warps per TMEM lane quadrant (64 columns each) to keep the
   // SwiGLU epilogue ahead of the tensor cores; staging 32 rows x 64 codes.
   static constexpr int kEpiWarps = kGlu ? 8 : 4;
-  static constexpr int kEpiBuf = kGlu ? 32 * 64 : kEpiBufBytes;
-  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBuf;
+  // GLU16 stages 32 rows x 64 bf16 (128 bytes) in one buffer per warp.
+  static constexpr int kEpiBuf = kOut16 ? 32 * 128 : (kGlu ? 32 * 64 : kEpiBufBytes);
+  static constexpr int kEpiNBuf = kOut16 ? 1 : 2;
+  static constexpr int kEpiBytes = kEpiWarps * kEpiNBuf * kEpiBuf;
 };
 
 template <Mode MODE, int CG>
@@ -349,14 +353,14 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     const int wq = warp & 3;              // TMEM lane quadrant this warp may access
     const int cp = (warp - 2) >> 2;       // GLU: which 64 of the tile's 128 columns
     constexpr int EB = C::kEpiBuf;
-    const uint32_t buf0 = sbase + L::kEpi + (uint32_t)((warp - 2) * 2 * EB);
-    uint8_t* buf0_ptr = smem + L::kEpi + (warp - 2) * 2 * EB;
+    const uint32_t buf0 = sbase + L::kEpi + (uint32_t)((warp - 2) * C::kEpiNBuf * EB);
+    uint8_t* buf0_ptr = smem + L::kEpi + (warp - 2) * C::kEpiNBuf * EB;
     int acc = 0;
     uint32_t acc_ph = 0;
     int nbuf = 0;
     float s_out = 1.0f, rs_out = 1.0f;
     bool exact_only = false;
-    if constexpr (kGlu) {
+    if constexpr (kGlu && !C::kOut16) {
       s_out = __ldg(args.s_out);
       rs_out = __frcp_rn(s_out);
       exact_only = !swiglu_fp8_scale_is_fast(s_out, rs_out);
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       float alpha = 1.0f, alpha_u = 1.0f;
       // BF16: the scale is already in the dequantized weight; y = bf16(acc).
       if constexpr (!C::kBf16) alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, kGlu ? 0 : g)));
-      if constexpr (kGlu) alpha_u = __fmul_rn(__ldg(args.s_in), __ldg(args.s_w[1]));
+      if constexpr (kGlu && !C::kBf16) alpha_u = __fmul_rn(__ldg(args.s_in), __ldg(args.s_w[1]));
       // Warp-uniform wait: the TMEM loads below are .sync.aligned.
       if (!mbar_wait_warp(tfull_bar(acc), acc_ph, abort, kWaitLimitNs)) {
         if (lane == 0) record_timeout(abort);
@@ -419,6 +423,53 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
             tma_store_commit();
           }
           nbuf ^= 1;
+        }
+      } else if constexpr (C::kOut16) {
+        // 16-bit step: bf16 SwiGLU of the bf16-rounded gate / up values.
+        // This warp takes columns cp*64 .. cp*64+63 (two 32-column chunks),
+        // staged as one 128-byte row per lane with the 128-byte swizzle
+        // (16-byte chunk j at j ^ (row & 7)); one buffer per warp.
+        if (lane == 0) tma_store_wait_read<0>();
+        __syncwarp();
+        uint8_t* bp = buf0_ptr + lane * 128;
+#pragma unroll 1
+        for (int lc = 0; lc < 2; ++lc) {
+          const int c = 2 * cp + lc;
+          uint32_t rg[32], ru[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, rg);
+          tmem_ld_32x32b_x32(tbase + C::kBN + c * 32, ru);
+          tmem_ld_wait();
+          if (lc == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
+              else mbar_arrive(tempty_bar(acc));
+            }
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t hw[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int e = 16 * hh + 2 * j;
+              // the bf16 values the separate gate / up GEMMs would have written
+              const uint32_t gw = cvt_bf16x2(__uint_as_float(rg[e]), __uint_as_float(rg[e + 1]));
+              const uint32_t uw = cvt_bf16x2(__uint_as_float(ru[e]), __uint_as_float(ru[e + 1]));
+              hw[j] = swiglu_bf16_pair(gw, uw);
+            }
+            const int j0 = 4 * lc + 2 * hh;
+            *reinterpret_cast<uint4*>(bp + ((j0 ^ (lane & 7)) * 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(bp + (((j0 + 1) ^ (lane & 7)) * 16)) =
+                make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int col0 = n0 + cp * 64;
+        if (lane == 0 && col0 < ng && row0 < args.M) {
+          tma_store_2d(map_y(maps, 0), buf0, col0, row0);
+          tma_store_commit();
         }
       } else {
         // 128 intermediate columns per tile: gate at tbase, up at tbase + 128.
@@ -844,7 +895,7 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
     args.N[g] = (int)p.N[g];
     args.tiles_n[g] = (int)((p.N[g] + C::kBN - 1) / C::kBN);
     args.tiles_per_m += args.tiles_n[g];
-    if (kGlu)  // E4M3 output [M, I]: 32 rows x 64 codes per epilogue warp
+    if (kGlu && !C::kOut16)  // E4M3 output [M, I]: 32 rows x 64 codes per epilogue warp
       ok &= encode_2d(&maps.y[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.y[g], p.N[g], p.M, p.N[g], 64,
                       32, CU_TENSOR_MAP_SWIZZLE_64B);
     else
@@ -938,6 +989,11 @@ cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int
 cudaError_t launch_gemm_bf16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
   return use_pair(p) ? launch<Mode::BF16, 2>(p, sms, st, tmap_err)
                      : launch<Mode::BF16, 1>(p, sms, st, tmap_err);
+}
+
+cudaError_t launch_gemm_glu16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  return use_pair(p) ? launch<Mode::GLU16, 2>(p, sms, st, tmap_err)
+                     : launch<Mode::GLU16, 1>(p, sms, st, tmap_err);
 }
 
 cudaError_t launch_gemm_glu(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {

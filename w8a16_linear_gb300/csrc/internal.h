@@ -56,6 +56,9 @@ cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, in
 // bf16 x bf16 GEMM of the W8A16 step on weights dequantized beforehand:
 // y_g = bf16(x . Wd_g^T), x bf16 [M,K], Wd_g bf16 [N_g,K] in w[g] (s_w unused).
 cudaError_t launch_gemm_bf16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
+// The gate/up pair of a 16-bit step on dequantized bf16 weights w[0] (gate)
+// and w[1] (up), [I, K] each, with h = SwiGLU written as bf16 into y[0] [M, I].
+cudaError_t launch_gemm_glu16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 cudaError_t launch_gemm_glu(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 
 // Launches a one-thread kernel whose mbarrier wait times out (0.2 s).
