@@ -41,7 +41,9 @@ def test_block_in_cuda_graph(W):
         "y16": torch.empty((M, H), **bf),
         "qkv16w": [torch.empty((M, H), **bf) for _ in range(3)],
         "y16w": torch.empty((M, H), **bf),
+        "h16f": torch.empty((M, I), **bf),
     }
+    wdg, wdu = W.fp8_dequant_weight(wg[0], wg[1]), W.fp8_dequant_weight(wu[0], wu[1])
     wsd = W.w8a16_workspace([wg[0], wu[0]])
     ws = torch.empty((M, H), dtype=torch.uint8, device="cuda")
     ws2 = torch.empty((M, H), dtype=torch.uint8, device="cuda")
@@ -59,6 +61,7 @@ def test_block_in_cuda_graph(W):
         W.qkv_shared_quant_gemm(W.MODE_A16, x, None, [q for q, _ in wq], [s for _, s in wq], outs=outs["qkv16w"],
                                 ws=wsd)
         W.qkv_shared_quant_gemm(W.MODE_A16, outs["h16"], None, [wd[0]], [wd[1]], outs=[outs["y16w"]], ws=wsd)
+        W.bf16_gate_up_swiglu(x, wdg, wdu, out=outs["h16f"])
 
     def snapshot():
         flat = []
