@@ -11,7 +11,7 @@
 //    activation precision).
 //
 // Each thread moves 16 elements per step with 128-bit loads and stores in a
-// grid-stride loop over a grid sized to the SM count.  Every output is the
+// grid-stride loop over a grid of as many blocks as fit on the GPU at once.  Every output is the
 // specification's bit pattern: a fast value with a proven error bound is
 // kept only where it provably rounds to the same code, everything else is
 // recomputed with correctly rounded, never-fused scalar operations.
@@ -182,9 +182,18 @@ __global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __res
   }
 }
 
-int grid_for(int64_t n16, int sms) {
+// Grid of 256-thread blocks for a grid-stride kernel: as many blocks as fit
+// on the GPU at once (blocks beyond that would run as a second, partly
+// occupied wave, which an HBM-bound kernel cannot afford), fewer for small
+// inputs.  The per-SM figure is the occupancy of `kern`, looked up once.
+int grid_for(const void* kern, int* per_sm, int64_t n16, int sms) {
+  if (*per_sm == 0) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, 256, 0) != cudaSuccess || b < 1) b = 1;
+    *per_sm = b;
+  }
   const int64_t want = (n16 + 255) / 256;
-  const int64_t cap = (int64_t)sms * 8;   // 8 resident 256-thread blocks per SM
+  const int64_t cap = (int64_t)sms * *per_sm;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
@@ -195,13 +204,23 @@ cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bo
                              cudaStream_t st) {
   const int64_t n16 = n / 16;
   const SwigluParams pr{a.limit, a.alpha, a.beta, a.has_limit ? 1 : 0, a.beta != 0.0f ? 1 : 0};
-  const int grid = grid_for(n16, sms);
+  static int occ[4] = {0, 0, 0, 0};
   if (in_f16) {
-    if (out_fp8) swiglu_ex_kernel<true, true><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
-    else swiglu_ex_kernel<true, false><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
+    if (out_fp8) {
+      auto k = swiglu_ex_kernel<true, true>;
+      k<<<grid_for((const void*)k, &occ[0], n16, sms), 256, 0, st>>>(g, u, n16, pr, s_out, out);
+    } else {
+      auto k = swiglu_ex_kernel<true, false>;
+      k<<<grid_for((const void*)k, &occ[1], n16, sms), 256, 0, st>>>(g, u, n16, pr, s_out, out);
+    }
   } else {
-    if (out_fp8) swiglu_ex_kernel<false, true><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
-    else swiglu_ex_kernel<false, false><<<grid, 256, 0, st>>>(g, u, n16, pr, s_out, out);
+    if (out_fp8) {
+      auto k = swiglu_ex_kernel<false, true>;
+      k<<<grid_for((const void*)k, &occ[2], n16, sms), 256, 0, st>>>(g, u, n16, pr, s_out, out);
+    } else {
+      auto k = swiglu_ex_kernel<false, false>;
+      k<<<grid_for((const void*)k, &occ[3], n16, sms), 256, 0, st>>>(g, u, n16, pr, s_out, out);
+    }
   }
   return cudaGetLastError();
 }
@@ -209,28 +228,33 @@ cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bo
 cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w, uint16_t* wd, int sms,
                                   cudaStream_t st) {
   const int64_t n16 = n / 16;
-  dequant_weight_kernel<<<grid_for(n16, sms), 256, 0, st>>>(q, n16, s_w, wd);
+  static int occ = 0;
+  dequant_weight_kernel<<<grid_for((const void*)dequant_weight_kernel, &occ, n16, sms), 256, 0, st>>>(q, n16, s_w,
+                                                                                                  wd);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_static(const uint16_t* x, int64_t n, const float* s_in, uint8_t* q,
                                 int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
-  quant_static_kernel<<<grid_for(n16, sms), 256, 0, st>>>(x, n16, s_in, q);
+  static int occ = 0;
+  quant_static_kernel<<<grid_for((const void*)quant_static_kernel, &occ, n16, sms), 256, 0, st>>>(x, n16, s_in, q);
   return cudaGetLastError();
 }
 
 cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, const float* s_out,
                               uint8_t* out, int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
-  swiglu_fp8_kernel<<<grid_for(n16, sms), 256, 0, st>>>(g, u, n16, s_out, out);
+  static int occ = 0;
+  swiglu_fp8_kernel<<<grid_for((const void*)swiglu_fp8_kernel, &occ, n16, sms), 256, 0, st>>>(g, u, n16, s_out, out);
   return cudaGetLastError();
 }
 
 cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* out,
                                int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
-  swiglu_bf16_kernel<<<grid_for(n16, sms), 256, 0, st>>>(g, u, n16, out);
+  static int occ = 0;
+  swiglu_bf16_kernel<<<grid_for((const void*)swiglu_bf16_kernel, &occ, n16, sms), 256, 0, st>>>(g, u, n16, out);
   return cudaGetLastError();
 }
 
