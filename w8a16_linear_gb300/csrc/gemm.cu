@@ -90,12 +90,14 @@ struct Cfg {
   static constexpr int kStages = CG == 1 ? 4 : 6;
   static constexpr uint32_t kIdesc =                        // E4M3 x E4M3 or BF16 x BF16 -> F32
       kBf16 ? make_idesc(1, 1, BM * CG, kMmaN) : make_idesc(0, 0, BM * CG, kMmaN);
-  // GLU: two warps per TMEM lane quadrant (64 columns each) to keep the
-  // SwiGLU epilogue ahead of the tensor cores; staging 32 rows x 64 codes.
-  static constexpr int kEpiWarps = kGlu ? 8 : 4;
-  // GLU16 stages 32 rows x 64 bf16 (128 bytes) in one buffer per warp.
+  // One epilogue warp per TMEM lane quadrant: more warps (each taking fewer
+  // columns) measured slower for the SwiGLU epilogues, their instruction
+  // issue competing with the producer and MMA threads.
+  static constexpr int kEpiWarps = 4;
+  // GLU staging per warp: 32 rows x 64 E4M3 codes (64 bytes) or, GLU16,
+  // 32 rows x 64 bf16 (128 bytes), double-buffered.
   static constexpr int kEpiBuf = kOut16 ? 32 * 128 : (kGlu ? 32 * 64 : kEpiBufBytes);
-  static constexpr int kEpiNBuf = kOut16 ? 1 : 2;
+  static constexpr int kEpiNBuf = 2;
   static constexpr int kEpiBytes = kEpiWarps * kEpiNBuf * kEpiBuf;
 };
 
@@ -351,7 +353,6 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     const int wq = warp & 3;              // TMEM lane quadrant this warp may access
-    const int cp = (warp - 2) >> 2;       // GLU: which 64 of the tile's 128 columns
     constexpr int EB = C::kEpiBuf;
     const uint32_t buf0 = sbase + L::kEpi + (uint32_t)((warp - 2) * C::kEpiNBuf * EB);
     uint8_t* buf0_ptr = smem + L::kEpi + (warp - 2) * C::kEpiNBuf * EB;
@@ -425,107 +426,115 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           nbuf ^= 1;
         }
       } else if constexpr (C::kOut16) {
-        // 16-bit step: bf16 SwiGLU of the bf16-rounded gate / up values.
-        // This warp takes columns cp*64 .. cp*64+63 (two 32-column chunks),
-        // staged as one 128-byte row per lane with the 128-byte swizzle
-        // (16-byte chunk j at j ^ (row & 7)); one buffer per warp.
-        if (lane == 0) tma_store_wait_read<0>();
-        __syncwarp();
-        uint8_t* bp = buf0_ptr + lane * 128;
+        // 16-bit step: bf16 SwiGLU of the bf16-rounded gate / up values.  The
+        // tile's 128 columns in two halves of 64 (two 32-column chunks each),
+        // each staged as one 128-byte row per lane with the 128-byte swizzle
+        // (16-byte chunk j at j ^ (row & 7)) and stored with one TMA store.
 #pragma unroll 1
-        for (int lc = 0; lc < 2; ++lc) {
-          const int c = 2 * cp + lc;
-          uint32_t rg[32], ru[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, rg);
-          tmem_ld_32x32b_x32(tbase + C::kBN + c * 32, ru);
-          tmem_ld_wait();
-          if (lc == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
-              else mbar_arrive(tempty_bar(acc));
+        for (int cp = 0; cp < 2; ++cp) {
+          if (lane == 0) tma_store_wait_read<1>();
+          __syncwarp();
+          uint8_t* bp = buf0_ptr + nbuf * EB + lane * 128;
+#pragma unroll 1
+          for (int lc = 0; lc < 2; ++lc) {
+            const int c = 2 * cp + lc;
+            uint32_t rg[32], ru[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, rg);
+            tmem_ld_32x32b_x32(tbase + C::kBN + c * 32, ru);
+            tmem_ld_wait();
+            if (c == 3) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
+                else mbar_arrive(tempty_bar(acc));
+              }
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t hw[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int e = 16 * hh + 2 * j;
+                // the bf16 values the separate gate / up GEMMs would have written
+                const uint32_t gw = cvt_bf16x2(__uint_as_float(rg[e]), __uint_as_float(rg[e + 1]));
+                const uint32_t uw = cvt_bf16x2(__uint_as_float(ru[e]), __uint_as_float(ru[e + 1]));
+                hw[j] = swiglu_bf16_pair(gw, uw);
+              }
+              const int j0 = 4 * lc + 2 * hh;
+              *reinterpret_cast<uint4*>(bp + ((j0 ^ (lane & 7)) * 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(bp + (((j0 + 1) ^ (lane & 7)) * 16)) =
+                  make_uint4(hw[4], hw[5], hw[6], hw[7]);
             }
           }
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t hw[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int e = 16 * hh + 2 * j;
-              // the bf16 values the separate gate / up GEMMs would have written
-              const uint32_t gw = cvt_bf16x2(__uint_as_float(rg[e]), __uint_as_float(rg[e + 1]));
-              const uint32_t uw = cvt_bf16x2(__uint_as_float(ru[e]), __uint_as_float(ru[e + 1]));
-              hw[j] = swiglu_bf16_pair(gw, uw);
-            }
-            const int j0 = 4 * lc + 2 * hh;
-            *reinterpret_cast<uint4*>(bp + ((j0 ^ (lane & 7)) * 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(bp + (((j0 + 1) ^ (lane & 7)) * 16)) =
-                make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int col0 = n0 + cp * 64;
+          if (lane == 0 && col0 < ng && row0 < args.M) {
+            tma_store_2d(map_y(maps, 0), buf0 + nbuf * EB, col0, row0);
+            tma_store_commit();
           }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        const int col0 = n0 + cp * 64;
-        if (lane == 0 && col0 < ng && row0 < args.M) {
-          tma_store_2d(map_y(maps, 0), buf0, col0, row0);
-          tma_store_commit();
+          nbuf ^= 1;
         }
       } else {
-        // 128 intermediate columns per tile: gate at tbase, up at tbase + 128.
-        // This warp takes columns cp*64 .. cp*64+63: two 32-column chunks of
-        // 32 E4M3 codes each, staged as one 64-byte row per lane with the
-        // 64-byte swizzle (16-byte chunk j at j ^ ((row >> 1) & 3)).
-        if (lane == 0) tma_store_wait_read<1>();
-        __syncwarp();
-        uint8_t* bp = buf0_ptr + nbuf * EB + lane * 64;
-        const int sw = (lane >> 1) & 3;
+        // 128 intermediate columns per tile: gate at tbase, up at tbase + 128,
+        // in two halves of 64 columns (two 32-column chunks of 32 E4M3 codes
+        // each), each staged as one 64-byte row per lane with the 64-byte
+        // swizzle (16-byte chunk j at j ^ ((row >> 1) & 3)) and stored with
+        // one TMA store.
 #pragma unroll 1
-        for (int lc = 0; lc < 2; ++lc) {
-          const int c = 2 * cp + lc;
-          uint32_t rg[32], ru[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, rg);
-          tmem_ld_32x32b_x32(tbase + C::kBN + c * 32, ru);
-          tmem_ld_wait();
-          if (lc == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
-              else mbar_arrive(tempty_bar(acc));
+        for (int cp = 0; cp < 2; ++cp) {
+          if (lane == 0) tma_store_wait_read<1>();
+          __syncwarp();
+          uint8_t* bp = buf0_ptr + nbuf * EB + lane * 64;
+          const int sw = (lane >> 1) & 3;
+#pragma unroll 1
+          for (int lc = 0; lc < 2; ++lc) {
+            const int c = 2 * cp + lc;
+            uint32_t rg[32], ru[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, rg);
+            tmem_ld_32x32b_x32(tbase + C::kBN + c * 32, ru);
+            tmem_ld_wait();
+            if (c == 3) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                if constexpr (CG == 2) mbar_arrive_cluster(leader_addr(tempty_bar(acc)));
+                else mbar_arrive(tempty_bar(acc));
+              }
             }
-          }
-          uint32_t codes[8];
+            uint32_t codes[8];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            // the bf16 values the separate gate / up GEMMs would have written
-            uint32_t gw[8], uw[8];
+            for (int hh = 0; hh < 2; ++hh) {
+              // the bf16 values the separate gate / up GEMMs would have written
+              uint32_t gw[8], uw[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int e = 16 * hh + 2 * j;
-              gw[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(rg[e]), alpha),
-                                 __fmul_rn(__uint_as_float(rg[e + 1]), alpha));
-              uw[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(ru[e]), alpha_u),
-                                 __fmul_rn(__uint_as_float(ru[e + 1]), alpha_u));
+              for (int j = 0; j < 8; ++j) {
+                const int e = 16 * hh + 2 * j;
+                gw[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(rg[e]), alpha),
+                                   __fmul_rn(__uint_as_float(rg[e + 1]), alpha));
+                uw[j] = cvt_bf16x2(__fmul_rn(__uint_as_float(ru[e]), alpha_u),
+                                   __fmul_rn(__uint_as_float(ru[e + 1]), alpha_u));
+              }
+              uint32_t c4[4];
+              swiglu_fp8_x16(gw, uw, s_out, rs_out, exact_only, c4);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) codes[4 * hh + j] = c4[j];
             }
-            uint32_t c4[4];
-            swiglu_fp8_x16(gw, uw, s_out, rs_out, exact_only, c4);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) codes[4 * hh + j] = c4[j];
+            *reinterpret_cast<uint4*>(bp + (((2 * lc) ^ sw) * 16)) =
+                make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            *reinterpret_cast<uint4*>(bp + (((2 * lc + 1) ^ sw) * 16)) =
+                make_uint4(codes[4], codes[5], codes[6], codes[7]);
           }
-          *reinterpret_cast<uint4*>(bp + (((2 * lc) ^ sw) * 16)) =
-              make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          *reinterpret_cast<uint4*>(bp + (((2 * lc + 1) ^ sw) * 16)) =
-              make_uint4(codes[4], codes[5], codes[6], codes[7]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int col0 = n0 + cp * 64;
+          if (lane == 0 && col0 < ng && row0 < args.M) {
+            tma_store_2d(map_y(maps, 0), buf0 + nbuf * EB, col0, row0);
+            tma_store_commit();
+          }
+          nbuf ^= 1;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        const int col0 = n0 + cp * 64;
-        if (lane == 0 && col0 < ng && row0 < args.M) {
-          tma_store_2d(map_y(maps, 0), buf0 + nbuf * EB, col0, row0);
-          tma_store_commit();
-        }
-        nbuf ^= 1;
       }
       if (++acc == 2) {
         acc = 0;
