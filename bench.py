@@ -261,7 +261,7 @@ class Block:
 # M=20670 from one ncu capture of the current gemm_kernel build (3128.7 MB read
 # + 1112.2 MB written; algorithmic 861 + 1185 MB).  Re-capture, or set to None,
 # whenever gemm_kernel changes.
-GEMM_TRAFFIC_BYTES = 4240.9e6
+GEMM_TRAFFIC_BYTES = None
 
 
 def flush_l2(buf):
