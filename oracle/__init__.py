@@ -21,6 +21,11 @@ the passage it follows:
   without re-quantizing them" (sections *Description*, *What changed*,
   *Denoising-step activation precision*, *Test Coverage*).
 
+Modules: ``e4m3`` (the FP8 codec), ``bf16`` and ``fp16`` (16-bit codecs),
+``linear`` (quantization, W8A8 / W8A16, the dequantized weight, the max(s)
+re-quantization, the sharing group), ``swiglu`` (the SwiGLU specification
+and its options), ``policy`` (the per-step precision policy and its JSON).
+
 Floating point: the GEMM oracles work in float64 on exactly decoded
 operands (the definition written out).  Where a floating-point value decides
 an integer -- an E4M3 code or a bf16 bit pattern -- the oracle takes that
