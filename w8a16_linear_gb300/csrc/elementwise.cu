@@ -20,6 +20,7 @@
 // swiglu_spec.cuh.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -186,14 +187,14 @@ __global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __res
 // on the GPU at once (blocks beyond that would run as a second, partly
 // occupied wave, which an HBM-bound kernel cannot afford), fewer for small
 // inputs.  The per-SM figure is the occupancy of `kern`, looked up once.
-int grid_for(const void* kern, int* per_sm, int64_t n16, int sms) {
-  if (*per_sm == 0) {
-    int b = 0;
+int grid_for(const void* kern, std::atomic<int>* per_sm, int64_t n16, int sms) {
+  int b = per_sm->load(std::memory_order_relaxed);
+  if (b == 0) {   // first call: look the figure up (threads racing here store the same value)
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, 256, 0) != cudaSuccess || b < 1) b = 1;
-    *per_sm = b;
+    per_sm->store(b, std::memory_order_relaxed);
   }
   const int64_t want = (n16 + 255) / 256;
-  const int64_t cap = (int64_t)sms * *per_sm;
+  const int64_t cap = (int64_t)sms * b;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
@@ -204,7 +205,7 @@ cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bo
                              cudaStream_t st) {
   const int64_t n16 = n / 16;
   const SwigluParams pr{a.limit, a.alpha, a.beta, a.has_limit ? 1 : 0, a.beta != 0.0f ? 1 : 0};
-  static int occ[4] = {0, 0, 0, 0};
+  static std::atomic<int> occ[4];
   if (in_f16) {
     if (out_fp8) {
       auto k = swiglu_ex_kernel<true, true>;
@@ -228,7 +229,7 @@ cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bo
 cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w, uint16_t* wd, int sms,
                                   cudaStream_t st) {
   const int64_t n16 = n / 16;
-  static int occ = 0;
+  static std::atomic<int> occ{0};
   dequant_weight_kernel<<<grid_for((const void*)dequant_weight_kernel, &occ, n16, sms), 256, 0, st>>>(q, n16, s_w,
                                                                                                   wd);
   return cudaGetLastError();
@@ -237,7 +238,7 @@ cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w,
 cudaError_t launch_quant_static(const uint16_t* x, int64_t n, const float* s_in, uint8_t* q,
                                 int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
-  static int occ = 0;
+  static std::atomic<int> occ{0};
   quant_static_kernel<<<grid_for((const void*)quant_static_kernel, &occ, n16, sms), 256, 0, st>>>(x, n16, s_in, q);
   return cudaGetLastError();
 }
@@ -245,7 +246,7 @@ cudaError_t launch_quant_static(const uint16_t* x, int64_t n, const float* s_in,
 cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, const float* s_out,
                               uint8_t* out, int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
-  static int occ = 0;
+  static std::atomic<int> occ{0};
   swiglu_fp8_kernel<<<grid_for((const void*)swiglu_fp8_kernel, &occ, n16, sms), 256, 0, st>>>(g, u, n16, s_out, out);
   return cudaGetLastError();
 }
@@ -253,7 +254,7 @@ cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, c
 cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* out,
                                int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
-  static int occ = 0;
+  static std::atomic<int> occ{0};
   swiglu_bf16_kernel<<<grid_for((const void*)swiglu_bf16_kernel, &occ, n16, sms), 256, 0, st>>>(g, u, n16, out);
   return cudaGetLastError();
 }
