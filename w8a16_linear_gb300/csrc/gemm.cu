@@ -17,15 +17,20 @@
 //        the same bf16 values the separate GEMMs would write, so the codes are
 //        those of swiglu_2in_fp8 applied to them; each projection keeps its
 //        own weight scale (TensorRT-LLM PR #17476, section What changed).
-//  W8A16 (kind::f16, below): y = bf16( sum_k x[m,k] * Wd[n,k] ),
-//        Wd = bf16( fl32(dec(qw) * s_w) ), the dequantized weight formed in
-//        TMEM; the static input scale is not used and no dequantized weight
-//        is written to global memory (TensorRT-LLM PR #17476, section
-//        Denoising-step activation precision; diffusers PR #14664,
-//        "[Cosmos3] Mixed W8A8/W8A16 denoising for ModelOpt FP8 checkpoints",
-//        section Behavior).
+//  BF16  (kind::f16): the "F.linear" half of the W8A16 path, y = bf16( sum_k
+//        x[m,k] * Wd[n,k] ) on a weight dequantized beforehand, Wd =
+//        bf16( fl32(dec(qw) * s_w) ); the static input scale is not used
+//        (TensorRT-LLM PR #17476, section Denoising-step activation precision;
+//        diffusers PR #14664, "[Cosmos3] Mixed W8A8/W8A16 denoising for
+//        ModelOpt FP8 checkpoints", section Behavior: dequant + F.linear).
+//  GLU16 (kind::f16): the gate and up projections of a 16-bit step on
+//        dequantized weights, with the SwiGLU written as bf16 -- the values
+//        swiglu_2in_bf16 would produce from the bf16 outputs of BF16.
+//  W8A16 (kind::f16, gemm_a16t_kernel below): the same product with the
+//        dequantized weight formed in TMEM inside the GEMM, for calls that
+//        provide no workspace.
 //
-// W8A8 / GLU kernel shapes (template parameter CG):
+// W8A8 / GLU / BF16 / GLU16 kernel shapes (template parameter CG):
 //   CG = 1  one CTA per SM computes a 128-row output tile.
 //   CG = 2  a cluster of two CTAs on two SMs computes a 256-row tile with
 //           CTA-pair MMAs (tcgen05 cta_group::2): each CTA stages its 128
@@ -36,9 +41,10 @@
 // Roles (per CTA, one CTA per SM, static round-robin over output tiles):
 //   warp 0      TMA producer: activation and weight tiles into a smem ring
 //   warp 1      TMEM allocator; MMA issuer (one thread of the even CTA)
-//   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 (or SwiGLU ->
-//               E4M3) -> swizzled smem -> TMA store; double-buffered TMEM
-//               accumulators let it overlap the next tile's main loop
+//   warps 2-5   epilogue, one warp per TMEM lane quadrant: TMEM -> registers
+//               -> scale -> bf16 (or SwiGLU -> E4M3 / bf16) -> swizzled smem ->
+//               TMA store; double-buffered TMEM accumulators let it overlap
+//               the next tile's main loop
 // Every mbarrier wait is bounded: on a timeout the kernel records an error
 // bit, the other roles stop at their next wait, in-flight copies and MMAs
 // are drained with bounded waits, TMEM is freed and the kernel returns.
