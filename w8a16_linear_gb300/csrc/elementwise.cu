@@ -8,13 +8,18 @@
 //    down projection's static input scale, or to bf16 on 16-bit steps
 //    (TensorRT-LLM PR #17476, "Load static FP8 Cosmos3 Nano/Super checkpoints
 //    without re-quantizing them", sections What changed and Denoising-step
-//    activation precision).
+//    activation precision), and its tested options (limit, alpha, beta;
+//    bf16 or binary16 inputs; section Test Coverage);
+//  * the W8A16 weight dequantization, bf16(fl32(dec(q) * s_w)) (diffusers PR
+//    #14664, "[Cosmos3] Mixed W8A8/W8A16 denoising for ModelOpt FP8
+//    checkpoints", section Behavior: dequant + F.linear).
 //
 // Each thread moves 16 elements per step with 128-bit loads and stores in a
-// grid-stride loop over a grid of as many blocks as fit on the GPU at once.  Every output is the
-// specification's bit pattern: a fast value with a proven error bound is
-// kept only where it provably rounds to the same code, everything else is
-// recomputed with correctly rounded, never-fused scalar operations.
+// grid-stride loop over a grid of as many blocks as fit on the GPU at once.
+// Every output is the specification's bit pattern: a fast value with a
+// proven error bound is kept only where it provably rounds to the same code,
+// everything else is recomputed with correctly rounded, never-fused scalar
+// operations.
 //
 // The SwiGLU specification and its guarded fast evaluation live in
 // swiglu_spec.cuh.
