@@ -609,6 +609,16 @@ def run_case(args):
         # dequant + F.linear: the three weights into a workspace, one bf16 group GEMM
         wsd = W.w8a16_workspace(qs)
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, qs, ss, outs=ys, ws=wsd)  # noqa: E731
+    elif args.case == "glu16_8k":
+        # the 16-bit steps' gate/up + bf16 SwiGLU on dequantized weights
+        def dq_weight():
+            w = torch.randn((INTER, HID), generator=gen, device=dev) * 0.02
+            sc = (w.abs().amax() / 448).reshape(1).contiguous()
+            q = (w / sc).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+            return W.fp8_dequant_weight(q, sc)
+        dg, du = dq_weight(), dq_weight()
+        h16 = torch.empty((M, INTER), dtype=torch.bfloat16, device=dev)
+        fn = lambda: W.bf16_gate_up_swiglu(x, dg, du, out=h16)  # noqa: E731
     elif args.case == "swiglu_ex8k":
         gg = (torch.randn((M, INTER), generator=gen, device=dev) * 2).to(torch.float16)
         uu = torch.randn((M, INTER), generator=gen, device=dev).to(torch.float16)
@@ -680,7 +690,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, swiglu8k, swiglu_ex8k, block_gemms) instead of the bench")
+                    help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, block_gemms) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.case:
