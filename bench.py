@@ -258,10 +258,10 @@ class Block:
 
 
 # DRAM bytes (read + write) of the A8 block step's four GEMM launches at
-# M=20670 from one ncu capture of the current gemm_kernel build (3228.4 MB read
-# + 1110.8 MB written; algorithmic 861 + 1185 MB).  Re-capture, or set to None,
+# M=20670 from one ncu capture of the current gemm_kernel build (2972.3 MB read
+# + 1110.0 MB written; algorithmic 861 + 1185 MB).  Re-capture, or set to None,
 # whenever gemm_kernel changes.
-GEMM_TRAFFIC_BYTES = 4339.2e6
+GEMM_TRAFFIC_BYTES = 4082.2e6
 
 
 def flush_l2(buf):

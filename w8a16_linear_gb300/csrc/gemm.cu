@@ -90,10 +90,17 @@ struct Cfg {
   static constexpr int kBN = kGlu ? 128 : 256;              // output columns per tile
   static constexpr int kMmaN = 256;
   static constexpr int kBRows = kMmaN / CG;                 // weight rows staged per CTA
-  static constexpr int kBK = kBf16 ? 64 : 128;              // K per stage (128 bytes per row)
-  static constexpr int kABytes = BM * 128;
-  static constexpr int kBBytes = kBRows * 128;
-  static constexpr int kStages = CG == 1 ? 4 : 6;
+  // A stage holds kAtoms 128-byte-wide K slices ("atoms", the span of the
+  // 128-byte swizzle) of each operand: more K per barrier round trip, fewer
+  // and larger stages in the same shared memory.  Two atoms (256 bytes of K,
+  // 8 MMAs per stage) measured 3-7% faster than one for W8A8, 14% for GLU,
+  // 8% for GLU16 and the same for BF16.
+  static constexpr int kAtoms = 2;
+  static constexpr int kAtomK = kBf16 ? 64 : 128;           // K elements per atom
+  static constexpr int kBK = kAtomK * kAtoms;               // K per stage
+  static constexpr int kABytes = BM * 128 * kAtoms;
+  static constexpr int kBBytes = kBRows * 128 * kAtoms;
+  static constexpr int kStages = (CG == 1 ? 4 : 6) / kAtoms;
   static constexpr uint32_t kIdesc =                        // E4M3 x E4M3 or BF16 x BF16 -> F32
       kBf16 ? make_idesc(1, 1, BM * CG, kMmaN) : make_idesc(0, 0, BM * CG, kMmaN);
   // One epilogue warp per TMEM lane quadrant: more warps (each taking fewer
@@ -271,13 +278,19 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           if (leader) mbar_arrive_expect_tx(full_bar(s), CG * (C::kABytes + C::kBBytes));
           const uint32_t fb = leader_addr(full_bar(s));
           const CUtensorMap* mb0 = kGlu ? (rank == 0 ? &maps.b[0] : &maps.b[1]) : map_b(maps, g);
-          if constexpr (CG == 2) {
-            tma_load_2d_pair(a_dst, &maps.a, fb, kc, a_row);
-            tma_load_2d_pair(b_dst, mb0, fb, kc, b_row);
-          } else {
-            tma_load_2d(a_dst, &maps.a, fb, kc, a_row);
-            tma_load_2d(b_dst, mb0, fb, kc, b_row);
-            if constexpr (kGlu) tma_load_2d(b_dst + 128 * 128, &maps.b[1], fb, kc, b_row);
+#pragma unroll
+          for (int at = 0; at < C::kAtoms; ++at) {
+            const uint32_t ad = a_dst + (uint32_t)(at * BM * 128);
+            const uint32_t bd = b_dst + (uint32_t)(at * C::kBRows * 128);
+            const int kx = kc + at * C::kAtomK;
+            if constexpr (CG == 2) {
+              tma_load_2d_pair(ad, &maps.a, fb, kx, a_row);
+              tma_load_2d_pair(bd, mb0, fb, kx, b_row);
+            } else {
+              tma_load_2d(ad, &maps.a, fb, kx, a_row);
+              tma_load_2d(bd, mb0, fb, kx, b_row);
+              if constexpr (kGlu) tma_load_2d(bd + 128 * 128, &maps.b[1], fb, kx, b_row);
+            }
           }
           ++issued;
           if (++s == S) {
@@ -323,9 +336,9 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           const uint32_t a_addr = sbase + L::kA + s * C::kABytes;
           const uint32_t b_addr = sbase + L::kB + s * C::kBBytes;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
-            const uint64_t ad = sw128_kmajor_desc(a_addr + 32 * k);
-            const uint64_t bd = sw128_kmajor_desc(b_addr + 32 * k);
+          for (int k = 0; k < 4 * C::kAtoms; ++k) {  // MMAs of 32 bytes of K each, 4 per atom
+            const uint64_t ad = sw128_kmajor_desc(a_addr + (k >> 2) * BM * 128 + 32 * (k & 3));
+            const uint64_t bd = sw128_kmajor_desc(b_addr + (k >> 2) * C::kBRows * 128 + 32 * (k & 3));
             const uint32_t accum = (kb | k) != 0;
             if constexpr (C::kBf16) {  // K = 16 per MMA: 32 bytes, as for E4M3
               if constexpr (CG == 2) mma_f16_pair(d, ad, bd, C::kIdesc, accum);
@@ -898,11 +911,11 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   const int tiles_m = (int)((p.M + BM * CG - 1) / (BM * CG));
   constexpr int kEl = C::kBf16 ? 2 : 1;  // operand element bytes
   const CUtensorMapDataType dt = C::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  bool ok = encode_2d(&maps.a, dt, p.x, p.K, p.M, p.K * kEl, C::kBK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  bool ok = encode_2d(&maps.a, dt, p.x, p.K, p.M, p.K * kEl, C::kAtomK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   const int nb = kGlu ? 2 : p.G;  // weight maps: GLU gate and up
   for (int g = 0; g < nb; ++g) {
     args.s_w[g] = p.s_w[g];
-    ok &= encode_2d(&maps.b[g], dt, p.w[g], p.K, p.N[kGlu ? 0 : g], p.K * kEl, C::kBK,
+    ok &= encode_2d(&maps.b[g], dt, p.w[g], p.K, p.N[kGlu ? 0 : g], p.K * kEl, C::kAtomK,
                     kGlu ? 128 : C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   for (int g = 0; g < args.G; ++g) {
