@@ -24,7 +24,9 @@ the passage it follows:
 Modules: ``e4m3`` (the FP8 codec), ``bf16`` and ``fp16`` (16-bit codecs),
 ``linear`` (quantization, W8A8 / W8A16, the dequantized weight, the max(s)
 re-quantization, the sharing group), ``swiglu`` (the SwiGLU specification
-and its options), ``policy`` (the per-step precision policy and its JSON).
+and its options), ``policy`` (the per-step precision policy and its JSON),
+``norm`` (the modulated LayerNorm that produces a linear layer's input, and
+the static quantization fused after it).
 
 Floating point: the GEMM oracles work in float64 on exactly decoded
 operands (the definition written out).  Where a floating-point value decides
@@ -42,6 +44,7 @@ from .linear import (quant_static, linear_w8a8, linear_w8a16,
 from .swiglu import (exp_spec, swiglu_2in_fp8, swiglu_2in_bf16, swiglu_h, swiglu_h_ex,
                      swiglu_2in_ex_fp8, swiglu_2in_ex_16)
 from .policy import StepPolicy, PolicyError, step_mode, parse_policy, A8, A16
+from .norm import ln_modulate, ln_modulate_bf16, ln_modulate_quant
 
 __all__ = [
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "e4m3_all_values",
@@ -51,4 +54,5 @@ __all__ = [
     "exp_spec", "swiglu_2in_fp8", "swiglu_2in_bf16", "swiglu_h", "swiglu_h_ex",
     "swiglu_2in_ex_fp8", "swiglu_2in_ex_16",
     "StepPolicy", "PolicyError", "step_mode", "parse_policy", "A8", "A16",
+    "ln_modulate", "ln_modulate_bf16", "ln_modulate_quant",
 ]
