@@ -493,6 +493,23 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     ms = _time(lambda: W.fp8_dequant_weight(blk.w_gu[0][0], blk.w_gu[0][1], out=blk.wsd[:INTER * HID].view(INTER, HID)),
                flush, stream, n)
     out["fp8_dequant_weight_16384x4096"] = {"us": ms * 1e3, "GB_s": 3 * INTER * HID / ms / 1e6}
+    # the producer of a linear input with the static quantization fused after
+    # it (modulated LayerNorm -> bf16 -> E4M3), against the same two steps
+    # run apart (bf16 h written and read back)
+    gen = torch.Generator(device=blk.x_qkv.device).manual_seed(31)
+    shift, scale = ((torch.randn((1, HID), generator=gen, device=blk.x_qkv.device) * 0.5).to(torch.bfloat16)
+                    for _ in range(2))
+    hb = blk.y_qkv[0]
+    ms = _time(lambda: W.ln_modulate_quant(blk.x_qkv, shift, scale, blk.s_qkv, out=blk.ws), flush, stream, n)
+    out["ln_modulate_quant"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6,
+                                "note": "LayerNorm + shift/scale + bf16 + E4M3 in one pass, [20670, 4096]"}
+
+    def ln_unfused():
+        W.ln_modulate_bf16(blk.x_qkv, shift, scale, out=hb)
+        W.fp8_quant_static(hb, blk.s_qkv, out=blk.ws)
+    ms = _time(ln_unfused, flush, stream, n)
+    out["ln_modulate_then_quant"] = {"us": ms * 1e3, "GB_s": 7 * blk.x_qkv.numel() / ms / 1e6,
+                                     "note": "the same as two launches (bf16 h through HBM)"}
     torch.cuda.synchronize()
     return out
 
@@ -644,6 +661,14 @@ def run_case(args):
         s_h = torch.tensor([0.02], device=dev)
         h8 = torch.empty((M, INTER), dtype=torch.uint8, device=dev)
         fn = lambda: W.gate_up_swiglu_fp8(x, s_x, wg, wu, sg, su, s_h, out=h8, ws=qx)  # noqa: E731
+    elif args.case == "ln20k":
+        # the producer of the Q/K/V input at the bench's size (x alone is
+        # larger than L2): modulated LayerNorm + static quantization
+        xl = (torch.randn((M_TOK, HID), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
+        ql = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
+        shift, scale = ((torch.randn((1, HID), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
+                        for _ in range(2))
+        fn = lambda: W.ln_modulate_quant(xl, shift, scale, s, out=ql)  # noqa: E731
     elif args.case == "swiglu8k":
         gg = (torch.randn((M, INTER), generator=gen, device=dev) * 2).to(torch.bfloat16)
         uu = torch.randn((M, INTER), generator=gen, device=dev).to(torch.bfloat16)

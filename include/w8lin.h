@@ -35,7 +35,8 @@
  *    argument returns its error code and enqueues nothing.  Thread-local
  *    detail is available from w8_last_error().
  *  - Kernels never trap.  A GEMM whose internal pipeline wait runs past its
- *    deadline (2 s) stops, records W8_ERR_TIMEOUT in a device error word and
+ *    deadline (2 s), or an ln_modulate_quant block whose row-buffer wait
+ *    does, stops, records W8_ERR_TIMEOUT in a device error word and
  *    returns; w8_poll_device_error() reports and clears it.
  */
 #ifndef W8LIN_H
@@ -324,6 +325,36 @@ w8_status swiglu_2in_ex_fp8(const void* gate, const void* up, int32_t in_dtype, 
  * 16-bit-step form. */
 w8_status swiglu_2in_ex_16(const void* gate, const void* up, int32_t in_dtype, int64_t M, int64_t I,
                            const w8_swiglu_params* prm, void* out, void* stream);
+
+/*
+ * ln_modulate_quant — the producer of a linear layer's input with the static
+ * quantization fused after it.  The pages place the quantization right after
+ * the block's norm/modulation ([P2] Verification: div -> clamp ->
+ * round-to-float8 on the activation) and give the norm no formula; this
+ * entry takes the diffusion-transformer form: per row of x,
+ *   n = (x - mean(x)) / sqrt(var(x) + eps)     (LayerNorm without affine,
+ *                                              biased variance over K)
+ *   h = bf16_RNE( n * (1 + scale[s]) + shift[s] ),   s = row / rows_per_sample
+ *   q = E4M3_satRNE( fl32(h / s_in) )          (exactly fp8_quant_static of h)
+ * Statistics in binary32: h equals the correctly rounded bf16 of the exact
+ * value except where that value lies within a few binary32 ulps of a bf16
+ * rounding boundary, where it may be the neighbouring bf16.  q is always the
+ * quantization of the h this call produces (written or not).
+ *   x      bf16 [M, K], device, read-only; 8 <= K <= 8192, K % 8 == 0
+ *   shift, scale  bf16 [M / rows_per_sample, K], device, read-only
+ *   rows_per_sample  tokens per sample (>= 1, divides M)
+ *   eps    LayerNorm epsilon, finite and >= 0 (eps = 0 on a constant row
+ *          gives NaN, as the formula does)
+ *   s_in   device float scalar; required iff q is given
+ *   q      E4M3 [M, K], device, written; may be NULL (bf16 h only)
+ *   h      bf16 [M, K], device, written; may be NULL (codes only)
+ * All arrays 16-byte aligned.  M == 0 launches nothing.
+ * Errors: NULL (x, shift, scale, both outputs, s_in with q), SHAPE, ALIGN,
+ * PARAM (eps), ARCH, CUDA.
+ */
+w8_status ln_modulate_quant(const uint16_t* x, int64_t M, int64_t K, const uint16_t* shift,
+                            const uint16_t* scale, int64_t rows_per_sample, float eps,
+                            const float* s_in, uint8_t* q, uint16_t* h, void* stream);
 
 /*
  * step_policy_dispatch — host-only, pure function of (policy, step, num_steps).

@@ -22,9 +22,11 @@ sample ``m // rows_per_sample``.  The quantization that follows is the
 path's own (``linear.quant_static``) applied to the bf16 h.
 
 The values here are the definition written out in float64 on exactly decoded
-inputs; h is rounded once to bf16.  A binary32 implementation can land one
-bf16 step away where the exact h sits within its rounding error of a bf16
-rounding boundary; the tests accept either neighbour there (and only there).
+inputs; h is rounded once to bf16.  A binary32 implementation can land on
+another bf16 where the exact h lies within its rounding error of a bf16
+rounding boundary (several bf16 steps away where h is small against its
+terms); the tests accept the bf16 values within that error there, and only
+there.
 """
 
 import numpy as np
@@ -78,8 +80,9 @@ def ln_modulate_quant(x_bits, shift_bits, scale_bits, eps, rows_per_sample, s_in
 
 def bf16_neighbours(h64, tol):
     """The bf16 roundings of ``h64 - tol`` and ``h64 + tol`` (uint16 bits):
-    equal where every value within ``tol`` of h rounds to the same bf16,
-    the two admissible results otherwise."""
+    equal where every value within ``tol`` of h rounds to the same bf16;
+    otherwise every bf16 between the two (inclusive) is the rounding of some
+    value within ``tol``."""
     return bf16_round(h64 - tol), bf16_round(h64 + tol)
 
 

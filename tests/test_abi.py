@@ -35,7 +35,7 @@ def test_header_symbols_exported(L):
     for n in names:
         assert hasattr(L, n), n
         assert n in binding.SIGNATURES, n
-    assert L.w8_abi_version() == 2
+    assert L.w8_abi_version() == 3
 
 
 def test_policy_matches_oracle_everywhere(L):
@@ -141,6 +141,29 @@ def test_swiglu_variant_validation_before_any_cuda_call(L):
     # zero rows: no launch
     assert L.swiglu_2in_ex_fp8(p16, p16, 0, 0, 16, ref(ok), p16, p16, None) == 0
     assert L.swiglu_2in_ex_16(p16, p16, 2, 0, 16, ref(ok), p16, None) == 0
+
+
+def test_ln_modulate_quant_validation_before_any_cuda_call(L):
+    p16, nul = _u(0x10000), None
+    f = L.ln_modulate_quant
+    # (x, M, K, shift, scale, rows_per_sample, eps, s_in, q, h, stream)
+    assert f(p16, 4, 12, p16, p16, 4, 1e-6, p16, p16, nul, nul) == 2        # K % 8
+    assert f(p16, 4, 8200, p16, p16, 4, 1e-6, p16, p16, nul, nul) == 2      # K > 8192
+    assert f(p16, 4, 0, p16, p16, 4, 1e-6, p16, p16, nul, nul) == 2
+    assert f(p16, -1, 16, p16, p16, 1, 1e-6, p16, p16, nul, nul) == 2
+    assert f(p16, 6, 16, p16, p16, 4, 1e-6, p16, p16, nul, nul) == 2        # 4 does not divide 6
+    assert f(p16, 6, 16, p16, p16, 0, 1e-6, p16, p16, nul, nul) == 2
+    for eps in (-1e-6, float("nan"), float("inf")):
+        assert f(p16, 4, 16, p16, p16, 4, eps, p16, p16, nul, nul) == 11
+    assert f(nul, 4, 16, p16, p16, 4, 1e-6, p16, p16, nul, nul) == 1
+    assert f(p16, 4, 16, nul, p16, 4, 1e-6, p16, p16, nul, nul) == 1
+    assert f(p16, 4, 16, p16, p16, 4, 1e-6, p16, nul, nul, nul) == 1        # no output
+    assert f(p16, 4, 16, p16, p16, 4, 1e-6, nul, p16, nul, nul) == 1        # q without s_in
+    assert f(p16, 4, 16, p16, _u(0x10008), 4, 1e-6, p16, p16, nul, nul) == 3
+    assert f(p16, 4, 16, p16, p16, 4, 1e-6, nul, nul, _u(0x10004), nul) == 3
+    assert b"ln_modulate_quant" in L.w8_last_error()
+    assert f(p16, 0, 16, p16, p16, 1, 1e-6, p16, p16, nul, nul) == 0        # zero rows: no launch
+    assert f(p16, 0, 4096, nul, nul, 7, 0.0, nul, nul, nul, nul) == 0
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

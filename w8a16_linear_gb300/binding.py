@@ -76,6 +76,8 @@ SIGNATURES = {
                                          _c_void_p, _c_void_p, _c_void_p]),
     "swiglu_2in_ex_16": (ctypes.c_int, [_c_void_p, _c_void_p, _i32, _i64, _i64, ctypes.POINTER(SwigluParams),
                                         _c_void_p, _c_void_p]),
+    "ln_modulate_quant": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i64, ctypes.c_float,
+                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "step_policy_dispatch": (ctypes.c_int, [_c_void_p, _i32, _i32, ctypes.POINTER(_i32)]),
     "w8_check_group_scales": (ctypes.c_int, [ctypes.POINTER(_c_void_p), _i32]),
     "w8_step_policy_parse": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(StepPolicy),
@@ -185,6 +187,42 @@ def fp8_quant_static(x, s_in, out=None, stream=None):
         out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     o = _as_u8(out, "out")
     _check(lib().fp8_quant_static(_ptr(x2), M, K, _ptr(_scalar(s_in, "s_in")), _ptr(o), _stream(stream)))
+    return out
+
+
+def _ln_call(x, shift, scale, eps, s_in, q, h, stream):
+    x = _as_bf16(x, "x")
+    x2 = _flat2(x)
+    M, K = x2.shape
+    sh = _flat2(_as_bf16(shift, "shift"))
+    sc = _flat2(_as_bf16(scale, "scale"))
+    S = sh.shape[0]
+    if sc.shape != sh.shape or sh.shape[1] != K or S < 1:
+        raise W8Error(2, f"shift/scale: expected [S, {K}], got {tuple(sh.shape)} and {tuple(sc.shape)}")
+    if M % S:
+        raise W8Error(2, f"{M} rows do not split into {S} samples")
+    rps = max(M // S, 1)
+    _check(lib().ln_modulate_quant(_ptr(x2), M, K, _ptr(sh), _ptr(sc), rps, float(eps),
+                                   _ptr(s_in), _ptr(q), _ptr(h), _stream(stream)))
+
+
+def ln_modulate_quant(x, shift, scale, s_in, eps=1e-6, out=None, h_out=None, stream=None):
+    """E4M3 codes of the modulated LayerNorm of ``x`` (rows split evenly into
+    ``shift.shape[0]`` samples), quantized with ``s_in``; also writes the
+    bf16 h into ``h_out`` when given.  Returns the codes."""
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    q = _as_u8(out, "out")
+    h = _as_bf16(h_out, "h_out") if h_out is not None else None
+    _ln_call(x, shift, scale, eps, _scalar(s_in, "s_in"), q, h, stream)
+    return out
+
+
+def ln_modulate_bf16(x, shift, scale, eps=1e-6, out=None, stream=None):
+    """The bf16 modulated LayerNorm alone (the unfused producer)."""
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _ln_call(x, shift, scale, eps, None, None, _as_bf16(out, "out"), stream)
     return out
 
 

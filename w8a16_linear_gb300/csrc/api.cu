@@ -95,7 +95,7 @@ int query_device(int* sms) { return device_info(sms); }
 
 extern "C" {
 
-int w8_abi_version(void) { return 2; }
+int w8_abi_version(void) { return 3; }
 
 const char* w8_last_error(void) { return g_last_error; }
 
@@ -106,10 +106,12 @@ w8_status w8_device_check(void) {
 }
 
 w8_status w8_poll_device_error(void* stream) {
-  uint32_t err = 0;
+  uint32_t err = 0, err2 = 0;
   cudaError_t e = w8::gemm_read_error(static_cast<cudaStream_t>(stream), &err);
+  if (e == cudaSuccess) e = w8::elementwise_read_error(static_cast<cudaStream_t>(stream), &err2);
   if (e != cudaSuccess) return fail(W8_ERR_CUDA, "reading device error word: %s", cudaGetErrorString(e));
   if (err & w8::kErrTimeout) return fail(W8_ERR_TIMEOUT, "a GEMM pipeline wait timed out");
+  if (err2 & w8::kErrTimeout) return fail(W8_ERR_TIMEOUT, "a row-buffer wait of ln_modulate_quant timed out");
   return ok();
 }
 
@@ -506,6 +508,31 @@ w8_status swiglu_2in_ex_16(const void* gate, const void* up, int32_t in_dtype, i
                                           M * I, in_dtype == W8_DTYPE_F16, false, a, nullptr, out, sms,
                                           static_cast<cudaStream_t>(stream)),
                      "swiglu_2in_ex_16 launch");
+}
+
+w8_status ln_modulate_quant(const uint16_t* x, int64_t M, int64_t K, const uint16_t* shift,
+                            const uint16_t* scale, int64_t rows_per_sample, float eps,
+                            const float* s_in, uint8_t* q, uint16_t* h, void* stream) {
+  if (M < 0 || K < 8 || K > 8192 || K % 8)
+    return fail(W8_ERR_SHAPE, "ln_modulate_quant: M=%lld K=%lld (need 8 <= K <= 8192, K %% 8 == 0)",
+                (long long)M, (long long)K);
+  if (rows_per_sample < 1 || (M % rows_per_sample) != 0)
+    return fail(W8_ERR_SHAPE, "ln_modulate_quant: rows_per_sample=%lld does not divide M=%lld",
+                (long long)rows_per_sample, (long long)M);
+  if (!std::isfinite(eps) || eps < 0.0f) return fail(W8_ERR_PARAM, "ln_modulate_quant: eps=%g", (double)eps);
+  if (M == 0) return ok();
+  if (!x || !shift || !scale) return fail(W8_ERR_NULL, "ln_modulate_quant: NULL input");
+  if (!q && !h) return fail(W8_ERR_NULL, "ln_modulate_quant: neither q nor h given");
+  if (q && !s_in) return fail(W8_ERR_NULL, "ln_modulate_quant: q needs s_in");
+  if (!aligned16(x) || !aligned16(shift) || !aligned16(scale) || (q && !aligned16(q)) || (h && !aligned16(h)) ||
+      (q && (reinterpret_cast<uintptr_t>(s_in) & 3u)))
+    return fail(W8_ERR_ALIGN, "ln_modulate_quant: arrays must be 16-byte aligned");
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  if (st != W8_OK) return st;
+  return cuda_status(w8::launch_ln_modulate_quant(x, M, (int)K, shift, scale, rows_per_sample, eps, s_in, q, h,
+                                                  sms, static_cast<cudaStream_t>(stream)),
+                     "ln_modulate_quant launch");
 }
 
 w8_status step_policy_dispatch(const w8_step_policy* policy, int32_t step, int32_t num_steps,

@@ -12,7 +12,12 @@
 //    bf16 or binary16 inputs; section Test Coverage);
 //  * the W8A16 weight dequantization, bf16(fl32(dec(q) * s_w)) (diffusers PR
 //    #14664, "[Cosmos3] Mixed W8A8/W8A16 denoising for ModelOpt FP8
-//    checkpoints", section Behavior: dequant + F.linear).
+//    checkpoints", section Behavior: dequant + F.linear);
+//  * the producer of a linear layer's input with the static quantization
+//    fused after it: LayerNorm (no affine) over each row, a per-sample
+//    shift/scale modulation, bf16 rounding, then the quantization above
+//    (the pages name the block's norm/modulation before the quantization
+//    without a formula; this is the diffusion-transformer form).
 //
 // Each thread moves 16 elements per step with 128-bit loads and stores in a
 // grid-stride loop over a grid of as many blocks as fit on the GPU at once.
@@ -188,6 +193,213 @@ __global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __res
   }
 }
 
+// ------------------------------------------------------------ norm + quant
+//
+// One block of 256 threads per row, grid-stride over rows.  The block's
+// coming rows stream into a ring of shared-memory row buffers by bulk copies
+// (one mbarrier per buffer), several rows ahead of the one being worked on:
+// that, not the register file, sets how many bytes are in flight.  Thread t
+// takes the row's 16-byte vectors t, t + 256, ... (kV of them, K <= 2048 kV)
+// into registers; the buffer is refilled once every thread has passed the
+// row's first reduction.  fl32(1 + scale) and the shift stay in registers
+// while consecutive rows belong to the same sample.  Statistics in binary32,
+// taken about the row's first element p = x_0 (so that a large common offset
+// of the row does not enter their rounding errors), with shallow summation
+// trees (the thread's 8 kV values as packed pairs pairwise, the last pair's
+// two halves, five butterfly levels, the 8 warp sums pairwise: depth 13 at
+// most):
+//   a   = fl32(x - p),   m = fl32(sum a * fl32(1/K))    (m = mean - p)
+//   var = fl32(sum fl32(a - m)^2 * fl32(1/K)),
+//   r   = rsqrt(fl32(var + eps))                        (within 2 ulps),
+//   n   = fma(a, r, -fl32(m r)),
+//   h   = bf16(fma(n, fl32(1 + scale), shift)).
+// h differs from the exactly computed value by a few binary32 ulps of its
+// terms, so it is the correctly rounded bf16 except where the exact value is
+// that close to a bf16 rounding boundary.  The E4M3 codes are the static
+// quantization of this bf16 h, bit for bit (quant_pair, as above).
+
+constexpr int kLnMaxStages = 8;
+constexpr int kLnRingBytes = 48 * 1024;       // row buffers per block (dynamic shared memory)
+constexpr uint64_t kLnWaitLimitNs = 2000000000ull;
+
+int ln_stages(int K) {
+  const int s = kLnRingBytes / (2 * K);
+  return s < kLnMaxStages ? s : kLnMaxStages;   // >= 3 for K <= 8192
+}
+
+__device__ uint32_t g_elem_err;                // kErrTimeout when a row-buffer wait gives up
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o /= 2) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Sum over the block: each warp's butterfly total, then the 8 warp totals
+// pairwise in a fixed order, so every thread gets the same value.
+__device__ __forceinline__ float block_sum(float v, float* slot) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) slot[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return __fadd_rn(__fadd_rn(__fadd_rn(slot[0], slot[1]), __fadd_rn(slot[2], slot[3])),
+                   __fadd_rn(__fadd_rn(slot[4], slot[5]), __fadd_rn(slot[6], slot[7])));
+}
+
+template <int kV>
+__device__ __forceinline__ void load_row(const uint16_t* __restrict__ src, int nvec, uint4 (&v)[kV]) {
+#pragma unroll
+  for (int i = 0; i < kV; ++i) {
+    const int j = threadIdx.x + 256 * i;
+    v[i] = j < nvec ? ldg16(src + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// kFull: K == 2048 kV, every vector slot of every thread holds row data.
+template <int kV, bool kFull>
+__global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulate_quant_kernel(
+    const uint16_t* __restrict__ x, int64_t M, int K, const uint16_t* __restrict__ shift,
+    const uint16_t* __restrict__ scale, int64_t rows_per_sample, float eps, int stages,
+    const float* __restrict__ s_in, uint8_t* __restrict__ q, uint16_t* __restrict__ h) {
+  extern __shared__ __align__(128) uint8_t ln_ring[];   // stages x K bf16
+  __shared__ __align__(8) uint64_t full[kLnMaxStages];
+  // [row parity][statistic][warp]: a row's two reductions and the next row's
+  // use different slots, so two barriers per row keep them apart.
+  __shared__ float red[2][2][8];
+  __shared__ int bad;
+  constexpr int kP = 4 * kV;                   // binary32 pairs per thread
+  const int nvec = K / 8;                      // 16-byte vectors per row
+  const uint32_t row_bytes = 2u * (uint32_t)K;
+  const int64_t G = gridDim.x;
+  if ((int64_t)blockIdx.x >= M) return;        // uniform over the block
+  const int64_t nrows = (M - 1 - blockIdx.x) / G + 1;   // rows of this block
+  const uint32_t ring = smem_u32(ln_ring);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < stages; ++st) mbar_init(smem_u32(&full[st]), 1);
+    fence_mbar_init();
+    bad = 0;
+  }
+  __syncthreads();
+  int64_t issued = 0;                          // rows whose copy is out (thread 0's count)
+  if (threadIdx.x == 0) {
+    for (; issued < nrows && issued < stages; ++issued) {
+      const uint32_t bar = smem_u32(&full[issued]);
+      mbar_arrive_expect_tx(bar, row_bytes);
+      bulk_load(ring + (uint32_t)issued * row_bytes, x + (blockIdx.x + issued * G) * K, row_bytes, bar);
+    }
+  }
+  float s = 1.0f, rs = 1.0f;
+  bool exact_only = false;
+  if (q != nullptr) {
+    s = __ldg(s_in);
+    rs = __frcp_rn(s);
+    exact_only = !scale_is_fast(s, rs);
+  }
+  const float inv_k = __frcp_rn((float)K);     // exact when K is a power of two
+  F2 g[kP];                                    // fl32(1 + scale) of the current sample
+  uint4 shv[kV];                               // its shift, bf16
+  int64_t smp_loaded = -1;
+  int never = 0;                               // nothing aborts these waits early
+  int64_t k = 0;
+  for (; k < nrows; ++k) {
+    const int par = (int)(k & 1);
+    const int64_t row = blockIdx.x + k * G;
+    const int st = (int)(k % stages);
+    const int64_t smp = row / rows_per_sample;
+    if (smp != smp_loaded) {                   // uniform over the block
+      uint4 scv[kV];
+      load_row<kV>(shift + smp * K, nvec, shv);
+      load_row<kV>(scale + smp * K, nvec, scv);
+#pragma unroll
+      for (int i = 0; i < kV; ++i) {
+        const uint32_t cw[4] = {scv[i].x, scv[i].y, scv[i].z, scv[i].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) g[4 * i + c] = add2(splat(1.0f), F2{bf16_lo(cw[c]), bf16_hi(cw[c])});
+      }
+      smp_loaded = smp;
+    }
+    if (!mbar_wait_warp(smem_u32(&full[st]), (uint32_t)((k / stages) & 1), &never, kLnWaitLimitNs))
+      bad = 1;
+    // the row into registers: a = x - p as packed pairs (padding pairs 0)
+    const uint16_t* rb = reinterpret_cast<const uint16_t*>(ln_ring + (size_t)st * row_bytes);
+    const float p = bf16_lo((uint32_t)rb[0]);
+    const F2 minus_p = splat(-p);
+    F2 a[kP];
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+      const int j = (int)threadIdx.x + 256 * i;
+      const bool live = kFull || j < nvec;
+      const uint4 v = live ? *reinterpret_cast<const uint4*>(rb + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        a[4 * i + c] = live ? add2(F2{bf16_lo(w[c]), bf16_hi(w[c])}, minus_p) : F2{0.0f, 0.0f};
+    }
+    // mean about the pivot: the thread's pairs pairwise, then the block
+    F2 t[kP];
+#pragma unroll
+    for (int i = 0; i < kP / 2; ++i) t[i] = add2(a[i], a[i + kP / 2]);
+#pragma unroll
+    for (int w = kP / 4; w >= 1; w /= 2) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) t[i] = add2(t[i], t[i + w]);
+    }
+    const float m = __fmul_rn(block_sum(__fadd_rn(t[0].x, t[0].y), red[par][0]), inv_k);
+    // every thread has its part of the row: the buffer takes row k + stages
+    if (bad) break;                            // uniform: set before the barrier above
+    if (threadIdx.x == 0 && issued < nrows) {
+      const uint32_t bar = smem_u32(&full[st]);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, row_bytes);
+      bulk_load(ring + (uint32_t)st * row_bytes, x + (blockIdx.x + issued * G) * K, row_bytes, bar);
+      ++issued;
+    }
+    // variance (two-pass: squared deviations from the mean)
+    const F2 minus_m = splat(-m);
+#pragma unroll
+    for (int i = 0; i < kP; ++i) {
+      const bool live = kFull || (int)threadIdx.x + 256 * (i / 4) < nvec;
+      const F2 d = add2(a[i], minus_m);
+      t[i] = live ? mul2(d, d) : F2{0.0f, 0.0f};
+    }
+#pragma unroll
+    for (int w = kP / 2; w >= 1; w /= 2) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) t[i] = add2(t[i], t[i + w]);
+    }
+    const float var = __fmul_rn(block_sum(__fadd_rn(t[0].x, t[0].y), red[par][1]), inv_k);
+    const float r = rsqrtf(__fadd_rn(var, eps));   // within 2 ulps of 1 / sqrt
+    // n = a r - m r in one rounding, h = bf16(n g + shift), then the codes
+    const F2 r2 = splat(r), mr2 = splat(-__fmul_rn(m, r));
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+      const int j = (int)threadIdx.x + 256 * i;
+      if (!kFull && j >= nvec) break;
+      const uint32_t sw[4] = {shv[i].x, shv[i].y, shv[i].z, shv[i].w};
+      uint32_t hb[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), g[4 * i + c], F2{bf16_lo(sw[c]), bf16_hi(sw[c])});
+        hb[c] = cvt_bf16x2(hv.x, hv.y);
+      }
+      if (h != nullptr) *reinterpret_cast<uint4*>(h + row * K + 8 * j) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+      if (q != nullptr) {
+        uint2 o;
+        o.x = quant_pair(hb[0], s, rs, exact_only) | (quant_pair(hb[1], s, rs, exact_only) << 16);
+        o.y = quant_pair(hb[2], s, rs, exact_only) | (quant_pair(hb[3], s, rs, exact_only) << 16);
+        *reinterpret_cast<uint2*>(q + row * K + 8 * j) = o;
+      }
+    }
+  }
+  if (bad && threadIdx.x == 0) {
+    // a wait gave up at row k: record it, then let the copies of rows k ..
+    // issued - 1, still in flight, land (each wait bounded) before the
+    // block's shared memory is released
+    atomicOr(&g_elem_err, kErrTimeout);
+    for (; k < issued; ++k)
+      mbar_wait(smem_u32(&full[k % stages]), (uint32_t)((k / stages) & 1), &never, kLnWaitLimitNs);
+  }
+}
+
 // Grid of 256-thread blocks for a grid-stride kernel: as many blocks as fit
 // on the GPU at once (blocks beyond that would run as a second, partly
 // occupied wave, which an HBM-bound kernel cannot afford), fewer for small
@@ -254,6 +466,44 @@ cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, c
   static std::atomic<int> occ{0};
   swiglu_fp8_kernel<<<grid_for((const void*)swiglu_fp8_kernel, &occ, n16, sms), 256, 0, st>>>(g, u, n16, s_out, out);
   return cudaGetLastError();
+}
+
+cudaError_t launch_ln_modulate_quant(const uint16_t* x, int64_t M, int K, const uint16_t* shift,
+                                     const uint16_t* scale, int64_t rows_per_sample, float eps,
+                                     const float* s_in, uint8_t* q, uint16_t* h, int sms, cudaStream_t st) {
+  // One row per block at a time: grid_for's 256 work items per block are one
+  // row.  The ring (at most 48 KB, with the static arrays just above the
+  // default per-block limit, hence the opt-in) stays below what the register
+  // limit leaves each block, so the occupancy figure without it stands.
+  static std::atomic<int> occ[3];              // full and ragged rows: same registers
+  const int64_t items = M * 256;
+  const int stages = ln_stages(K);
+  const int ring = stages * 2 * K;
+#define W8_LN_LAUNCH(V, SLOT)                                                                     \
+  {                                                                                               \
+    auto k = K == 2048 * V ? ln_modulate_quant_kernel<V, true> : ln_modulate_quant_kernel<V, false>; \
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ring);   \
+    if (e != cudaSuccess) return e;                                                               \
+    k<<<grid_for((const void*)k, &occ[SLOT], items, sms), 256, ring, st>>>(                       \
+        x, M, K, shift, scale, rows_per_sample, eps, stages, s_in, q, h);                         \
+  }
+  if (K <= 2048) W8_LN_LAUNCH(1, 0)
+  else if (K <= 4096) W8_LN_LAUNCH(2, 1)
+  else W8_LN_LAUNCH(4, 2)
+#undef W8_LN_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t elementwise_read_error(cudaStream_t st, uint32_t* err) {
+  *err = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(err, g_elem_err, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && *err != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_elem_err, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  }
+  return e;
 }
 
 cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* out,

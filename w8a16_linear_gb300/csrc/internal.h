@@ -24,6 +24,16 @@ cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, 
 cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w, uint16_t* wd, int sms,
                                   cudaStream_t st);
 
+// Modulated LayerNorm of each [K] row, rounded to bf16 (h) and/or quantized
+// to E4M3 with s_in (q); either output may be null, not both; 8 <= K <= 8192,
+// K % 8 == 0; row m uses shift/scale row m / rows_per_sample.
+// Reads and clears the elementwise kernels' device error word (synchronises `st`).
+cudaError_t elementwise_read_error(cudaStream_t st, uint32_t* err);
+
+cudaError_t launch_ln_modulate_quant(const uint16_t* x, int64_t M, int K, const uint16_t* shift,
+                                     const uint16_t* scale, int64_t rows_per_sample, float eps,
+                                     const float* s_in, uint8_t* q, uint16_t* h, int sms, cudaStream_t st);
+
 struct SwigluExArgs {            // validated by the caller
   bool has_limit;
   float limit, alpha, beta;

@@ -26,8 +26,8 @@ def normal_f32(seed, shape, std):
     return t.numpy()
 
 
-def activations_bf16(seed, shape, std, outlier_frac=0.0, outlier_mult=8.0):
-    """bf16 activations ~ N(0, std^2), with a fraction of randomly placed
+def activations_bf16(seed, shape, std, outlier_frac=0.0, outlier_mult=8.0, mean=0.0):
+    """bf16 activations ~ N(mean, std^2), with a fraction of randomly placed
     elements multiplied by ``outlier_mult`` (heavy-tailed channels of a
     diffusion transformer's hidden state).  Returns uint16 bf16 bits."""
     g = _gen(seed)
@@ -37,6 +37,8 @@ def activations_bf16(seed, shape, std, outlier_frac=0.0, outlier_mult=8.0):
         k = max(1, int(round(n * outlier_frac)))
         idx = torch.randint(0, n, (k,), generator=g)
         t.view(-1)[idx] *= float(outlier_mult)
+    if mean:
+        t += float(mean)
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
