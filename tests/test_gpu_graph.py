@@ -1,7 +1,8 @@
 """The path's entry points only enqueue work on the caller's stream, so a
 whole W8A8 block (shared-quant Q/K/V group, out-projection, fused gate/up +
-SwiGLU, down projection) and a W8A16 block (fused, and through the
-dequantization workspace) can be captured in a CUDA graph;
+SwiGLU, down projection), a W8A16 block (fused, and through the
+dequantization workspace) and the input producer (modulated LayerNorm with
+the quantization fused) can be captured in a CUDA graph;
 replaying the graph reproduces the eager results bit for bit."""
 
 import numpy as np
@@ -42,7 +43,10 @@ def test_block_in_cuda_graph(W):
         "qkv16w": [torch.empty((M, H), **bf) for _ in range(3)],
         "y16w": torch.empty((M, H), **bf),
         "h16f": torch.empty((M, I), **bf),
+        "qn": torch.empty((M, H), dtype=torch.uint8, device="cuda"),
+        "hn": torch.empty((M, H), **bf),
     }
+    mod = [(torch.randn((2, H), generator=gen, device="cuda") * 0.5).to(torch.bfloat16) for _ in range(2)]
     wdg, wdu = W.fp8_dequant_weight(wg[0], wg[1]), W.fp8_dequant_weight(wu[0], wu[1])
     wsd = W.w8a16_workspace([wg[0], wu[0]])
     ws = torch.empty((M, H), dtype=torch.uint8, device="cuda")
@@ -62,6 +66,8 @@ def test_block_in_cuda_graph(W):
                                 ws=wsd)
         W.qkv_shared_quant_gemm(W.MODE_A16, outs["h16"], None, [wd[0]], [wd[1]], outs=[outs["y16w"]], ws=wsd)
         W.bf16_gate_up_swiglu(x, wdg, wdu, out=outs["h16f"])
+        # the input producer with the quantization fused (two samples of 500 rows)
+        W.ln_modulate_quant(x, mod[0], mod[1], s_in, out=outs["qn"], h_out=outs["hn"])
 
     def snapshot():
         flat = []
