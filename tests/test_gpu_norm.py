@@ -180,3 +180,41 @@ def test_zero_rows_and_refusals(W):
         W.ln_modulate_quant(xs, v4, v4, dev_f32(1.0))          # 6 rows, 4 samples
     with pytest.raises(W.W8Error):
         W.ln_modulate_bf16(xs, v, v, eps=-1.0)
+
+
+def _midpoint_shift(K, n_mid, seed):
+    """A shift vector with n_mid entries at E4M3 rounding midpoints (ties of
+    the quantization at s = 1) and the rest at E4M3 values (far from any
+    rounding boundary)."""
+    v = O.e4m3_decode(np.arange(0x08, 0x7E, dtype=np.uint8)).astype(np.float64)   # normal E4M3
+    mids = (v[:-1] + v[1:]) / 2                                                        # exact in bf16
+    rng = np.random.default_rng(seed)
+    vals = v[rng.integers(0, len(v), K)] * rng.choice([-1.0, 1.0], K)
+    vals[:n_mid] = mids[rng.integers(0, len(mids), n_mid)] * rng.choice([-1.0, 1.0], n_mid)
+    rng.shuffle(vals)
+    return O.bf16_round(vals).astype(np.uint16)[None, :]
+
+
+@pytest.mark.parametrize("n_mid", [40, 4096])
+def test_unsettled_pairs(W, n_mid):
+    """Rows whose h are E4M3 ties at s = 1: with a few per row the kernel's
+    per-row list of unsettled pairs takes the division; with every element a
+    tie the list overflows and the whole row is redone.  Codes equal the
+    static quantization of h (ties to even)."""
+    M, K = 24, 4096
+    x = np.repeat(O.bf16_round(np.linspace(-1, 1, M)).astype(np.uint16)[:, None], K, axis=1)   # constant rows
+    shift = _midpoint_shift(K, n_mid, seed=n_mid)
+    scale = np.zeros((1, K), dtype=np.uint16)
+    q, h = _run(W, x, shift, scale, 1e-6, np.float32(1.0))
+    assert np.array_equal(h, np.repeat(shift, M, axis=0))
+    assert np.array_equal(q, O.quant_static(h, np.float32(1.0)))
+
+
+@pytest.mark.parametrize("s", [2e38, 1e-39])
+def test_scale_outside_fast_range(W, s):
+    """Scales whose reciprocal is not a normal binary32 number: every pair
+    takes the division (the list overflows on every row)."""
+    M, K, S = 40, 2048, 2
+    x, shift, scale = _problem(M, K, S, seed=13)
+    q, h = _run(W, x, shift, scale, 1e-6, np.float32(s))
+    assert np.array_equal(q, O.quant_static(h, np.float32(s)))

@@ -61,6 +61,13 @@ __device__ __forceinline__ uint32_t quant_pair(uint32_t w, float s, float r, boo
   return code;
 }
 
+// The specification's codes of one packed bf16 pair: correctly rounded
+// division, then the E4M3 rounding.  Kept out of line: it is the rare path of
+// the fused producer's row fix-up.
+__device__ __noinline__ uint32_t quant_pair_exact(uint32_t w, float s) {
+  return cvt_e4m3x2(__fdiv_rn(bf16_lo(w), s), __fdiv_rn(bf16_hi(w), s));
+}
+
 __global__ void __launch_bounds__(256, 8) quant_static_kernel(const uint16_t* __restrict__ x,
                                                               int64_t n16,
                                                               const float* __restrict__ s_in,
@@ -266,6 +273,13 @@ __global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulat
   // use different slots, so two barriers per row keep them apart.
   __shared__ float red[2][2][8];
   __shared__ int bad;
+  // Per-row list of the pairs whose fast code the bracket test could not
+  // settle (column, bf16 pair), by row parity like `red`: they get the
+  // correctly rounded division after the row's third barrier, so that the
+  // division's code is not in the per-pair loop.
+  constexpr int kFixCap = 128;
+  __shared__ uint32_t fix_n[2];
+  __shared__ uint2 fix[2][kFixCap];
   constexpr int kP = 4 * kV;                   // binary32 pairs per thread
   const int nvec = K / 8;                      // 16-byte vectors per row
   const uint32_t row_bytes = 2u * (uint32_t)K;
@@ -277,6 +291,7 @@ __global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulat
     for (int st = 0; st < stages; ++st) mbar_init(smem_u32(&full[st]), 1);
     fence_mbar_init();
     bad = 0;
+    fix_n[0] = fix_n[1] = 0;
   }
   __syncthreads();
   int64_t issued = 0;                          // rows whose copy is out (thread 0's count)
@@ -344,6 +359,8 @@ __global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulat
       for (int i = 0; i < w; ++i) t[i] = add2(t[i], t[i + w]);
     }
     const float m = __fmul_rn(block_sum(__fadd_rn(t[0].x, t[0].y), red[par][0]), inv_k);
+    // every thread is past the previous row's fix-up: its list may be reused
+    if (threadIdx.x == 0) fix_n[par ^ 1] = 0;
     // every thread has its part of the row: the buffer takes row k + stages
     if (bad) break;                            // uniform: set before the barrier above
     if (threadIdx.x == 0 && issued < nrows) {
@@ -383,10 +400,49 @@ __global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulat
       }
       if (h != nullptr) *reinterpret_cast<uint4*>(h + row * K + 8 * j) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
       if (q != nullptr) {
-        uint2 o;
-        o.x = quant_pair(hb[0], s, rs, exact_only) | (quant_pair(hb[1], s, rs, exact_only) << 16);
-        o.y = quant_pair(hb[2], s, rs, exact_only) | (quant_pair(hb[3], s, rs, exact_only) << 16);
-        *reinterpret_cast<uint2*>(q + row * K + 8 * j) = o;
+        uint32_t code[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          bool unsettled;
+          code[c] = e4m3x2_bracket(mul2(F2{bf16_lo(hb[c]), bf16_hi(hb[c])}, splat(rs)), kQuantBracketLo,
+                                   kQuantBracketHi, unsettled);
+          if (unsettled | exact_only) {
+            const uint32_t slot = atomicAdd(&fix_n[par], 1u);
+            if (slot < kFixCap) fix[par][slot] = make_uint2((uint32_t)(8 * j + 2 * c), hb[c]);
+          }
+        }
+        *reinterpret_cast<uint2*>(q + row * K + 8 * j) =
+            make_uint2(code[0] | (code[1] << 16), code[2] | (code[3] << 16));
+      }
+    }
+    if (q != nullptr) {
+      // the row's unsettled pairs: the fast codes above are stored; the
+      // barrier orders those stores before the exact ones
+      __syncthreads();
+      const uint32_t n = fix_n[par];
+      if (n <= (uint32_t)kFixCap) {
+        for (uint32_t e = threadIdx.x; e < n; e += 256) {
+          const uint2 f = fix[par][e];
+          *reinterpret_cast<uint16_t*>(q + row * K + f.x) = (uint16_t)quant_pair_exact(f.y, s);
+        }
+      } else {
+        // list overflow (a row with more than kFixCap unsettled pairs, as
+        // every pair is when the scale is outside the fast range): the block
+        // redoes the row's codes with the division
+#pragma unroll
+        for (int i = 0; i < kV; ++i) {
+          const int j = (int)threadIdx.x + 256 * i;
+          if (!kFull && j >= nvec) break;
+          const uint32_t sw[4] = {shv[i].x, shv[i].y, shv[i].z, shv[i].w};
+          uint32_t code[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), g[4 * i + c], F2{bf16_lo(sw[c]), bf16_hi(sw[c])});
+            code[c] = quant_pair_exact(cvt_bf16x2(hv.x, hv.y), s);
+          }
+          *reinterpret_cast<uint2*>(q + row * K + 8 * j) =
+              make_uint2(code[0] | (code[1] << 16), code[2] | (code[3] << 16));
+        }
       }
     }
   }
