@@ -337,8 +337,9 @@ w8_status swiglu_2in_ex_16(const void* gate, const void* up, int32_t in_dtype, i
  *   h = bf16_RNE( n * (1 + scale[s]) + shift[s] ),   s = row / rows_per_sample
  *   q = E4M3_satRNE( fl32(h / s_in) )          (exactly fp8_quant_static of h)
  * Statistics in binary32: h equals the correctly rounded bf16 of the exact
- * value except where that value lies within a few binary32 ulps of a bf16
- * rounding boundary, where it may be the neighbouring bf16.  q is always the
+ * value except where that value lies within the binary32 rounding error of
+ * its terms (a few ulps of |n (1 + scale)| and |h|) of a bf16 rounding
+ * boundary, where it may be another bf16 within that error.  q is always the
  * quantization of the h this call produces (written or not).
  *   x      bf16 [M, K], device, read-only; 8 <= K <= 8192, K % 8 == 0
  *   shift, scale  bf16 [M / rows_per_sample, K], device, read-only
