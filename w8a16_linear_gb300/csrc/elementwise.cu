@@ -208,8 +208,10 @@ __global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __res
 // that, not the register file, sets how many bytes are in flight.  Thread t
 // takes the row's 16-byte vectors t, t + 256, ... (kV of them, K <= 2048 kV)
 // into registers; the buffer is refilled once every thread has passed the
-// row's first reduction.  fl32(1 + scale) and the shift stay in registers
-// while consecutive rows belong to the same sample.  Statistics in binary32,
+// row's first reduction.  The sample's scale and shift stay in registers
+// (packed bf16; fl32(1 + scale) is formed where it is used, which keeps the
+// kernel at 64 registers and 4 blocks per SM) while consecutive rows belong
+// to the same sample.  Statistics in binary32,
 // taken about the row's first element p = x_0 (so that a large common offset
 // of the row does not enter their rounding errors), with shallow summation
 // trees (the thread's 8 kV values as packed pairs pairwise, the last pair's
@@ -263,7 +265,7 @@ __device__ __forceinline__ void load_row(const uint16_t* __restrict__ src, int n
 
 // kFull: K == 2048 kV, every vector slot of every thread holds row data.
 template <int kV, bool kFull>
-__global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulate_quant_kernel(
+__global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel(
     const uint16_t* __restrict__ x, int64_t M, int K, const uint16_t* __restrict__ shift,
     const uint16_t* __restrict__ scale, int64_t rows_per_sample, float eps, int stages,
     const float* __restrict__ s_in, uint8_t* __restrict__ q, uint16_t* __restrict__ h) {
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulat
     exact_only = !scale_is_fast(s, rs);
   }
   const float inv_k = __frcp_rn((float)K);     // exact when K is a power of two
-  F2 g[kP];                                    // fl32(1 + scale) of the current sample
+  uint4 scv[kV];                               // the current sample's scale, bf16
   uint4 shv[kV];                               // its shift, bf16
   int64_t smp_loaded = -1;
   int never = 0;                               // nothing aborts these waits early
@@ -321,15 +323,8 @@ __global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulat
     const int st = (int)(k % stages);
     const int64_t smp = row / rows_per_sample;
     if (smp != smp_loaded) {                   // uniform over the block
-      uint4 scv[kV];
       load_row<kV>(shift + smp * K, nvec, shv);
       load_row<kV>(scale + smp * K, nvec, scv);
-#pragma unroll
-      for (int i = 0; i < kV; ++i) {
-        const uint32_t cw[4] = {scv[i].x, scv[i].y, scv[i].z, scv[i].w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) g[4 * i + c] = add2(splat(1.0f), F2{bf16_lo(cw[c]), bf16_hi(cw[c])});
-      }
       smp_loaded = smp;
     }
     if (!mbar_wait_warp(smem_u32(&full[st]), (uint32_t)((k / stages) & 1), &never, kLnWaitLimitNs))
@@ -392,10 +387,12 @@ __global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulat
       const int j = (int)threadIdx.x + 256 * i;
       if (!kFull && j >= nvec) break;
       const uint32_t sw[4] = {shv[i].x, shv[i].y, shv[i].z, shv[i].w};
+      const uint32_t cw[4] = {scv[i].x, scv[i].y, scv[i].z, scv[i].w};
       uint32_t hb[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), g[4 * i + c], F2{bf16_lo(sw[c]), bf16_hi(sw[c])});
+        const F2 gc = add2(splat(1.0f), F2{bf16_lo(cw[c]), bf16_hi(cw[c])});
+        const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), gc, F2{bf16_lo(sw[c]), bf16_hi(sw[c])});
         hb[c] = cvt_bf16x2(hv.x, hv.y);
       }
       if (h != nullptr) *reinterpret_cast<uint4*>(h + row * K + 8 * j) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
@@ -434,10 +431,12 @@ __global__ void __launch_bounds__(256, kV == 1 ? 4 : kV == 2 ? 3 : 1) ln_modulat
           const int j = (int)threadIdx.x + 256 * i;
           if (!kFull && j >= nvec) break;
           const uint32_t sw[4] = {shv[i].x, shv[i].y, shv[i].z, shv[i].w};
+          const uint32_t cw[4] = {scv[i].x, scv[i].y, scv[i].z, scv[i].w};
           uint32_t code[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), g[4 * i + c], F2{bf16_lo(sw[c]), bf16_hi(sw[c])});
+            const F2 gc = add2(splat(1.0f), F2{bf16_lo(cw[c]), bf16_hi(cw[c])});
+            const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), gc, F2{bf16_lo(sw[c]), bf16_hi(sw[c])});
             code[c] = quant_pair_exact(cvt_bf16x2(hv.x, hv.y), s);
           }
           *reinterpret_cast<uint2*>(q + row * K + 8 * j) =
