@@ -211,12 +211,11 @@ __global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __res
 // row's first reduction.  The sample's scale and shift stay in registers
 // (packed bf16; fl32(1 + scale) is formed where it is used, which keeps the
 // kernel at 64 registers and 4 blocks per SM) while consecutive rows belong
-// to the same sample.  Statistics in binary32,
-// taken about the row's first element p = x_0 (so that a large common offset
-// of the row does not enter their rounding errors), with shallow summation
-// trees (the thread's 8 kV values as packed pairs pairwise, the last pair's
-// two halves, five butterfly levels, the 8 warp sums pairwise: depth 13 at
-// most):
+// to the same sample.  Statistics in binary32, taken about the row's first
+// element p = x_0 (so that a large common offset of the row does not enter
+// their rounding errors), with shallow summation trees (the thread's 8 kV
+// values as packed pairs pairwise, the last pair's two halves, five butterfly
+// levels, the 8 warp sums pairwise: depth 13 at most):
 //   a   = fl32(x - p),   m = fl32(sum a * fl32(1/K))    (m = mean - p)
 //   var = fl32(sum fl32(a - m)^2 * fl32(1/K)),
 //   r   = rsqrt(fl32(var + eps))                        (within 2 ulps),
@@ -225,7 +224,10 @@ __global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __res
 // h differs from the exactly computed value by a few binary32 ulps of its
 // terms, so it is the correctly rounded bf16 except where the exact value is
 // that close to a bf16 rounding boundary.  The E4M3 codes are the static
-// quantization of this bf16 h, bit for bit (quant_pair, as above).
+// quantization of this bf16 h, bit for bit: the bracket test of quant_pair
+// above, with the pairs it cannot settle collected in a per-row list and
+// given the correctly rounded division after the row's third barrier (so
+// that the division's code is not in the per-pair loop).
 
 constexpr int kLnMaxStages = 8;
 constexpr int kLnRingBytes = 48 * 1024;       // row buffers per block (dynamic shared memory)
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel
   extern __shared__ __align__(128) uint8_t ln_ring[];   // stages x K bf16
   __shared__ __align__(8) uint64_t full[kLnMaxStages];
   // [row parity][statistic][warp]: a row's two reductions and the next row's
-  // use different slots, so two barriers per row keep them apart.
+  // use different slots, so the row's own barriers keep them apart.
   __shared__ float red[2][2][8];
   __shared__ int bad;
   // Per-row list of the pairs whose fast code the bracket test could not
