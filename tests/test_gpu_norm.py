@@ -95,7 +95,8 @@ def _s_in(x, shift, scale, eps, T):
 
 
 @pytest.mark.parametrize("M,K,S", [(64, 256, 1), (300, 4096, 3), (37, 1000, 1), (16, 8, 2), (5, 8192, 1),
-                                   (130, 2048, 2), (1, 4096, 1), (9, 1024, 3), (24, 5120, 2), (8, 3000, 4)])
+                                   (130, 2048, 2), (1, 4096, 1), (9, 1024, 3), (24, 5120, 2), (8, 3000, 4),
+                                   (12, 4096, 12), (6, 8192, 3)])
 def test_shapes(W, M, K, S):
     x, shift, scale = _problem(M, K, S, seed=M + K)
     T = M // S
@@ -210,11 +211,12 @@ def test_unsettled_pairs(W, n_mid):
     assert np.array_equal(q, O.quant_static(h, np.float32(1.0)))
 
 
-@pytest.mark.parametrize("s", [2e38, 1e-39])
-def test_scale_outside_fast_range(W, s):
+@pytest.mark.parametrize("s,K", [(2e38, 2048), (1e-39, 2048), (2e38, 8192), (1e-39, 200)])
+def test_scale_outside_fast_range(W, s, K):
     """Scales whose reciprocal is not a normal binary32 number: every pair
-    takes the division (the list overflows on every row)."""
-    M, K, S = 40, 2048, 2
+    takes the division (through the list when a row has at most 128 pairs,
+    else by redoing the row)."""
+    M, S = 40, 2
     x, shift, scale = _problem(M, K, S, seed=13)
     q, h = _run(W, x, shift, scale, 1e-6, np.float32(s))
     assert np.array_equal(q, O.quant_static(h, np.float32(s)))
