@@ -77,8 +77,8 @@ template <Mode MODE, int CG>
 struct Cfg {
   static constexpr bool kGlu = (MODE == Mode::GLU || MODE == Mode::GLU16);
   // BF16: the W8A16 product on an already dequantized weight (bf16 x bf16,
-  // kind::f16): the same tiles and pipeline with 64 K-values (128 bytes) per
-  // stage and an unscaled epilogue.  GLU16: the gate/up pair of a 16-bit
+  // kind::f16): the same tiles and pipeline (a 128-byte swizzle atom holds
+  // 64 K-values instead of 128) and an unscaled epilogue.  GLU16: the gate/up pair of a 16-bit
   // step on dequantized weights, with the SwiGLU written as bf16.
   static constexpr bool kBf16 = (MODE == Mode::BF16 || MODE == Mode::GLU16);
   static constexpr bool kOut16 = (MODE == Mode::GLU16);
