@@ -220,3 +220,20 @@ def test_scale_outside_fast_range(W, s, K):
     x, shift, scale = _problem(M, K, S, seed=13)
     q, h = _run(W, x, shift, scale, 1e-6, np.float32(s))
     assert np.array_equal(q, O.quant_static(h, np.float32(s)))
+
+
+def test_random_shapes(W):
+    """Seeded random shapes: M in [1, 300], K any multiple of 8 up to 8192,
+    samples dividing M."""
+    rng = np.random.default_rng(2024)
+    for t in range(10):
+        K = int(rng.integers(1, 1025)) * 8
+        M = int(rng.integers(1, 301))
+        divisors = [d for d in range(1, M + 1) if M % d == 0]
+        S = int(rng.choice(divisors))
+        x, shift, scale = _problem(M, K, S, seed=100 + t, x_std=float(rng.uniform(0.1, 3.0)),
+                                   x_mean=float(rng.uniform(-2.0, 2.0)))
+        eps = float(rng.choice([0.0, 1e-6, 1e-5, 1e-3]))
+        s_in = _s_in(x, shift, scale, eps, M // S)
+        q, h = _run(W, x, shift, scale, eps, s_in)
+        _check(x, shift, scale, eps, M // S, s_in, q, h, max_ambiguous=0.05)
