@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -661,6 +662,68 @@ def run_case(args):
         s_h = torch.tensor([0.02], device=dev)
         h8 = torch.empty((M, INTER), dtype=torch.uint8, device=dev)
         fn = lambda: W.gate_up_swiglu_fp8(x, s_x, wg, wu, sg, su, s_h, out=h8, ws=qx)  # noqa: E731
+    elif args.case == "qkv_sustained":
+        # Sustained comparison under the power cap: the Q/K/V group launch
+        # (20670 x 4096 -> 3 x 4096, E4M3 input) and cuBLASLt FP8 on the same
+        # operands, each looped for about 3 s, alternating, three rounds, with
+        # the SM clock and board power sampled every 100 ms.  Prints one JSON
+        # line per phase.
+        blk = Block(dev)
+        qq = W.fp8_quant_static(blk.x_qkv, blk.s_qkv)
+        wq, sq = [w for w, _ in blk.w_qkv], [sc for _, sc in blk.w_qkv]
+        qf = qq.view(torch.float8_e4m3fn)
+        wt = [w.view(torch.float8_e4m3fn).t() for w in wq]
+
+        def ours():
+            W.fp8_linear_w8a8_group(qq, blk.s_qkv, wq, sq, outs=blk.y_qkv)
+
+        def lib():
+            for w_t, sw, y in zip(wt, sq, blk.y_qkv):
+                torch._scaled_mm(qf, w_t, scale_a=blk.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+        samples = []
+        smi = None
+        try:
+            smi = subprocess.Popen(["nvidia-smi", "--query-gpu=clocks.sm,power.draw", "--format=csv,noheader,nounits",
+                                    "-lms", "100"], stdout=subprocess.PIPE, text=True)
+        except OSError:
+            pass
+        def reader():
+            for line in smi.stdout:
+                parts = [v.strip() for v in line.split(",")]
+                try:
+                    samples.append((time.time(), float(parts[0]), float(parts[1])))
+                except (ValueError, IndexError):
+                    pass
+        if smi is not None:
+            threading.Thread(target=reader, daemon=True).start()
+        time.sleep(1.0)
+        for rnd in range(3):
+            for name, f in (("ours", ours), ("cublaslt_fp8", lib)):
+                for _ in range(5):
+                    f()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0, n = time.time(), 0
+                e0.record()
+                while time.time() - t0 < 3.0:
+                    for _ in range(20):
+                        f()
+                    n += 20
+                    torch.cuda.synchronize()
+                e1.record()
+                torch.cuda.synchronize()
+                t1 = time.time()
+                sel = [(c, pw) for ts, c, pw in samples if t0 + 0.3 <= ts <= t1]
+                us = e0.elapsed_time(e1) * 1e3 / n
+                print(json.dumps({"case": "qkv_sustained", "impl": name, "round": rnd, "us_per_launch": us,
+                                  "TFLOPS": QKV_FLOPS / us / 1e6, "launches": n,
+                                  "sm_mhz_median": statistics.median(c for c, _ in sel) if sel else None,
+                                  "power_w_median": statistics.median(pw for _, pw in sel) if sel else None}))
+                time.sleep(1.0)
+        if smi is not None:
+            smi.terminate()
+        W.poll_device_error()
+        return 0
     elif args.case == "ln20k":
         # the producer of the Q/K/V input at the bench's size (x alone is
         # larger than L2): modulated LayerNorm + static quantization
