@@ -476,6 +476,36 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     out["lib_matmul_bf16_qkv"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
                                   "note": "torch.matmul (cuBLAS) x3 on pre-dequantized bf16 weights; reference point"}
     del qx, wd
+    # The block step composed as the pages run it, for context: the same
+    # static quantizations, every projection through cuBLASLt FP8
+    # (torch._scaled_mm, bf16 out), the SwiGLU as its own op on the bf16
+    # gate/up outputs, the down projection on its E4M3 output.
+    try:
+        f8 = torch.float8_e4m3fn
+        wts = {k: [w.view(f8).t() for w, _ in ws] for k, ws in
+               (("qkv", blk.w_qkv), ("out", [blk.w_out]), ("gu", blk.w_gu), ("down", [blk.w_down]))}
+        sws = {k: [sc for _, sc in ws] for k, ws in
+               (("qkv", blk.w_qkv), ("out", [blk.w_out]), ("gu", blk.w_gu), ("down", [blk.w_down]))}
+
+        def lib_block():
+            qa = W.fp8_quant_static(blk.x_qkv, blk.s_qkv, out=blk.ws).view(f8)
+            for w_t, sw, y in zip(wts["qkv"], sws["qkv"], blk.y_qkv):
+                torch._scaled_mm(qa, w_t, scale_a=blk.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+            qa = W.fp8_quant_static(blk.x_out, blk.s_out, out=blk.ws).view(f8)
+            torch._scaled_mm(qa, wts["out"][0], scale_a=blk.s_out, scale_b=sws["out"][0],
+                             out_dtype=torch.bfloat16, out=blk.y_out)
+            qa = W.fp8_quant_static(blk.x_mlp, blk.s_mlp, out=blk.ws).view(f8)
+            for w_t, sw, y in zip(wts["gu"], sws["gu"], blk.y_gu):
+                torch._scaled_mm(qa, w_t, scale_a=blk.s_mlp, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+            W.swiglu_2in_fp8(blk.y_gu[0], blk.y_gu[1], blk.s_h, out=blk.h8)
+            torch._scaled_mm(blk.h8.view(f8), wts["down"][0], scale_a=blk.s_h, scale_b=sws["down"][0],
+                             out_dtype=torch.bfloat16, out=blk.y_down)
+        ms = _time(lib_block, flush, stream, n)
+        out["lib_block_a8_step"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
+                                    "note": "the A8 block step with every GEMM through torch._scaled_mm "
+                                            "(cuBLASLt FP8) and the SwiGLU unfused; reference point"}
+    except Exception as e:  # noqa: BLE001
+        out["lib_block_a8_step"] = {"error": str(e).splitlines()[0][:160]}
     q = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
     ms = _time(lambda: W.gate_up_swiglu_fp8(q, blk.s_mlp, blk.w_gu[0][0], blk.w_gu[1][0], blk.w_gu[0][1],
                                             blk.w_gu[1][1], blk.s_h, out=blk.h8), flush, stream, n)
