@@ -694,10 +694,11 @@ def run_case(args):
         fn = lambda: W.gate_up_swiglu_fp8(x, s_x, wg, wu, sg, su, s_h, out=h8, ws=qx)  # noqa: E731
     elif args.case == "qkv_sustained":
         # Sustained comparison under the power cap: the Q/K/V group launch
-        # (20670 x 4096 -> 3 x 4096, E4M3 input) and cuBLASLt FP8 on the same
-        # operands, each looped for about 3 s, alternating, three rounds, with
-        # the SM clock and board power sampled every 100 ms.  Prints one JSON
-        # line per phase.
+        # (20670 x 4096 -> 3 x 4096, E4M3 input) against cuBLASLt FP8 on the
+        # same operands, and the W8A16 bf16 group GEMM on the dequantized
+        # weights against cuBLAS bf16 (torch.matmul), each looped for about
+        # 3 s, alternating, three rounds, with the SM clock and board power
+        # sampled every 100 ms.  Prints one JSON line per phase.
         blk = Block(dev)
         qq = W.fp8_quant_static(blk.x_qkv, blk.s_qkv)
         wq, sq = [w for w, _ in blk.w_qkv], [sc for _, sc in blk.w_qkv]
@@ -710,6 +711,16 @@ def run_case(args):
         def lib():
             for w_t, sw, y in zip(wt, sq, blk.y_qkv):
                 torch._scaled_mm(qf, w_t, scale_a=blk.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+        for (qw, sc), o in zip(blk.w_qkv, blk.wd_qkv):
+            W.fp8_dequant_weight(qw, sc, out=o)
+        wdt = [o.t() for o in blk.wd_qkv]
+
+        def ours16():
+            W.bf16_linear_group(blk.x_qkv, blk.wd_qkv, outs=blk.y_qkv)
+
+        def lib16():
+            for w_t, y in zip(wdt, blk.y_qkv):
+                torch.matmul(blk.x_qkv, w_t, out=y)
         samples = []
         smi = None
         try:
@@ -728,7 +739,8 @@ def run_case(args):
             threading.Thread(target=reader, daemon=True).start()
         time.sleep(1.0)
         for rnd in range(3):
-            for name, f in (("ours", ours), ("cublaslt_fp8", lib)):
+            for name, f in (("ours_w8a8", ours), ("cublaslt_fp8", lib), ("ours_bf16", ours16),
+                            ("cublas_bf16", lib16)):
                 for _ in range(5):
                     f()
                 torch.cuda.synchronize()
