@@ -191,6 +191,29 @@ class Block:
                              self.w_gu[1][1], self.s_h, out=self.h8)
         W.fp8_linear_w8a8_group(self.h8, self.s_h, [self.w_down[0]], [self.w_down[1]], outs=[self.y_down])
 
+    def lib_step(self, W):
+        """The A8 block step composed as the pages run it, for context: the
+        same static quantizations, every projection through cuBLASLt FP8
+        (torch._scaled_mm, bf16 out), the SwiGLU as its own op on the bf16
+        gate/up outputs, the down projection on its E4M3 output."""
+        f8 = torch.float8_e4m3fn
+        if not hasattr(self, "_lib_w"):
+            self._lib_w = {k: [(w.view(f8).t(), sc) for w, sc in ws] for k, ws in
+                           (("qkv", self.w_qkv), ("out", [self.w_out]), ("gu", self.w_gu), ("down", [self.w_down]))}
+        lw = self._lib_w
+        qa = W.fp8_quant_static(self.x_qkv, self.s_qkv, out=self.ws).view(f8)
+        for (w_t, sw), y in zip(lw["qkv"], self.y_qkv):
+            torch._scaled_mm(qa, w_t, scale_a=self.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+        qa = W.fp8_quant_static(self.x_out, self.s_out, out=self.ws).view(f8)
+        torch._scaled_mm(qa, lw["out"][0][0], scale_a=self.s_out, scale_b=lw["out"][0][1],
+                         out_dtype=torch.bfloat16, out=self.y_out)
+        qa = W.fp8_quant_static(self.x_mlp, self.s_mlp, out=self.ws).view(f8)
+        for (w_t, sw), y in zip(lw["gu"], self.y_gu):
+            torch._scaled_mm(qa, w_t, scale_a=self.s_mlp, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+        W.swiglu_2in_fp8(self.y_gu[0], self.y_gu[1], self.s_h, out=self.h8)
+        torch._scaled_mm(self.h8.view(f8), lw["down"][0][0], scale_a=self.s_h, scale_b=lw["down"][0][1],
+                         out_dtype=torch.bfloat16, out=self.y_down)
+
     def step(self, W, policy, step_index, num_steps, x_qkv=None, x_out=None, x_mlp=None, fused=True):
         """One block pass in the precision the policy selects for this step;
         returns the number of kernel launches.  `fused` selects the fused
@@ -476,30 +499,10 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     out["lib_matmul_bf16_qkv"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
                                   "note": "torch.matmul (cuBLAS) x3 on pre-dequantized bf16 weights; reference point"}
     del qx, wd
-    # The block step composed as the pages run it, for context: the same
-    # static quantizations, every projection through cuBLASLt FP8
-    # (torch._scaled_mm, bf16 out), the SwiGLU as its own op on the bf16
-    # gate/up outputs, the down projection on its E4M3 output.
+    # The block step composed as the pages run it (cuBLASLt FP8 GEMMs, the
+    # SwiGLU as its own op), for context.
     try:
-        f8 = torch.float8_e4m3fn
-        wts = {k: [w.view(f8).t() for w, _ in ws] for k, ws in
-               (("qkv", blk.w_qkv), ("out", [blk.w_out]), ("gu", blk.w_gu), ("down", [blk.w_down]))}
-        sws = {k: [sc for _, sc in ws] for k, ws in
-               (("qkv", blk.w_qkv), ("out", [blk.w_out]), ("gu", blk.w_gu), ("down", [blk.w_down]))}
-
-        def lib_block():
-            qa = W.fp8_quant_static(blk.x_qkv, blk.s_qkv, out=blk.ws).view(f8)
-            for w_t, sw, y in zip(wts["qkv"], sws["qkv"], blk.y_qkv):
-                torch._scaled_mm(qa, w_t, scale_a=blk.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
-            qa = W.fp8_quant_static(blk.x_out, blk.s_out, out=blk.ws).view(f8)
-            torch._scaled_mm(qa, wts["out"][0], scale_a=blk.s_out, scale_b=sws["out"][0],
-                             out_dtype=torch.bfloat16, out=blk.y_out)
-            qa = W.fp8_quant_static(blk.x_mlp, blk.s_mlp, out=blk.ws).view(f8)
-            for w_t, sw, y in zip(wts["gu"], sws["gu"], blk.y_gu):
-                torch._scaled_mm(qa, w_t, scale_a=blk.s_mlp, scale_b=sw, out_dtype=torch.bfloat16, out=y)
-            W.swiglu_2in_fp8(blk.y_gu[0], blk.y_gu[1], blk.s_h, out=blk.h8)
-            torch._scaled_mm(blk.h8.view(f8), wts["down"][0], scale_a=blk.s_h, scale_b=sws["down"][0],
-                             out_dtype=torch.bfloat16, out=blk.y_down)
+        lib_block = lambda: blk.lib_step(W)  # noqa: E731
         ms = _time(lib_block, flush, stream, n)
         out["lib_block_a8_step"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
                                     "note": "the A8 block step with every GEMM through torch._scaled_mm "
@@ -695,10 +698,12 @@ def run_case(args):
     elif args.case == "qkv_sustained":
         # Sustained comparison under the power cap: the Q/K/V group launch
         # (20670 x 4096 -> 3 x 4096, E4M3 input) against cuBLASLt FP8 on the
-        # same operands, and the W8A16 bf16 group GEMM on the dequantized
-        # weights against cuBLAS bf16 (torch.matmul), each looped for about
-        # 3 s, alternating, three rounds, with the SM clock and board power
-        # sampled every 100 ms.  Prints one JSON line per phase.
+        # same operands, the W8A16 bf16 group GEMM on the dequantized weights
+        # against cuBLAS bf16 (torch.matmul), and the whole A8 block step
+        # against the same step composed from cuBLASLt GEMMs (Block.lib_step),
+        # each looped for about 3 s, alternating, three rounds, with the SM
+        # clock and board power sampled every 100 ms.  Prints one JSON line
+        # per phase.
         blk = Block(dev)
         qq = W.fp8_quant_static(blk.x_qkv, blk.s_qkv)
         wq, sq = [w for w, _ in blk.w_qkv], [sc for _, sc in blk.w_qkv]
@@ -738,9 +743,17 @@ def run_case(args):
         if smi is not None:
             threading.Thread(target=reader, daemon=True).start()
         time.sleep(1.0)
+        policy = W.StepPolicy(1, 1, 3, 3)
+
+        def ours_block():
+            blk.step(W, policy, POLICY_STEP, POLICY_STEPS)
+
+        def lib_block():
+            blk.lib_step(W)
         for rnd in range(3):
             for name, f in (("ours_w8a8", ours), ("cublaslt_fp8", lib), ("ours_bf16", ours16),
-                            ("cublas_bf16", lib16)):
+                            ("cublas_bf16", lib16), ("ours_block_a8", ours_block),
+                            ("cublaslt_block_a8", lib_block)):
                 for _ in range(5):
                     f()
                 torch.cuda.synchronize()
@@ -757,8 +770,9 @@ def run_case(args):
                 t1 = time.time()
                 sel = [(c, pw) for ts, c, pw in samples if t0 + 0.3 <= ts <= t1]
                 us = e0.elapsed_time(e1) * 1e3 / n
+                flops = BLOCK_FLOPS if name.endswith("block_a8") else QKV_FLOPS
                 print(json.dumps({"case": "qkv_sustained", "impl": name, "round": rnd, "us_per_launch": us,
-                                  "TFLOPS": QKV_FLOPS / us / 1e6, "launches": n,
+                                  "TFLOPS": flops / us / 1e6, "launches": n,
                                   "sm_mhz_median": statistics.median(c for c, _ in sel) if sel else None,
                                   "power_w_median": statistics.median(pw for _, pw in sel) if sel else None}))
                 time.sleep(1.0)
