@@ -17,9 +17,14 @@ One step runs every row of the path through the public C ABI:
 Metric: W8A8 FP8 linear TFLOPS = the block's linear FLOPs (32 * M * 4096^2)
 per step / step time (quantization and SwiGLU kernels included in the time).
 The W8A16 rows (16-bit steps), the 8-step schedule, the split-QKV group
-alone and each kernel are timed after the headline under "breakdown".
+alone, each kernel (including the fused LayerNorm + quantization producer)
+and library reference points (cuBLASLt / cuBLAS GEMMs, the block step
+composed from cuBLASLt GEMMs) are timed after the headline under
+"breakdown".  `--case NAME` runs one fixed workload for profiling instead
+(see run_case), e.g. `--case qkv_sustained` for the seconds-long comparison
+with the libraries under the power cap.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--case NAME]
 For N > 1 run under torchrun; every rank runs an independent replica (the
 path has no cross-GPU step) and rank 0 prints the aggregate.
 """
