@@ -36,11 +36,10 @@ import torch
 import oracle as O
 from oracle import norm as N
 from gpu_util import W, dev_bf16, dev_f32, host_bits, host_u8  # noqa: F401
+from norm_bound import window as _window
 from w8a16_linear_gb300 import synth
 
 pytestmark = pytest.mark.gpu
-
-U = 2.0 ** -24
 
 
 def _problem(M, K, S, seed=0, x_std=1.0, x_mean=0.0, mod_std=0.5, outliers=0.001):
@@ -48,22 +47,6 @@ def _problem(M, K, S, seed=0, x_std=1.0, x_mean=0.0, mod_std=0.5, outliers=0.001
     shift = synth.activations_bf16(seed + 100, (S, K), mod_std)
     scale = synth.activations_bf16(seed + 200, (S, K), mod_std)
     return x, shift, scale
-
-
-def _window(x, shift, scale, eps, T):
-    """Exact h and the kernel's error bound for each element."""
-    h64, mu, var = N.ln_modulate(x, shift, scale, eps, T)
-    xf = O.bf16_decode(x).astype(np.float64)
-    r = 1.0 / np.sqrt(var + float(np.float32(eps)))
-    n = (xf - mu[:, None]) * r[:, None]
-    smp = np.arange(x.shape[0]) // T
-    sc = N.bf16_value(scale)[smp]
-    xp = np.abs(xf - xf[:, :1])                  # |x_k - p|, p = the row's first element
-    rho = np.sqrt((xp * xp).mean(axis=1)) * r
-    m_abs = np.abs(mu - xf[:, 0])                # |m| = |mean - p|
-    lead = r[:, None] * (xp + (16 * xp.mean(axis=1) + m_abs)[:, None])
-    tol = 2 * U * ((lead + np.abs(n) * (15.5 + rho)[:, None]) * (1 + np.abs(sc)) + np.abs(h64))
-    return h64, tol
 
 
 def _check(x, shift, scale, eps, T, s_in, q_gpu, h_gpu, max_ambiguous=0.03):
