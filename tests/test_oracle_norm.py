@@ -99,3 +99,29 @@ def test_neighbours_bracket_the_rounding():
     lo, hi = N.bf16_neighbours(np.array([1.0 + 2.0 ** -10, one_plus_half_ulp]), 2.0 ** -12)
     assert lo[0] == hi[0] == _bits(1.0)
     assert lo[1] == _bits(1.0) and hi[1] == _bits(1.0 + 2.0 ** -7)
+
+
+def test_brute_force_decimal():
+    """Tiny rows in 50-digit decimal arithmetic (exact mean and variance of
+    the decoded bf16 values, a 50-digit square root), against the float64
+    oracle."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    M, K, S = 4, 8, 2
+    x = synth.activations_bf16(50, (M, K), 1.3, mean=0.7)
+    shift = synth.activations_bf16(51, (S, K), 0.5)
+    scale = synth.activations_bf16(52, (S, K), 0.5)
+    eps = 1e-3
+    h64, _, _ = N.ln_modulate(x, shift, scale, eps, M // S)
+    e = Decimal(float(np.float32(eps)))
+    for m in range(M):
+        xs = [Decimal(float(v)) for v in O.bf16_decode(x[m])]
+        mu = sum(xs) / K
+        var = sum((v - mu) ** 2 for v in xs) / K
+        root = (var + e).sqrt()
+        s = m // (M // S)
+        for k in range(K):
+            sc = Decimal(float(O.bf16_decode(scale[s, k])))
+            sh = Decimal(float(O.bf16_decode(shift[s, k])))
+            want = (xs[k] - mu) / root * (1 + sc) + sh
+            assert abs(Decimal(float(h64[m, k])) - want) <= Decimal("1e-14") * (abs(want) + 1)
