@@ -785,6 +785,40 @@ def run_case(args):
             smi.terminate()
         W.poll_device_error()
         return 0
+    elif args.case == "host_link":
+        # The host link the end-to-end loop is bound by: pinned host buffers
+        # of the e2e step's sizes (inputs 508 MB in, outputs 847 MB out),
+        # host -> device alone, device -> host alone, and both at once on two
+        # streams; best of five, CUDA events.  Prints one JSON line.
+        nin, nout = 3 * M_TOK * HID * 2, 5 * M_TOK * HID * 2
+        hin = torch.empty(nin, dtype=torch.uint8, pin_memory=True)
+        hout = torch.empty(nout, dtype=torch.uint8, pin_memory=True)
+        din = torch.empty(nin, dtype=torch.uint8, device=dev)
+        dout = torch.empty(nout, dtype=torch.uint8, device=dev)
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def timed(fn):
+            best = float("inf")
+            for _ in range(5):
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                fn()
+                torch.cuda.synchronize()
+                best = min(best, time.perf_counter() - t0)
+            return best
+        t_h2d = timed(lambda: din.copy_(hin, non_blocking=True))
+        t_d2h = timed(lambda: hout.copy_(dout, non_blocking=True))
+
+        def both():
+            with torch.cuda.stream(s1):
+                din.copy_(hin, non_blocking=True)
+            with torch.cuda.stream(s2):
+                hout.copy_(dout, non_blocking=True)
+        t_both = timed(both)
+        print(json.dumps({"case": "host_link", "h2d_GB_s": nin / t_h2d / 1e9, "d2h_GB_s": nout / t_d2h / 1e9,
+                          "both_GB_s": (nin + nout) / t_both / 1e9, "bytes_per_e2e_step": nin + nout,
+                          "link_bound_ms_per_step": t_both * 1e3}))
+        return 0
     elif args.case == "ln20k":
         # the producer of the Q/K/V input at the bench's size (x alone is
         # larger than L2): modulated LayerNorm + static quantization
