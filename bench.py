@@ -1,28 +1,33 @@
 """Benchmark of the static per-tensor FP8 linear path on GB300.
 
-Workload: one denoising-block pass of a 4096-wide diffusion transformer at
-20670 tokens (a 13x30x53 latent grid) on a W8A8 step of the 8-step policy.
-One step runs every row of the path through the public C ABI:
+Headline workload: the W8A8 FP8 linear at K = N = 4096 over M = 20670 tokens
+(a 13x30x53 latent grid) in the form a diffusion transformer block runs it,
+the split Q/K/V projections sharing one activation quantization:
 
-  step_policy_dispatch(step 3 of 8)                       -> W8A8
-  qkv_shared_quant_gemm  Q/K/V, one shared quantization, 3 x 4096x4096
-  fp8_linear_w8a8        out-projection 4096x4096
-  (the out-projection's and the MLP's fp8_quant_static run on a second
-  stream, overlapped with the Q/K/V GEMM)
-  gate_up_swiglu_fp8     gate/up (one shared quantization, 2 x 4096->16384) with
-                         SiLU(gate)*up written straight to E4M3 in the GEMM
-                         epilogue (same codes as the group GEMM + swiglu_2in_fp8)
-  fp8_linear_w8a8        down projection 16384->4096 on the E4M3 codes
+  qkv_shared_quant_gemm(W8A8)  one fp8_quant_static of the bf16 block input
+                               (static s_in), then one persistent W8A8 launch
+                               over the tiles of the three 4096x4096
+                               projections, each with its own weight scale
+                               and its own bf16 output
 
-Metric: W8A8 FP8 linear TFLOPS = the block's linear FLOPs (32 * M * 4096^2)
-per step / step time (quantization and SwiGLU kernels included in the time).
-The W8A16 rows (16-bit steps), the 8-step schedule, the split-QKV group
-alone, each kernel (including the fused LayerNorm + quantization producer)
-and library reference points (cuBLASLt / cuBLAS GEMMs, the block step
-composed from cuBLASLt GEMMs) are timed after the headline under
-"breakdown".  `--case NAME` runs one fixed workload for profiling instead
-(see run_case), e.g. `--case qkv_sustained` for the seconds-long comparison
-with the libraries under the power cap.
+Metric: W8A8 FP8 linear TFLOPS = 3 * 2 * M * 4096^2 FLOP per step / step
+time, the quantization included in the time.  A step is one such call on
+inputs resident in HBM; L2 is flushed between steps (512 MiB write outside
+the events).  `roofline` is the dominant kernel, the grouped GEMM launch,
+timed alone on the same shapes; `e2e` is the same call through the public
+API with the activation copied in from pinned host memory and the three
+outputs copied out every step.
+
+After the headline, "breakdown" times the rest of the path and its context:
+the whole block step on a W8A8 and a W8A16 step of the 8-step policy, the
+8-step schedule of one block, the 8-step x 4-block stack at the CFG batch
+(M = 41340), every kernel on its own (quantization, SwiGLU FP8/bf16 and its
+options, weight dequantization, the fused LayerNorm + quantization
+producer, the fused gate/up + SwiGLU GEMM, the gate/up and down GEMMs, the
+exported fp8_linear_w8a16), library reference points (cuBLASLt FP8,
+cuBLAS bf16, the block step composed from cuBLASLt GEMMs), and the CPU
+oracle timed on the host cores beside the kernels it checks.
+`--case NAME` runs one fixed workload for profiling instead (see run_case).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--case NAME]
 For N > 1 run under torchrun; every rank runs an independent replica (the
@@ -45,12 +50,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 M_TOK, HID, INTER = 20670, 4096, 16384
+M_CFG = 2 * M_TOK                                 # CFG batch of the 8-step stack
 BLOCK_FLOPS = 32.0 * M_TOK * HID * HID           # QKV 6 + out 2 + gate/up 16 + down 8
 QKV_FLOPS = 6.0 * M_TOK * HID * HID
+STEP_FLOPS = QKV_FLOPS                           # the headline step: the Q/K/V W8A8 group
 METRIC = "W8A8 FP8 linear TFLOPS (M≈20k, K=N=4096) and % of GB300 dense FP8 peak"
-WORKLOAD = ("A8 denoising-block step, M=20670 tokens (13x30x53), hidden 4096: split-QKV shared "
-            "quant 3x4096x4096, out-proj 4096x4096, split gate/up shared quant 2x4096->16384 fused "
-            "with swiglu_2in FP8, down 16384->4096")
+WORKLOAD = ("W8A8 FP8 linear, M=20670 tokens (13x30x53), K=N=4096, split Q/K/V: one static "
+            "quantization of the bf16 input shared by three 4096x4096 E4M3 projections with "
+            "their own weight scales (qkv_shared_quant_gemm), bf16 outputs")
 L2_FLUSH_BYTES = 512 << 20
 POLICY_STEP, POLICY_STEPS = 3, 8
 
@@ -119,82 +126,87 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- inputs
 
+def _act(gen, dev, n_rows, n_cols):
+    """bf16 activations ~ N(0, 0.25^2) with 0.1% of elements x8."""
+    t = torch.randn((n_rows, n_cols), generator=gen, device=dev) * 0.25
+    k = int(t.numel() * 0.001)
+    idx = torch.randint(0, t.numel(), (k,), generator=gen, device=dev)
+    t.view(-1)[idx] *= 8.0
+    return t.to(torch.bfloat16)
+
+
+def _amax_scale(t):
+    return (t.float().abs().amax() / 448.0).reshape(1).contiguous()
+
+
+def _weight(gen, dev, n, k):
+    """N(0, 0.02^2) scaled by c ~ U[0.5, 1], E4M3 with an amax/448 scale."""
+    c = float(torch.rand((), generator=gen, device=dev)) * 0.5 + 0.5
+    w = torch.randn((n, k), generator=gen, device=dev) * (0.02 * c)
+    s = _amax_scale(w)
+    q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    return q, s
+
+
+def block_weights(gen, dev):
+    """One block's E4M3 weights and static scales (BlockWeights); input
+    scales from separately drawn calibration batches (amax/448), so the live
+    batch may saturate."""
+    from w8a16_linear_gb300.stack import BlockWeights
+    qkv = [_weight(gen, dev, HID, HID) for _ in range(3)]
+    out = _weight(gen, dev, HID, HID)
+    gu = [_weight(gen, dev, INTER, HID) for _ in range(2)]
+    down = _weight(gen, dev, HID, INTER)
+    s_qkv, s_out, s_mlp = (_amax_scale(_act(gen, dev, 4096, HID)) for _ in range(3))
+    return BlockWeights(qkv=qkv, out=out, gu=gu, down=down, s_qkv=s_qkv, s_out=s_out, s_mlp=s_mlp,
+                        s_h=torch.tensor([0.02], device=dev))
+
+
 class Block:
-    """Device-resident synthetic inputs and outputs of one block.
+    """Device-resident synthetic inputs of one block at M = 20670 tokens, its
+    weights, and the runner (w8a16_linear_gb300.stack.BlockStep) that owns the
+    outputs, workspaces and side streams.  Activations are drawn on the GPU
+    with a seeded torch generator."""
 
-    Activations ~ N(0, 0.25^2) with 0.1% outliers x8 (drawn on the GPU with a
-    seeded torch generator); weights N(0, 0.02^2) scaled per projection by
-    c ~ U[0.5, 1], E4M3 with amax/448 weight scales; static input scales from
-    a separately drawn calibration batch (amax/448), so the live batch may
-    saturate."""
-
-    def __init__(self, dev, seed=0):
+    def __init__(self, dev, seed=0, M=M_TOK):
+        from w8a16_linear_gb300.stack import BlockStep
         g = torch.Generator(device=dev).manual_seed(seed)
-        self.dev = dev
-
-        def act(n_rows, n_cols):
-            t = torch.randn((n_rows, n_cols), generator=g, device=dev) * 0.25
-            k = int(t.numel() * 0.001)
-            idx = torch.randint(0, t.numel(), (k,), generator=g, device=dev)
-            t.view(-1)[idx] *= 8.0
-            return t.to(torch.bfloat16)
-
-        def scale(t):
-            return (t.float().abs().amax() / 448.0).reshape(1).contiguous()
-
-        def weight(n, k):
-            c = float(torch.rand((), generator=g, device=dev)) * 0.5 + 0.5
-            w = torch.randn((n, k), generator=g, device=dev) * (0.02 * c)
-            s = scale(w)
-            q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
-            return q, s
-
-        self.x_qkv, self.x_out, self.x_mlp = act(M_TOK, HID), act(M_TOK, HID), act(M_TOK, HID)
-        self.s_qkv = scale(act(4096, HID))
-        self.s_out = scale(act(4096, HID))
-        self.s_mlp = scale(act(4096, HID))
-        self.w_qkv = [weight(HID, HID) for _ in range(3)]
-        self.w_out = weight(HID, HID)
-        self.w_gu = [weight(INTER, HID) for _ in range(2)]
-        self.w_down = weight(HID, INTER)
-        self.s_h = torch.tensor([0.02], device=dev)        # down projection's input scale
-        bf = dict(dtype=torch.bfloat16, device=dev)
-        self.y_qkv = [torch.empty((M_TOK, HID), **bf) for _ in range(3)]
-        self.y_out = torch.empty((M_TOK, HID), **bf)
-        self.y_gu = [torch.empty((M_TOK, INTER), **bf) for _ in range(2)]
-        self.h8 = torch.empty((M_TOK, INTER), dtype=torch.uint8, device=dev)
-        self.h16 = torch.empty((M_TOK, INTER), **bf)
-        self.y_down = torch.empty((M_TOK, HID), **bf)
-        self.ws = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
-        self.q_out = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
-        self.q_mlp = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
-        self.side = torch.cuda.Stream(device=dev)
-        # W8A16 steps: transient bf16 weights of the largest group (gate/up) for
-        # the one-call form, and of every site of the block for the scheduled
-        # form (dequantized on a side stream ahead of the GEMMs that read them)
+        self.dev, self.M = dev, M
+        self.x_qkv, self.x_out, self.x_mlp = (_act(g, dev, M, HID) for _ in range(3))
+        self.w = block_weights(g, dev)
+        self.run = BlockStep(M, HID, INTER, dev)
+        self.ws = self.run.ws
         self.wsd = torch.empty((2 * INTER * HID,), dtype=torch.bfloat16, device=dev)
-        wd_all = torch.empty((4 * HID * HID + 3 * INTER * HID,), dtype=torch.bfloat16, device=dev)
-        shapes = [(HID, HID)] * 4 + [(INTER, HID)] * 2 + [(HID, INTER)]
-        views, off = [], 0
-        for n_, k_ in shapes:
-            views.append(wd_all[off:off + n_ * k_].view(n_, k_))
-            off += n_ * k_
-        self.wd_qkv, self.wd_out, self.wd_gu, self.wd_down = views[:3], views[3], views[4:6], views[6]
-        self.dq = torch.cuda.Stream(device=dev)
-        self.dq_ev = [torch.cuda.Event() for _ in range(4)]
 
-    def outputs(self):
-        return self.y_qkv + [self.y_out, self.y_down]
+    # shorthands used by the timings below
+    @property
+    def wq(self):
+        return [q for q, _ in self.w.qkv]
+
+    @property
+    def sq(self):
+        return [s for _, s in self.w.qkv]
+
+    def qkv_step(self, W, x=None, outs=None):
+        """The headline step: the Q/K/V W8A8 group with its shared quantization."""
+        W.qkv_shared_quant_gemm(W.MODE_A8, self.x_qkv if x is None else x, self.w.s_qkv, self.wq, self.sq,
+                                outs=self.run.y_qkv if outs is None else outs, ws=self.ws)
+        return 2                                   # quantization + one grouped GEMM launch
+
+    def step(self, W, policy, step_index, num_steps, fused=True):
+        """One block pass in the precision the policy selects for this step;
+        returns the number of kernel launches."""
+        mode = W.step_policy_dispatch(policy, step_index, num_steps)
+        return self.run.run(W, mode, self.w, self.x_qkv, self.x_out, self.x_mlp, fused=fused)
 
     def gemm_launches(self, W, q_qkv, q_out, q_mlp):
         """The A8 block's four GEMM launches alone on E4M3 activations: Q/K/V
         group, out-projection, fused gate/up + SwiGLU, down projection."""
-        W.fp8_linear_w8a8_group(q_qkv, self.s_qkv, [q for q, _ in self.w_qkv], [s for _, s in self.w_qkv],
-                                outs=self.y_qkv)
-        W.fp8_linear_w8a8_group(q_out, self.s_out, [self.w_out[0]], [self.w_out[1]], outs=[self.y_out])
-        W.gate_up_swiglu_fp8(q_mlp, self.s_mlp, self.w_gu[0][0], self.w_gu[1][0], self.w_gu[0][1],
-                             self.w_gu[1][1], self.s_h, out=self.h8)
-        W.fp8_linear_w8a8_group(self.h8, self.s_h, [self.w_down[0]], [self.w_down[1]], outs=[self.y_down])
+        w, r = self.w, self.run
+        W.fp8_linear_w8a8_group(q_qkv, w.s_qkv, self.wq, self.sq, outs=r.y_qkv)
+        W.fp8_linear_w8a8_group(q_out, w.s_out, [w.out[0]], [w.out[1]], outs=[r.y_out])
+        W.gate_up_swiglu_fp8(q_mlp, w.s_mlp, w.gu[0][0], w.gu[1][0], w.gu[0][1], w.gu[1][1], w.s_h, out=r.h8)
+        W.fp8_linear_w8a8_group(r.h8, w.s_h, [w.down[0]], [w.down[1]], outs=[r.y_down])
 
     def lib_step(self, W):
         """The A8 block step composed as the pages run it, for context: the
@@ -202,95 +214,32 @@ class Block:
         (torch._scaled_mm, bf16 out), the SwiGLU as its own op on the bf16
         gate/up outputs, the down projection on its E4M3 output."""
         f8 = torch.float8_e4m3fn
+        w, r = self.w, self.run
         if not hasattr(self, "_lib_w"):
-            self._lib_w = {k: [(w.view(f8).t(), sc) for w, sc in ws] for k, ws in
-                           (("qkv", self.w_qkv), ("out", [self.w_out]), ("gu", self.w_gu), ("down", [self.w_down]))}
+            self._lib_w = {k: [(q.view(f8).t(), sc) for q, sc in ws] for k, ws in
+                           (("qkv", w.qkv), ("out", [w.out]), ("gu", w.gu), ("down", [w.down]))}
         lw = self._lib_w
-        qa = W.fp8_quant_static(self.x_qkv, self.s_qkv, out=self.ws).view(f8)
-        for (w_t, sw), y in zip(lw["qkv"], self.y_qkv):
-            torch._scaled_mm(qa, w_t, scale_a=self.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
-        qa = W.fp8_quant_static(self.x_out, self.s_out, out=self.ws).view(f8)
-        torch._scaled_mm(qa, lw["out"][0][0], scale_a=self.s_out, scale_b=lw["out"][0][1],
-                         out_dtype=torch.bfloat16, out=self.y_out)
-        qa = W.fp8_quant_static(self.x_mlp, self.s_mlp, out=self.ws).view(f8)
-        for (w_t, sw), y in zip(lw["gu"], self.y_gu):
-            torch._scaled_mm(qa, w_t, scale_a=self.s_mlp, scale_b=sw, out_dtype=torch.bfloat16, out=y)
-        W.swiglu_2in_fp8(self.y_gu[0], self.y_gu[1], self.s_h, out=self.h8)
-        torch._scaled_mm(self.h8.view(f8), lw["down"][0][0], scale_a=self.s_h, scale_b=lw["down"][0][1],
-                         out_dtype=torch.bfloat16, out=self.y_down)
-
-    def step(self, W, policy, step_index, num_steps, x_qkv=None, x_out=None, x_mlp=None, fused=True):
-        """One block pass in the precision the policy selects for this step;
-        returns the number of kernel launches.  `fused` selects the fused
-        gate/up + SwiGLU kernel (E4M3 out on W8A8 steps, bf16 out on W8A16
-        steps); else the group GEMM followed by the SwiGLU kernel."""
-        x_qkv = self.x_qkv if x_qkv is None else x_qkv
-        x_out = self.x_out if x_out is None else x_out
-        x_mlp = self.x_mlp if x_mlp is None else x_mlp
-        mode = W.step_policy_dispatch(policy, step_index, num_steps)
-        wq = [q for q, _ in self.w_qkv]
-        sq = [s for _, s in self.w_qkv]
-        wgu = [q for q, _ in self.w_gu]
-        sgu = [s for _, s in self.w_gu]
-        if mode == W.MODE_A8 and fused:
-            # The out-projection's and the MLP's activation quantizations do
-            # not depend on the Q/K/V GEMM: run them on a second stream while
-            # it occupies the tensor cores, then feed the E4M3 codes in.
-            main = torch.cuda.current_stream()
-            self.side.wait_stream(main)
-            with torch.cuda.stream(self.side):
-                W.fp8_quant_static(x_out, self.s_out, out=self.q_out)
-                W.fp8_quant_static(x_mlp, self.s_mlp, out=self.q_mlp)
-            W.qkv_shared_quant_gemm(W.MODE_A8, x_qkv, self.s_qkv, wq, sq, outs=self.y_qkv, ws=self.ws)
-            main.wait_stream(self.side)
-            W.fp8_linear_w8a8(self.q_out, self.w_out[0], self.s_out, self.w_out[1], out=self.y_out)
-            W.gate_up_swiglu_fp8(self.q_mlp, self.s_mlp, wgu[0], wgu[1], sgu[0], sgu[1], self.s_h,
-                                 out=self.h8)
-            W.fp8_linear_w8a8(self.h8, self.w_down[0], self.s_h, self.w_down[1], out=self.y_down)
-            return 7
-        if mode == W.MODE_A8:
-            W.qkv_shared_quant_gemm(W.MODE_A8, x_qkv, self.s_qkv, wq, sq, outs=self.y_qkv, ws=self.ws)
-            W.fp8_linear_w8a8(x_out, self.w_out[0], self.s_out, self.w_out[1], out=self.y_out, ws=self.ws)
-            if fused:
-                W.gate_up_swiglu_fp8(x_mlp, self.s_mlp, wgu[0], wgu[1], sgu[0], sgu[1], self.s_h,
-                                     out=self.h8, ws=self.ws)
-            else:
-                W.qkv_shared_quant_gemm(W.MODE_A8, x_mlp, self.s_mlp, wgu, sgu, outs=self.y_gu, ws=self.ws)
-                W.swiglu_2in_fp8(self.y_gu[0], self.y_gu[1], self.s_h, out=self.h8)
-            W.fp8_linear_w8a8(self.h8, self.w_down[0], self.s_h, self.w_down[1], out=self.y_down)
-            return 7 if fused else 8
-        # dequant + F.linear, scheduled: the weights do not depend on the
-        # activations, so all seven dequantizations run on a side stream in
-        # the order the GEMMs need them, overlapping the earlier GEMMs
-        main = torch.cuda.current_stream()
-        self.dq.wait_stream(main)          # the previous step's GEMMs are done with the buffers
-        sites = [(list(zip(wq, sq)), self.wd_qkv), ([self.w_out], [self.wd_out]),
-                 (list(zip(wgu, sgu)), self.wd_gu), ([self.w_down], [self.wd_down])]
-        with torch.cuda.stream(self.dq):
-            for (ws_, outs_), ev in zip(sites, self.dq_ev):
-                for (q, sc), o in zip(ws_, outs_):
-                    W.fp8_dequant_weight(q, sc, out=o)
-                ev.record(self.dq)
-        main.wait_event(self.dq_ev[0])
-        W.bf16_linear_group(x_qkv, self.wd_qkv, outs=self.y_qkv)
-        main.wait_event(self.dq_ev[1])
-        W.bf16_linear_group(x_out, [self.wd_out], outs=[self.y_out])
-        main.wait_event(self.dq_ev[2])
-        if fused:       # gate/up GEMMs with the bf16 SwiGLU in their epilogue
-            W.bf16_gate_up_swiglu(x_mlp, self.wd_gu[0], self.wd_gu[1], out=self.h16)
-        else:
-            W.bf16_linear_group(x_mlp, self.wd_gu, outs=self.y_gu)
-            W.swiglu_2in_bf16(self.y_gu[0], self.y_gu[1], out=self.h16)
-        main.wait_event(self.dq_ev[3])
-        W.bf16_linear_group(self.h16, [self.wd_down], outs=[self.y_down])
-        return 11 if fused else 12
+        qa = W.fp8_quant_static(self.x_qkv, w.s_qkv, out=self.ws).view(f8)
+        for (w_t, sw), y in zip(lw["qkv"], r.y_qkv):
+            torch._scaled_mm(qa, w_t, scale_a=w.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+        qa = W.fp8_quant_static(self.x_out, w.s_out, out=self.ws).view(f8)
+        torch._scaled_mm(qa, lw["out"][0][0], scale_a=w.s_out, scale_b=lw["out"][0][1],
+                         out_dtype=torch.bfloat16, out=r.y_out)
+        qa = W.fp8_quant_static(self.x_mlp, w.s_mlp, out=self.ws).view(f8)
+        for (w_t, sw), y in zip(lw["gu"], r.y_gu):
+            torch._scaled_mm(qa, w_t, scale_a=w.s_mlp, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+        W.swiglu_2in_fp8(r.y_gu[0], r.y_gu[1], w.s_h, out=r.h8)
+        torch._scaled_mm(r.h8.view(f8), lw["down"][0][0], scale_a=w.s_h, scale_b=lw["down"][0][1],
+                         out_dtype=torch.bfloat16, out=r.y_down)
 
 
-# DRAM bytes (read + write) of the A8 block step's four GEMM launches at
-# M=20670 from one ncu capture of the current gemm_kernel build (2972.3 MB read
-# + 1110.0 MB written; algorithmic 861 + 1185 MB).  Re-capture, or set to None,
-# whenever gemm_kernel changes.
-GEMM_TRAFFIC_BYTES = 4082.2e6
+# DRAM bytes (read + write) of one grouped Q/K/V W8A8 GEMM launch at
+# M=20670, K=N=4096 x3, from one ncu capture of the current gemm_kernel build
+# (profiles/gemm_w8a8_qkv_20670x4096x4096.md: 372.1 MB read + 487.7 MB
+# written; algorithmic 84.7 + 50.3 MB read, 508.0 MB written).  Re-capture,
+# or set to None, whenever gemm_kernel changes.
+QKV_GEMM_TRAFFIC_BYTES = 859.8e6
+QKV_GEMM_ALGO_BYTES = M_TOK * HID + 3 * HID * HID + 3 * 2 * M_TOK * HID
 
 
 def flush_l2(buf):
@@ -321,15 +270,14 @@ def run_ours(args, rank, world, dev):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     blk = Block(dev)
-    policy = W.StepPolicy(1, 1, 3, 3)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     for _ in range(args.warmup):
-        blk.step(W, policy, POLICY_STEP, POLICY_STEPS)
+        blk.qkv_step(W)
     torch.cuda.synchronize()
     W.poll_device_error()
 
-    # ---- timed region: K block steps, L2 flushed between steps (outside the events)
+    # ---- timed region: K headline steps, L2 flushed between steps (outside the events)
     ev = _events(args.steps)
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     if world > 1:
@@ -340,7 +288,7 @@ def run_ours(args, rank, world, dev):
     for i in range(args.steps):
         flush_l2(flush)
         ev[i][0].record(stream)
-        launches += blk.step(W, policy, POLICY_STEP, POLICY_STEPS)
+        launches += blk.qkv_step(W)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -349,44 +297,38 @@ def run_ours(args, rank, world, dev):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     W.poll_device_error()
 
-    # ---- dominant kernel: the block's four W8A8 GEMM launches alone, same
-    # shapes, on pre-quantized activations, same stream
-    q_qkv = W.fp8_quant_static(blk.x_qkv, blk.s_qkv)
-    q_out = W.fp8_quant_static(blk.x_out, blk.s_out)
-    q_mlp = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
-
-    gemm_ms = _time(lambda: blk.gemm_launches(W, q_qkv, q_out, q_mlp), flush, stream, args.steps)
-    del q_qkv, q_out, q_mlp
+    # ---- dominant kernel: the grouped Q/K/V GEMM launch alone on the
+    # quantized activation, same shapes, same stream
+    q_qkv = W.fp8_quant_static(blk.x_qkv, blk.w.s_qkv)
+    gemm_ms = _time(lambda: W.fp8_linear_w8a8_group(q_qkv, blk.w.s_qkv, blk.wq, blk.sq, outs=blk.run.y_qkv),
+                    flush, stream, args.steps)
+    del q_qkv
 
     # ---- end to end through the public API with host buffers
     e2e_steps = max(3, min(args.steps, 10))
-    e2e_pipeline(W, blk, policy, stream, 2)                 # warm-up of the copy path
-    e2e_ms, h2d, d2h = e2e_pipeline(W, blk, policy, stream, e2e_steps)
+    e2e_pipeline(W, blk, stream, 2)                 # warm-up of the copy path
+    e2e_ms, h2d, d2h = e2e_pipeline(W, blk, stream, e2e_steps)
 
-    breakdown = breakdown_ours(W, blk, policy, flush, stream, args)
+    breakdown = breakdown_ours(W, blk, flush, stream, args)
     W.poll_device_error()
     return {"total_ms": sum(step_ms), "step_ms": step_ms, "gemm_ms": gemm_ms, "e2e_ms": e2e_ms,
             "h2d": h2d, "d2h": d2h, "clocks": clk, "launches": launches, "breakdown": breakdown}
 
 
-def e2e_pipeline(W, blk, policy, stream, n):
-    """n block steps end to end through the public API with pinned host
-    buffers, pipelined as a serving loop would: step i's inputs are copied in
-    (host -> device, one copy stream) while step i-1 computes, and step i's
-    outputs are copied out (device -> host, another copy stream) while step
-    i+1 computes; two device buffer sets alternate.  Every step moves its
-    full inputs in and its full outputs out.  Returns (ms per step over the
-    whole pipeline, H2D bytes per step, D2H bytes per step)."""
+def e2e_pipeline(W, blk, stream, n):
+    """n headline steps end to end through the public API with pinned host
+    buffers, pipelined as a serving loop would: step i's activation is copied
+    in (host -> device) while step i-1 computes, and step i's three outputs
+    are copied out (device -> host, two copy streams) while step i+1
+    computes; two device buffer sets alternate.  Every step moves its full
+    input in and its full outputs out.  Returns (ms per step over the whole
+    pipeline, H2D bytes per step, D2H bytes per step)."""
     dev = blk.dev
-    xs = (blk.x_qkv, blk.x_out, blk.x_mlp)
-    xh = [t.cpu().pin_memory() for t in xs]
-    outs = [blk.y_qkv + [blk.y_out, blk.y_down]]
-    outs.append([torch.empty_like(t) for t in outs[0]])
+    xh = blk.x_qkv.cpu().pin_memory()
+    outs = [blk.run.y_qkv, [torch.empty_like(t) for t in blk.run.y_qkv]]
     yh = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[0]] for _ in range(2)]
-    xd = [[torch.empty_like(t) for t in xs] for _ in range(2)]
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    # a second stream per direction, so that two copy engines move each direction
-    s_in2, s_out2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    xd = [torch.empty_like(blk.x_qkv) for _ in range(2)]
+    s_in, s_out, s_out2 = (torch.cuda.Stream(device=dev) for _ in range(3))
 
     def mk():
         return torch.cuda.Event(enable_timing=False)
@@ -400,18 +342,14 @@ def e2e_pipeline(W, blk, policy, stream, n):
         b = i % 2
         if i >= 2:
             s_in.wait_event(comp_done[i - 2])          # step i-2 no longer reads xd[b]
-        s_in2.wait_stream(s_in)
-        for j, (d, h) in enumerate(zip(xd[b], xh)):
-            with torch.cuda.stream(s_in if j % 2 == 0 else s_in2):
-                d.copy_(h, non_blocking=True)
-        s_in.wait_stream(s_in2)
+        with torch.cuda.stream(s_in):
+            xd[b].copy_(xh, non_blocking=True)
         in_done[i].record(s_in)
         stream.wait_event(in_done[i])
         if i >= 2:
             stream.wait_event(out_done[i - 2])         # outs[b] copied out before reuse
-        blk.y_qkv, (blk.y_out, blk.y_down) = outs[b][:3], outs[b][3:]
         with torch.cuda.stream(stream):
-            blk.step(W, policy, POLICY_STEP, POLICY_STEPS, *xd[b])
+            blk.qkv_step(W, x=xd[b], outs=outs[b])
         comp_done[i].record(stream)
         s_out.wait_event(comp_done[i])
         s_out2.wait_event(comp_done[i])
@@ -422,17 +360,54 @@ def e2e_pipeline(W, blk, policy, stream, n):
         out_done[i].record(s_out)
     t1.record(s_out)
     torch.cuda.synchronize()
-    blk.y_qkv, (blk.y_out, blk.y_down) = outs[0][:3], outs[0][3:]
-    h2d = sum(t.numel() * t.element_size() for t in xd[0])
+    h2d = xd[0].numel() * xd[0].element_size()
     d2h = sum(t.numel() * t.element_size() for t in outs[0])
     return t0.elapsed_time(t1) / n, h2d, d2h
 
 
-def breakdown_ours(W, blk, policy, flush, stream, args):
+def _stack_cfg5(W, dev, flush, stream):
+    """The 8-step x 4-block stack at the CFG batch (M = 41340): every block's
+    own weights, the policy's mode per step (A16 x3, A8 x2, A16 x3).  One
+    untimed pass, then one timed pass (L2 flushed before it)."""
+    g = torch.Generator(device=dev).manual_seed(77)
+    blocks = [block_weights(g, dev) for _ in range(4)]
+    from w8a16_linear_gb300.stack import BlockStep
+    runner = BlockStep(M_CFG, HID, INTER, dev)
+    xs = [_act(g, dev, M_CFG, HID) for _ in range(3)]
+    policy = W.StepPolicy(1, 1, 3, 3)
+    modes = [W.step_policy_dispatch(policy, s, POLICY_STEPS) for s in range(POLICY_STEPS)]
+
+    def stack():
+        for m in modes:
+            for w in blocks:
+                runner.run(W, m, w, *xs)
+    stack()
+    torch.cuda.synchronize()
+    ev = _events(1)
+    flush_l2(flush)
+    ev[0][0].record(stream)
+    stack()
+    ev[0][1].record(stream)
+    torch.cuda.synchronize()
+    ms = ev[0][0].elapsed_time(ev[0][1])
+    flops = POLICY_STEPS * 4 * 32.0 * M_CFG * HID * HID
+    del blocks, runner, xs
+    torch.cuda.empty_cache()
+    return {"ms": ms, "TFLOPS": flops / ms / 1e9,
+            "modes": "".join("8" if m == W.MODE_A8 else "6" for m in modes).replace("6", "A16 ").replace("8", "A8 ").strip(),
+            "note": "8 steps x 4 blocks, M=41340 (CFG batch 2 x 20670), each block its own E4M3 weights"}
+
+
+def breakdown_ours(W, blk, flush, stream, args):
     n = max(3, min(args.steps, 10))
     out = {}
-    wq = [q for q, _ in blk.w_qkv]
-    sq = [s for _, s in blk.w_qkv]
+    w, r = blk.w, blk.run
+    wq, sq = blk.wq, blk.sq
+    policy = W.StepPolicy(1, 1, 3, 3)
+    ms = _time(lambda: blk.step(W, policy, POLICY_STEP, POLICY_STEPS), flush, stream, n)
+    out["block_a8_step"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
+                            "note": "whole block on a W8A8 step: Q/K/V group (shared quant), out-proj, "
+                                    "gate/up + SwiGLU->E4M3 fused, down; 32*M*4096^2 FLOP"}
     ms = _time(lambda: blk.step(W, policy, POLICY_STEP, POLICY_STEPS, fused=False), flush, stream, n)
     out["block_a8_step_unfused_mlp"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
                                         "note": "gate/up group GEMM -> bf16 -> swiglu_2in_fp8 instead of the fused kernel"}
@@ -453,53 +428,64 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     ms = ev[0][0].elapsed_time(ev[0][1])
     out["schedule_8_steps_one_block"] = {"ms": ms, "TFLOPS": 8 * BLOCK_FLOPS / ms / 1e9,
                                          "modes": "A16 x3, A8 x2, A16 x3"}
-    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A8, blk.x_qkv, blk.s_qkv, wq, sq, outs=blk.y_qkv,
-                                               ws=blk.ws), flush, stream, n)
-    out["qkv_group_a8"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
-                           "note": "quant + one 3-projection W8A8 launch, M=20670, 3x4096x4096"}
-    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, blk.x_qkv, None, wq, sq, outs=blk.y_qkv,
+    out["stack_cfg5_8_steps_4_blocks"] = _stack_cfg5(W, blk.dev, flush, stream)
+    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, blk.x_qkv, None, wq, sq, outs=r.y_qkv,
                                                ws=blk.wsd), flush, stream, n)
     out["qkv_group_a16"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
                             "note": "3 weight dequantizations into the workspace + one bf16 GEMM launch"}
-    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, blk.x_qkv, None, wq, sq, outs=blk.y_qkv),
+    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, blk.x_qkv, None, wq, sq, outs=r.y_qkv),
                flush, stream, n)
     out["qkv_group_a16_fused"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
                                   "note": "no workspace: weights converted inside the GEMM (TMEM A operand)"}
-    ms = _time(lambda: W.fp8_quant_static(blk.x_qkv, blk.s_qkv, out=blk.ws), flush, stream, n)
+    lin_flops = 2.0 * M_TOK * HID * HID
+    ms = _time(lambda: W.fp8_linear_w8a16(blk.x_qkv, wq[0], sq[0], out=r.y_qkv[0], ws=blk.wsd), flush, stream, n)
+    out["fp8_linear_w8a16_4096x4096"] = {"us": ms * 1e3, "TFLOPS": lin_flops / ms / 1e9,
+                                         "note": "the exported W8A16 linear with its workspace: "
+                                                 "dequantization + bf16 GEMM, M=20670"}
+    ms = _time(lambda: W.fp8_linear_w8a16(blk.x_qkv, wq[0], sq[0], out=r.y_qkv[0]), flush, stream, n)
+    out["fp8_linear_w8a16_4096x4096_no_ws"] = {"us": ms * 1e3, "TFLOPS": lin_flops / ms / 1e9,
+                                               "note": "the same call without a workspace (dequantization in the GEMM)"}
+    ms = _time(lambda: W.fp8_linear_w8a8(blk.x_qkv, wq[0], w.s_qkv, sq[0], out=r.y_qkv[0], ws=blk.ws),
+               flush, stream, n)
+    out["fp8_linear_w8a8_4096x4096"] = {"us": ms * 1e3, "TFLOPS": lin_flops / ms / 1e9,
+                                        "note": "one projection: quantization + W8A8 GEMM, M=20670"}
+    ms = _time(lambda: W.fp8_quant_static(blk.x_qkv, w.s_qkv, out=blk.ws), flush, stream, n)
     out["fp8_quant_static"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6}
-    ms = _time(lambda: W.swiglu_2in_fp8(blk.y_gu[0], blk.y_gu[1], blk.s_h, out=blk.h8), flush, stream, n)
-    out["swiglu_2in_fp8"] = {"us": ms * 1e3, "GB_s": 5 * blk.h8.numel() / ms / 1e6}
-    ms = _time(lambda: W.swiglu_2in_bf16(blk.y_gu[0], blk.y_gu[1], out=blk.h16), flush, stream, n)
-    out["swiglu_2in_bf16"] = {"us": ms * 1e3, "GB_s": 6 * blk.h16.numel() / ms / 1e6}
+    gu = r.y_gu
+    W.fp8_linear_w8a8_group(W.fp8_quant_static(blk.x_mlp, w.s_mlp), w.s_mlp, [q for q, _ in w.gu],
+                            [s for _, s in w.gu], outs=gu)
+    ms = _time(lambda: W.swiglu_2in_fp8(gu[0], gu[1], w.s_h, out=r.h8), flush, stream, n)
+    out["swiglu_2in_fp8"] = {"us": ms * 1e3, "GB_s": 5 * r.h8.numel() / ms / 1e6}
+    ms = _time(lambda: W.swiglu_2in_bf16(gu[0], gu[1], out=r.h16), flush, stream, n)
+    out["swiglu_2in_bf16"] = {"us": ms * 1e3, "GB_s": 6 * r.h16.numel() / ms / 1e6}
     # the variant op with the limit / alpha / beta options on the same tensors
     opts = dict(limit=7.0, alpha=1.702, beta=1.0)
-    ms = _time(lambda: W.swiglu_2in_ex_fp8(blk.y_gu[0], blk.y_gu[1], blk.s_h, out=blk.h8, **opts),
-               flush, stream, n)
-    out["swiglu_2in_ex_fp8"] = {"us": ms * 1e3, "GB_s": 5 * blk.h8.numel() / ms / 1e6,
+    ms = _time(lambda: W.swiglu_2in_ex_fp8(gu[0], gu[1], w.s_h, out=r.h8, **opts), flush, stream, n)
+    out["swiglu_2in_ex_fp8"] = {"us": ms * 1e3, "GB_s": 5 * r.h8.numel() / ms / 1e6,
                                 "note": "limit 7, alpha 1.702, beta 1, bf16 in"}
-    ms = _time(lambda: W.swiglu_2in_ex_16(blk.y_gu[0], blk.y_gu[1], out=blk.h16, **opts), flush, stream, n)
-    out["swiglu_2in_ex_16"] = {"us": ms * 1e3, "GB_s": 6 * blk.h16.numel() / ms / 1e6,
+    ms = _time(lambda: W.swiglu_2in_ex_16(gu[0], gu[1], out=r.h16, **opts), flush, stream, n)
+    out["swiglu_2in_ex_16"] = {"us": ms * 1e3, "GB_s": 6 * r.h16.numel() / ms / 1e6,
                                "note": "limit 7, alpha 1.702, beta 1, bf16 in and out"}
     # library reference points on the Q/K/V shape (context only, not this path):
     # cuBLASLt FP8 through torch._scaled_mm on the pre-quantized activation,
     # cuBLAS bf16 through torch.matmul on weights dequantized beforehand
-    qx = W.fp8_quant_static(blk.x_qkv, blk.s_qkv).view(torch.float8_e4m3fn)
+    qx = W.fp8_quant_static(blk.x_qkv, w.s_qkv).view(torch.float8_e4m3fn)
     try:
-        wt = [q.view(torch.float8_e4m3fn).t() for q, _ in blk.w_qkv]
+        wt = [q.view(torch.float8_e4m3fn).t() for q in wq]
 
         def lib_fp8():
-            for w_t, (_, sw) in zip(wt, blk.w_qkv):
-                torch._scaled_mm(qx, w_t, scale_a=blk.s_qkv, scale_b=sw, out_dtype=torch.bfloat16)
+            for w_t, sw in zip(wt, sq):
+                torch._scaled_mm(qx, w_t, scale_a=w.s_qkv, scale_b=sw, out_dtype=torch.bfloat16)
         ms = _time(lib_fp8, flush, stream, n)
         out["lib_scaled_mm_fp8_qkv"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
                                         "note": "torch._scaled_mm (cuBLASLt) x3, E4M3 input; reference point"}
     except Exception as e:  # noqa: BLE001
         out["lib_scaled_mm_fp8_qkv"] = {"error": str(e).splitlines()[0][:160]}
-    wd = [(q.view(torch.float8_e4m3fn).float() * sw).to(torch.bfloat16) for q, sw in blk.w_qkv]
+    wd = [(q.view(torch.float8_e4m3fn).float() * sw).to(torch.bfloat16) for q, sw in w.qkv]
 
     def lib_bf16():
-        for w in wd:
-            torch.matmul(blk.x_qkv, w.t())
+        for wdi in wd:
+            torch.matmul(blk.x_qkv, wdi.t())
     ms = _time(lib_bf16, flush, stream, n)
     out["lib_matmul_bf16_qkv"] = {"us": ms * 1e3, "TFLOPS": QKV_FLOPS / ms / 1e9,
                                   "note": "torch.matmul (cuBLAS) x3 on pre-dequantized bf16 weights; reference point"}
@@ -507,87 +493,65 @@ def breakdown_ours(W, blk, policy, flush, stream, args):
     # The block step composed as the pages run it (cuBLASLt FP8 GEMMs, the
     # SwiGLU as its own op), for context.
     try:
-        lib_block = lambda: blk.lib_step(W)  # noqa: E731
-        ms = _time(lib_block, flush, stream, n)
+        ms = _time(lambda: blk.lib_step(W), flush, stream, n)
         out["lib_block_a8_step"] = {"us": ms * 1e3, "TFLOPS": BLOCK_FLOPS / ms / 1e9,
                                     "note": "the A8 block step with every GEMM through torch._scaled_mm "
                                             "(cuBLASLt FP8) and the SwiGLU unfused; reference point"}
     except Exception as e:  # noqa: BLE001
         out["lib_block_a8_step"] = {"error": str(e).splitlines()[0][:160]}
-    q = W.fp8_quant_static(blk.x_mlp, blk.s_mlp)
-    ms = _time(lambda: W.gate_up_swiglu_fp8(q, blk.s_mlp, blk.w_gu[0][0], blk.w_gu[1][0], blk.w_gu[0][1],
-                                            blk.w_gu[1][1], blk.s_h, out=blk.h8), flush, stream, n)
+    q = W.fp8_quant_static(blk.x_mlp, w.s_mlp)
+    ms = _time(lambda: W.gate_up_swiglu_fp8(q, w.s_mlp, w.gu[0][0], w.gu[1][0], w.gu[0][1], w.gu[1][1], w.s_h,
+                                            out=r.h8), flush, stream, n)
     out["glu_gate_up_swiglu_fp8"] = {"us": ms * 1e3, "TFLOPS": 4.0 * M_TOK * HID * INTER / ms / 1e9,
                                      "note": "fused gate+up GEMMs (E4M3 input) with SwiGLU->E4M3 epilogue"}
-    ms = _time(lambda: W.fp8_linear_w8a8_group(q, blk.s_mlp, [blk.w_gu[0][0]], [blk.w_gu[0][1]],
-                                               outs=[blk.y_gu[0]]), flush, stream, n)
+    ms = _time(lambda: W.fp8_linear_w8a8_group(q, w.s_mlp, [w.gu[0][0]], [w.gu[0][1]], outs=[gu[0]]),
+               flush, stream, n)
     out["w8a8_gate_4096x16384"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
-    ms = _time(lambda: W.fp8_linear_w8a8_group(blk.h8, blk.s_h, [blk.w_down[0]], [blk.w_down[1]],
-                                               outs=[blk.y_down]), flush, stream, n)
+    ms = _time(lambda: W.fp8_linear_w8a8_group(r.h8, w.s_h, [w.down[0]], [w.down[1]], outs=[r.y_down]),
+               flush, stream, n)
     out["w8a8_down_16384x4096"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}
-    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, blk.h16, None, [blk.w_down[0]], [blk.w_down[1]],
-                                               outs=[blk.y_down], ws=blk.wsd), flush, stream, n)
+    ms = _time(lambda: W.qkv_shared_quant_gemm(W.MODE_A16, r.h16, None, [w.down[0]], [w.down[1]],
+                                               outs=[r.y_down], ws=blk.wsd), flush, stream, n)
     out["w8a16_down_16384x4096"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9,
                                     "note": "dequantization into the workspace + bf16 GEMM"}
-    ms = _time(lambda: W.fp8_dequant_weight(blk.w_gu[0][0], blk.w_gu[0][1], out=blk.wsd[:INTER * HID].view(INTER, HID)),
+    ms = _time(lambda: W.fp8_dequant_weight(w.gu[0][0], w.gu[0][1], out=blk.wsd[:INTER * HID].view(INTER, HID)),
                flush, stream, n)
     out["fp8_dequant_weight_16384x4096"] = {"us": ms * 1e3, "GB_s": 3 * INTER * HID / ms / 1e6}
     # the producer of a linear input with the static quantization fused after
     # it (modulated LayerNorm -> bf16 -> E4M3), against the same two steps
     # run apart (bf16 h written and read back)
-    gen = torch.Generator(device=blk.x_qkv.device).manual_seed(31)
-    shift, scale = ((torch.randn((1, HID), generator=gen, device=blk.x_qkv.device) * 0.5).to(torch.bfloat16)
+    gen = torch.Generator(device=blk.dev).manual_seed(31)
+    shift, scale = ((torch.randn((1, HID), generator=gen, device=blk.dev) * 0.5).to(torch.bfloat16)
                     for _ in range(2))
-    hb = blk.y_qkv[0]
-    ms = _time(lambda: W.ln_modulate_quant(blk.x_qkv, shift, scale, blk.s_qkv, out=blk.ws), flush, stream, n)
+    hb = r.y_qkv[0]
+    ms = _time(lambda: W.ln_modulate_quant(blk.x_qkv, shift, scale, w.s_qkv, out=blk.ws), flush, stream, n)
     out["ln_modulate_quant"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6,
                                 "note": "LayerNorm + shift/scale + bf16 + E4M3 in one pass, [20670, 4096]"}
 
     def ln_unfused():
         W.ln_modulate_bf16(blk.x_qkv, shift, scale, out=hb)
-        W.fp8_quant_static(hb, blk.s_qkv, out=blk.ws)
+        W.fp8_quant_static(hb, w.s_qkv, out=blk.ws)
     ms = _time(ln_unfused, flush, stream, n)
     out["ln_modulate_then_quant"] = {"us": ms * 1e3, "GB_s": 7 * blk.x_qkv.numel() / ms / 1e6,
                                      "note": "the same as two launches (bf16 h through HBM)"}
+    # configs 1 and 2 of the workload list on the GPU, next to their oracle
+    # timings below
+    for name, (M, K, N) in (("config1_64x256x256", (64, 256, 256)), ("config2_4096x4096x4096", (4096, 4096, 4096))):
+        xs = blk.x_qkv[:M, :K].contiguous()
+        wq0 = wq[0][:N, :K].contiguous()
+        y0 = torch.empty((M, N), dtype=torch.bfloat16, device=blk.dev)
+        ws0 = torch.empty((M, K), dtype=torch.uint8, device=blk.dev)
+        wsd0 = torch.empty((N * K,), dtype=torch.bfloat16, device=blk.dev)
+        fl = 2.0 * M * N * K
+        ms8 = _time(lambda: W.fp8_linear_w8a8(xs, wq0, w.s_qkv, sq[0], out=y0, ws=ws0), flush, stream, n)
+        ms16 = _time(lambda: W.fp8_linear_w8a16(xs, wq0, sq[0], out=y0, ws=wsd0), flush, stream, n)
+        out[name] = {"w8a8_us": ms8 * 1e3, "w8a8_TFLOPS": fl / ms8 / 1e9,
+                     "w8a16_us": ms16 * 1e3, "w8a16_TFLOPS": fl / ms16 / 1e9}
     torch.cuda.synchronize()
     return out
 
 
 # ---------------------------------------------------------------- oracle arm
-
-class OracleBlock:
-    """The same block for the CPU oracle on a sample of tokens (set-up draws
-    E4M3 weights of the same shapes; scales as in `Block`)."""
-
-    def __init__(self, rows, seed=0):
-        import oracle as O
-        from w8a16_linear_gb300 import synth
-        self.O = O
-        self.rows = rows
-        self.x = [synth.activations_bf16(seed + i, (rows, HID), 0.25, outlier_frac=0.001) for i in range(3)]
-        self.s_in = [np.float32(np.abs(O.bf16_decode(x)).max() / 448) for x in self.x]
-
-        def weight(sd, n, k):
-            w = torch.randn((n, k), generator=torch.Generator().manual_seed(sd)) * 0.02
-            s = float(w.abs().max()) / 448.0
-            q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-            return q, np.float32(s)
-
-        self.w_qkv = [weight(10 + i, HID, HID) for i in range(3)]
-        self.w_out = weight(13, HID, HID)
-        self.w_gu = [weight(20 + i, INTER, HID) for i in range(2)]
-        self.w_down = weight(30, HID, INTER)
-
-    def step(self):
-        O = self.O
-        O.qkv_shared_quant_gemm("A8", self.x[0], self.s_in[0], [q for q, _ in self.w_qkv],
-                                [s for _, s in self.w_qkv])
-        O.linear_w8a8(O.quant_static(self.x[1], self.s_in[1]), self.w_out[0], self.s_in[1], self.w_out[1])
-        g, u = O.qkv_shared_quant_gemm("A8", self.x[2], self.s_in[2], [q for q, _ in self.w_gu],
-                                       [s for _, s in self.w_gu])
-        h = O.swiglu_2in_fp8(g[1], u[1], np.float32(0.02))
-        O.linear_w8a8(h, self.w_down[0], np.float32(0.02), self.w_down[1])
-
 
 def cpu_cores():
     try:
@@ -596,20 +560,106 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def oracle_sample(rows=64, reps=1):
-    ob = OracleBlock(rows)
+class OracleQKV:
+    """The headline workload for the CPU oracle on a sample of tokens: the
+    same shapes and laws as `Block` (set-up draws the E4M3 weights once)."""
+
+    def __init__(self, rows, seed=0):
+        import oracle as O
+        from w8a16_linear_gb300 import synth
+        self.O = O
+        self.rows = rows
+        self.x = synth.activations_bf16(seed, (rows, HID), 0.25, outlier_frac=0.001)
+        xc = synth.activations_bf16(seed + 1, (rows, HID), 0.25, outlier_frac=0.001)
+        self.s_in = np.float32(np.abs(O.bf16_decode(xc)).max() / 448)
+        self.w = []
+        for i in range(3):
+            w = torch.randn((HID, HID), generator=torch.Generator().manual_seed(10 + i)) * 0.02
+            s = float(w.abs().max()) / 448.0
+            q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            self.w.append((q, np.float32(s)))
+
+    def step(self):
+        self.O.qkv_shared_quant_gemm("A8", self.x, self.s_in, [q for q, _ in self.w], [s for _, s in self.w])
+
+    def flops(self):
+        return 6.0 * self.rows * HID * HID
+
+
+def oracle_headline(rows=4096):
+    """The oracle on a bounded sample of the headline workload; returns
+    (TFLOPS, seconds)."""
+    ob = OracleQKV(rows)
     t0 = time.perf_counter()
-    for _ in range(reps):
-        ob.step()
-    dt = (time.perf_counter() - t0) / reps
-    return 32.0 * rows * HID * HID / dt / 1e12, dt
+    ob.step()
+    dt = time.perf_counter() - t0
+    return ob.flops() / dt / 1e12, dt
+
+
+def oracle_timings():
+    """The CPU oracle on the host cores beside the kernels it checks:
+    configs 1 and 2 in full, each elementwise kernel on the bench's shapes
+    (in full where it takes a few seconds, else on a stated sample of rows,
+    the rate scaled from the sample)."""
+    import oracle as O
+    from w8a16_linear_gb300 import synth
+    cores = cpu_cores()
+    res = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    for name, (M, K, N) in (("config1_64x256x256", (64, 256, 256)), ("config2_4096x4096x4096", (4096, 4096, 4096))):
+        x = synth.activations_bf16(0, (M, K), 0.25, outlier_frac=0.001)
+        w = synth.normal_f32(1, (N, K), 0.02)
+        s_w = np.float32(np.abs(w).max() / 448)
+        qw = O.e4m3_encode(w / s_w)
+        s_in = np.float32(np.abs(O.bf16_decode(x)).max() / 448)
+        fl = 2.0 * M * N * K
+        t8 = timed(lambda: O.linear_w8a8(O.quant_static(x, s_in), qw, s_in, s_w))
+        t16 = timed(lambda: O.linear_w8a16(x, qw, s_w))
+        res[name] = {"w8a8": {"value": fl / t8 / 1e12, "unit": "TFLOPS", "s": t8},
+                     "w8a16": {"value": fl / t16 / 1e12, "unit": "TFLOPS", "s": t16},
+                     "sample": "full"}
+    # elementwise kernels: bytes each kernel moves per element, as the GPU lines
+    xq = synth.activations_bf16(2, (M_TOK, HID), 0.25, outlier_frac=0.001)
+    s = np.float32(0.003)
+    t = timed(lambda: O.quant_static(xq, s))
+    res["fp8_quant_static"] = {"value": 3 * xq.size / t / 1e9, "unit": "GB/s", "s": t, "sample": "full [20670, 4096]"}
+    rows = 1024
+    g = synth.activations_bf16(3, (rows, INTER), 1.0)
+    u = synth.activations_bf16(4, (rows, INTER), 1.0)
+    smp = f"{rows} of {M_TOK} rows of [20670, 16384]"
+    t = timed(lambda: O.swiglu_2in_fp8(g, u, np.float32(0.02)))
+    res["swiglu_2in_fp8"] = {"value": 5 * g.size / t / 1e9, "unit": "GB/s", "s": t, "sample": smp}
+    t = timed(lambda: O.swiglu_2in_bf16(g, u))
+    res["swiglu_2in_bf16"] = {"value": 6 * g.size / t / 1e9, "unit": "GB/s", "s": t, "sample": smp}
+    t = timed(lambda: O.swiglu_2in_ex_fp8(g, u, np.float32(0.02), limit=7.0, alpha=1.702, beta=1.0))
+    res["swiglu_2in_ex_fp8"] = {"value": 5 * g.size / t / 1e9, "unit": "GB/s", "s": t, "sample": smp}
+    qw = synth.random_bf16_bits(5, (INTER, HID), 0, 256).astype(np.uint8)
+    t = timed(lambda: O.dequant_weight_bf16(qw, np.float32(1e-4)))
+    res["fp8_dequant_weight_16384x4096"] = {"value": 3 * qw.size / t / 1e9, "unit": "GB/s", "s": t,
+                                            "sample": "full [16384, 4096]"}
+    rows = 1024
+    xl = synth.activations_bf16(6, (rows, HID), 0.5)
+    sh = synth.activations_bf16(7, (1, HID), 0.5)
+    sc = synth.activations_bf16(8, (1, HID), 0.5)
+    t = timed(lambda: O.ln_modulate_quant(xl, sh, sc, 1e-6, rows, np.float32(0.01)))
+    res["ln_modulate_quant"] = {"value": 3 * xl.size / t / 1e9, "unit": "GB/s", "s": t,
+                                "sample": f"{rows} of {M_TOK} rows of [20670, 4096]"}
+    for v in res.values():
+        v["cores"] = cores
+        v["kind"] = "oracle"
+    return res
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    rows = 256                  # a bounded sample: 13 steps stay within a minute or two
-    ob = OracleBlock(rows)
+    rows = 512                  # a bounded sample: a step takes about a second
+    ob = OracleQKV(rows)
     for _ in range(args.warmup):
         ob.step()
     secs = []
@@ -618,14 +668,14 @@ def run_reference(args, rank, world):
         ob.step()
         secs.append(time.perf_counter() - t0)
     ms = statistics.mean(secs) * 1e3
-    value = 32.0 * rows * HID * HID / (ms / 1e3) / 1e12
+    value = ob.flops() / (ms / 1e3) / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample_rows": rows, "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{rows} of {M_TOK} tokens of the block per step"},
+                         "sample": f"{rows} of {M_TOK} tokens of the Q/K/V group per step"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -656,8 +706,8 @@ def run_case(args):
         # the bench's four GEMM launches of one A8 block step at M=20670
         # (for the DRAM-traffic capture of the dominant kernel)
         blk = Block(dev)
-        qa = [W.fp8_quant_static(t, sc) for t, sc in ((blk.x_qkv, blk.s_qkv), (blk.x_out, blk.s_out),
-                                                         (blk.x_mlp, blk.s_mlp))]
+        qa = [W.fp8_quant_static(t, sc) for t, sc in ((blk.x_qkv, blk.w.s_qkv), (blk.x_out, blk.w.s_out),
+                                                         (blk.x_mlp, blk.w.s_mlp))]
         fn = lambda: blk.gemm_launches(W, *qa)  # noqa: E731
     elif args.case == "qkv8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A8, x, s, qs, ss, outs=ys, ws=qx)  # noqa: E731
@@ -710,26 +760,27 @@ def run_case(args):
         # clock and board power sampled every 100 ms.  Prints one JSON line
         # per phase.
         blk = Block(dev)
-        qq = W.fp8_quant_static(blk.x_qkv, blk.s_qkv)
-        wq, sq = [w for w, _ in blk.w_qkv], [sc for _, sc in blk.w_qkv]
+        qq = W.fp8_quant_static(blk.x_qkv, blk.w.s_qkv)
+        wq, sq = blk.wq, blk.sq
+        y_qkv, wd_qkv = blk.run.y_qkv, blk.run.wd_qkv
         qf = qq.view(torch.float8_e4m3fn)
         wt = [w.view(torch.float8_e4m3fn).t() for w in wq]
 
         def ours():
-            W.fp8_linear_w8a8_group(qq, blk.s_qkv, wq, sq, outs=blk.y_qkv)
+            W.fp8_linear_w8a8_group(qq, blk.w.s_qkv, wq, sq, outs=y_qkv)
 
         def lib():
-            for w_t, sw, y in zip(wt, sq, blk.y_qkv):
-                torch._scaled_mm(qf, w_t, scale_a=blk.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
-        for (qw, sc), o in zip(blk.w_qkv, blk.wd_qkv):
+            for w_t, sw, y in zip(wt, sq, y_qkv):
+                torch._scaled_mm(qf, w_t, scale_a=blk.w.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
+        for (qw, sc), o in zip(blk.w.qkv, wd_qkv):
             W.fp8_dequant_weight(qw, sc, out=o)
-        wdt = [o.t() for o in blk.wd_qkv]
+        wdt = [o.t() for o in wd_qkv]
 
         def ours16():
-            W.bf16_linear_group(blk.x_qkv, blk.wd_qkv, outs=blk.y_qkv)
+            W.bf16_linear_group(blk.x_qkv, wd_qkv, outs=y_qkv)
 
         def lib16():
-            for w_t, y in zip(wdt, blk.y_qkv):
+            for w_t, y in zip(wdt, y_qkv):
                 torch.matmul(blk.x_qkv, w_t, out=y)
         samples = []
         smi = None
@@ -787,10 +838,12 @@ def run_case(args):
         return 0
     elif args.case == "host_link":
         # The host link the end-to-end loop is bound by: pinned host buffers
-        # of the e2e step's sizes (inputs 508 MB in, outputs 847 MB out),
-        # host -> device alone, device -> host alone, and both at once on two
-        # streams; best of five, CUDA events.  Prints one JSON line.
-        nin, nout = 3 * M_TOK * HID * 2, 5 * M_TOK * HID * 2
+        # of the e2e step's sizes (the bf16 activation in, the three bf16
+        # outputs out), host -> device alone, device -> host alone, and both
+        # at once on two streams; best of five, each timed on the host clock
+        # (time.perf_counter) between two device synchronizations.  Prints
+        # one JSON line.
+        nin, nout = M_TOK * HID * 2, 3 * M_TOK * HID * 2
         hin = torch.empty(nin, dtype=torch.uint8, pin_memory=True)
         hout = torch.empty(nout, dtype=torch.uint8, pin_memory=True)
         din = torch.empty(nin, dtype=torch.uint8, device=dev)
@@ -859,8 +912,8 @@ def max_over_ranks(value, device):
 
 
 def job_tflops(world, steps, max_total_ms):
-    """Whole-job throughput: every replica runs `steps` full block steps."""
-    return world * BLOCK_FLOPS * steps / (max_total_ms / 1e3) / 1e12
+    """Whole-job throughput: every replica runs `steps` headline steps."""
+    return world * STEP_FLOPS * steps / (max_total_ms / 1e3) / 1e12
 
 
 # ---------------------------------------------------------------- main
@@ -910,36 +963,43 @@ def main():
     if rank == 0:
         peaks = load_peaks()
         fp8_peak = peaks["bf16_tflops"] * 2.0          # nominal FP8:BF16 dense ratio 4.5:2.25
-        achieved = BLOCK_FLOPS / (r["gemm_ms"] / 1e3) / 1e12
+        achieved = STEP_FLOPS / (r["gemm_ms"] / 1e3) / 1e12
+        bd = r["breakdown"]
         cpu = None
         if not args.no_cpu_baseline and world == 1:     # the oracle is timed at N=1 only
-            rows = 2560                                  # about 10 s of the oracle on 16 cores
-            v, dt = oracle_sample(rows=rows)
+            rows = 4096
+            v, dt = oracle_headline(rows=rows)
             cpu = {"value": v, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-                   "sample": f"{rows} of {M_TOK} tokens of the block step ({dt:.1f} s)"}
+                   "sample": f"{rows} of {M_TOK} tokens of the Q/K/V group ({dt:.1f} s)"}
+            # the oracle beside the kernels it checks (host cores, same run)
+            for name, ob in oracle_timings().items():
+                if name in bd:
+                    bd[name]["cpu_baseline"] = ob
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "intermediate": INTER,
-                       "policy_step": f"{POLICY_STEP} of {POLICY_STEPS} (W8A8)",
+            "config": {"workload": WORKLOAD, "M": M_TOK, "K": HID, "N": [HID, HID, HID],
                        "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "tensor", "kernel": "gemm_kernel<W8A8|GLU, CTA pair> (the block's 4 GEMM launches: QKV group, out-proj, gate/up+SwiGLU, down)",
+            "roofline": {"bound": "tensor", "kernel": "gemm_kernel<W8A8, CTA pair>: the grouped Q/K/V launch "
+                                                      "(3 x 4096x4096, M=20670)",
                          "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                         "frac": achieved / fp8_peak, "traffic": GEMM_TRAFFIC_BYTES,
-                         "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of the four launches "
-                                         "(one ncu capture at M=20670, caches flushed per launch)",
+                         "frac": achieved / fp8_peak, "traffic": QKV_GEMM_TRAFFIC_BYTES,
+                         "algorithmic_bytes": QKV_GEMM_ALGO_BYTES,
+                         "launch_us": r["gemm_ms"] * 1e3,
+                         "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch "
+                                         "(ncu capture at M=20670, caches flushed per launch)",
                          "peak_note": f"{peaks['source']} bf16 burst x 2 (nominal FP8/BF16 ratio)"},
             "pct_of_5pf_fp8": value / 5000.0,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOPS",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                    "note": "pinned host buffers; each step's inputs copied in while the previous step "
-                            "computes and its outputs copied out while the next one computes (two copy "
-                            "streams per direction, two device buffer sets); inputs larger than L2"},
+                    "note": "pinned host buffers; each step's activation copied in while the previous step "
+                            "computes and its three outputs copied out while the next one computes (two "
+                            "device buffer sets); inputs larger than L2"},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
-            "breakdown": r["breakdown"],
+            "breakdown": bd,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -53,7 +53,7 @@ typedef enum {
   W8_ERR_NULL = 1,     /* a required pointer is NULL */
   W8_ERR_SHAPE = 2,    /* negative or unsupported size, or group size outside 1..3 */
   W8_ERR_ALIGN = 3,    /* a pointer or row pitch is not 16-byte aligned */
-  W8_ERR_STRIDE = 4,   /* reserved: non-dense layouts are rejected by the binding */
+  W8_ERR_STRIDE = 4,   /* a row pitch differs from the row length (non-dense layout) */
   W8_ERR_DTYPE = 5,    /* activation dtype not accepted by this path */
   W8_ERR_ARCH = 6,     /* current device is not sm_103 */
   W8_ERR_POLICY = 7,   /* step policy refused (schema, window, step range) */
@@ -104,13 +104,18 @@ w8_status w8_selftest_timeout(void* stream);
  * correctly rounded binary32 division, then one round-to-nearest-even to
  * E4M3 with saturation at +-448 ([P2] Verification: div -> clamp ->
  * round-to-float8 with the exported input_scale).  NaN inputs give a NaN code.
- *   x    bf16 [M, K], device, read-only
+ *   x    bf16 [M, K], device, read-only; ldx = elements between row starts
  *   s_in float scalar, device
- *   q    E4M3 [M, K], device, written
- * Errors: NULL, SHAPE (M<0, K<=0, K%16), ALIGN, ARCH, CUDA.
+ *   q    E4M3 [M, K], device, written; ldq = bytes between row starts
+ * Rows must be dense: ldx and ldq must both equal K.  A padded or strided
+ * (non-contiguous) tensor is refused with W8_ERR_STRIDE rather than read or
+ * written with the wrong pitch ([P4] Test Coverage: the op rejects
+ * non-contiguous inputs).
+ * Errors: SHAPE (M<0, K<=0, K%16), STRIDE (ldx != K or ldq != K), NULL,
+ * ALIGN, ARCH, CUDA.
  */
-w8_status fp8_quant_static(const uint16_t* x, int64_t M, int64_t K, const float* s_in, uint8_t* q,
-                           void* stream);
+w8_status fp8_quant_static(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* s_in,
+                           uint8_t* q, int64_t ldq, void* stream);
 
 /*
  * fp8_linear_w8a8 — W8A8 FP8 linear.
@@ -133,17 +138,22 @@ w8_status fp8_linear_w8a8(const void* x, int32_t x_dtype, int64_t M, int64_t K, 
 
 /*
  * fp8_linear_w8a16 — W8A16 linear on the same E4M3 weight.
- * y = bf16_RNE( sum_k x[m,k] * Wd[n,k] ), Wd = bf16_RNE( fl32(dec(w) * s_w) ),
- * the dequantization done inside the GEMM with no dequantized copy in global
- * memory; input_scale is unused ([P3] Behavior: dequant + F.linear; [P4]
+ * y = bf16_RNE( sum_k x[m,k] * Wd[n,k] ), Wd = bf16_RNE( fl32(dec(w) * s_w) );
+ * input_scale is unused ([P3] Behavior: dequant + F.linear; [P4]
  * Denoising-step activation precision: same weights, same scales).
  *   x_dtype must be W8_DTYPE_BF16: an already-quantized activation is refused
  *   with W8_ERR_DTYPE ([P4] Denoising-step activation precision: the W8A16
  *   linear raises rather than accept an already-quantized activation).
+ *   ws   optional bf16 scratch of N*K values (16-byte aligned), device.  With
+ *        ws the weight is dequantized into it (a transient copy, overwritten
+ *        by the next call that is given the same ws) and a bf16 tensor-core
+ *        GEMM runs on it: the faster form.  With ws == NULL the dequantization
+ *        happens inside the GEMM and nothing is written besides y.  Both forms
+ *        use the same operand bits; they may differ in accumulation order only.
  * Errors: NULL, SHAPE (K%16, N%16), DTYPE, ALIGN, ARCH, CUDA.
  */
 w8_status fp8_linear_w8a16(const void* x, int32_t x_dtype, int64_t M, int64_t K, const uint8_t* w,
-                           int64_t N, const float* s_w, uint16_t* y, void* stream);
+                           int64_t N, const float* s_w, uint16_t* y, uint16_t* ws, void* stream);
 
 /*
  * qkv_shared_quant_gemm — a group of G projections sharing one activation

@@ -35,7 +35,7 @@ def test_header_symbols_exported(L):
     for n in names:
         assert hasattr(L, n), n
         assert n in binding.SIGNATURES, n
-    assert L.w8_abi_version() == 3
+    assert L.w8_abi_version() == 4
 
 
 def test_policy_matches_oracle_everywhere(L):
@@ -71,14 +71,14 @@ def test_validation_before_any_cuda_call(L):
     # Non-null fake device addresses; validation must reject before use.
     p16 = _u(0x10000)
     # NULL pointers
-    assert L.fp8_quant_static(None, 4, 16, p16, p16, None) == 1
+    assert L.fp8_quant_static(None, 4, 16, 16, p16, p16, 16, None) == 1
     # K not a multiple of 16 / negative M
-    assert L.fp8_quant_static(p16, 4, 24, p16, p16, None) == 2
-    assert L.fp8_quant_static(p16, -1, 16, p16, p16, None) == 2
+    assert L.fp8_quant_static(p16, 4, 24, 24, p16, p16, 24, None) == 2
+    assert L.fp8_quant_static(p16, -1, 16, 16, p16, p16, 16, None) == 2
     # misaligned
-    assert L.fp8_quant_static(_u(0x10008), 4, 16, p16, p16, None) == 3
+    assert L.fp8_quant_static(_u(0x10008), 4, 16, 16, p16, p16, 16, None) == 3
     # W8A16 refuses an already-quantized (E4M3) activation
-    assert L.fp8_linear_w8a16(p16, 1, 4, 16, p16, 16, p16, p16, None) == 5
+    assert L.fp8_linear_w8a16(p16, 1, 4, 16, p16, 16, p16, p16, None, None) == 5
     assert b"already-quantized" in L.w8_last_error()
     # unknown dtype, N not a multiple of 16, missing workspace for bf16 input
     assert L.fp8_linear_w8a8(p16, 7, 4, 16, p16, 16, p16, p16, p16, None, None) == 5
@@ -110,12 +110,40 @@ def test_zero_rows_is_a_noop(L):
     p16 = _u(0x10000)
     arr = (ctypes.c_void_p * 3)(0x10000, 0x10000, 0x10000)
     ns = (ctypes.c_int64 * 3)(16, 16, 16)
-    assert L.fp8_quant_static(p16, 0, 16, p16, p16, None) == 0
+    assert L.fp8_quant_static(p16, 0, 16, 16, p16, p16, 16, None) == 0
     assert L.fp8_linear_w8a8(p16, 0, 0, 16, p16, 16, p16, p16, p16, None, None) == 0
-    assert L.fp8_linear_w8a16(p16, 0, 0, 16, p16, 16, p16, p16, None) == 0
+    assert L.fp8_linear_w8a16(p16, 0, 0, 16, p16, 16, p16, p16, None, None) == 0
     assert L.qkv_shared_quant_gemm(0, p16, 0, 16, p16, 3, arr, ns, arr, arr, None, None) == 0
     assert L.swiglu_2in_fp8(p16, p16, 0, 16, p16, p16, None) == 0
     assert L.swiglu_2in_bf16(p16, p16, 0, 16, p16, None) == 0
+
+
+def test_non_dense_rows_are_refused(L):
+    """A row pitch other than the row length is refused with W8_ERR_STRIDE
+    before anything else is looked at (TensorRT-LLM PR #17476, Test
+    Coverage: the op rejects non-contiguous inputs)."""
+    p16 = _u(0x10000)
+    for ldx, ldq in ((32, 16), (16, 32), (8, 16), (16, 0), (-1, 16), (16, -1)):
+        assert L.fp8_quant_static(p16, 4, 16, ldx, p16, p16, ldq, None) == 4
+        assert b"dense" in L.w8_last_error()
+    # refused even for zero rows and before the NULL check
+    assert L.fp8_quant_static(None, 0, 16, 32, None, None, 16, None) == 4
+    # dense rows pass validation (M == 0: nothing is launched)
+    assert L.fp8_quant_static(p16, 0, 4096, 4096, p16, p16, 4096, None) == 0
+
+
+def test_binding_reports_row_pitch():
+    """The binding hands the library the tensor's real row pitch (or -1 for
+    a layout that has none), so a strided view reaches the library's refusal."""
+    import torch
+    from w8a16_linear_gb300.binding import _row_pitch
+    x = torch.empty((6, 64), dtype=torch.bfloat16)
+    assert _row_pitch(x) == 64
+    assert _row_pitch(x[:, :32]) == 64          # a column slice keeps the parent's pitch
+    assert _row_pitch(x.t()) == -1              # columns not contiguous
+    assert _row_pitch(x.view(2, 3, 64)) == 64
+    assert _row_pitch(torch.empty((2, 3, 80))[:, :, :64]) == 80
+    assert _row_pitch(torch.empty((4, 3, 64))[::2]) == -1   # every other batch: rows not packed
 
 
 def test_swiglu_variant_validation_before_any_cuda_call(L):

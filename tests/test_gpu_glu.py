@@ -8,7 +8,8 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_util import W, dev_bf16, dev_f32, dev_u8, host_bits, host_u8, amax_scale  # noqa: F401
+from gpu_util import (W, dev_bf16, dev_f32, dev_u8, host_bits, host_u8, amax_scale,  # noqa: F401
+                      assert_swiglu_within_one_ulp)
 from w8a16_linear_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -67,14 +68,11 @@ def test_fused_vs_oracle_chain(W):
     out = host_u8(W.gate_up_swiglu_fp8(dev_bf16(x), dev_f32(s_in), dev_u8(ws[0]), dev_u8(ws[1]),
                                        dev_f32(ss[0]), dev_f32(ss[1]), dev_f32(s_out)))
     (_, gb), (_, ub) = O.qkv_shared_quant_gemm("A8", x, s_in, ws, ss)
-    want = O.swiglu_2in_fp8(gb, ub, s_out)
     # codes can differ only where the GPU's bf16 gate/up differ from the
-    # correctly rounded ones (accumulation order); then by one E4M3 step
-    diff = out != want
-    assert diff.mean() < 2e-3
-    dv = np.abs(O.e4m3_decode(out[diff]).astype(np.float64) - O.e4m3_decode(want[diff]))
-    step = np.maximum(np.abs(O.e4m3_decode(want[diff])).astype(np.float64), 2.0 ** -6) / 8
-    assert np.all(dv <= step * 1.0001)
+    # correctly rounded ones (accumulation order), and then only as the
+    # SwiGLU of a gate/up one bf16 ulp away
+    assert_swiglu_within_one_ulp(out, O.swiglu_2in_fp8(gb, ub, s_out), gb, ub,
+                                 lambda g, u: O.swiglu_2in_fp8(g, u, s_out), 2e-3)
 
 
 def test_fused_full_size(W):
@@ -104,5 +102,5 @@ def test_fused_full_size(W):
     sws = [np.float32(s.item()) for s in sw]
     (_, gb), (_, ub) = O.qkv_shared_quant_gemm("A8", xs, np.float32(s_in.item()), qws, sws)
     want = O.swiglu_2in_fp8(gb, ub, np.float32(0.02))
-    got = host_u8(fused[ri])
-    assert (got != want).mean() < 2e-3
+    assert_swiglu_within_one_ulp(host_u8(fused[ri]), want, gb, ub,
+                                 lambda g, u: O.swiglu_2in_fp8(g, u, np.float32(0.02)), 2e-3)

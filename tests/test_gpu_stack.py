@@ -1,91 +1,148 @@
-"""The step-scheduled block at the CFG batch size (M = 2 x 20670 = 41340):
-the policy picks W8A16 for step 2 and W8A8 for step 3 of 8; every row of the
-block (Q/K/V group, out-projection, gate/up + SwiGLU, down) is checked on
-sampled rows plus the ragged tail against the oracle."""
+"""The step-scheduled stack as a whole: 8 denoising steps x 4 blocks at the
+CFG batch size (M = 2 x 20670 = 41340 tokens), hidden 4096, intermediate
+16384, every weight a static per-tensor E4M3 tensor with its own scale.
+
+The policy (first 3 + last 3 steps W8A16; diffusers PR #14664, "[Cosmos3]
+Mixed W8A8/W8A16 denoising for ModelOpt FP8 checkpoints", sections Behavior
+and Tests) must give the trace A16 x3, A8 x2, A16 x3.  Each (step, block,
+site) draws a fresh seeded activation (seed step*100 + block*10 + site; the
+out-projection's input stands in for the attention output) and the MLP
+chains gate/up -> SwiGLU -> down.  The blocks run through
+``w8a16_linear_gb300.stack.BlockStep``, the call sequence the bench times.
+
+Every site's output is checked against the oracle on sampled rows plus the
+124-row ragged tail (41340 = 161 x 256 + 124), on a sample of output
+columns (weight rows are independent outputs, so the oracle computes only
+those): the GEMMs within the stated tolerance, the SwiGLU outputs equal to
+the oracle's or, where the kernel's own bf16 gate/up differ from the
+correctly rounded ones, the SwiGLU of a gate/up one bf16 ulp away, and the
+down projection on the kernel's own SwiGLU output."""
 
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
-from gpu_util import W, GEMM_TOL, dev_f32, host_bits, host_u8, gemm_err  # noqa: F401
+from gpu_util import W, GEMM_TOL, host_bits, host_u8, gemm_err, assert_swiglu_within_one_ulp  # noqa: F401
 from w8a16_linear_gb300 import synth
+from w8a16_linear_gb300.stack import BlockStep, BlockWeights
 
 pytestmark = pytest.mark.gpu
 
 M, H, I = 41340, 4096, 16384
+STEPS, BLOCKS = 8, 4
+TAIL = 124
+N_RAND_ROWS = 8
+N_COLS = 512
 
 
-def _weight(gen, n, k, c):
-    w = torch.randn((n, k), generator=gen, device="cuda") * (0.02 * c)
+def _act(seed, rows):
+    """x ~ N(0, 0.25^2) with 0.1% outliers x8, drawn on the GPU (seeded)."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    t = torch.randn((rows, H), generator=g, device="cuda") * 0.25
+    k = int(t.numel() * 0.001)
+    idx = torch.randint(0, t.numel(), (k,), generator=g, device="cuda")
+    t.view(-1)[idx] *= 8.0
+    return t.to(torch.bfloat16)
+
+
+def _weight(g, n, k):
+    """N(0, 0.02^2) scaled by c ~ U[0.5, 1], E4M3 with the amax/448 scale."""
+    c = float(torch.rand((), generator=g, device="cuda")) * 0.5 + 0.5
+    w = torch.randn((n, k), generator=g, device="cuda") * (0.02 * c)
     s = (w.abs().amax() / 448).reshape(1).contiguous()
-    q = (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
-    return q, s
+    return (w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous(), s
 
 
-@pytest.fixture(scope="module")
-def block(W):
-    gen = torch.Generator(device="cuda").manual_seed(11)
-    x = (torch.randn((M, H), generator=gen, device="cuda") * 0.25).to(torch.bfloat16)
-    s_in = (x.float().abs().amax() / 448).reshape(1).contiguous()
-    wqkv = [_weight(gen, H, H, c) for c in (0.6, 0.8, 1.0)]
-    wout = _weight(gen, H, H, 0.9)
-    wgu = [_weight(gen, I, H, c) for c in (0.7, 1.0)]
-    wdown = _weight(gen, H, I, 0.8)
-    return dict(x=x, s_in=s_in, wqkv=wqkv, wout=wout, wgu=wgu, wdown=wdown,
-                s_h=dev_f32(0.02), rows=np.concatenate([synth.random_rows(12, M, 24), np.arange(M - 124, M)]))
+def _amax_scale(t):
+    return (t.float().abs().amax() / 448).reshape(1).contiguous()
 
 
-def _run(W, b, step):
+def _block_weights(b):
+    g = torch.Generator(device="cuda").manual_seed(500 + b)
+    qkv = [_weight(g, H, H) for _ in range(3)]
+    out = _weight(g, H, H)
+    gu = [_weight(g, I, H) for _ in range(2)]
+    down = _weight(g, H, I)
+    # static input scales from a calibration pass (separately seeded batches);
+    # the down projection's input scale from the SwiGLU of the calibration
+    # batch, computed in plain float32 on the dequantized weights
+    cal = [_act(10000 + b * 10 + site, 2048) for site in range(3)]
+    s_qkv, s_out, s_mlp = (_amax_scale(c) for c in cal)
+    deq = [(q.view(torch.float8_e4m3fn).float() * s) for q, s in gu]
+    xg = cal[2].float()
+    hcal = torch.nn.functional.silu(xg @ deq[0].t()) * (xg @ deq[1].t())
+    s_h = _amax_scale(hcal)
+    del deq, hcal
+    return BlockWeights(qkv=qkv, out=out, gu=gu, down=down, s_qkv=s_qkv, s_out=s_out, s_mlp=s_mlp, s_h=s_h)
+
+
+def _f(t):
+    return np.float32(t.item())
+
+
+def test_eight_step_four_block_stack_at_cfg_batch(W):
+    blocks = [_block_weights(b) for b in range(BLOCKS)]
+    runner = BlockStep(M, H, I, torch.device("cuda"))
     pol = W.StepPolicy(1, 1, 3, 3)
-    mode = W.step_policy_dispatch(pol, step, 8)
-    x = b["x"]
-    if mode == W.MODE_A8:
-        qkv = W.qkv_shared_quant_gemm(W.MODE_A8, x, b["s_in"], [q for q, _ in b["wqkv"]], [s for _, s in b["wqkv"]])
-        out = W.fp8_linear_w8a8(x, b["wout"][0], b["s_in"], b["wout"][1])
-        h = W.gate_up_swiglu_fp8(x, b["s_in"], b["wgu"][0][0], b["wgu"][1][0], b["wgu"][0][1], b["wgu"][1][1], b["s_h"])
-        y = W.fp8_linear_w8a8(h, b["wdown"][0], b["s_h"], b["wdown"][1])
-    else:
-        qkv = W.qkv_shared_quant_gemm(W.MODE_A16, x, None, [q for q, _ in b["wqkv"]], [s for _, s in b["wqkv"]])
-        out = W.fp8_linear_w8a16(x, b["wout"][0], b["wout"][1])
-        g, u = W.qkv_shared_quant_gemm(W.MODE_A16, x, None, [q for q, _ in b["wgu"]], [s for _, s in b["wgu"]])
-        h = W.swiglu_2in_bf16(g, u)
-        y = W.fp8_linear_w8a16(h, b["wdown"][0], b["wdown"][1])
-    torch.cuda.synchronize()
-    W.poll_device_error()
-    return mode, qkv, out, h, y
+    gen = np.random.default_rng(7)
+    cols = {name: np.sort(gen.choice(n, N_COLS, replace=False)) for name, n in (("h", H), ("i", I))}
+    ch_d = torch.from_numpy(cols["h"]).cuda()
+    modes = []
+    # per block and mode: the sampled inputs and outputs of every step, so
+    # that the oracle decodes each weight once per block and mode
+    rec = {(b, m): [] for b in range(BLOCKS) for m in ("A8", "A16")}
+    for step in range(STEPS):
+        mode = W.step_policy_dispatch(pol, step, STEPS)
+        om = "A8" if mode == W.MODE_A8 else "A16"
+        modes.append(om)
+        rows = np.concatenate([synth.random_rows(step * 100, M - TAIL, N_RAND_ROWS), np.arange(M - TAIL, M)])
+        ri = torch.from_numpy(rows).cuda()
+        for b, w in enumerate(blocks):
+            xs = [_act(step * 100 + b * 10 + site, M) for site in range(3)]
+            runner.run(W, mode, w, *xs)
+            torch.cuda.synchronize()
+            W.poll_device_error()
+            h = runner.h8 if om == "A8" else runner.h16
+            rec[(b, om)].append(dict(
+                x=[host_bits(x[ri]) for x in xs],
+                qkv=[host_bits(y[ri][:, ch_d]) for y in runner.y_qkv],
+                out=host_bits(runner.y_out[ri][:, ch_d]),
+                h_full=host_u8(h[ri]) if om == "A8" else host_bits(h[ri]),
+                down=host_bits(runner.y_down[ri][:, ch_d])))
+            del xs
+    assert modes == ["A16"] * 3 + ["A8"] * 2 + ["A16"] * 3
 
-
-@pytest.mark.parametrize("step", [2, 3])
-def test_block_step_at_cfg_batch(W, block, step):
-    mode, qkv, out, h, y = _run(W, block, step)
-    rows = block["rows"]
-    ri = torch.from_numpy(rows).cuda()
-    xs = host_bits(block["x"][ri])
-    s_in = np.float32(block["s_in"].item())
-    sc = lambda t: np.float32(t.item())  # noqa: E731
-    qkv_w = [host_u8(q) for q, _ in block["wqkv"]]
-    qkv_s = [sc(s) for _, s in block["wqkv"]]
-    om = "A8" if mode == W.MODE_A8 else "A16"
-    assert om == ("A16" if step == 2 else "A8")
-    for yg, (r64, _) in zip(qkv, O.qkv_shared_quant_gemm(om, xs, s_in, qkv_w, qkv_s)):
-        assert gemm_err(host_bits(yg[ri]), r64) <= GEMM_TOL
-    wo, so = host_u8(block["wout"][0]), sc(block["wout"][1])
-    r_out = (O.linear_w8a8(O.quant_static(xs, s_in), wo, s_in, so) if om == "A8"
-             else O.linear_w8a16(xs, wo, so))[0]
-    assert gemm_err(host_bits(out[ri]), r_out) <= GEMM_TOL
-    gu_w = [host_u8(q) for q, _ in block["wgu"]]
-    gu_s = [sc(s) for _, s in block["wgu"]]
-    (_, gb), (_, ub) = O.qkv_shared_quant_gemm(om, xs, s_in, gu_w, gu_s)
-    wd, sd = host_u8(block["wdown"][0]), sc(block["wdown"][1])
-    if om == "A8":
-        want = O.swiglu_2in_fp8(gb, ub, np.float32(0.02))
-        got = host_u8(h[ri])
-        assert (got != want).mean() < 2e-3
-        r_y, _ = O.linear_w8a8(got, wd, np.float32(0.02), sd)      # down on the GPU's own codes
-    else:
-        want = O.swiglu_2in_bf16(gb, ub)
-        got = host_bits(h[ri])
-        assert (got != want).mean() < 2e-2                           # bf16 gate/up may differ by an ulp
-        r_y, _ = O.linear_w8a16(got, wd, sd)
-    assert gemm_err(host_bits(y[ri]), r_y) <= GEMM_TOL
+    for (b, om), recs in rec.items():
+        if not recs:
+            continue
+        w = blocks[b]
+        cat = lambda key, i=None: np.concatenate([r[key] if i is None else r[key][i] for r in recs])  # noqa: E731
+        x_qkv, x_out, x_mlp = (cat("x", i) for i in range(3))
+        s_qkv, s_out, s_mlp, s_h = _f(w.s_qkv), _f(w.s_out), _f(w.s_mlp), _f(w.s_h)
+        ci = cols["i"]
+        ci_d = torch.from_numpy(ci).cuda()
+        # Q/K/V: one shared quantization (A8) or three W8A16 linears
+        qkv_w = [host_u8(q[ch_d]) for q, _ in w.qkv]
+        ref = O.qkv_shared_quant_gemm(om, x_qkv, s_qkv, qkv_w, [_f(s) for _, s in w.qkv])
+        for i, (y64, _) in enumerate(ref):
+            assert gemm_err(cat("qkv", i), y64) <= GEMM_TOL, (b, om, "qkv", i)
+        # out-projection
+        wo = host_u8(w.out[0][ch_d])
+        y64 = (O.linear_w8a8(O.quant_static(x_out, s_out), wo, s_out, _f(w.out[1])) if om == "A8"
+               else O.linear_w8a16(x_out, wo, _f(w.out[1])))[0]
+        assert gemm_err(cat("out"), y64) <= GEMM_TOL, (b, om, "out")
+        # gate/up -> SwiGLU on the sampled intermediate columns
+        gu_w = [host_u8(q[ci_d]) for q, _ in w.gu]
+        (_, gb), (_, ub) = O.qkv_shared_quant_gemm(om, x_mlp, s_mlp, gu_w, [_f(s) for _, s in w.gu])
+        h_full = cat("h_full")
+        if om == "A8":
+            spec = lambda g, u: O.swiglu_2in_fp8(g, u, s_h)  # noqa: E731
+        else:
+            spec = O.swiglu_2in_bf16
+        assert_swiglu_within_one_ulp(h_full[:, ci], spec(gb, ub), gb, ub, spec, 2e-3 if om == "A8" else 1e-2)
+        # down projection on the kernel's own SwiGLU output (whole rows)
+        wd = host_u8(w.down[0][ch_d])
+        y64 = (O.linear_w8a8(h_full, wd, s_h, _f(w.down[1])) if om == "A8"
+               else O.linear_w8a16(h_full, wd, _f(w.down[1])))[0]
+        assert gemm_err(cat("down"), y64) <= GEMM_TOL, (b, om, "down")

@@ -43,7 +43,7 @@ def test_two_gloo_ranks_take_the_max_time():
     assert out[0] == out[1] == 125.0
     import bench
     # whole-job throughput: both replicas' work over the slowest replica's time
-    assert bench.job_tflops(2, 10, 125.0) == pytest.approx(2 * bench.BLOCK_FLOPS * 10 / 0.125 / 1e12)
+    assert bench.job_tflops(2, 10, 125.0) == pytest.approx(2 * bench.STEP_FLOPS * 10 / 0.125 / 1e12)
 
 
 def test_single_rank_needs_no_process_group():

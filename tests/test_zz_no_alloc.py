@@ -1,9 +1,10 @@
 """The allocation-free W8A8 entry point, for callers that cannot allocate
 device memory (operator/plugin interfaces that pass only inputs and outputs,
 fixed memory pools, code that may not call cudaMalloc during a stream
-capture).  It is called through the C ABI and compared with the existing
-workspace-based entry point on two calls in a row.  This file is collected
-last on purpose."""
+capture).  It is called through the C ABI on consecutive calls and must give
+exactly the output of the workspace-based entry point (the same quantization
+and GEMM kernels on the same bits), and the oracle's on sampled rows.  This
+file is collected last on purpose."""
 
 import ctypes
 
@@ -11,34 +12,43 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import W, GEMM_TOL, dev_bf16, dev_f32, dev_u8, linear_problem  # noqa: F401
+import oracle as O
+from gpu_util import W, GEMM_TOL, dev_bf16, dev_f32, dev_u8, host_bits, linear_problem, gemm_err  # noqa: F401
+from w8a16_linear_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-
-def _rel(a, b):
-    a, b = a.float(), b.float()
-    return float((a - b).abs().max() / b.abs().max().clamp_min(1e-30))
+SCRATCH_BYTES = 32 << 20            # the entry point's fixed limit on M * K
 
 
-def test_noalloc_matches_workspace_entry_point_twice(W):
+def _noalloc(L, xd, M, K, wd, N, si, sw, y, stream):
+    return L.fp8_linear_w8a8_noalloc(ctypes.c_void_p(xd.data_ptr()), M, K, ctypes.c_void_p(wd.data_ptr()), N,
+                                     ctypes.c_void_p(si.data_ptr()), ctypes.c_void_p(sw.data_ptr()),
+                                     ctypes.c_void_p(y.data_ptr()), stream)
+
+
+def test_noalloc_matches_workspace_entry_point_consecutive_calls(W):
     from w8a16_linear_gb300 import binding
     L = binding.lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    # two calls in a row, the second smaller than the first, so that scratch
-    # left by the first call must not leak into the second result
-    for (M, K, N, seed) in [(2048, 4096, 512, 0), (333, 1024, 256, 1)]:
+    # consecutive calls: one that fills the scratch array exactly (M*K = 32 MiB),
+    # then smaller ones, so scratch left by an earlier call must not leak into
+    # a later result
+    cases = [(8192, 4096, 256, 0), (2048, 4096, 512, 1), (333, 1024, 256, 2)]
+    assert cases[0][0] * cases[0][1] == SCRATCH_BYTES
+    for (M, K, N, seed) in cases:
         x, qw, s_in, s_w = linear_problem(M, K, N, seed_x=seed, seed_w=seed + 10)
         xd, wd, si, sw = dev_bf16(x), dev_u8(qw), dev_f32(s_in), dev_f32(s_w)
         y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        st = L.fp8_linear_w8a8_noalloc(ctypes.c_void_p(xd.data_ptr()), M, K, ctypes.c_void_p(wd.data_ptr()), N,
-                                       ctypes.c_void_p(si.data_ptr()), ctypes.c_void_p(sw.data_ptr()),
-                                       ctypes.c_void_p(y.data_ptr()), stream)
+        st = _noalloc(L, xd, M, K, wd, N, si, sw, y, stream)
         assert st == 0, L.w8_last_error()
         ref = W.fp8_linear_w8a8(xd, wd, si, sw)
         torch.cuda.synchronize()
         W.poll_device_error()
-        assert _rel(y, ref) <= GEMM_TOL
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+        rows = np.concatenate([synth.random_rows(40 + seed, M, min(M, 24)), np.arange(max(M - 8, 0), M)])
+        y64, _ = O.linear_w8a8(O.quant_static(x[rows], s_in), qw, s_in, s_w)
+        assert gemm_err(host_bits(y)[rows], y64) <= GEMM_TOL
 
 
 def test_noalloc_refuses_more_than_its_scratch(W):

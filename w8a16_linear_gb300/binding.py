@@ -46,11 +46,11 @@ SIGNATURES = {
     "w8_device_check": (ctypes.c_int, []),
     "w8_poll_device_error": (ctypes.c_int, [_c_void_p]),
     "w8_selftest_timeout": (ctypes.c_int, [_c_void_p]),
-    "fp8_quant_static": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "fp8_quant_static": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _i64, _c_void_p]),
     "fp8_linear_w8a8": (ctypes.c_int, [_c_void_p, _i32, _i64, _i64, _c_void_p, _i64, _c_void_p,
                                        _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "fp8_linear_w8a16": (ctypes.c_int, [_c_void_p, _i32, _i64, _i64, _c_void_p, _i64, _c_void_p,
-                                        _c_void_p, _c_void_p]),
+                                        _c_void_p, _c_void_p, _c_void_p]),
     "qkv_shared_quant_gemm": (ctypes.c_int, [_i32, _c_void_p, _i64, _i64, _c_void_p, _i32,
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_i64),
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
@@ -179,15 +179,41 @@ def selftest_timeout(stream=None):
 
 
 def fp8_quant_static(x, s_in, out=None, stream=None):
-    """E4M3 codes (uint8) of ``x / s_in``; same shape as ``x``."""
-    x = _as_bf16(x, "x")
-    x2 = _flat2(x)
-    M, K = x2.shape
+    """E4M3 codes (uint8) of ``x / s_in``; same shape as ``x``.  Row pitches
+    are passed as they are: a tensor whose rows are not dense is refused by
+    the library (W8_ERR_STRIDE)."""
+    if x.dtype != torch.bfloat16:
+        raise W8Error(5, f"x: expected bfloat16, got {x.dtype}")
+    if not x.is_cuda:
+        raise W8Error(1, "x: must be a CUDA tensor")
+    if x.dim() < 2:
+        raise W8Error(2, "x: expected at least 2 dimensions")
     if out is None:
         out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-    o = _as_u8(out, "out")
-    _check(lib().fp8_quant_static(_ptr(x2), M, K, _ptr(_scalar(s_in, "s_in")), _ptr(o), _stream(stream)))
+    if out.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) or out.shape != x.shape:
+        raise W8Error(5, "out: expected E4M3 codes of x's shape")
+    K = x.shape[-1]
+    M = x.numel() // K if K else 0
+    ldx = _row_pitch(x)
+    ldq = _row_pitch(out)
+    _check(lib().fp8_quant_static(_ptr(x), M, K, ldx, _ptr(_scalar(s_in, "s_in")), _ptr(out), ldq,
+                                  _stream(stream)))
     return out
+
+
+def _row_pitch(t):
+    """Elements between consecutive row starts when the last dimension is
+    contiguous and every leading dimension is packed row after row; -1 for
+    any other layout (refused by the library as non-dense)."""
+    if t.dim() < 2 or t.stride(-1) != 1:
+        return -1
+    pitch = t.stride(-2)
+    expect = pitch * t.shape[-2]
+    for d in range(t.dim() - 3, -1, -1):
+        if t.shape[d] != 1 and t.stride(d) != expect:
+            return -1
+        expect *= t.shape[d]
+    return pitch
 
 
 def _ln_call(x, shift, scale, eps, s_in, q, h, stream):
@@ -247,8 +273,10 @@ def fp8_linear_w8a8(x, w, s_in, s_w, out=None, ws=None, stream=None):
     return out
 
 
-def fp8_linear_w8a16(x, w, s_w, out=None, stream=None):
-    """W8A16 linear (dequantization inside the GEMM).  ``x`` must be bf16."""
+def fp8_linear_w8a16(x, w, s_w, out=None, ws=None, stream=None):
+    """W8A16 linear.  ``x`` must be bf16.  With ``ws`` (bf16, at least N*K
+    values) the weight is dequantized into it and a bf16 GEMM runs on it;
+    without, the dequantization happens inside the GEMM."""
     dt = DTYPE_BF16 if x.dtype == torch.bfloat16 else DTYPE_E4M3
     xd = _dense(x, "x")
     x2 = _flat2(xd)
@@ -258,8 +286,12 @@ def fp8_linear_w8a16(x, w, s_w, out=None, stream=None):
     if out is None:
         out = torch.empty(*x.shape[:-1], N, dtype=torch.bfloat16, device=x.device)
     _as_bf16(out, "out")
+    if ws is not None:
+        _as_bf16(ws, "ws")
+        if ws.numel() < N * K:
+            raise W8Error(2, f"ws: {ws.numel()} bf16 values, the weight needs {N * K}")
     _check(lib().fp8_linear_w8a16(_ptr(x2), dt, M, K, _ptr(wq), N, _ptr(_scalar(s_w, "s_w")),
-                                  _ptr(out), _stream(stream)))
+                                  _ptr(out), _ptr(ws), _stream(stream)))
     return out
 
 

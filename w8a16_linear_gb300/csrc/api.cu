@@ -95,7 +95,7 @@ int query_device(int* sms) { return device_info(sms); }
 
 extern "C" {
 
-int w8_abi_version(void) { return 3; }
+int w8_abi_version(void) { return 4; }
 
 const char* w8_last_error(void) { return g_last_error; }
 
@@ -123,10 +123,15 @@ w8_status w8_selftest_timeout(void* stream) {
                      "w8_selftest_timeout launch");
 }
 
-w8_status fp8_quant_static(const uint16_t* x, int64_t M, int64_t K, const float* s_in, uint8_t* q,
-                           void* stream) {
+w8_status fp8_quant_static(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const float* s_in,
+                           uint8_t* q, int64_t ldq, void* stream) {
   if (M < 0 || K <= 0) return fail(W8_ERR_SHAPE, "fp8_quant_static: M=%lld K=%lld", (long long)M, (long long)K);
   if (K % 16) return fail(W8_ERR_SHAPE, "fp8_quant_static: K=%lld is not a multiple of 16", (long long)K);
+  // Rows must be dense: a padded or strided activation is refused rather
+  // than read with the wrong pitch.
+  if (ldx != K || ldq != K)
+    return fail(W8_ERR_STRIDE, "fp8_quant_static: ldx=%lld ldq=%lld, both must equal K=%lld (dense rows)",
+                (long long)ldx, (long long)ldq, (long long)K);
   if (M == 0) return ok();
   if (!x || !s_in || !q) return fail(W8_ERR_NULL, "fp8_quant_static: NULL pointer");
   if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(s_in) & 3u))
@@ -192,15 +197,17 @@ w8_status fp8_linear_w8a8(const void* x, int32_t x_dtype, int64_t M, int64_t K, 
 }
 
 w8_status fp8_linear_w8a16(const void* x, int32_t x_dtype, int64_t M, int64_t K, const uint8_t* w,
-                           int64_t N, const float* s_w, uint16_t* y, void* stream) {
+                           int64_t N, const float* s_w, uint16_t* y, uint16_t* ws, void* stream) {
   if (x_dtype != W8_DTYPE_BF16)
     return fail(W8_ERR_DTYPE,
                 "fp8_linear_w8a16: activation must be bf16; an already-quantized input is refused");
   w8_status st = check_linear_common("fp8_linear_w8a16", x, M, K, w, N, s_w, y);
   if (st != W8_OK) return st;
   if (M == 0) return ok();
+  if (ws && !aligned16(ws)) return fail(W8_ERR_ALIGN, "fp8_linear_w8a16: ws must be 16-byte aligned");
   int sms = 0;
   if ((st = device_info(&sms)) != W8_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   w8::GemmProblem p{};
   p.M = M;
   p.K = K;
@@ -211,7 +218,16 @@ w8_status fp8_linear_w8a16(const void* x, int32_t x_dtype, int64_t M, int64_t K,
   p.s_w[0] = s_w;
   p.y[0] = y;
   int terr = 0;
-  cudaError_t e = w8::launch_gemm_w8a16(p, sms, static_cast<cudaStream_t>(stream), &terr);
+  cudaError_t e;
+  if (ws) {
+    // dequant + F.linear: the weight into ws, then the bf16 GEMM on it
+    e = w8::launch_dequant_weight(w, N * K, s_w, ws, sms, s);
+    if (e != cudaSuccess) return cuda_status(e, "fp8_linear_w8a16: dequantization launch");
+    p.w[0] = reinterpret_cast<const uint8_t*>(ws);
+    e = w8::launch_gemm_bf16(p, sms, s, &terr);
+  } else {
+    e = w8::launch_gemm_w8a16(p, sms, s, &terr);
+  }
   if (terr) return fail(W8_ERR_ALIGN, "fp8_linear_w8a16: tensor map encoding rejected the operands");
   return cuda_status(e, "fp8_linear_w8a16: GEMM launch");
 }
