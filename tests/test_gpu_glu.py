@@ -9,7 +9,7 @@ import torch
 
 import oracle as O
 from gpu_util import (W, dev_bf16, dev_f32, dev_u8, host_bits, host_u8, amax_scale,  # noqa: F401
-                      assert_swiglu_within_one_ulp)
+                      abs_product_sums, accumulation_window, assert_swiglu_consistent)
 from w8a16_linear_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -67,12 +67,13 @@ def test_fused_vs_oracle_chain(W):
     s_out = np.float32(0.004)
     out = host_u8(W.gate_up_swiglu_fp8(dev_bf16(x), dev_f32(s_in), dev_u8(ws[0]), dev_u8(ws[1]),
                                        dev_f32(ss[0]), dev_f32(ss[1]), dev_f32(s_out)))
-    (_, gb), (_, ub) = O.qkv_shared_quant_gemm("A8", x, s_in, ws, ss)
-    # codes can differ only where the GPU's bf16 gate/up differ from the
-    # correctly rounded ones (accumulation order), and then only as the
-    # SwiGLU of a gate/up one bf16 ulp away
-    assert_swiglu_within_one_ulp(out, O.swiglu_2in_fp8(gb, ub, s_out), gb, ub,
-                                 lambda g, u: O.swiglu_2in_fp8(g, u, s_out), 2e-3)
+    (g64, gb), (u64, ub) = O.qkv_shared_quant_gemm("A8", x, s_in, ws, ss)
+    # codes can differ from the oracle's only where the kernel's own bf16
+    # gate/up differ from the correctly rounded ones, within the binary32
+    # accumulation window of the exact sums
+    wg = accumulation_window(g64, abs_product_sums("A8", x, s_in, ws[0], ss[0]), K)
+    wu = accumulation_window(u64, abs_product_sums("A8", x, s_in, ws[1], ss[1]), K)
+    assert_swiglu_consistent(out, O.swiglu_2in_fp8(gb, ub, s_out), g64, u64, wg, wu, "e4m3", s_out, 2e-3)
 
 
 def test_fused_full_size(W):
@@ -100,7 +101,9 @@ def test_fused_full_size(W):
     xs = host_bits(x[ri])
     qws = [host_u8(w) for w in wq]
     sws = [np.float32(s.item()) for s in sw]
-    (_, gb), (_, ub) = O.qkv_shared_quant_gemm("A8", xs, np.float32(s_in.item()), qws, sws)
+    si = np.float32(s_in.item())
+    (g64, gb), (u64, ub) = O.qkv_shared_quant_gemm("A8", xs, si, qws, sws)
     want = O.swiglu_2in_fp8(gb, ub, np.float32(0.02))
-    assert_swiglu_within_one_ulp(host_u8(fused[ri]), want, gb, ub,
-                                 lambda g, u: O.swiglu_2in_fp8(g, u, np.float32(0.02)), 2e-3)
+    wg = accumulation_window(g64, abs_product_sums("A8", xs, si, qws[0], sws[0]), K)
+    wu = accumulation_window(u64, abs_product_sums("A8", xs, si, qws[1], sws[1]), K)
+    assert_swiglu_consistent(host_u8(fused[ri]), want, g64, u64, wg, wu, "e4m3", np.float32(0.02), 2e-3)
