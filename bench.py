@@ -175,8 +175,7 @@ class Block:
         self.x_qkv, self.x_out, self.x_mlp = (_act(g, dev, M, HID) for _ in range(3))
         self.w = block_weights(g, dev)
         self.run = BlockStep(M, HID, INTER, dev)
-        self.ws = self.run.ws                      # workspace of the bf16-input W8A8 calls
-        self.ws_codes = self.run.ws_codes          # its [M, K] E4M3 codes
+        self.ws = self.run.ws
         self.wsd = torch.empty((2 * INTER * HID,), dtype=torch.bfloat16, device=dev)
 
     # shorthands used by the timings below
@@ -220,13 +219,13 @@ class Block:
             self._lib_w = {k: [(q.view(f8).t(), sc) for q, sc in ws] for k, ws in
                            (("qkv", w.qkv), ("out", [w.out]), ("gu", w.gu), ("down", [w.down]))}
         lw = self._lib_w
-        qa = W.fp8_quant_static(self.x_qkv, w.s_qkv, out=self.ws_codes).view(f8)
+        qa = W.fp8_quant_static(self.x_qkv, w.s_qkv, out=self.ws).view(f8)
         for (w_t, sw), y in zip(lw["qkv"], r.y_qkv):
             torch._scaled_mm(qa, w_t, scale_a=w.s_qkv, scale_b=sw, out_dtype=torch.bfloat16, out=y)
-        qa = W.fp8_quant_static(self.x_out, w.s_out, out=self.ws_codes).view(f8)
+        qa = W.fp8_quant_static(self.x_out, w.s_out, out=self.ws).view(f8)
         torch._scaled_mm(qa, lw["out"][0][0], scale_a=w.s_out, scale_b=lw["out"][0][1],
                          out_dtype=torch.bfloat16, out=r.y_out)
-        qa = W.fp8_quant_static(self.x_mlp, w.s_mlp, out=self.ws_codes).view(f8)
+        qa = W.fp8_quant_static(self.x_mlp, w.s_mlp, out=self.ws).view(f8)
         for (w_t, sw), y in zip(lw["gu"], r.y_gu):
             torch._scaled_mm(qa, w_t, scale_a=w.s_mlp, scale_b=sw, out_dtype=torch.bfloat16, out=y)
         W.swiglu_2in_fp8(r.y_gu[0], r.y_gu[1], w.s_h, out=r.h8)
@@ -450,7 +449,7 @@ def breakdown_ours(W, blk, flush, stream, args):
                flush, stream, n)
     out["fp8_linear_w8a8_4096x4096"] = {"us": ms * 1e3, "TFLOPS": lin_flops / ms / 1e9,
                                         "note": "one projection: quantization + W8A8 GEMM, M=20670"}
-    ms = _time(lambda: W.fp8_quant_static(blk.x_qkv, w.s_qkv, out=blk.ws_codes), flush, stream, n)
+    ms = _time(lambda: W.fp8_quant_static(blk.x_qkv, w.s_qkv, out=blk.ws), flush, stream, n)
     out["fp8_quant_static"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6}
     gu = r.y_gu
     W.fp8_linear_w8a8_group(W.fp8_quant_static(blk.x_mlp, w.s_mlp), w.s_mlp, [q for q, _ in w.gu],
@@ -525,13 +524,13 @@ def breakdown_ours(W, blk, flush, stream, args):
     shift, scale = ((torch.randn((1, HID), generator=gen, device=blk.dev) * 0.5).to(torch.bfloat16)
                     for _ in range(2))
     hb = r.y_qkv[0]
-    ms = _time(lambda: W.ln_modulate_quant(blk.x_qkv, shift, scale, w.s_qkv, out=blk.ws_codes), flush, stream, n)
+    ms = _time(lambda: W.ln_modulate_quant(blk.x_qkv, shift, scale, w.s_qkv, out=blk.ws), flush, stream, n)
     out["ln_modulate_quant"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6,
                                 "note": "LayerNorm + shift/scale + bf16 + E4M3 in one pass, [20670, 4096]"}
 
     def ln_unfused():
         W.ln_modulate_bf16(blk.x_qkv, shift, scale, out=hb)
-        W.fp8_quant_static(hb, w.s_qkv, out=blk.ws_codes)
+        W.fp8_quant_static(hb, w.s_qkv, out=blk.ws)
     ms = _time(ln_unfused, flush, stream, n)
     out["ln_modulate_then_quant"] = {"us": ms * 1e3, "GB_s": 7 * blk.x_qkv.numel() / ms / 1e6,
                                      "note": "the same as two launches (bf16 h through HBM)"}
@@ -541,7 +540,7 @@ def breakdown_ours(W, blk, flush, stream, args):
         xs = blk.x_qkv[:M, :K].contiguous()
         wq0 = wq[0][:N, :K].contiguous()
         y0 = torch.empty((M, N), dtype=torch.bfloat16, device=blk.dev)
-        ws0 = W.a8_workspace(M, K, blk.dev)
+        ws0 = torch.empty((M, K), dtype=torch.uint8, device=blk.dev)
         wsd0 = torch.empty((N * K,), dtype=torch.bfloat16, device=blk.dev)
         fl = 2.0 * M * N * K
         ms8 = _time(lambda: W.fp8_linear_w8a8(xs, wq0, w.s_qkv, sq[0], out=y0, ws=ws0), flush, stream, n)
@@ -702,7 +701,7 @@ def run_case(args):
           .to(torch.float8_e4m3fn).view(torch.uint8) for _ in range(3)]
     ss = [torch.tensor([0.02 * 4 / 448], device=dev) for _ in range(3)]
     ys = [torch.empty((M, HID), dtype=torch.bfloat16, device=dev) for _ in range(3)]
-    qx = W.a8_workspace(M, HID, dev)
+    qx = torch.empty((M, HID), dtype=torch.uint8, device=dev)
     if args.case == "block_gemms":
         # the bench's four GEMM launches of one A8 block step at M=20670
         # (for the DRAM-traffic capture of the dominant kernel)

@@ -80,15 +80,6 @@ typedef struct {
 /* Version of this ABI (bumped on any signature change). */
 int w8_abi_version(void);
 
-/* Bytes of the E4M3 workspace `ws` that a W8A8 call on a bf16 activation of
- * M rows and K columns needs (fp8_linear_w8a8, qkv_shared_quant_gemm in
- * W8_MODE_A8, gate_up_swiglu_fp8): the [M, K] codes of the quantized
- * activation from ws[0] on (row-major, M*K bytes), then, from the next
- * 256-byte boundary, a few progress words (4 * (16 + ceil(M / 128)) bytes,
- * rounded up to 16) that let one GEMM launch quantize the activation ahead
- * of the tiles that read it.  -1 for negative sizes. */
-int64_t w8_a8_workspace_bytes(int64_t M, int64_t K);
-
 /* Thread-local text of the last error returned on this thread ("" if none). */
 const char* w8_last_error(void);
 
@@ -137,14 +128,8 @@ w8_status fp8_quant_static(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
  *           a pre-quantized input goes straight to the GEMM)
  *   w       E4M3 weight [N, K]; s_in, s_w device float scalars
  *   y       bf16 output [M, N], written
- *   ws      scratch of w8_a8_workspace_bytes(M, K) bytes, 16-byte aligned,
- *           required iff x_dtype == W8_DTYPE_BF16, else ignored (may be
- *           NULL); on return its first M*K bytes hold the E4M3 codes of x.
- *           Calls that share a ws must be ordered (one stream, or events).
- * A bf16 activation with 128 < M <= 262144 is quantized by the GEMM launch
- * itself (extra warps write the codes into ws ahead of the tiles that read
- * them); otherwise by fp8_quant_static first.  Codes and outputs are the
- * same either way.
+ *   ws      E4M3 scratch [M, K], required iff x_dtype == W8_DTYPE_BF16,
+ *           else ignored (may be NULL)
  * Errors: NULL, SHAPE (K%16, N%16), DTYPE, ALIGN, ARCH, CUDA.
  */
 w8_status fp8_linear_w8a8(const void* x, int32_t x_dtype, int64_t M, int64_t K, const uint8_t* w,
@@ -176,12 +161,9 @@ w8_status fp8_linear_w8a16(const void* x, int32_t x_dtype, int64_t M, int64_t K,
  * weight scale and contiguous output ([P4] Description and What changed:
  * projections stay split, the shared activation is quantized once and the
  * same FP8 tensor is handed to every projection).
- *   mode == W8_MODE_A8:  one quantization of x into ws and one persistent
- *                        W8A8 launch over the tiles of all G projections,
- *                        all reading ws.  For 128 < M <= 262144 the
- *                        quantization runs inside that launch, ahead of the
- *                        tiles that read each row block; otherwise
- *                        fp8_quant_static runs first.
+ *   mode == W8_MODE_A8:  one fp8_quant_static of x into ws, then one
+ *                        persistent W8A8 launch over the tiles of all G
+ *                        projections, all reading ws.
  *   mode == W8_MODE_A16: no quantization (sharing stands down on 16-bit
  *                        steps, [P4] Denoising-step activation precision).
  *                        With ws: each weight is dequantized into ws
@@ -196,11 +178,9 @@ w8_status fp8_linear_w8a16(const void* x, int32_t x_dtype, int64_t M, int64_t K,
  *   s_in       device float scalar shared by the group (A8 only)
  *   w, N, s_w, y  HOST arrays of G entries: device weight [N_g, K], its row
  *              count, device weight scale, device output [M, N_g]
- *   ws         A8: scratch of w8_a8_workspace_bytes(M, K) bytes, required
- *              (its first M*K bytes receive the E4M3 codes of x).  A16:
- *              optional bf16 scratch of sum_g N_g * K values (2 bytes
- *              each), the dequantized weights of the group in order.
- *              16-byte aligned; calls that share a ws must be ordered.
+ *   ws         A8: E4M3 scratch [M, K], required.  A16: optional bf16
+ *              scratch of sum_g N_g * K values (2 bytes each), the
+ *              dequantized weights of the group in order; 16-byte aligned.
  * Errors: NULL, SHAPE (G outside 2..3 or 1, K%16, N_g%16), ALIGN, ARCH, CUDA.
  */
 w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int64_t K,
@@ -271,8 +251,7 @@ w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const f
  *   x      activation [M, K]: bf16 if x_dtype == W8_DTYPE_BF16 (quantized
  *          first with s_in into `ws`), or E4M3 codes quantized with s_in
  *   w_gate, w_up  E4M3 [I, K];  s_in, s_w_gate, s_w_up, s_out device floats
- *   out    E4M3 [M, I], written;  ws (bf16 input only) scratch of
- *          w8_a8_workspace_bytes(M, K) bytes, receives the codes of x
+ *   out    E4M3 [M, I], written;  ws E4M3 [M, K] scratch (bf16 input only)
  * Errors: NULL, SHAPE (K%16, I%16), DTYPE, ALIGN, ARCH, CUDA.
  */
 w8_status gate_up_swiglu_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t K,

@@ -118,18 +118,6 @@ def test_zero_rows_is_a_noop(L):
     assert L.swiglu_2in_bf16(p16, p16, 0, 16, p16, None) == 0
 
 
-def test_a8_workspace_size(L):
-    """The W8A8 workspace: the [M, K] codes, then from the next 256-byte
-    boundary 4 * (16 + ceil(M / 128)) bytes of progress words, rounded up to 16."""
-    f = L.w8_a8_workspace_bytes
-    for M, K in ((0, 16), (1, 16), (128, 4096), (129, 4096), (20670, 4096), (41340, 16384), (7, 48)):
-        codes = -(-M * K // 256) * 256
-        ctl = -(-(4 * (16 + -(-M // 128))) // 16) * 16
-        assert f(M, K) == codes + ctl
-        assert f(M, K) >= M * K
-    assert f(-1, 16) == -1
-
-
 def test_non_dense_rows_are_refused(L):
     """A row pitch other than the row length is refused with W8_ERR_STRIDE
     before anything else is looked at (TensorRT-LLM PR #17476, Test

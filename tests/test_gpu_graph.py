@@ -49,8 +49,8 @@ def test_block_in_cuda_graph(W):
     mod = [(torch.randn((2, H), generator=gen, device="cuda") * 0.5).to(torch.bfloat16) for _ in range(2)]
     wdg, wdu = W.fp8_dequant_weight(wg[0], wg[1]), W.fp8_dequant_weight(wu[0], wu[1])
     wsd = W.w8a16_workspace([wg[0], wu[0]])
-    ws = W.a8_workspace(M, H, "cuda")
-    ws2 = W.a8_workspace(M, H, "cuda")
+    ws = torch.empty((M, H), dtype=torch.uint8, device="cuda")
+    ws2 = torch.empty((M, H), dtype=torch.uint8, device="cuda")
 
     def block():
         W.qkv_shared_quant_gemm(W.MODE_A8, x, s_in, [q for q, _ in wq], [s for _, s in wq], outs=outs["qkv"], ws=ws)

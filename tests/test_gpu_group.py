@@ -47,12 +47,11 @@ def test_a8_single_quantization_by_storage(W):
     storage: outputs equal separate W8A8 calls fed with the workspace."""
     x, s_in, qws, s_ws = _group(512, 512, (512, 512, 512))
     xd, wd, sd, si = dev_bf16(x), [dev_u8(q) for q in qws], [dev_f32(s) for s in s_ws], dev_f32(s_in)
-    ws = torch.full((W.a8_workspace_bytes(512, 512),), 0xAA, dtype=torch.uint8, device="cuda")
+    ws = torch.full((512, 512), 0xAA, dtype=torch.uint8, device="cuda")
     ys = W.qkv_shared_quant_gemm(W.MODE_A8, xd, si, wd, sd, ws=ws)
-    codes = W.a8_codes(ws, 512, 512)
-    assert np.array_equal(host_u8(codes), O.quant_static(x, s_in))
+    assert np.array_equal(host_u8(ws), O.quant_static(x, s_in))
     for y, w, s in zip(ys, wd, sd):
-        y1 = W.fp8_linear_w8a8(codes, w, si, s)
+        y1 = W.fp8_linear_w8a8(ws, w, si, s)
         assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
 
 

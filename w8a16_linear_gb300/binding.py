@@ -42,7 +42,6 @@ class SwigluParams(ctypes.Structure):
 
 SIGNATURES = {
     "w8_abi_version": (ctypes.c_int, []),
-    "w8_a8_workspace_bytes": (_i64, [_i64, _i64]),
     "w8_last_error": (ctypes.c_char_p, []),
     "w8_device_check": (ctypes.c_int, []),
     "w8_poll_device_error": (ctypes.c_int, [_c_void_p]),
@@ -179,36 +178,6 @@ def selftest_timeout(stream=None):
     _check(lib().w8_selftest_timeout(_stream(stream)))
 
 
-def a8_workspace_bytes(M, K):
-    """Bytes of the workspace a W8A8 call on a bf16 [M, K] activation needs."""
-    return int(lib().w8_a8_workspace_bytes(int(M), int(K)))
-
-
-def a8_workspace(M, K, device):
-    """Caller-side allocation of that workspace (uint8, flat)."""
-    return torch.empty((a8_workspace_bytes(M, K),), dtype=torch.uint8, device=device)
-
-
-def _a8_ws(ws, M, K, device):
-    """The workspace of a bf16-input W8A8 call: allocated when not given,
-    else checked to be a dense byte buffer of the size the library needs."""
-    if ws is None:
-        return a8_workspace(M, K, device)
-    _dense(ws, "ws")
-    if ws.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
-        raise W8Error(5, f"ws: expected a uint8 buffer, got {ws.dtype}")
-    need = a8_workspace_bytes(M, K)
-    if ws.numel() < need:
-        raise W8Error(2, f"ws: {ws.numel()} bytes, a [{M}, {K}] activation needs {need} "
-                         "(w8_a8_workspace_bytes)")
-    return ws.view(torch.uint8)
-
-
-def a8_codes(ws, M, K):
-    """The E4M3 codes [M, K] of the activation a W8A8 call left in its workspace."""
-    return ws.view(torch.uint8)[:M * K].view(M, K)
-
-
 def fp8_quant_static(x, s_in, out=None, stream=None):
     """E4M3 codes (uint8) of ``x / s_in``; same shape as ``x``.  Row pitches
     are passed as they are: a tensor whose rows are not dense is refused by
@@ -296,12 +265,11 @@ def fp8_linear_w8a8(x, w, s_in, s_w, out=None, ws=None, stream=None):
     if out is None:
         out = torch.empty(*x.shape[:-1], N, dtype=torch.bfloat16, device=x.device)
     _as_bf16(out, "out")
-    if dt == DTYPE_BF16:
-        ws = _a8_ws(ws, M, K, x.device)
-    else:
-        ws = None
+    if dt == DTYPE_BF16 and ws is None:
+        ws = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     _check(lib().fp8_linear_w8a8(_ptr(x2), dt, M, K, _ptr(wq), N, _ptr(_scalar(s_in, "s_in")),
-                                 _ptr(_scalar(s_w, "s_w")), _ptr(out), _ptr(ws), _stream(stream)))
+                                 _ptr(_scalar(s_w, "s_w")), _ptr(out),
+                                 _ptr(_as_u8(ws, "ws") if ws is not None else None), _stream(stream)))
     return out
 
 
@@ -338,10 +306,10 @@ def qkv_shared_quant_gemm(mode, x, s_in, weights, weight_scales, outs=None, ws=N
         outs = [torch.empty(*x.shape[:-1], w.shape[0], dtype=torch.bfloat16, device=x.device) for w in ws_q]
     for i, o in enumerate(outs):
         _as_bf16(o, f"y[{i}]")
-    if mode == MODE_A8:
-        ws_p = _ptr(_a8_ws(ws, M, K, x.device))
-    elif ws is None:
-        ws_p = _ptr(None)
+    if mode == MODE_A8 and ws is None:
+        ws = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if mode == MODE_A8 or ws is None:
+        ws_p = _ptr(_as_u8(ws, "ws") if ws is not None else None)
     else:   # A16 with a workspace: room for the group's dequantized bf16 weights
         _as_bf16(ws, "ws")
         need = sum(int(w.shape[0]) * K for w in ws_q)
@@ -445,10 +413,12 @@ def gate_up_swiglu_fp8(x, s_in, w_gate, w_up, s_w_gate, s_w_up, s_out, out=None,
     if out is None:
         out = torch.empty(*x.shape[:-1], I, dtype=torch.uint8, device=x.device)
     o = _as_u8(out, "out")
-    ws = _a8_ws(ws, M, K, x.device) if dt == DTYPE_BF16 else None
+    if dt == DTYPE_BF16 and ws is None:
+        ws = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     _check(lib().gate_up_swiglu_fp8(_ptr(x2), dt, M, K, _ptr(_scalar(s_in, "s_in")), _ptr(wg), _ptr(wu), I,
                                     _ptr(_scalar(s_w_gate, "s_w_gate")), _ptr(_scalar(s_w_up, "s_w_up")),
-                                    _ptr(_scalar(s_out, "s_out")), _ptr(o), _ptr(ws), _stream(stream)))
+                                    _ptr(_scalar(s_out, "s_out")), _ptr(o),
+                                    _ptr(_as_u8(ws, "ws") if ws is not None else None), _stream(stream)))
     return out
 
 

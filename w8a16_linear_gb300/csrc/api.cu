@@ -97,11 +97,6 @@ extern "C" {
 
 int w8_abi_version(void) { return 4; }
 
-int64_t w8_a8_workspace_bytes(int64_t M, int64_t K) {
-  if (M < 0 || K < 0) return -1;
-  return w8::a8_ws_bytes(M, K);
-}
-
 const char* w8_last_error(void) { return g_last_error; }
 
 w8_status w8_device_check(void) {
@@ -173,38 +168,30 @@ w8_status fp8_linear_w8a8(const void* x, int32_t x_dtype, int64_t M, int64_t K, 
   if (M == 0) return ok();
   if (!s_in) return fail(W8_ERR_NULL, "fp8_linear_w8a8: NULL s_in");
   if (x_dtype == W8_DTYPE_BF16) {
-    if (!ws) return fail(W8_ERR_NULL, "fp8_linear_w8a8: bf16 input needs the workspace (w8_a8_workspace_bytes)");
+    if (!ws) return fail(W8_ERR_NULL, "fp8_linear_w8a8: bf16 input needs the [M,K] E4M3 workspace");
     if (!aligned16(ws)) return fail(W8_ERR_ALIGN, "fp8_linear_w8a8: ws must be 16-byte aligned");
   }
   int sms = 0;
   if ((st = device_info(&sms)) != W8_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* qx = static_cast<const uint8_t*>(x);
+  if (x_dtype == W8_DTYPE_BF16) {
+    cudaError_t e = w8::launch_quant_static(static_cast<const uint16_t*>(x), M * K, s_in, ws, sms, s);
+    if (e != cudaSuccess) return cuda_status(e, "fp8_linear_w8a8: quant launch");
+    qx = ws;
+  }
   w8::GemmProblem p{};
   p.M = M;
   p.K = K;
   p.G = 1;
-  p.x = x;
+  p.x = qx;
   p.w[0] = w;
   p.N[0] = N;
   p.s_in = s_in;
   p.s_w[0] = s_w;
   p.y[0] = y;
   int terr = 0;
-  cudaError_t e;
-  if (x_dtype == W8_DTYPE_BF16 && w8::gemm_quant_in_launch(M)) {
-    // one launch: the GEMM quantizes the activation into ws ahead of its tiles
-    p.xq = static_cast<const uint16_t*>(x);
-    p.x = ws;
-    p.qctl = reinterpret_cast<uint32_t*>(ws + w8::a8_codes_bytes(M, K));
-    e = w8::launch_gemm_w8a8_quant(p, sms, s, &terr);
-  } else {
-    if (x_dtype == W8_DTYPE_BF16) {
-      e = w8::launch_quant_static(static_cast<const uint16_t*>(x), M * K, s_in, ws, sms, s);
-      if (e != cudaSuccess) return cuda_status(e, "fp8_linear_w8a8: quant launch");
-      p.x = ws;
-    }
-    e = w8::launch_gemm_w8a8(p, sms, s, &terr);
-  }
+  cudaError_t e = w8::launch_gemm_w8a8(p, sms, s, &terr);
   if (terr) return fail(W8_ERR_ALIGN, "fp8_linear_w8a8: tensor map encoding rejected the operands");
   return cuda_status(e, "fp8_linear_w8a8: GEMM launch");
 }
@@ -261,7 +248,7 @@ w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int6
   if (M == 0) return ok();
   if (mode == W8_MODE_A8) {
     if (!s_in) return fail(W8_ERR_NULL, "qkv_shared_quant_gemm: NULL s_in");
-    if (!ws) return fail(W8_ERR_NULL, "qkv_shared_quant_gemm: A8 needs the workspace (w8_a8_workspace_bytes)");
+    if (!ws) return fail(W8_ERR_NULL, "qkv_shared_quant_gemm: A8 needs the [M,K] E4M3 workspace");
   }
   if (ws && !aligned16(ws)) return fail(W8_ERR_ALIGN, "qkv_shared_quant_gemm: ws must be 16-byte aligned");
   int sms = 0;
@@ -281,20 +268,11 @@ w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int6
   int terr = 0;
   cudaError_t e;
   if (mode == W8_MODE_A8) {
-    // the shared activation is quantized once into ws, and every projection
-    // of the group reads those codes: inside the GEMM launch, ahead of the
-    // tiles that need them, or by the quantization kernel before it
+    e = w8::launch_quant_static(x, M * K, s_in, ws, sms, s);
+    if (e != cudaSuccess) return cuda_status(e, "qkv_shared_quant_gemm: quant launch");
     p.x = ws;
     p.s_in = s_in;
-    if (w8::gemm_quant_in_launch(M)) {
-      p.xq = x;
-      p.qctl = reinterpret_cast<uint32_t*>(ws + w8::a8_codes_bytes(M, K));
-      e = w8::launch_gemm_w8a8_quant(p, sms, s, &terr);
-    } else {
-      e = w8::launch_quant_static(x, M * K, s_in, ws, sms, s);
-      if (e != cudaSuccess) return cuda_status(e, "qkv_shared_quant_gemm: quant launch");
-      e = w8::launch_gemm_w8a8(p, sms, s, &terr);
-    }
+    e = w8::launch_gemm_w8a8(p, sms, s, &terr);
   } else if (ws) {
     // dequant + F.linear: the group's weights into ws, then one bf16 launch
     uint16_t* wd = reinterpret_cast<uint16_t*>(ws);
@@ -432,7 +410,7 @@ w8_status gate_up_swiglu_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t 
   if (!w_up || !s_w_up || !s_in || !s_out) return fail(W8_ERR_NULL, "gate_up_swiglu_fp8: NULL pointer");
   if (!aligned16(w_up)) return fail(W8_ERR_ALIGN, "gate_up_swiglu_fp8: w_up must be 16-byte aligned");
   if (x_dtype == W8_DTYPE_BF16) {
-    if (!ws) return fail(W8_ERR_NULL, "gate_up_swiglu_fp8: bf16 input needs the workspace (w8_a8_workspace_bytes)");
+    if (!ws) return fail(W8_ERR_NULL, "gate_up_swiglu_fp8: bf16 input needs the [M,K] E4M3 workspace");
     if (!aligned16(ws)) return fail(W8_ERR_ALIGN, "gate_up_swiglu_fp8: ws must be 16-byte aligned");
   }
   int sms = 0;

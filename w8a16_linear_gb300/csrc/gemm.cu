@@ -57,7 +57,6 @@
 
 #include "internal.h"
 #include "ptx.cuh"
-#include "quant_spec.cuh"
 #include "swiglu_spec.cuh"
 
 namespace w8 {
@@ -71,12 +70,10 @@ constexpr uint32_t kTmemCols = 512;               // two 256-column F32 accumula
 constexpr uint32_t kAccCols = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kEpiBufBytes = 32 * 128;            // W8A8 staging: 32 rows x 64 bf16
-constexpr int kQuantMaskWords = kQuantMaxRowBlocks / 32;
-constexpr int kQuantUnroll = 8;                   // 16-column vectors in flight per lane
 
 enum class Mode { W8A8, GLU, BF16, GLU16 };
 
-template <Mode MODE, int CG, bool Q = false>
+template <Mode MODE, int CG>
 struct Cfg {
   static constexpr bool kGlu = (MODE == Mode::GLU || MODE == Mode::GLU16);
   // BF16: the W8A16 product on an already dequantized weight (bf16 x bf16,
@@ -115,14 +112,11 @@ struct Cfg {
   static constexpr int kEpiBuf = kOut16 ? 32 * 128 : (kGlu ? 32 * 64 : kEpiBufBytes);
   static constexpr int kEpiNBuf = 2;
   static constexpr int kEpiBytes = kEpiWarps * kEpiNBuf * kEpiBuf;
-  // Q: warps that quantize the bf16 activation inside the launch, ahead of
-  // the tiles that read it.
-  static constexpr int kQuantWarps = Q ? 8 : 0;
 };
 
-template <Mode MODE, int CG, bool Q = false>
+template <Mode MODE, int CG>
 struct Layout {
-  using C = Cfg<MODE, CG, Q>;
+  using C = Cfg<MODE, CG>;
   static constexpr int kA = 0;
   static constexpr int kB = kA + C::kStages * C::kABytes;
   static constexpr int kEpi = kB + C::kStages * C::kBBytes;
@@ -131,11 +125,9 @@ struct Layout {
   static constexpr int kNumBars = 2 * C::kStages + 5;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  // Q: one bit per 128-row block that this CTA's producer has seen quantized
-  static constexpr int kRbMask = kAbort + 4;
-  static constexpr int kEnd = kRbMask + (Q ? 4 * kQuantMaskWords : 0);
+  static constexpr int kEnd = kAbort + 4;
   static constexpr int kAlloc = kEnd + 1024;  // slack for 1024-byte alignment
-  static constexpr int kThreads = (2 + C::kEpiWarps + C::kQuantWarps) * 32;
+  static constexpr int kThreads = (2 + C::kEpiWarps) * 32;
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -152,45 +144,26 @@ struct Args {
   int tiles_n[kMaxGroup];
   int tiles_per_m;
   int tiles_m;
-  int group_m;         // m-blocks swept together down each column of tiles
-  int first_group_m;   // m-blocks of the first group (may be smaller)
+  int group_m;   // m-blocks swept together down each column of tiles
   int num_tiles;
   int num_kb;
   const float* s_in;
   const float* s_w[kMaxGroup];
   const float* s_out;  // GLU: the down projection's input scale
-  // Q: the bf16 activation [M, K] the launch quantizes with s_in into qx (the
-  // memory the A operand's tensor map reads); qctl[0] hands out 4-row units,
-  // qctl[kQctlRows + rb] counts the units of 128-row block rb written so far.
-  const uint16_t* xq;
-  uint8_t* qx;
-  uint32_t* qctl;
-  int n_units;
 };
 
 // Tile t -> first output row of the (cluster) tile, projection, first column.
-// Tiles are rasterised in groups of `group_m` m-blocks (the first group has
-// `first_group_m`): within a group the m-block varies fastest, then the
-// column of tiles (projection, n-block), so the CTAs running at the same time
-// share each weight tile through L2 and the group's activation rows stay
-// L2-resident while it sweeps the columns.
+// Tiles are rasterised in groups of `group_m` m-blocks: within a group the
+// m-block varies fastest, then the column of tiles (projection, n-block), so
+// the CTAs running at the same time share each weight tile through L2 and
+// the group's activation rows stay L2-resident while it sweeps the columns.
 __device__ __forceinline__ void decode_tile(const Args& a, int t, int rows_per_tile, int cols_per_tile,
                                             int& m0, int& g, int& n0) {
-  const int g0 = min(a.first_group_m, a.tiles_m);
-  const int first = g0 * a.tiles_per_m;
-  int mb0, gm, rr;
-  if (t < first) {
-    mb0 = 0;
-    gm = g0;
-    rr = t;
-  } else {
-    const int per_group = a.group_m * a.tiles_per_m;
-    const int tt = t - first;
-    const int grp = tt / per_group;
-    mb0 = g0 + grp * a.group_m;
-    gm = min(a.group_m, a.tiles_m - mb0);
-    rr = tt - grp * per_group;
-  }
+  const int per_group = a.group_m * a.tiles_per_m;
+  const int grp = t / per_group;
+  const int mb0 = grp * a.group_m;
+  const int gm = min(a.group_m, a.tiles_m - mb0);
+  const int rr = t - grp * per_group;
   int r = rr / gm;                       // column of tiles
   const int mb = mb0 + (rr - r * gm);
   g = 0;
@@ -200,27 +173,6 @@ __device__ __forceinline__ void decode_tile(const Args& a, int t, int rows_per_t
   }
   m0 = mb * rows_per_tile;
   n0 = r * cols_per_tile;
-}
-
-// Q: waits (bounded) until the count at `p` reaches `need`, then orders this
-// thread's later TMA reads after the data the count published.
-__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need, volatile int* abort,
-                                           uint64_t limit_ns) {
-  if (ld_acquire(p) < need) {
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-      __nanosleep(128);
-      if (ld_acquire(p) >= need) break;
-      if (*abort || globaltimer_ns() - t0 > limit_ns) return false;
-    }
-  }
-  fence_proxy_async_global();
-  return true;
-}
-
-// Units (4 rows each) of the 128-row block rb.
-__device__ __forceinline__ uint32_t units_in_block(const Args& a, int rb) {
-  return (uint32_t)((min(128, a.M - rb * 128) + 3) >> 2);
 }
 
 __device__ __forceinline__ const CUtensorMap* map_b(const Maps& m, int g) {
@@ -238,11 +190,11 @@ __device__ __forceinline__ void record_timeout(volatile int* abort) {
   atomicOr(&g_gemm_err, kErrTimeout);
 }
 
-template <Mode MODE, int CG, bool Q>
-__global__ void __launch_bounds__(Layout<MODE, CG, Q>::kThreads, 1)
+template <Mode MODE, int CG>
+__global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Args args) {
-  using C = Cfg<MODE, CG, Q>;
-  using L = Layout<MODE, CG, Q>;
+  using C = Cfg<MODE, CG>;
+  using L = Layout<MODE, CG>;
   constexpr int S = C::kStages;
   constexpr bool kGlu = C::kGlu;
 
@@ -279,10 +231,6 @@ __global__ void __launch_bounds__(Layout<MODE, CG, Q>::kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     *abort = 0;
-    if constexpr (Q) {
-      uint32_t* mask = reinterpret_cast<uint32_t*>(smem + L::kRbMask);
-      for (int i = 0; i < kQuantMaskWords; ++i) mask[i] = 0u;
-    }
     fence_mbar_init();
     prefetch_tensormap(&maps.a);
     for (int g = 0; g < (kGlu ? 2 : args.G); ++g) prefetch_tensormap(map_b(maps, g));
@@ -310,27 +258,10 @@ __global__ void __launch_bounds__(Layout<MODE, CG, Q>::kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued = 0;
       bool ok = true;
-      uint32_t* rb_seen = reinterpret_cast<uint32_t*>(smem + L::kRbMask);
       for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
         int m0, g, n0;
         decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
         const int a_row = m0 + (int)rank * BM;
-        if constexpr (Q) {
-          // The first load of a 128-row block waits until the quantization
-          // warps (of any CTA) have written all its rows.
-          if (a_row < args.M) {
-            const int rb = a_row >> 7;
-            const uint32_t bit = 1u << (rb & 31);
-            if (!(rb_seen[rb >> 5] & bit)) {
-              if (!wait_count(args.qctl + kQctlRows + rb, units_in_block(args, rb), abort, kWaitLimitNs)) {
-                record_timeout(abort);
-                ok = false;
-                break;
-              }
-              rb_seen[rb >> 5] |= bit;
-            }
-          }
-        }
         // W8A8: this CTA's half (pair) or all of the tile's weight rows.
         // GLU: the slice's rows n0 .. n0+127 of gate (even CTA / first half)
         // and of up (odd CTA / second half).
@@ -438,7 +369,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG, Q>::kThreads, 1)
       volatile int never = 0;
       if (!mbar_wait(drain_bar, 0, &never, kWaitLimitNs)) atomicOr(&g_gemm_err, kErrTimeout);
     }
-  } else if (warp < 2 + C::kEpiWarps) {
+  } else {
     // ---------------------------------------------------------------- epilogue
     const int wq = warp & 3;              // TMEM lane quadrant this warp may access
     constexpr int EB = C::kEpiBuf;
@@ -630,69 +561,6 @@ __global__ void __launch_bounds__(Layout<MODE, CG, Q>::kThreads, 1)
       }
     }
     if (lane == 0) tma_store_wait_all();
-  } else if constexpr (Q) {
-    // ---------------------------------------------------------------- quantization
-    // q = E4M3_satRNE(fl32(x / s_in)) of the activation, 4 rows per unit;
-    // units are claimed in row order from one counter, so the rows the
-    // first tiles need are written first and no CTA depends on another one
-    // being resident.  The first quantization warp of each CTA starts at
-    // once; the others join when the first group's rows are written, so
-    // those go out at full speed.  After a unit's stores every lane fences
-    // them for the tensor-memory-accelerator reads, and lane 0 publishes
-    // the unit with a release add on its 128-row block's count.
-    const int qw = warp - (2 + C::kEpiWarps);
-    const float sq = __ldg(args.s_in);
-    const float rq = __frcp_rn(sq);
-    const bool exact_only = !scale_is_fast(sq, rq);
-    if (qw != 0) {
-      const int rb_first = min(2 * min(args.first_group_m, args.tiles_m), (args.M + 127) >> 7);
-      for (int rb = 0; rb < rb_first; ++rb) {
-        bool ready = true;
-        if (lane == 0) ready = wait_count(args.qctl + kQctlRows + rb, units_in_block(args, rb), abort, kWaitLimitNs);
-        if (!__shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0)) break;  // join anyway; nothing depends on this wait
-      }
-    }
-    const int K = args.K;
-    const int nch = (K + 511) >> 9;   // 512-column chunks of a row (16 columns per lane)
-    const int nseg = 4 * nch;
-    for (;;) {
-      if (*abort) break;
-      uint32_t u = 0;
-      if (lane == 0) u = atomicAdd(args.qctl, 1u);
-      u = __shfl_sync(0xFFFFFFFFu, u, 0);
-      if (u >= (uint32_t)args.n_units) break;
-      const int row0 = (int)u * 4;
-      const int rows = min(4, args.M - row0);
-      for (int s0 = 0; s0 < nseg; s0 += kQuantUnroll) {
-        uint4 va[kQuantUnroll], vb[kQuantUnroll];
-        int64_t off[kQuantUnroll];
-#pragma unroll
-        for (int j = 0; j < kQuantUnroll; ++j) {
-          const int sg = s0 + j;
-          const int rr = sg / nch;
-          const int col = (sg - rr * nch) * 512 + lane * 16;
-          off[j] = (sg < nseg && rr < rows && col < K) ? (int64_t)(row0 + rr) * K + col : -1;
-          if (off[j] >= 0) {
-            va[j] = ldg16(args.xq + off[j]);
-            vb[j] = ldg16(args.xq + off[j] + 8);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kQuantUnroll; ++j) {
-          if (off[j] < 0) continue;
-          uint4 o;
-          o.x = quant_pair(va[j].x, sq, rq, exact_only) | (quant_pair(va[j].y, sq, rq, exact_only) << 16);
-          o.y = quant_pair(va[j].z, sq, rq, exact_only) | (quant_pair(va[j].w, sq, rq, exact_only) << 16);
-          o.z = quant_pair(vb[j].x, sq, rq, exact_only) | (quant_pair(vb[j].y, sq, rq, exact_only) << 16);
-          o.w = quant_pair(vb[j].z, sq, rq, exact_only) | (quant_pair(vb[j].w, sq, rq, exact_only) << 16);
-          *reinterpret_cast<uint4*>(args.qx + off[j]) = o;
-        }
-      }
-      fence_proxy_async_global();
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) red_release_add(args.qctl + kQctlRows + (row0 >> 7), 1u);
-    }
   }
 
   tc_fence_before();
@@ -1024,10 +892,10 @@ cudaError_t launch_cluster(void (*kern)(Maps, Args), int grid, int threads, int 
   return cudaGetLastError();
 }
 
-template <Mode MODE, int CG, bool Q = false>
+template <Mode MODE, int CG>
 cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  using C = Cfg<MODE, CG, Q>;
-  using L = Layout<MODE, CG, Q>;
+  using C = Cfg<MODE, CG>;
+  using L = Layout<MODE, CG>;
   constexpr bool kGlu = C::kGlu;
   *tmap_err = 0;
   Maps maps;
@@ -1069,21 +937,9 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   args.num_tiles = tiles_m * args.tiles_per_m;
   args.tiles_m = tiles_m;
   args.group_m = group_rows(BM * CG, p.K, kEl, tiles_m);
-  args.first_group_m = args.group_m;
-  if constexpr (Q) {
-    // A first group of two m-blocks: the first wave of tiles needs only the
-    // rows the quantization warps write first.
-    args.first_group_m = args.group_m < 2 ? args.group_m : 2;
-    args.xq = p.xq;
-    args.qx = static_cast<uint8_t*>(const_cast<void*>(p.x));
-    args.qctl = p.qctl;
-    args.n_units = (int)((p.M + 3) / 4);
-    cudaError_t e = cudaMemsetAsync(p.qctl, 0, (size_t)a8_ctl_bytes(p.M), st);
-    if (e != cudaSuccess) return e;
-  }
   const int max_clusters = sms / CG;
   const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
-  return launch_cluster(gemm_kernel<MODE, CG, Q>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
+  return launch_cluster(gemm_kernel<MODE, CG>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
                         args);
 }
 
@@ -1122,7 +978,6 @@ cudaError_t launch_a16t(const GemmProblem& p, int sms, cudaStream_t st, int* tma
   args.num_tiles = tiles_m * args.tiles_per_m;
   args.tiles_m = tiles_m;
   args.group_m = group_rows(BT, p.K, 2, tiles_m);
-  args.first_group_m = args.group_m;
   const int grid = args.num_tiles < sms ? args.num_tiles : sms;
   cudaError_t e =
       cudaFuncSetAttribute(gemm_a16t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
@@ -1156,12 +1011,6 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
 cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
   return use_pair(p) ? launch<Mode::W8A8, 2>(p, sms, st, tmap_err)
                      : launch<Mode::W8A8, 1>(p, sms, st, tmap_err);
-}
-
-bool gemm_quant_in_launch(int64_t M) { return M > BM && M <= (int64_t)kQuantMaxRowBlocks * 128; }
-
-cudaError_t launch_gemm_w8a8_quant(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
-  return launch<Mode::W8A8, 2, true>(p, sms, st, tmap_err);
 }
 
 cudaError_t launch_gemm_bf16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {

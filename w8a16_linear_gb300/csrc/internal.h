@@ -45,16 +45,6 @@ cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bo
 // ---- GEMMs (gemm.cu)
 constexpr int kMaxGroup = 3;
 
-// Workspace of a W8A8 call on a bf16 activation: the [M, K] E4M3 codes of the
-// activation, then, from the next 256-byte boundary, the control words of
-// the quantization the GEMM launch does itself: word 0 hands out 4-row
-// units, word kQctlRows + rb counts the units of 128-row block rb written.
-constexpr int kQctlRows = 16;
-constexpr int kQuantMaxRowBlocks = 2048;   // in-launch quantization for M <= 262144
-inline int64_t a8_codes_bytes(int64_t M, int64_t K) { return (M * K + 255) / 256 * 256; }
-inline int64_t a8_ctl_bytes(int64_t M) { return (4 * (kQctlRows + (M + 127) / 128) + 15) / 16 * 16; }
-inline int64_t a8_ws_bytes(int64_t M, int64_t K) { return a8_codes_bytes(M, K) + a8_ctl_bytes(M); }
-
 struct GemmProblem {
   int64_t M, K;
   int G;                         // projections sharing the activation (1..3)
@@ -65,22 +55,11 @@ struct GemmProblem {
   const float* s_w[kMaxGroup];
   void* y[kMaxGroup];            // bf16 [M, N_g] (GLU: E4M3 [M, I])
   const float* s_out;            // GLU: input scale of the down projection
-  // W8A8 with the quantization in the launch: the bf16 activation [M, K];
-  // x then points at the E4M3 codes the launch writes, qctl at the control
-  // words after them (a8_ws_bytes layout), zeroed by the launcher.
-  const uint16_t* xq;
-  uint32_t* qctl;
 };
 
 // Returns cudaSuccess or the CUDA error; *tmap_err is set non-zero when a
 // tensor map could not be encoded.
 cudaError_t launch_gemm_w8a8(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
-// The W8A8 GEMM quantizing its own bf16 activation (p.xq) into p.x with
-// p.s_in ahead of the tiles that read it: one launch (after a small memset of
-// p.qctl) with the same codes and outputs as the quantization kernel followed
-// by launch_gemm_w8a8.  Only where gemm_quant_in_launch(M) holds.
-bool gemm_quant_in_launch(int64_t M);
-cudaError_t launch_gemm_w8a8_quant(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 cudaError_t launch_gemm_w8a16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err);
 // Gate/up W8A8 GEMMs with the SwiGLU-to-E4M3 epilogue: x E4M3 [M,K], w[0] gate
 // and w[1] up [I,K] with s_w[0], s_w[1]; N[0] = I; y[0] E4M3 [M,I]; s_out.

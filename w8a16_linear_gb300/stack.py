@@ -29,8 +29,6 @@ from typing import List, Tuple
 
 import torch
 
-from . import binding
-
 
 @dataclass
 class BlockWeights:
@@ -60,10 +58,7 @@ class BlockStep:
         self.y_down = torch.empty((M, H), **bf)
         self.h8 = torch.empty((M, I), **u8)
         self.h16 = torch.empty((M, I), **bf)
-        # workspace of the bf16-input W8A8 calls (the quantized activation
-        # and the progress words of the in-launch quantization)
-        self.ws = torch.empty((binding.a8_workspace_bytes(M, H),), **u8)
-        self.ws_codes = self.ws[:M * H].view(M, H)
+        self.ws = torch.empty((M, H), **u8)
         self.q_out = torch.empty((M, H), **u8)
         self.q_mlp = torch.empty((M, H), **u8)
         self._y_gu = None
