@@ -46,64 +46,122 @@ namespace {
 // quant_pair / quant_pair_exact (quant_spec.cuh): the specification's codes
 // of one packed bf16 pair.
 
-__global__ void __launch_bounds__(256, 8) quant_static_kernel(const uint16_t* __restrict__ x,
-                                                              int64_t n16,
+// Work distribution of the elementwise kernels: 16-element vectors, U per
+// thread per iteration, taken a grid stride apart (vector i + j * stride for
+// j < U), so each load instruction of a warp covers contiguous memory and a
+// thread has all U vectors' loads in flight before it converts any of them.
+// Blocks per SM that each kernel's launch bounds are written for.  Measured
+// at the bench's sizes (20670x4096, 16384x4096, 20670x16384): one vector per
+// iteration with 4 blocks per SM for the quantization and the two SwiGLU
+// kernels, two with 4 blocks for the (write-heavy) dequantization, one with 6
+// blocks for the SwiGLU options; 2-4 vectors per iteration, or the full
+// 8 / 6 blocks per SM, measured 1-10% slower.
+constexpr int kQuantU = 1, kQuantBlocks = 4;
+constexpr int kDequantU = 2, kDequantBlocks = 4;
+constexpr int kSwigluU = 1, kSwigluBlocks = 4;
+constexpr int kSwigluExU = 1, kSwigluExBlocks = 6;
+
+template <int U>
+__global__ void __launch_bounds__(256, kQuantBlocks) quant_static_kernel(const uint16_t* __restrict__ x, int64_t n16,
                                                               const float* __restrict__ s_in,
                                                               uint8_t* __restrict__ q) {
+  griddep_launch_dependents();   // a GEMM launched next may start its prologue
   const float s = __ldg(s_in);
   const float r = __frcp_rn(s);
   const bool exact_only = !scale_is_fast(s, r);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-    const uint4 a = ldg16(x + i * 16);
-    const uint4 b = ldg16(x + i * 16 + 8);
-    uint4 o;
-    o.x = quant_pair(a.x, s, r, exact_only) | (quant_pair(a.y, s, r, exact_only) << 16);
-    o.y = quant_pair(a.z, s, r, exact_only) | (quant_pair(a.w, s, r, exact_only) << 16);
-    o.z = quant_pair(b.x, s, r, exact_only) | (quant_pair(b.y, s, r, exact_only) << 16);
-    o.w = quant_pair(b.z, s, r, exact_only) | (quant_pair(b.w, s, r, exact_only) << 16);
-    *reinterpret_cast<uint4*>(q + i * 16) = o;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
+    uint4 a[U], b[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v < n16) {
+        a[j] = ldg16(x + v * 16);
+        b[j] = ldg16(x + v * 16 + 8);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v >= n16) break;
+      uint4 o;
+      o.x = quant_pair(a[j].x, s, r, exact_only) | (quant_pair(a[j].y, s, r, exact_only) << 16);
+      o.y = quant_pair(a[j].z, s, r, exact_only) | (quant_pair(a[j].w, s, r, exact_only) << 16);
+      o.z = quant_pair(b[j].x, s, r, exact_only) | (quant_pair(b[j].y, s, r, exact_only) << 16);
+      o.w = quant_pair(b[j].z, s, r, exact_only) | (quant_pair(b[j].w, s, r, exact_only) << 16);
+      *reinterpret_cast<uint4*>(q + v * 16) = o;
+    }
   }
 }
 
-__global__ void __launch_bounds__(256, 6) swiglu_fp8_kernel(const uint16_t* __restrict__ g,
-                                                            const uint16_t* __restrict__ u,
-                                                            int64_t n16,
+template <int U>
+__global__ void __launch_bounds__(256, kSwigluBlocks) swiglu_fp8_kernel(const uint16_t* __restrict__ g,
+                                                            const uint16_t* __restrict__ u, int64_t n16,
                                                             const float* __restrict__ s_out,
                                                             uint8_t* __restrict__ out) {
+  griddep_launch_dependents();   // a GEMM launched next may start its prologue
   const float s = __ldg(s_out);
   const float rs = __frcp_rn(s);
   const bool exact_only = !swiglu_fp8_scale_is_fast(s, rs);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-    const uint4 ga = ldg16(g + i * 16), gb = ldg16(g + i * 16 + 8);
-    const uint4 ua = ldg16(u + i * 16), ub = ldg16(u + i * 16 + 8);
-    uint4 o;
-    o.x = swiglu_fp8_pair(ga.x, ua.x, s, rs, exact_only) |
-          (swiglu_fp8_pair(ga.y, ua.y, s, rs, exact_only) << 16);
-    o.y = swiglu_fp8_pair(ga.z, ua.z, s, rs, exact_only) |
-          (swiglu_fp8_pair(ga.w, ua.w, s, rs, exact_only) << 16);
-    o.z = swiglu_fp8_pair(gb.x, ub.x, s, rs, exact_only) |
-          (swiglu_fp8_pair(gb.y, ub.y, s, rs, exact_only) << 16);
-    o.w = swiglu_fp8_pair(gb.z, ub.z, s, rs, exact_only) |
-          (swiglu_fp8_pair(gb.w, ub.w, s, rs, exact_only) << 16);
-    *reinterpret_cast<uint4*>(out + i * 16) = o;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
+    uint4 ga[U], gb[U], ua[U], ub[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v < n16) {
+        ga[j] = ldg16(g + v * 16);
+        gb[j] = ldg16(g + v * 16 + 8);
+        ua[j] = ldg16(u + v * 16);
+        ub[j] = ldg16(u + v * 16 + 8);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v >= n16) break;
+      uint4 o;
+      o.x = swiglu_fp8_pair(ga[j].x, ua[j].x, s, rs, exact_only) |
+            (swiglu_fp8_pair(ga[j].y, ua[j].y, s, rs, exact_only) << 16);
+      o.y = swiglu_fp8_pair(ga[j].z, ua[j].z, s, rs, exact_only) |
+            (swiglu_fp8_pair(ga[j].w, ua[j].w, s, rs, exact_only) << 16);
+      o.z = swiglu_fp8_pair(gb[j].x, ub[j].x, s, rs, exact_only) |
+            (swiglu_fp8_pair(gb[j].y, ub[j].y, s, rs, exact_only) << 16);
+      o.w = swiglu_fp8_pair(gb[j].z, ub[j].z, s, rs, exact_only) |
+            (swiglu_fp8_pair(gb[j].w, ub[j].w, s, rs, exact_only) << 16);
+      *reinterpret_cast<uint4*>(out + v * 16) = o;
+    }
   }
 }
 
-__global__ void __launch_bounds__(256, 6) swiglu_bf16_kernel(const uint16_t* __restrict__ g,
-                                                             const uint16_t* __restrict__ u,
-                                                             int64_t n16,
+template <int U>
+__global__ void __launch_bounds__(256, kSwigluBlocks) swiglu_bf16_kernel(const uint16_t* __restrict__ g,
+                                                             const uint16_t* __restrict__ u, int64_t n16,
                                                              uint16_t* __restrict__ out) {
+  griddep_launch_dependents();   // a GEMM launched next may start its prologue
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-    const uint4 ga = ldg16(g + i * 16), gb = ldg16(g + i * 16 + 8);
-    const uint4 ua = ldg16(u + i * 16), ub = ldg16(u + i * 16 + 8);
-    uint4* dst = reinterpret_cast<uint4*>(out + i * 16);
-    dst[0] = make_uint4(swiglu_bf16_pair(ga.x, ua.x), swiglu_bf16_pair(ga.y, ua.y),
-                        swiglu_bf16_pair(ga.z, ua.z), swiglu_bf16_pair(ga.w, ua.w));
-    dst[1] = make_uint4(swiglu_bf16_pair(gb.x, ub.x), swiglu_bf16_pair(gb.y, ub.y),
-                        swiglu_bf16_pair(gb.z, ub.z), swiglu_bf16_pair(gb.w, ub.w));
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
+    uint4 ga[U], gb[U], ua[U], ub[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v < n16) {
+        ga[j] = ldg16(g + v * 16);
+        gb[j] = ldg16(g + v * 16 + 8);
+        ua[j] = ldg16(u + v * 16);
+        ub[j] = ldg16(u + v * 16 + 8);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v >= n16) break;
+      uint4* dst = reinterpret_cast<uint4*>(out + v * 16);
+      dst[0] = make_uint4(swiglu_bf16_pair(ga[j].x, ua[j].x), swiglu_bf16_pair(ga[j].y, ua[j].y),
+                          swiglu_bf16_pair(ga[j].z, ua[j].z), swiglu_bf16_pair(ga[j].w, ua[j].w));
+      dst[1] = make_uint4(swiglu_bf16_pair(gb[j].x, ub[j].x), swiglu_bf16_pair(gb[j].y, ub[j].y),
+                          swiglu_bf16_pair(gb[j].z, ub[j].z), swiglu_bf16_pair(gb[j].w, ub[j].w));
+    }
   }
 }
 
@@ -113,37 +171,49 @@ __global__ void __launch_bounds__(256, 6) swiglu_bf16_kernel(const uint16_t* __r
 // ("dequant + F.linear").  E4M3 -> f16 is exact (cvt e4m3x2 -> f16x2), f16 ->
 // f32 exact, one correctly rounded binary32 multiply, one bf16 rounding.
 
-__global__ void __launch_bounds__(256, 8) dequant_weight_kernel(const uint8_t* __restrict__ q, int64_t n16,
+template <int U>
+__global__ void __launch_bounds__(256, kDequantBlocks) dequant_weight_kernel(const uint8_t* __restrict__ q, int64_t n16,
                                                                 const float* __restrict__ s_w,
                                                                 uint16_t* __restrict__ wd) {
+  griddep_launch_dependents();   // a GEMM launched next may start its prologue
   const float sw = __ldg(s_w);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-    const uint4 c = ldg16(q + i * 16);
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    uint32_t o[8];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
+    uint4 c[U];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] & 0xFFFF));
-      const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] >> 16));
-      F2 a, b;
-      f16x2_to_f32(f01, a.x, a.y);
-      f16x2_to_f32(f23, b.x, b.y);
-      a = mul2(a, splat(sw));
-      b = mul2(b, splat(sw));
-      o[2 * e] = cvt_bf16x2(a.x, a.y);
-      o[2 * e + 1] = cvt_bf16x2(b.x, b.y);
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v < n16) c[j] = ldg16(q + v * 16);
     }
-    uint4* dst = reinterpret_cast<uint4*>(wd + i * 16);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v >= n16) break;
+      const uint32_t cw[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] & 0xFFFF));
+        const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] >> 16));
+        F2 a, b;
+        f16x2_to_f32(f01, a.x, a.y);
+        f16x2_to_f32(f23, b.x, b.y);
+        a = mul2(a, splat(sw));
+        b = mul2(b, splat(sw));
+        o[2 * e] = cvt_bf16x2(a.x, a.y);
+        o[2 * e + 1] = cvt_bf16x2(b.x, b.y);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(wd + v * 16);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
   }
 }
 
 // The SwiGLU variants (swiglu_spec.cuh): bf16 or binary16 inputs, FP8 output
 // or a 16-bit output in the input's format.
-template <bool kF16, bool kFp8>
-__global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __restrict__ g,
+template <bool kF16, bool kFp8, int U>
+__global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const uint16_t* __restrict__ g,
                                                            const uint16_t* __restrict__ u,
                                                            int64_t n16, SwigluParams pr,
                                                            const float* __restrict__ s_out,
@@ -156,24 +226,38 @@ __global__ void __launch_bounds__(256, 6) swiglu_ex_kernel(const uint16_t* __res
     exact_only = !swiglu_fp8_scale_is_fast(s, rs);
   }
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-    const uint4 ga = ldg16(g + i * 16), gb = ldg16(g + i * 16 + 8);
-    const uint4 ua = ldg16(u + i * 16), ub = ldg16(u + i * 16 + 8);
-    const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-    const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
-    if constexpr (kFp8) {
-      uint32_t c[8];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
+    uint4 ga[U], gb[U], ua[U], ub[U];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = swiglu_ex_fp8_pair<kF16>(gw[j], uw[j], pr, s, rs, exact_only);
-      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + i * 16) =
-          make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
-    } else {
-      uint32_t h[8];
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v < n16) {
+        ga[j] = ldg16(g + v * 16);
+        gb[j] = ldg16(g + v * 16 + 8);
+        ua[j] = ldg16(u + v * 16);
+        ub[j] = ldg16(u + v * 16 + 8);
+      }
+    }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) h[j] = swiglu_ex_16_pair<kF16>(gw[j], uw[j], pr);
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + i * 16);
-      dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-      dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = i + j * stride;
+      if (v >= n16) break;
+      const uint32_t gw[8] = {ga[j].x, ga[j].y, ga[j].z, ga[j].w, gb[j].x, gb[j].y, gb[j].z, gb[j].w};
+      const uint32_t uw[8] = {ua[j].x, ua[j].y, ua[j].z, ua[j].w, ub[j].x, ub[j].y, ub[j].z, ub[j].w};
+      if constexpr (kFp8) {
+        uint32_t c[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = swiglu_ex_fp8_pair<kF16>(gw[e], uw[e], pr, s, rs, exact_only);
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + v * 16) =
+            make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
+      } else {
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = swiglu_ex_16_pair<kF16>(gw[e], uw[e], pr);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + v * 16);
+        dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+      }
     }
   }
 }
@@ -439,13 +523,13 @@ __global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel
 // on the GPU at once (blocks beyond that would run as a second, partly
 // occupied wave, which an HBM-bound kernel cannot afford), fewer for small
 // inputs.  The per-SM figure is the occupancy of `kern`, looked up once.
-int grid_for(const void* kern, std::atomic<int>* per_sm, int64_t n16, int sms) {
+int grid_for(const void* kern, std::atomic<int>* per_sm, int64_t n16, int sms, int u = 1) {
   int b = per_sm->load(std::memory_order_relaxed);
   if (b == 0) {   // first call: look the figure up (threads racing here store the same value)
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, 256, 0) != cudaSuccess || b < 1) b = 1;
     per_sm->store(b, std::memory_order_relaxed);
   }
-  const int64_t want = (n16 + 255) / 256;
+  const int64_t want = (n16 + 256 * u - 1) / (256 * u);
   const int64_t cap = (int64_t)sms * b;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
@@ -460,19 +544,19 @@ cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bo
   static std::atomic<int> occ[4];
   if (in_f16) {
     if (out_fp8) {
-      auto k = swiglu_ex_kernel<true, true>;
-      k<<<grid_for((const void*)k, &occ[0], n16, sms), 256, 0, st>>>(g, u, n16, pr, s_out, out);
+      auto k = swiglu_ex_kernel<true, true, kSwigluExU>;
+      k<<<grid_for((const void*)k, &occ[0], n16, sms, kSwigluExU), 256, 0, st>>>(g, u, n16, pr, s_out, out);
     } else {
-      auto k = swiglu_ex_kernel<true, false>;
-      k<<<grid_for((const void*)k, &occ[1], n16, sms), 256, 0, st>>>(g, u, n16, pr, s_out, out);
+      auto k = swiglu_ex_kernel<true, false, kSwigluExU>;
+      k<<<grid_for((const void*)k, &occ[1], n16, sms, kSwigluExU), 256, 0, st>>>(g, u, n16, pr, s_out, out);
     }
   } else {
     if (out_fp8) {
-      auto k = swiglu_ex_kernel<false, true>;
-      k<<<grid_for((const void*)k, &occ[2], n16, sms), 256, 0, st>>>(g, u, n16, pr, s_out, out);
+      auto k = swiglu_ex_kernel<false, true, kSwigluExU>;
+      k<<<grid_for((const void*)k, &occ[2], n16, sms, kSwigluExU), 256, 0, st>>>(g, u, n16, pr, s_out, out);
     } else {
-      auto k = swiglu_ex_kernel<false, false>;
-      k<<<grid_for((const void*)k, &occ[3], n16, sms), 256, 0, st>>>(g, u, n16, pr, s_out, out);
+      auto k = swiglu_ex_kernel<false, false, kSwigluExU>;
+      k<<<grid_for((const void*)k, &occ[3], n16, sms, kSwigluExU), 256, 0, st>>>(g, u, n16, pr, s_out, out);
     }
   }
   return cudaGetLastError();
@@ -482,8 +566,8 @@ cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w,
                                   cudaStream_t st) {
   const int64_t n16 = n / 16;
   static std::atomic<int> occ{0};
-  dequant_weight_kernel<<<grid_for((const void*)dequant_weight_kernel, &occ, n16, sms), 256, 0, st>>>(q, n16, s_w,
-                                                                                                  wd);
+  auto k = dequant_weight_kernel<kDequantU>;
+  k<<<grid_for((const void*)k, &occ, n16, sms, kDequantU), 256, 0, st>>>(q, n16, s_w, wd);
   return cudaGetLastError();
 }
 
@@ -491,7 +575,8 @@ cudaError_t launch_quant_static(const uint16_t* x, int64_t n, const float* s_in,
                                 int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
   static std::atomic<int> occ{0};
-  quant_static_kernel<<<grid_for((const void*)quant_static_kernel, &occ, n16, sms), 256, 0, st>>>(x, n16, s_in, q);
+  auto k = quant_static_kernel<kQuantU>;
+  k<<<grid_for((const void*)k, &occ, n16, sms, kQuantU), 256, 0, st>>>(x, n16, s_in, q);
   return cudaGetLastError();
 }
 
@@ -499,7 +584,8 @@ cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, c
                               uint8_t* out, int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
   static std::atomic<int> occ{0};
-  swiglu_fp8_kernel<<<grid_for((const void*)swiglu_fp8_kernel, &occ, n16, sms), 256, 0, st>>>(g, u, n16, s_out, out);
+  auto k = swiglu_fp8_kernel<kSwigluU>;
+  k<<<grid_for((const void*)k, &occ, n16, sms, kSwigluU), 256, 0, st>>>(g, u, n16, s_out, out);
   return cudaGetLastError();
 }
 
@@ -545,7 +631,8 @@ cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, 
                                int sms, cudaStream_t st) {
   const int64_t n16 = n / 16;
   static std::atomic<int> occ{0};
-  swiglu_bf16_kernel<<<grid_for((const void*)swiglu_bf16_kernel, &occ, n16, sms), 256, 0, st>>>(g, u, n16, out);
+  auto k = swiglu_bf16_kernel<kSwigluU>;
+  k<<<grid_for((const void*)k, &occ, n16, sms, kSwigluU), 256, 0, st>>>(g, u, n16, out);
   return cudaGetLastError();
 }
 

@@ -250,6 +250,10 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
   if constexpr (CG == 2) cluster_sync();  // peer barriers initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above overlaps the previous kernel on the stream; from here
+  // on every thread may read what it wrote (activations, scales) and write
+  // what it may still read (outputs).
+  griddep_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -880,13 +884,18 @@ cudaError_t launch_cluster(void (*kern)(Maps, Args), int grid, int threads, int 
   cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cg;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // The prologue (barriers, TMEM allocation, tensor-map prefetch) may run
+  // while the previous kernel finishes; the kernel waits for it before
+  // touching global memory.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, maps, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
