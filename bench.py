@@ -517,19 +517,6 @@ def breakdown_ours(W, blk, flush, stream, args):
     ms = _time(lambda: W.fp8_dequant_weight(w.gu[0][0], w.gu[0][1], out=blk.wsd[:INTER * HID].view(INTER, HID)),
                flush, stream, n)
     out["fp8_dequant_weight_16384x4096"] = {"us": ms * 1e3, "GB_s": 3 * INTER * HID / ms / 1e6}
-    # library kernels with the same traffic shapes, for the bandwidth those
-    # read:write mixes reach on this GPU (context only): torch's dtype
-    # conversions bf16 -> uint8 (2 bytes read per byte written, as the
-    # quantization) and uint8 -> bf16 (1 read per 2 written, as the
-    # dequantization), on the same tensors
-    cv8 = blk.ws
-    ms = _time(lambda: cv8.copy_(blk.x_qkv), flush, stream, n)
-    out["lib_convert_bf16_to_u8_20670x4096"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6,
-                                                "note": "torch dtype conversion, quantization's traffic shape; reference point"}
-    wdv = blk.wsd[:INTER * HID].view(INTER, HID)
-    ms = _time(lambda: wdv.copy_(w.gu[0][0]), flush, stream, n)
-    out["lib_convert_u8_to_bf16_16384x4096"] = {"us": ms * 1e3, "GB_s": 3 * INTER * HID / ms / 1e6,
-                                                "note": "torch dtype conversion, dequantization's traffic shape; reference point"}
     # the producer of a linear input with the static quantization fused after
     # it (modulated LayerNorm -> bf16 -> E4M3), against the same two steps
     # run apart (bf16 h written and read back)

@@ -150,7 +150,17 @@ struct Args {
   const float* s_in;
   const float* s_w[kMaxGroup];
   const float* s_out;  // GLU: the down projection's input scale
+  // L2 policies of the operand loads and the output stores (kL2Normal,
+  // kL2Keep, kL2Stream), chosen per launch from what fits in L2
+  int l2_a, l2_b, l2_y;
 };
+
+enum : int { kL2Normal = 0, kL2Keep = 1, kL2Stream = 2 };
+
+__device__ __forceinline__ uint64_t l2_policy(int kind) {
+  return kind == kL2Keep ? l2_policy_evict_last()
+                         : (kind == kL2Stream ? l2_policy_evict_first() : l2_policy_evict_normal());
+}
 
 // Tile t -> first output row of the (cluster) tile, projection, first column.
 // Tiles are rasterised in groups of `group_m` m-blocks: within a group the
@@ -262,6 +272,8 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued = 0;
       bool ok = true;
+      const uint64_t pol_a = l2_policy(args.l2_a);
+      const uint64_t pol_b = l2_policy(args.l2_b);
       for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
         int m0, g, n0;
         decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
@@ -288,12 +300,12 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
             const uint32_t bd = b_dst + (uint32_t)(at * C::kBRows * 128);
             const int kx = kc + at * C::kAtomK;
             if constexpr (CG == 2) {
-              tma_load_2d_pair(ad, &maps.a, fb, kx, a_row);
-              tma_load_2d_pair(bd, mb0, fb, kx, b_row);
+              tma_load_2d_pair_hint(ad, &maps.a, fb, kx, a_row, pol_a);
+              tma_load_2d_pair_hint(bd, mb0, fb, kx, b_row, pol_b);
             } else {
-              tma_load_2d(ad, &maps.a, fb, kx, a_row);
-              tma_load_2d(bd, mb0, fb, kx, b_row);
-              if constexpr (kGlu) tma_load_2d(bd + 128 * 128, &maps.b[1], fb, kx, b_row);
+              tma_load_2d_hint(ad, &maps.a, fb, kx, a_row, pol_a);
+              tma_load_2d_hint(bd, mb0, fb, kx, b_row, pol_b);
+              if constexpr (kGlu) tma_load_2d_hint(bd + 128 * 128, &maps.b[1], fb, kx, b_row, pol_b);
             }
           }
           ++issued;
@@ -384,6 +396,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
     int nbuf = 0;
     float s_out = 1.0f, rs_out = 1.0f;
     bool exact_only = false;
+    const uint64_t pol_y = l2_policy(args.l2_y);
     if constexpr (kGlu && !C::kOut16) {
       s_out = __ldg(args.s_out);
       rs_out = __frcp_rn(s_out);
@@ -443,7 +456,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(map_y(maps, g), buf0 + nbuf * EB, col0, row0);
+            tma_store_2d_hint(map_y(maps, g), buf0 + nbuf * EB, col0, row0, pol_y);
             tma_store_commit();
           }
           nbuf ^= 1;
@@ -494,7 +507,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           __syncwarp();
           const int col0 = n0 + cp * 64;
           if (lane == 0 && col0 < ng && row0 < args.M) {
-            tma_store_2d(map_y(maps, 0), buf0 + nbuf * EB, col0, row0);
+            tma_store_2d_hint(map_y(maps, 0), buf0 + nbuf * EB, col0, row0, pol_y);
             tma_store_commit();
           }
           nbuf ^= 1;
@@ -553,7 +566,7 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
           __syncwarp();
           const int col0 = n0 + cp * 64;
           if (lane == 0 && col0 < ng && row0 < args.M) {
-            tma_store_2d(map_y(maps, 0), buf0 + nbuf * EB, col0, row0);
+            tma_store_2d_hint(map_y(maps, 0), buf0 + nbuf * EB, col0, row0, pol_y);
             tma_store_commit();
           }
           nbuf ^= 1;
@@ -860,6 +873,36 @@ int group_rows(int rows_per_tile, int64_t K, int elem_bytes, int tiles_m) {
   return gm < tiles_m ? gm : tiles_m;
 }
 
+// What a launch asks L2 to keep.  The outputs are written once and never
+// read back by the launch: streamed.  When all weights and a group of
+// activation rows fit in kL2KeepBytes (of the 129 MB L2; the rest holds the
+// output stream and the tiles in flight), both are kept -- the group made
+// smaller if that makes them fit -- so each is read from DRAM once.
+// Otherwise the group's rows are kept and the weights streamed, with groups
+// of up to kL2GroupBytes of rows, split evenly, so that the weights are swept
+// as few times as possible (once per group).
+constexpr int64_t kL2KeepBytes = 96ll << 20;
+constexpr int64_t kL2GroupBytes = 48ll << 20;
+
+void l2_plan(int64_t w_bytes, int64_t a_block_bytes, int tiles_m, Args& a) {
+  int gm = a.group_m;
+  a.l2_y = kL2Stream;
+  if (w_bytes + gm * a_block_bytes <= kL2KeepBytes) {
+    a.l2_a = a.l2_b = kL2Keep;
+  } else if (kL2KeepBytes - w_bytes >= 2 * a_block_bytes) {
+    gm = (int)((kL2KeepBytes - w_bytes) / a_block_bytes);
+    a.l2_a = a.l2_b = kL2Keep;
+  } else {
+    int gmax = (int)(kL2GroupBytes / a_block_bytes);
+    gmax = gmax < 1 ? 1 : gmax;
+    const int ngroups = (tiles_m + gmax - 1) / gmax;
+    gm = (tiles_m + ngroups - 1) / ngroups;
+    a.l2_a = kL2Keep;
+    a.l2_b = kL2Stream;
+  }
+  a.group_m = gm < tiles_m ? gm : tiles_m;
+}
+
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle sw) {
@@ -946,6 +989,9 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   args.num_tiles = tiles_m * args.tiles_per_m;
   args.tiles_m = tiles_m;
   args.group_m = group_rows(BM * CG, p.K, kEl, tiles_m);
+  int64_t w_bytes = 0;
+  for (int g = 0; g < nb; ++g) w_bytes += p.N[kGlu ? 0 : g] * p.K * kEl;
+  l2_plan(w_bytes, (int64_t)BM * CG * p.K * kEl, tiles_m, args);
   const int max_clusters = sms / CG;
   const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   return launch_cluster(gemm_kernel<MODE, CG>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
