@@ -79,7 +79,7 @@ def _s_in(x, shift, scale, eps, T):
 
 @pytest.mark.parametrize("M,K,S", [(64, 256, 1), (300, 4096, 3), (37, 1000, 1), (16, 8, 2), (5, 8192, 1),
                                    (130, 2048, 2), (1, 4096, 1), (9, 1024, 3), (24, 5120, 2), (8, 3000, 4),
-                                   (12, 4096, 12), (6, 8192, 3)])
+                                   (12, 4096, 12), (6, 8192, 3), (7, 512, 7), (3, 4096, 3), (45, 6144, 5)])
 def test_shapes(W, M, K, S):
     x, shift, scale = _problem(M, K, S, seed=M + K)
     T = M // S

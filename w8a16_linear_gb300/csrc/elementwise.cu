@@ -264,20 +264,24 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
 
 // ------------------------------------------------------------ norm + quant
 //
-// One block of 256 threads per row, grid-stride over rows.  The block's
-// coming rows stream into a ring of shared-memory row buffers by bulk copies
-// (one mbarrier per buffer), several rows ahead of the one being worked on:
-// that, not the register file, sets how many bytes are in flight.  Thread t
-// takes the row's 16-byte vectors t, t + 256, ... (kV of them, K <= 2048 kV)
-// into registers; the buffer is refilled once every thread has passed the
-// row's first reduction.  The sample's scale and shift stay in registers
-// (packed bf16; fl32(1 + scale) is formed where it is used, which keeps the
-// kernel at 64 registers and 4 blocks per SM) while consecutive rows belong
-// to the same sample.  Statistics in binary32, taken about the row's first
-// element p = x_0 (so that a large common offset of the row does not enter
-// their rounding errors), with shallow summation trees (the thread's 8 kV
-// values as packed pairs pairwise, the last pair's two halves, five butterfly
-// levels, the 8 warp sums pairwise: depth 13 at most):
+// A block of 256 threads works on kG = 256 / kT rows at a time: row group g
+// (threads g kT .. g kT + kT - 1, kT = 64 for K <= 4096, else 128) takes row
+// blockIdx.x kG + g, then every gridDim.x kG-th row after it, with its own
+// named barrier, its own shared-memory ring of row buffers and its own
+// reduction slots, so the groups of a block never wait for one another.  A
+// group's coming rows stream into its ring by bulk copies (cp.async.bulk,
+// one mbarrier per buffer), several rows ahead of the one being worked on;
+// a buffer is refilled after the row's first reduction, when every thread
+// of the group holds its part of the row in registers.  Thread t of a group
+// takes the row's 16-byte vectors t, t + kT, ... (kV of them, K <= 8 kT kV):
+// 64 elements per thread at K = 4096, so the per-row reductions and barriers
+// are spread over many elements.  The sample's scale and shift are read
+// from global memory (L1-resident: all rows of a sample share them) where
+// h is formed.  Statistics in binary32, taken about the row's first element
+// p = x_0 (so that a large common offset of the row does not enter their
+// rounding errors), with summation trees of depth <= 13 (the thread's 4 kV
+// pairs pairwise, the last pair's two halves, five butterfly levels, the
+// group's 2 or 4 warp sums pairwise):
 //   a   = fl32(x - p),   m = fl32(sum a * fl32(1/K))    (m = mean - p)
 //   var = fl32(sum fl32(a - m)^2 * fl32(1/K)),
 //   r   = rsqrt(fl32(var + eps))                        (within 2 ulps),
@@ -286,17 +290,21 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
 // h differs from the exactly computed value by a few binary32 ulps of its
 // terms, so it is the correctly rounded bf16 except where the exact value is
 // that close to a bf16 rounding boundary.  The E4M3 codes are the static
-// quantization of this bf16 h, bit for bit: the bracket test of quant_pair
-// above, with the pairs it cannot settle collected in a per-row list and
-// given the correctly rounded division after the row's third barrier (so
-// that the division's code is not in the per-pair loop).
+// quantization of this bf16 h, bit for bit: the bracket test of quant_pair,
+// with the pairs it cannot settle collected in a per-row list and given the
+// correctly rounded division after the row's third barrier (so that the
+// division's code is not in the per-pair loop).
 
 constexpr int kLnMaxStages = 8;
-constexpr int kLnRingBytes = 48 * 1024;       // row buffers per block (dynamic shared memory)
+constexpr int kLnRingBytes = 96 * 1024;       // row buffers per block, split among its row groups
+constexpr int kLnFixCap = 128;                // unsettled pairs listed per row
 constexpr uint64_t kLnWaitLimitNs = 2000000000ull;
 
+int ln_group_threads(int K) { return K <= 4096 ? 64 : 128; }
+
 int ln_stages(int K) {
-  const int s = kLnRingBytes / (2 * K);
+  const int groups = 256 / ln_group_threads(K);
+  const int s = kLnRingBytes / groups / (2 * K);
   return s < kLnMaxStages ? s : kLnMaxStages;   // >= 3 for K <= 8192
 }
 
@@ -308,64 +316,63 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Sum over the block: each warp's butterfly total, then the 8 warp totals
-// pairwise in a fixed order, so every thread gets the same value.
-__device__ __forceinline__ float block_sum(float v, float* slot) {
+__device__ __forceinline__ void group_bar(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Sum over a row group of kW warps: each warp's butterfly total, then the
+// warp totals pairwise in a fixed order, so every thread gets the same value.
+template <int kW>
+__device__ __forceinline__ float group_sum(float v, float* slot, uint32_t bar_id) {
   v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) slot[threadIdx.x >> 5] = v;
-  __syncthreads();
-  return __fadd_rn(__fadd_rn(__fadd_rn(slot[0], slot[1]), __fadd_rn(slot[2], slot[3])),
-                   __fadd_rn(__fadd_rn(slot[4], slot[5]), __fadd_rn(slot[6], slot[7])));
+  if ((threadIdx.x & 31) == 0) slot[(threadIdx.x >> 5) % kW] = v;
+  group_bar(bar_id, 32 * kW);
+  if constexpr (kW == 2) return __fadd_rn(slot[0], slot[1]);
+  else return __fadd_rn(__fadd_rn(slot[0], slot[1]), __fadd_rn(slot[2], slot[3]));
 }
 
-template <int kV>
-__device__ __forceinline__ void load_row(const uint16_t* __restrict__ src, int nvec, uint4 (&v)[kV]) {
-#pragma unroll
-  for (int i = 0; i < kV; ++i) {
-    const int j = threadIdx.x + 256 * i;
-    v[i] = j < nvec ? ldg16(src + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-// kFull: K == 2048 kV, every vector slot of every thread holds row data.
-template <int kV, bool kFull>
-__global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel(
+// kFull: K == 8 kT kV, every vector slot of every thread holds row data.
+template <int kT, int kV, bool kFull>
+__global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
     const uint16_t* __restrict__ x, int64_t M, int K, const uint16_t* __restrict__ shift,
     const uint16_t* __restrict__ scale, int64_t rows_per_sample, float eps, int stages,
     const float* __restrict__ s_in, uint8_t* __restrict__ q, uint16_t* __restrict__ h) {
-  extern __shared__ __align__(128) uint8_t ln_ring[];   // stages x K bf16
-  __shared__ __align__(8) uint64_t full[kLnMaxStages];
-  // [row parity][statistic][warp]: a row's two reductions and the next row's
-  // use different slots, so the row's own barriers keep them apart.
-  __shared__ float red[2][2][8];
-  __shared__ int bad;
-  // Per-row list of the pairs whose fast code the bracket test could not
-  // settle (column, bf16 pair), by row parity like `red`: they get the
-  // correctly rounded division after the row's third barrier, so that the
-  // division's code is not in the per-pair loop.
-  constexpr int kFixCap = 128;
-  __shared__ uint32_t fix_n[2];
-  __shared__ uint2 fix[2][kFixCap];
+  constexpr int kG = 256 / kT;                 // row groups per block
+  constexpr int kW = kT / 32;                  // warps per row group
   constexpr int kP = 4 * kV;                   // binary32 pairs per thread
+  extern __shared__ __align__(128) uint8_t ln_ring[];   // kG x stages x K bf16
+  __shared__ __align__(8) uint64_t full[kG][kLnMaxStages];
+  // [group][row parity][statistic][warp]: a row's two reductions and the
+  // next row's use different slots, so the row's own barriers keep them apart.
+  __shared__ float red[kG][2][2][kW];
+  __shared__ int bad[kG];
+  // Per-row list of the pairs whose fast code the bracket test could not
+  // settle (column, bf16 pair), by row parity like `red`.
+  __shared__ uint32_t fix_n[kG][2];
+  __shared__ uint2 fix[kG][2][kLnFixCap];
+  const int g = (int)threadIdx.x / kT;
+  const int lt = (int)threadIdx.x % kT;
+  const uint32_t bar_id = 1u + (uint32_t)g;
   const int nvec = K / 8;                      // 16-byte vectors per row
   const uint32_t row_bytes = 2u * (uint32_t)K;
-  const int64_t G = gridDim.x;
-  if ((int64_t)blockIdx.x >= M) return;        // uniform over the block
-  const int64_t nrows = (M - 1 - blockIdx.x) / G + 1;   // rows of this block
-  const uint32_t ring = smem_u32(ln_ring);
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < stages; ++st) mbar_init(smem_u32(&full[st]), 1);
+  const int64_t G = (int64_t)gridDim.x * kG;   // rows between a group's consecutive rows
+  const int64_t first = (int64_t)blockIdx.x * kG + g;
+  if (first >= M) return;                      // uniform over the group
+  const int64_t nrows = (M - 1 - first) / G + 1;
+  const uint32_t ring = smem_u32(ln_ring) + (uint32_t)(g * stages) * row_bytes;
+  if (lt == 0) {
+    for (int st = 0; st < stages; ++st) mbar_init(smem_u32(&full[g][st]), 1);
     fence_mbar_init();
-    bad = 0;
-    fix_n[0] = fix_n[1] = 0;
+    bad[g] = 0;
+    fix_n[g][0] = fix_n[g][1] = 0;
   }
-  __syncthreads();
-  int64_t issued = 0;                          // rows whose copy is out (thread 0's count)
-  if (threadIdx.x == 0) {
+  group_bar(bar_id, kT);
+  int64_t issued = 0;                          // rows whose copy is out (lt 0's count)
+  if (lt == 0) {
     for (; issued < nrows && issued < stages; ++issued) {
-      const uint32_t bar = smem_u32(&full[issued]);
+      const uint32_t bar = smem_u32(&full[g][issued]);
       mbar_arrive_expect_tx(bar, row_bytes);
-      bulk_load(ring + (uint32_t)issued * row_bytes, x + (blockIdx.x + issued * G) * K, row_bytes, bar);
+      bulk_load(ring + (uint32_t)issued * row_bytes, x + (first + issued * G) * K, row_bytes, bar);
     }
   }
   float s = 1.0f, rs = 1.0f;
@@ -376,31 +383,25 @@ __global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel
     exact_only = !scale_is_fast(s, rs);
   }
   const float inv_k = __frcp_rn((float)K);     // exact when K is a power of two
-  uint4 scv[kV];                               // the current sample's scale, bf16
-  uint4 shv[kV];                               // its shift, bf16
-  int64_t smp_loaded = -1;
   int never = 0;                               // nothing aborts these waits early
   int64_t k = 0;
   for (; k < nrows; ++k) {
     const int par = (int)(k & 1);
-    const int64_t row = blockIdx.x + k * G;
+    const int64_t row = first + k * G;
     const int st = (int)(k % stages);
     const int64_t smp = row / rows_per_sample;
-    if (smp != smp_loaded) {                   // uniform over the block
-      load_row<kV>(shift + smp * K, nvec, shv);
-      load_row<kV>(scale + smp * K, nvec, scv);
-      smp_loaded = smp;
-    }
-    if (!mbar_wait_warp(smem_u32(&full[st]), (uint32_t)((k / stages) & 1), &never, kLnWaitLimitNs))
-      bad = 1;
+    const uint16_t* sh_row = shift + smp * K;
+    const uint16_t* sc_row = scale + smp * K;
+    if (!mbar_wait_warp(smem_u32(&full[g][st]), (uint32_t)((k / stages) & 1), &never, kLnWaitLimitNs))
+      bad[g] = 1;
     // the row into registers: a = x - p as packed pairs (padding pairs 0)
-    const uint16_t* rb = reinterpret_cast<const uint16_t*>(ln_ring + (size_t)st * row_bytes);
+    const uint16_t* rb = reinterpret_cast<const uint16_t*>(ln_ring + (size_t)(g * stages + st) * row_bytes);
     const float p = bf16_lo((uint32_t)rb[0]);
     const F2 minus_p = splat(-p);
     F2 a[kP];
 #pragma unroll
     for (int i = 0; i < kV; ++i) {
-      const int j = (int)threadIdx.x + 256 * i;
+      const int j = lt + kT * i;
       const bool live = kFull || j < nvec;
       const uint4 v = live ? *reinterpret_cast<const uint4*>(rb + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -408,8 +409,8 @@ __global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel
       for (int c = 0; c < 4; ++c)
         a[4 * i + c] = live ? add2(F2{bf16_lo(w[c]), bf16_hi(w[c])}, minus_p) : F2{0.0f, 0.0f};
     }
-    // mean about the pivot: the thread's pairs pairwise, then the block
-    F2 t[kP];
+    // mean about the pivot: the thread's pairs pairwise, then the group
+    F2 t[kP / 2];
 #pragma unroll
     for (int i = 0; i < kP / 2; ++i) t[i] = add2(a[i], a[i + kP / 2]);
 #pragma unroll
@@ -417,41 +418,47 @@ __global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel
 #pragma unroll
       for (int i = 0; i < w; ++i) t[i] = add2(t[i], t[i + w]);
     }
-    const float m = __fmul_rn(block_sum(__fadd_rn(t[0].x, t[0].y), red[par][0]), inv_k);
+    const float m = __fmul_rn(group_sum<kW>(__fadd_rn(t[0].x, t[0].y), red[g][par][0], bar_id), inv_k);
     // every thread is past the previous row's fix-up: its list may be reused
-    if (threadIdx.x == 0) fix_n[par ^ 1] = 0;
-    // every thread has its part of the row: the buffer takes row k + stages
-    if (bad) break;                            // uniform: set before the barrier above
-    if (threadIdx.x == 0 && issued < nrows) {
-      const uint32_t bar = smem_u32(&full[st]);
+    if (lt == 0) fix_n[g][par ^ 1] = 0;
+    // every thread has its part of the row: the buffer takes the group's
+    // row k + stages
+    if (bad[g]) break;                         // uniform: set before the barrier above
+    if (lt == 0 && issued < nrows) {
+      const uint32_t bar = smem_u32(&full[g][st]);
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, row_bytes);
-      bulk_load(ring + (uint32_t)st * row_bytes, x + (blockIdx.x + issued * G) * K, row_bytes, bar);
+      bulk_load(ring + (uint32_t)st * row_bytes, x + (first + issued * G) * K, row_bytes, bar);
       ++issued;
     }
     // variance (two-pass: squared deviations from the mean)
     const F2 minus_m = splat(-m);
 #pragma unroll
-    for (int i = 0; i < kP; ++i) {
-      const bool live = kFull || (int)threadIdx.x + 256 * (i / 4) < nvec;
-      const F2 d = add2(a[i], minus_m);
-      t[i] = live ? mul2(d, d) : F2{0.0f, 0.0f};
+    for (int i = 0; i < kP / 2; ++i) {
+      const bool live_lo = kFull || lt + kT * (i / 4) < nvec;
+      const bool live_hi = kFull || lt + kT * ((i + kP / 2) / 4) < nvec;
+      const F2 d0 = add2(a[i], minus_m), d1 = add2(a[i + kP / 2], minus_m);
+      const F2 q0 = live_lo ? mul2(d0, d0) : F2{0.0f, 0.0f};
+      const F2 q1 = live_hi ? mul2(d1, d1) : F2{0.0f, 0.0f};
+      t[i] = add2(q0, q1);
     }
 #pragma unroll
-    for (int w = kP / 2; w >= 1; w /= 2) {
+    for (int w = kP / 4; w >= 1; w /= 2) {
 #pragma unroll
       for (int i = 0; i < w; ++i) t[i] = add2(t[i], t[i + w]);
     }
-    const float var = __fmul_rn(block_sum(__fadd_rn(t[0].x, t[0].y), red[par][1]), inv_k);
+    const float var = __fmul_rn(group_sum<kW>(__fadd_rn(t[0].x, t[0].y), red[g][par][1], bar_id), inv_k);
     const float r = rsqrtf(__fadd_rn(var, eps));   // within 2 ulps of 1 / sqrt
     // n = a r - m r in one rounding, h = bf16(n g + shift), then the codes
     const F2 r2 = splat(r), mr2 = splat(-__fmul_rn(m, r));
 #pragma unroll
     for (int i = 0; i < kV; ++i) {
-      const int j = (int)threadIdx.x + 256 * i;
+      const int j = lt + kT * i;
       if (!kFull && j >= nvec) break;
-      const uint32_t sw[4] = {shv[i].x, shv[i].y, shv[i].z, shv[i].w};
-      const uint32_t cw[4] = {scv[i].x, scv[i].y, scv[i].z, scv[i].w};
+      const uint4 shv = ldg16(sh_row + 8 * j);
+      const uint4 scv = ldg16(sc_row + 8 * j);
+      const uint32_t sw[4] = {shv.x, shv.y, shv.z, shv.w};
+      const uint32_t cw[4] = {scv.x, scv.y, scv.z, scv.w};
       uint32_t hb[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -468,8 +475,8 @@ __global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel
           code[c] = e4m3x2_bracket(mul2(F2{bf16_lo(hb[c]), bf16_hi(hb[c])}, splat(rs)), kQuantBracketLo,
                                    kQuantBracketHi, unsettled);
           if (unsettled | exact_only) {
-            const uint32_t slot = atomicAdd(&fix_n[par], 1u);
-            if (slot < kFixCap) fix[par][slot] = make_uint2((uint32_t)(8 * j + 2 * c), hb[c]);
+            const uint32_t slot = atomicAdd(&fix_n[g][par], 1u);
+            if (slot < kLnFixCap) fix[g][par][slot] = make_uint2((uint32_t)(8 * j + 2 * c), hb[c]);
           }
         }
         *reinterpret_cast<uint2*>(q + row * K + 8 * j) =
@@ -479,23 +486,25 @@ __global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel
     if (q != nullptr) {
       // the row's unsettled pairs: the fast codes above are stored; the
       // barrier orders those stores before the exact ones
-      __syncthreads();
-      const uint32_t n = fix_n[par];
-      if (n <= (uint32_t)kFixCap) {
-        for (uint32_t e = threadIdx.x; e < n; e += 256) {
-          const uint2 f = fix[par][e];
+      group_bar(bar_id, kT);
+      const uint32_t n = fix_n[g][par];
+      if (n <= (uint32_t)kLnFixCap) {
+        for (uint32_t e = (uint32_t)lt; e < n; e += kT) {
+          const uint2 f = fix[g][par][e];
           *reinterpret_cast<uint16_t*>(q + row * K + f.x) = (uint16_t)quant_pair_exact(f.y, s);
         }
       } else {
-        // list overflow (a row with more than kFixCap unsettled pairs, as
-        // every pair is when the scale is outside the fast range): the block
+        // list overflow (a row with more than kLnFixCap unsettled pairs, as
+        // every pair is when the scale is outside the fast range): the group
         // redoes the row's codes with the division
 #pragma unroll
         for (int i = 0; i < kV; ++i) {
-          const int j = (int)threadIdx.x + 256 * i;
+          const int j = lt + kT * i;
           if (!kFull && j >= nvec) break;
-          const uint32_t sw[4] = {shv[i].x, shv[i].y, shv[i].z, shv[i].w};
-          const uint32_t cw[4] = {scv[i].x, scv[i].y, scv[i].z, scv[i].w};
+          const uint4 shv = ldg16(sh_row + 8 * j);
+          const uint4 scv = ldg16(sc_row + 8 * j);
+          const uint32_t sw[4] = {shv.x, shv.y, shv.z, shv.w};
+          const uint32_t cw[4] = {scv.x, scv.y, scv.z, scv.w};
           uint32_t code[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -509,13 +518,13 @@ __global__ void __launch_bounds__(256, kV <= 2 ? 4 : 1) ln_modulate_quant_kernel
       }
     }
   }
-  if (bad && threadIdx.x == 0) {
+  if (bad[g] && lt == 0) {
     // a wait gave up at row k: record it, then let the copies of rows k ..
     // issued - 1, still in flight, land (each wait bounded) before the
     // block's shared memory is released
     atomicOr(&g_elem_err, kErrTimeout);
     for (; k < issued; ++k)
-      mbar_wait(smem_u32(&full[k % stages]), (uint32_t)((k / stages) & 1), &never, kLnWaitLimitNs);
+      mbar_wait(smem_u32(&full[g][k % stages]), (uint32_t)((k / stages) & 1), &never, kLnWaitLimitNs);
   }
 }
 
@@ -592,25 +601,34 @@ cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, c
 cudaError_t launch_ln_modulate_quant(const uint16_t* x, int64_t M, int K, const uint16_t* shift,
                                      const uint16_t* scale, int64_t rows_per_sample, float eps,
                                      const float* s_in, uint8_t* q, uint16_t* h, int sms, cudaStream_t st) {
-  // One row per block at a time: grid_for's 256 work items per block are one
-  // row.  The ring (at most 48 KB, with the static arrays just above the
-  // default per-block limit, hence the opt-in) stays below what the register
-  // limit leaves each block, so the occupancy figure without it stands.
-  static std::atomic<int> occ[3];              // full and ragged rows: same registers
-  const int64_t items = M * 256;
+  // kG = 256 / kT rows per block at a time; as many blocks as fit at once
+  // (the ring is the kernel's dynamic shared memory, opted in above the
+  // default per-block limit).
+  static std::atomic<int> occ[10];
+  const int kt = ln_group_threads(K);
+  const int groups = 256 / kt;
   const int stages = ln_stages(K);
-  const int ring = stages * 2 * K;
-#define W8_LN_LAUNCH(V, SLOT)                                                                     \
-  {                                                                                               \
-    auto k = K == 2048 * V ? ln_modulate_quant_kernel<V, true> : ln_modulate_quant_kernel<V, false>; \
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ring);   \
-    if (e != cudaSuccess) return e;                                                               \
-    k<<<grid_for((const void*)k, &occ[SLOT], items, sms), 256, ring, st>>>(                       \
-        x, M, K, shift, scale, rows_per_sample, eps, stages, s_in, q, h);                         \
+  const int ring = groups * stages * 2 * K;
+  const int64_t blocks_wanted = (M + groups - 1) / groups;
+#define W8_LN_LAUNCH(T, V, SLOT)                                                                      \
+  {                                                                                                  \
+    auto k = K == 8 * T * V ? ln_modulate_quant_kernel<T, V, true> : ln_modulate_quant_kernel<T, V, false>; \
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ring);      \
+    if (e != cudaSuccess) return e;                                                                  \
+    int b = occ[SLOT].load(std::memory_order_relaxed);                                               \
+    if (b == 0) {                                                                                    \
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, 256, ring) != cudaSuccess || b < 1) b = 1; \
+      occ[SLOT].store(b, std::memory_order_relaxed);                                                 \
+    }                                                                                                \
+    const int64_t cap = (int64_t)sms * b;                                                            \
+    const int grid = (int)(blocks_wanted < cap ? blocks_wanted : cap);                               \
+    k<<<grid, 256, ring, st>>>(x, M, K, shift, scale, rows_per_sample, eps, stages, s_in, q, h);     \
   }
-  if (K <= 2048) W8_LN_LAUNCH(1, 0)
-  else if (K <= 4096) W8_LN_LAUNCH(2, 1)
-  else W8_LN_LAUNCH(4, 2)
+  if (K <= 512) W8_LN_LAUNCH(64, 1, 0)
+  else if (K <= 1024) W8_LN_LAUNCH(64, 2, 1)
+  else if (K <= 2048) W8_LN_LAUNCH(64, 4, 2)
+  else if (K <= 4096) W8_LN_LAUNCH(64, 8, 3)
+  else W8_LN_LAUNCH(128, 8, 4)
 #undef W8_LN_LAUNCH
   return cudaGetLastError();
 }
