@@ -309,7 +309,7 @@ def run_ours(args, rank, world, dev):
     e2e_pipeline(W, blk, stream, 2)                 # warm-up of the copy path
     e2e_ms, h2d, d2h = e2e_pipeline(W, blk, stream, e2e_steps)
 
-    breakdown = breakdown_ours(W, blk, flush, stream, args)
+    breakdown = {} if args.no_breakdown else breakdown_ours(W, blk, flush, stream, args)
     W.poll_device_error()
     return {"total_ms": sum(step_ms), "step_ms": step_ms, "gemm_ms": gemm_ms, "e2e_ms": e2e_ms,
             "h2d": h2d, "d2h": d2h, "clocks": clk, "launches": launches, "breakdown": breakdown}
@@ -925,6 +925,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-breakdown", action="store_true",
+                    help="print the headline line without the breakdown (for launch-list captures)")
     ap.add_argument("--case", default=None,
                     help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, block_gemms) instead of the bench")
     args = ap.parse_args()
