@@ -275,9 +275,10 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
 // of the group holds its part of the row in registers.  Thread t of a group
 // takes the row's 16-byte vectors t, t + kT, ... (kV of them, K <= 8 kT kV):
 // 64 elements per thread at K = 4096, so the per-row reductions and barriers
-// are spread over many elements.  The sample's scale and shift are read
-// from global memory (L1-resident: all rows of a sample share them) where
-// h is formed.  Statistics in binary32, taken about the row's first element
+// are spread over many elements.  For K <= 4096 the block keeps a table of
+// fl32(1 + scale) and shift in binary32 for the sample of its first row
+// (shared memory, filled once); rows of another sample, and all rows when
+// K > 4096, read the bf16 modulation from global memory where h is formed.  Statistics in binary32, taken about the row's first element
 // p = x_0 (so that a large common offset of the row does not enter their
 // rounding errors), with summation trees of depth <= 13 (the thread's 4 kV
 // pairs pairwise, the last pair's two halves, five butterfly levels, the
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
 // division's code is not in the per-pair loop).
 
 constexpr int kLnMaxStages = 8;
-constexpr int kLnRingBytes = 96 * 1024;       // row buffers per block, split among its row groups
+constexpr int kLnRingBytes = 64 * 1024;       // row buffers per block, split among its row groups
 constexpr int kLnFixCap = 128;                // unsettled pairs listed per row
 constexpr uint64_t kLnWaitLimitNs = 2000000000ull;
 
@@ -305,8 +306,11 @@ int ln_group_threads(int K) { return K <= 4096 ? 64 : 128; }
 int ln_stages(int K) {
   const int groups = 256 / ln_group_threads(K);
   const int s = kLnRingBytes / groups / (2 * K);
-  return s < kLnMaxStages ? s : kLnMaxStages;   // >= 3 for K <= 8192
+  return s < kLnMaxStages ? s : kLnMaxStages;   // >= 2 for K <= 8192
 }
+
+// Bytes of the modulation table (fl32(1 + scale), shift) of the kT = 64 forms.
+int ln_table_bytes(int K) { return K <= 4096 ? 8 * K : 0; }
 
 __device__ uint32_t g_elem_err;                // kErrTimeout when a row-buffer wait gives up
 
@@ -331,6 +335,31 @@ __device__ __forceinline__ float group_sum(float v, float* slot, uint32_t bar_id
   else return __fadd_rn(__fadd_rn(slot[0], slot[1]), __fadd_rn(slot[2], slot[3]));
 }
 
+// fl32(1 + scale) and shift of the 8 columns of vector j, as 4 packed pairs:
+// from the block's table, or from the bf16 rows in global memory.
+template <bool kTable>
+__device__ __forceinline__ void ln_modulation(bool from_table, const float4* table, int nvec, const uint16_t* sh_row,
+                                              const uint16_t* sc_row, int j, F2 (&gc)[4], F2 (&sf)[4]) {
+  if (kTable && from_table) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float4 v = table[c * nvec + j];    // columns 8j + 2c, + 1: (1 + scale, shift) each
+      gc[c] = F2{v.x, v.z};
+      sf[c] = F2{v.y, v.w};
+    }
+  } else {
+    const uint4 shv = ldg16(sh_row + 8 * j);
+    const uint4 scv = ldg16(sc_row + 8 * j);
+    const uint32_t sw[4] = {shv.x, shv.y, shv.z, shv.w};
+    const uint32_t cw[4] = {scv.x, scv.y, scv.z, scv.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      gc[c] = add2(splat(1.0f), F2{bf16_lo(cw[c]), bf16_hi(cw[c])});
+      sf[c] = F2{bf16_lo(sw[c]), bf16_hi(sw[c])};
+    }
+  }
+}
+
 // kFull: K == 8 kT kV, every vector slot of every thread holds row data.
 template <int kT, int kV, bool kFull>
 __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
@@ -340,7 +369,10 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
   constexpr int kG = 256 / kT;                 // row groups per block
   constexpr int kW = kT / 32;                  // warps per row group
   constexpr int kP = 4 * kV;                   // binary32 pairs per thread
-  extern __shared__ __align__(128) uint8_t ln_ring[];   // kG x stages x K bf16
+  constexpr bool kTable = (kT == 64);          // modulation table in shared memory
+  // dynamic shared memory: [table: K x (1 + scale, shift) binary32] then the
+  // row rings, kG x stages x K bf16
+  extern __shared__ __align__(128) uint8_t ln_smem[];
   __shared__ __align__(8) uint64_t full[kG][kLnMaxStages];
   // [group][row parity][statistic][warp]: a row's two reductions and the
   // next row's use different slots, so the row's own barriers keep them apart.
@@ -357,6 +389,23 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
   const uint32_t row_bytes = 2u * (uint32_t)K;
   const int64_t G = (int64_t)gridDim.x * kG;   // rows between a group's consecutive rows
   const int64_t first = (int64_t)blockIdx.x * kG + g;
+  const uint32_t table_bytes = kTable ? 8u * (uint32_t)K : 0u;
+  float4* table = reinterpret_cast<float4*>(ln_smem);
+  uint8_t* ln_ring = ln_smem + table_bytes;
+  // The table holds the sample of the block's first row: entry c * nvec + j
+  // = (1 + scale, shift) of columns 8 j + 2 c and 8 j + 2 c + 1, so that
+  // the lanes of a warp (consecutive j) read consecutive 16-byte words.
+  const int64_t table_smp = ((int64_t)blockIdx.x * kG) / rows_per_sample;
+  if constexpr (kTable) {
+    const uint32_t* sh0 = reinterpret_cast<const uint32_t*>(shift + table_smp * K);
+    const uint32_t* sc0 = reinterpret_cast<const uint32_t*>(scale + table_smp * K);
+    for (int pi = (int)threadIdx.x; pi < K / 2; pi += 256) {
+      const uint32_t sw = __ldg(sh0 + pi), cw = __ldg(sc0 + pi);
+      table[(pi & 3) * nvec + (pi >> 2)] = make_float4(__fadd_rn(1.0f, bf16_lo(cw)), bf16_lo(sw),
+                                                       __fadd_rn(1.0f, bf16_hi(cw)), bf16_hi(sw));
+    }
+    __syncthreads();
+  }
   if (first >= M) return;                      // uniform over the group
   const int64_t nrows = (M - 1 - first) / G + 1;
   const uint32_t ring = smem_u32(ln_ring) + (uint32_t)(g * stages) * row_bytes;
@@ -451,19 +500,17 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
     const float r = rsqrtf(__fadd_rn(var, eps));   // within 2 ulps of 1 / sqrt
     // n = a r - m r in one rounding, h = bf16(n g + shift), then the codes
     const F2 r2 = splat(r), mr2 = splat(-__fmul_rn(m, r));
+    const bool from_table = kTable && smp == table_smp;   // uniform over the group
 #pragma unroll
     for (int i = 0; i < kV; ++i) {
       const int j = lt + kT * i;
       if (!kFull && j >= nvec) break;
-      const uint4 shv = ldg16(sh_row + 8 * j);
-      const uint4 scv = ldg16(sc_row + 8 * j);
-      const uint32_t sw[4] = {shv.x, shv.y, shv.z, shv.w};
-      const uint32_t cw[4] = {scv.x, scv.y, scv.z, scv.w};
+      F2 gc[4], sf[4];
+      ln_modulation<kTable>(from_table, table, nvec, sh_row, sc_row, j, gc, sf);
       uint32_t hb[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const F2 gc = add2(splat(1.0f), F2{bf16_lo(cw[c]), bf16_hi(cw[c])});
-        const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), gc, F2{bf16_lo(sw[c]), bf16_hi(sw[c])});
+        const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), gc[c], sf[c]);
         hb[c] = cvt_bf16x2(hv.x, hv.y);
       }
       if (h != nullptr) *reinterpret_cast<uint4*>(h + row * K + 8 * j) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
@@ -501,15 +548,12 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
         for (int i = 0; i < kV; ++i) {
           const int j = lt + kT * i;
           if (!kFull && j >= nvec) break;
-          const uint4 shv = ldg16(sh_row + 8 * j);
-          const uint4 scv = ldg16(sc_row + 8 * j);
-          const uint32_t sw[4] = {shv.x, shv.y, shv.z, shv.w};
-          const uint32_t cw[4] = {scv.x, scv.y, scv.z, scv.w};
+          F2 gc[4], sf[4];
+          ln_modulation<kTable>(from_table, table, nvec, sh_row, sc_row, j, gc, sf);
           uint32_t code[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const F2 gc = add2(splat(1.0f), F2{bf16_lo(cw[c]), bf16_hi(cw[c])});
-            const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), gc, F2{bf16_lo(sw[c]), bf16_hi(sw[c])});
+            const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), gc[c], sf[c]);
             code[c] = quant_pair_exact(cvt_bf16x2(hv.x, hv.y), s);
           }
           *reinterpret_cast<uint2*>(q + row * K + 8 * j) =
@@ -608,7 +652,7 @@ cudaError_t launch_ln_modulate_quant(const uint16_t* x, int64_t M, int K, const 
   const int kt = ln_group_threads(K);
   const int groups = 256 / kt;
   const int stages = ln_stages(K);
-  const int ring = groups * stages * 2 * K;
+  const int ring = ln_table_bytes(K) + groups * stages * 2 * K;
   const int64_t blocks_wanted = (M + groups - 1) / groups;
 #define W8_LN_LAUNCH(T, V, SLOT)                                                                      \
   {                                                                                                  \
