@@ -126,3 +126,27 @@ def test_gated_mlp_chain(W):
     # the down projection is within tolerance given those codes
     r64, _ = O.linear_w8a8(host_u8(h), q_dn, s_out, s_dn)
     assert gemm_err(host_bits(y), r64) <= GEMM_TOL
+
+
+def test_full_size_group_equals_separate_calls_bit_for_bit(W):
+    """M = 20670, 3 x 4096 x 4096: the group launch (3888 tiles) cuts its last
+    wave's 12 tiles into four column slices each, the single-projection
+    launches (1296 tiles) cut their last 4 tiles; every output element is
+    accumulated in the same order either way, so the outputs are identical."""
+    M, K, N = 20670, 4096, 4096
+    gen = torch.Generator(device="cuda").manual_seed(21)
+    q = (torch.randn((M, K), generator=gen, device="cuda") * 40).clamp(-448, 448).to(torch.float8_e4m3fn)
+    q = q.view(torch.uint8).contiguous()
+    ws, ss = [], []
+    for i in range(3):
+        w = torch.randn((N, K), generator=gen, device="cuda") * (0.02 * (0.5 + 0.25 * i))
+        s = (w.abs().amax() / 448).reshape(1).contiguous()
+        ws.append((w / s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
+        ss.append(s)
+    s_in = dev_f32(0.003)
+    group = W.fp8_linear_w8a8_group(q, s_in, ws, ss)
+    for y, w, s in zip(group, ws, ss):
+        y1 = W.fp8_linear_w8a8(q, w, s_in, s)
+        assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
+    torch.cuda.synchronize()
+    W.poll_device_error()

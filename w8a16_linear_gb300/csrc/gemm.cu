@@ -146,6 +146,15 @@ struct Args {
   int tiles_m;
   int group_m;   // m-blocks swept together down each column of tiles
   int num_tiles;
+  // Work units of gemm_kernel: tiles [0, num_full) whole, then each of the
+  // num_tiles - num_full tail tiles cut into tail_split column slices (of
+  // kBN / tail_split columns) that separate CTAs (pairs) compute, so that the
+  // last, partly filled wave is short.  num_units = num_full + tail tiles x
+  // tail_split.  Every output element is accumulated over the same k order
+  // whichever way its tile is cut.
+  int num_full;
+  int tail_split;
+  int num_units;
   int num_kb;
   const float* s_in;
   const float* s_w[kMaxGroup];
@@ -183,6 +192,21 @@ __device__ __forceinline__ void decode_tile(const Args& a, int t, int rows_per_t
   }
   m0 = mb * rows_per_tile;
   n0 = r * cols_per_tile;
+}
+
+// Work unit u -> its tile's first row, projection, first column, and width.
+__device__ __forceinline__ void decode_unit(const Args& a, int u, int rows_per_tile, int cols_per_tile,
+                                            int& m0, int& g, int& n0, int& width) {
+  if (u < a.num_full) {
+    decode_tile(a, u, rows_per_tile, cols_per_tile, m0, g, n0);
+    width = cols_per_tile;
+  } else {
+    const int v = u - a.num_full;
+    const int piece = v % a.tail_split;
+    decode_tile(a, a.num_full + v / a.tail_split, rows_per_tile, cols_per_tile, m0, g, n0);
+    width = cols_per_tile / a.tail_split;
+    n0 += piece * width;
+  }
 }
 
 __device__ __forceinline__ const CUtensorMap* map_b(const Maps& m, int g) {
@@ -274,14 +298,15 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       bool ok = true;
       const uint64_t pol_a = l2_policy(args.l2_a);
       const uint64_t pol_b = l2_policy(args.l2_b);
-      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
-        int m0, g, n0;
-        decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
+      for (int t = cluster_id; ok && t < args.num_units; t += num_clusters) {
+        int m0, g, n0, width;
+        decode_unit(args, t, BM * CG, C::kBN, m0, g, n0, width);
         const int a_row = m0 + (int)rank * BM;
-        // W8A8: this CTA's half (pair) or all of the tile's weight rows.
+        // W8A8: this CTA's half (pair) or all of the unit's weight rows (a
+        // tail slice uses the first width / CG rows of the box it loads).
         // GLU: the slice's rows n0 .. n0+127 of gate (even CTA / first half)
         // and of up (odd CTA / second half).
-        const int b_row = kGlu ? n0 : n0 + (int)rank * C::kBRows;
+        const int b_row = kGlu ? n0 : n0 + (int)rank * (width / CG);
         for (int kb = 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1, abort, kWaitLimitNs)) {
             record_timeout(abort);
@@ -335,7 +360,11 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < args.num_tiles; t += num_clusters) {
+      for (int t = cluster_id; ok && t < args.num_units; t += num_clusters) {
+        // a tail slice of width w: an N = w MMA (its descriptor), else the tile's
+        const int w = t < args.num_full ? C::kMmaN : C::kMmaN / args.tail_split;
+        const uint32_t idesc = w == C::kMmaN ? C::kIdesc
+                                             : (C::kBf16 ? make_idesc(1, 1, BM * CG, w) : make_idesc(0, 0, BM * CG, w));
         if (!mbar_wait(tempty_bar(acc), acc_ph ^ 1, abort, kWaitLimitNs)) {
           record_timeout(abort);
           break;
@@ -357,11 +386,11 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
             const uint64_t bd = sw128_kmajor_desc(b_addr + (k >> 2) * C::kBRows * 128 + 32 * (k & 3));
             const uint32_t accum = (kb | k) != 0;
             if constexpr (C::kBf16) {  // K = 16 per MMA: 32 bytes, as for E4M3
-              if constexpr (CG == 2) mma_f16_pair(d, ad, bd, C::kIdesc, accum);
-              else mma_f16(d, ad, bd, C::kIdesc, accum);
+              if constexpr (CG == 2) mma_f16_pair(d, ad, bd, idesc, accum);
+              else mma_f16(d, ad, bd, idesc, accum);
             } else {
-              if constexpr (CG == 2) mma_f8f6f4_pair(d, ad, bd, C::kIdesc, accum);
-              else mma_f8f6f4(d, ad, bd, C::kIdesc, accum);
+              if constexpr (CG == 2) mma_f8f6f4_pair(d, ad, bd, idesc, accum);
+              else mma_f8f6f4(d, ad, bd, idesc, accum);
             }
           }
           if constexpr (CG == 2) mma_commit_pair_mc(empty_bar(s), 0x3);
@@ -402,9 +431,9 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       rs_out = __frcp_rn(s_out);
       exact_only = !swiglu_fp8_scale_is_fast(s_out, rs_out);
     }
-    for (int t = cluster_id; t < args.num_tiles; t += num_clusters) {
-      int m0, g, n0;
-      decode_tile(args, t, BM * CG, C::kBN, m0, g, n0);
+    for (int t = cluster_id; t < args.num_units; t += num_clusters) {
+      int m0, g, n0, width;
+      decode_unit(args, t, BM * CG, C::kBN, m0, g, n0, width);
       float alpha = 1.0f, alpha_u = 1.0f;
       // BF16: the scale is already in the dequantized weight; y = bf16(acc).
       if constexpr (!C::kBf16) alpha = __fmul_rn(__ldg(args.s_in), __ldg(scale_w(args, kGlu ? 0 : g)));
@@ -419,13 +448,14 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
       const int ng = args.N[g];
       const uint32_t tbase = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * kAccCols);
       if constexpr (!kGlu) {
+        const int chunks = width / 64;
 #pragma unroll 1
-        for (int c = 0; c < C::kBN / 64; ++c) {
+        for (int c = 0; c < chunks; ++c) {
           uint32_t r0[32], r1[32];
           tmem_ld_32x32b_x32(tbase + c * 64, r0);
           tmem_ld_32x32b_x32(tbase + c * 64 + 32, r1);
           tmem_ld_wait();
-          if (c == C::kBN / 64 - 1) {
+          if (c == chunks - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -994,6 +1024,17 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   l2_plan(w_bytes, (int64_t)BM * CG * p.K * kEl, tiles_m, args);
   const int max_clusters = sms / CG;
   const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
+  // The last wave's tiles, if they fill at most half (a quarter) of the
+  // clusters, are cut in two (four) column slices (not GLU, whose tile
+  // columns pair gate with up; not single CTAs).
+  const int tail = args.num_tiles % clusters;
+  args.tail_split = 1;
+  if (!kGlu && CG == 2 && tail > 0) {
+    if (4 * tail <= clusters) args.tail_split = 4;
+    else if (2 * tail <= clusters) args.tail_split = 2;
+  }
+  args.num_full = args.num_tiles - (args.tail_split > 1 ? tail : 0);
+  args.num_units = args.num_full + (args.num_tiles - args.num_full) * args.tail_split;
   return launch_cluster(gemm_kernel<MODE, CG>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
                         args);
 }
@@ -1031,6 +1072,8 @@ cudaError_t launch_a16t(const GemmProblem& p, int sms, cudaStream_t st, int* tma
     return cudaSuccess;
   }
   args.num_tiles = tiles_m * args.tiles_per_m;
+  args.num_full = args.num_units = args.num_tiles;
+  args.tail_split = 1;
   args.tiles_m = tiles_m;
   args.group_m = group_rows(BT, p.K, 2, tiles_m);
   const int grid = args.num_tiles < sms ? args.num_tiles : sms;
