@@ -235,10 +235,10 @@ class Block:
 
 # DRAM bytes (read + write) of one grouped Q/K/V W8A8 GEMM launch at
 # M=20670, K=N=4096 x3, from one ncu capture of the current gemm_kernel build
-# (profiles/gemm_w8a8_qkv_20670x4096x4096.md: 372.1 MB read + 487.7 MB
-# written; algorithmic 84.7 + 50.3 MB read, 508.0 MB written).  Re-capture,
-# or set to None, whenever gemm_kernel changes.
-QKV_GEMM_TRAFFIC_BYTES = 859.8e6
+# (profiles/gemm_traffic_block_20670.md: 368.2 MB read + 484.8 MB written;
+# algorithmic 84.7 + 50.3 MB read, 508.0 MB written).  Re-capture, or set to
+# None, whenever gemm_kernel changes.
+QKV_GEMM_TRAFFIC_BYTES = 853.0e6
 QKV_GEMM_ALGO_BYTES = M_TOK * HID + 3 * HID * HID + 3 * 2 * M_TOK * HID
 
 
