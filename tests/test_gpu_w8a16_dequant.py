@@ -151,3 +151,29 @@ def test_bf16_gate_up_swiglu_exact_sums_vs_oracle(W):
     nan = np.isnan(O.bf16_decode(want))
     assert np.array_equal(np.isnan(O.bf16_decode(h)), nan)
     assert np.array_equal(h[~nan], want[~nan])
+
+
+@pytest.mark.parametrize("M,K,N", [(64, 256, 256), (300, 512, 1024), (4096, 4096, 4096), (20670, 4096, 4096)])
+def test_exported_linear_with_workspace(W, M, K, N):
+    """fp8_linear_w8a16 with its optional workspace: the weight dequantized
+    into the workspace, then the bf16 GEMM.  Against the oracle (sampled rows
+    plus the tail at full size), bit for bit against the A16 group call with
+    a workspace (the same two kernels), and within the tolerance of the form
+    without a workspace (same operand bits, other accumulation order); the
+    workspace holds the dequantized weight afterwards."""
+    x, qws, s_ws = _group(M, K, (N,), seed=M)
+    xd, wd, sd = dev_bf16(x), dev_u8(qws[0]), dev_f32(s_ws[0])
+    ws = torch.empty((N * K,), dtype=torch.bfloat16, device="cuda")
+    y = W.fp8_linear_w8a16(xd, wd, sd, ws=ws)
+    y_group = W.qkv_shared_quant_gemm(W.MODE_A16, xd, None, [wd], [sd], ws=W.w8a16_workspace([wd]))[0]
+    y_fused = W.fp8_linear_w8a16(xd, wd, sd)
+    torch.cuda.synchronize()
+    W.poll_device_error()
+    assert torch.equal(y.view(torch.int16), y_group.view(torch.int16))
+    assert np.array_equal(host_bits(ws.view(N, K)), O.dequant_weight_bf16(qws[0], s_ws[0]))
+    rows = (np.arange(M) if M <= 4096 else
+            np.concatenate([synth.random_rows(M, M, 64), np.arange(M - 62, M)]))
+    y64, _ = O.linear_w8a16(x, qws[0], s_ws[0], rows=rows)
+    assert gemm_err(host_bits(y)[rows], y64) <= GEMM_TOL
+    yf = O.bf16_decode(host_bits(y_fused)[rows]).astype(np.float64)
+    assert np.abs(yf - y64).max() / np.abs(y64).max() <= GEMM_TOL
