@@ -69,7 +69,6 @@ __global__ void __launch_bounds__(256, kQuantBlocks) quant_static_kernel(const u
   const float s = __ldg(s_in);
   const float r = __frcp_rn(s);
   const bool exact_only = !scale_is_fast(s, r);
-  const L2Stream l2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
     uint4 a[U], b[U];
@@ -77,8 +76,8 @@ __global__ void __launch_bounds__(256, kQuantBlocks) quant_static_kernel(const u
     for (int j = 0; j < U; ++j) {
       const int64_t v = i + j * stride;
       if (v < n16) {
-        a[j] = l2.load(x + v * 16);
-        b[j] = l2.load(x + v * 16 + 8);
+        a[j] = ldg16(x + v * 16);
+        b[j] = ldg16(x + v * 16 + 8);
       }
     }
 #pragma unroll
@@ -90,7 +89,7 @@ __global__ void __launch_bounds__(256, kQuantBlocks) quant_static_kernel(const u
       o.y = quant_pair(a[j].z, s, r, exact_only) | (quant_pair(a[j].w, s, r, exact_only) << 16);
       o.z = quant_pair(b[j].x, s, r, exact_only) | (quant_pair(b[j].y, s, r, exact_only) << 16);
       o.w = quant_pair(b[j].z, s, r, exact_only) | (quant_pair(b[j].w, s, r, exact_only) << 16);
-      l2.store(q + v * 16, o);
+      *reinterpret_cast<uint4*>(q + v * 16) = o;
     }
   }
 }
@@ -104,7 +103,6 @@ __global__ void __launch_bounds__(256, kSwigluBlocks) swiglu_fp8_kernel(const ui
   const float s = __ldg(s_out);
   const float rs = __frcp_rn(s);
   const bool exact_only = !swiglu_fp8_scale_is_fast(s, rs);
-  const L2Stream l2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
     uint4 ga[U], gb[U], ua[U], ub[U];
@@ -112,10 +110,10 @@ __global__ void __launch_bounds__(256, kSwigluBlocks) swiglu_fp8_kernel(const ui
     for (int j = 0; j < U; ++j) {
       const int64_t v = i + j * stride;
       if (v < n16) {
-        ga[j] = l2.load(g + v * 16);
-        gb[j] = l2.load(g + v * 16 + 8);
-        ua[j] = l2.load(u + v * 16);
-        ub[j] = l2.load(u + v * 16 + 8);
+        ga[j] = ldg16(g + v * 16);
+        gb[j] = ldg16(g + v * 16 + 8);
+        ua[j] = ldg16(u + v * 16);
+        ub[j] = ldg16(u + v * 16 + 8);
       }
     }
 #pragma unroll
@@ -131,7 +129,7 @@ __global__ void __launch_bounds__(256, kSwigluBlocks) swiglu_fp8_kernel(const ui
             (swiglu_fp8_pair(gb[j].y, ub[j].y, s, rs, exact_only) << 16);
       o.w = swiglu_fp8_pair(gb[j].z, ub[j].z, s, rs, exact_only) |
             (swiglu_fp8_pair(gb[j].w, ub[j].w, s, rs, exact_only) << 16);
-      l2.store(out + v * 16, o);
+      *reinterpret_cast<uint4*>(out + v * 16) = o;
     }
   }
 }
@@ -141,7 +139,6 @@ __global__ void __launch_bounds__(256, kSwigluBlocks) swiglu_bf16_kernel(const u
                                                              const uint16_t* __restrict__ u, int64_t n16,
                                                              uint16_t* __restrict__ out) {
   griddep_launch_dependents();   // a GEMM launched next may start its prologue
-  const L2Stream l2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
     uint4 ga[U], gb[U], ua[U], ub[U];
@@ -149,20 +146,21 @@ __global__ void __launch_bounds__(256, kSwigluBlocks) swiglu_bf16_kernel(const u
     for (int j = 0; j < U; ++j) {
       const int64_t v = i + j * stride;
       if (v < n16) {
-        ga[j] = l2.load(g + v * 16);
-        gb[j] = l2.load(g + v * 16 + 8);
-        ua[j] = l2.load(u + v * 16);
-        ub[j] = l2.load(u + v * 16 + 8);
+        ga[j] = ldg16(g + v * 16);
+        gb[j] = ldg16(g + v * 16 + 8);
+        ua[j] = ldg16(u + v * 16);
+        ub[j] = ldg16(u + v * 16 + 8);
       }
     }
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const int64_t v = i + j * stride;
       if (v >= n16) break;
-      l2.store(out + v * 16, make_uint4(swiglu_bf16_pair(ga[j].x, ua[j].x), swiglu_bf16_pair(ga[j].y, ua[j].y),
-                                        swiglu_bf16_pair(ga[j].z, ua[j].z), swiglu_bf16_pair(ga[j].w, ua[j].w)));
-      l2.store(out + v * 16 + 8, make_uint4(swiglu_bf16_pair(gb[j].x, ub[j].x), swiglu_bf16_pair(gb[j].y, ub[j].y),
-                                            swiglu_bf16_pair(gb[j].z, ub[j].z), swiglu_bf16_pair(gb[j].w, ub[j].w)));
+      uint4* dst = reinterpret_cast<uint4*>(out + v * 16);
+      dst[0] = make_uint4(swiglu_bf16_pair(ga[j].x, ua[j].x), swiglu_bf16_pair(ga[j].y, ua[j].y),
+                          swiglu_bf16_pair(ga[j].z, ua[j].z), swiglu_bf16_pair(ga[j].w, ua[j].w));
+      dst[1] = make_uint4(swiglu_bf16_pair(gb[j].x, ub[j].x), swiglu_bf16_pair(gb[j].y, ub[j].y),
+                          swiglu_bf16_pair(gb[j].z, ub[j].z), swiglu_bf16_pair(gb[j].w, ub[j].w));
     }
   }
 }
@@ -179,14 +177,13 @@ __global__ void __launch_bounds__(256, kDequantBlocks) dequant_weight_kernel(con
                                                                 uint16_t* __restrict__ wd) {
   griddep_launch_dependents();   // a GEMM launched next may start its prologue
   const float sw = __ldg(s_w);
-  const L2Stream l2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
     uint4 c[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const int64_t v = i + j * stride;
-      if (v < n16) c[j] = l2.load(q + v * 16);
+      if (v < n16) c[j] = ldg16(q + v * 16);
     }
 #pragma unroll
     for (int j = 0; j < U; ++j) {
@@ -206,8 +203,9 @@ __global__ void __launch_bounds__(256, kDequantBlocks) dequant_weight_kernel(con
         o[2 * e] = cvt_bf16x2(a.x, a.y);
         o[2 * e + 1] = cvt_bf16x2(b.x, b.y);
       }
-      l2.store(wd + v * 16, make_uint4(o[0], o[1], o[2], o[3]));
-      l2.store(wd + v * 16 + 8, make_uint4(o[4], o[5], o[6], o[7]));
+      uint4* dst = reinterpret_cast<uint4*>(wd + v * 16);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
 }
@@ -227,7 +225,6 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
     rs = __frcp_rn(s);
     exact_only = !swiglu_fp8_scale_is_fast(s, rs);
   }
-  const L2Stream l2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
     uint4 ga[U], gb[U], ua[U], ub[U];
@@ -235,10 +232,10 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
     for (int j = 0; j < U; ++j) {
       const int64_t v = i + j * stride;
       if (v < n16) {
-        ga[j] = l2.load(g + v * 16);
-        gb[j] = l2.load(g + v * 16 + 8);
-        ua[j] = l2.load(u + v * 16);
-        ub[j] = l2.load(u + v * 16 + 8);
+        ga[j] = ldg16(g + v * 16);
+        gb[j] = ldg16(g + v * 16 + 8);
+        ua[j] = ldg16(u + v * 16);
+        ub[j] = ldg16(u + v * 16 + 8);
       }
     }
 #pragma unroll
@@ -251,14 +248,15 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
         uint32_t c[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) c[e] = swiglu_ex_fp8_pair<kF16>(gw[e], uw[e], pr, s, rs, exact_only);
-        l2.store(static_cast<uint8_t*>(out) + v * 16,
-                 make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16)));
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + v * 16) =
+            make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
       } else {
         uint32_t h[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) h[e] = swiglu_ex_16_pair<kF16>(gw[e], uw[e], pr);
-        l2.store(static_cast<uint16_t*>(out) + v * 16, make_uint4(h[0], h[1], h[2], h[3]));
-        l2.store(static_cast<uint16_t*>(out) + v * 16 + 8, make_uint4(h[4], h[5], h[6], h[7]));
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + v * 16);
+        dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
       }
     }
   }

@@ -168,30 +168,6 @@ __device__ __forceinline__ uint4 ldg16(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// The elementwise kernels read each input once and write an output that the
-// next kernel (a GEMM) reads: inputs are loaded with an evict_first L2 policy
-// and outputs stored with evict_last, so that the output rather than the
-// spent input stays in L2 for its reader.
-struct L2Stream {
-  uint64_t in, out;
-  __device__ __forceinline__ L2Stream() {
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(in));
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(out));
-  }
-  __device__ __forceinline__ uint4 load(const void* p) const {
-    uint4 v;
-    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p), "l"(in));
-    return v;
-  }
-  __device__ __forceinline__ void store(void* p, uint4 v) const {
-    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w), "l"(out)
-                 : "memory");
-  }
-};
-
 __device__ __forceinline__ bool scale_is_fast(float s, float r) {
   const float kMinNormal = 1.17549435e-38f;
   return fabsf(s) >= kMinNormal && fabsf(r) >= kMinNormal && fabsf(r) < __int_as_float(0x7F800000);
