@@ -150,3 +150,45 @@ def test_full_size_group_equals_separate_calls_bit_for_bit(W):
         assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
     torch.cuda.synchronize()
     W.poll_device_error()
+
+
+@pytest.mark.parametrize("M,Ns", [(2600, (4096,)),          # 11 x 16 = 176 tiles: 2 x 76 + 24 -> halves
+                                  (4990, (2048, 2048)),     # 20 x 16 = 320 tiles: 4 x 76 + 16 -> quarters
+                                  (8192, (4096, 1024)),     # 32 x 20 = 640 tiles: 8 x 76 + 32 -> halves
+                                  (3000, (1024, 1024, 1024))])  # 12 x 12 = 144 tiles: 76 + 68 -> not cut
+def test_tail_slices_against_oracle(W, M, Ns):
+    """Launches whose last wave is cut into column slices: every projection
+    against the oracle on sampled rows plus the ragged tail, and against its
+    own single-projection launch (cut differently, or not at all) bit for bit."""
+    K = 1024
+    x, s_in, qws, s_ws = _group(M, K, Ns)
+    xd, wd, sd, si = dev_bf16(x), [dev_u8(q) for q in qws], [dev_f32(s) for s in s_ws], dev_f32(s_in)
+    q = W.fp8_quant_static(xd, si)
+    ys = W.fp8_linear_w8a8_group(q, si, wd, sd)
+    rows = np.concatenate([synth.random_rows(M, M - 300, 40), np.arange(M - 300, M)])
+    qx = host_u8(q)[rows]
+    for y, w, s, qw, sw in zip(ys, wd, sd, qws, s_ws):
+        y64, _ = O.linear_w8a8(qx, qw, s_in, sw)
+        assert gemm_err(host_bits(y)[rows], y64) <= GEMM_TOL
+        assert torch.equal(y.view(torch.int16), W.fp8_linear_w8a8(q, w, si, s).view(torch.int16))
+    torch.cuda.synchronize()
+    W.poll_device_error()
+
+
+def test_tail_slices_bf16_group(W):
+    """The bf16 GEMM of the W8A16 path cuts its tail the same way (N = 128 or
+    64 kind::f16 MMAs): a 3-projection group (20 x 48 = 960 tiles, 12 x 76 +
+    48: not cut) against single projections (320 tiles, 4 x 76 + 16: cut in
+    four) bit for bit, and against the oracle."""
+    M, K, Ns = 4990, 1024, (4096, 4096, 4096)
+    x, _, qws, s_ws = _group(M, K, Ns, seed=3)
+    xd = dev_bf16(x)
+    wds = [W.fp8_dequant_weight(dev_u8(q), dev_f32(s)) for q, s in zip(qws, s_ws)]
+    ys = W.bf16_linear_group(xd, wds)
+    rows = np.concatenate([synth.random_rows(8, M - 200, 32), np.arange(M - 200, M)])
+    for y, wd, qw, sw in zip(ys, wds, qws, s_ws):
+        assert torch.equal(y.view(torch.int16), W.bf16_linear_group(xd, [wd])[0].view(torch.int16))
+        y64, _ = O.linear_w8a16(x, qw, sw, rows=rows)
+        assert gemm_err(host_bits(y)[rows], y64) <= GEMM_TOL
+    torch.cuda.synchronize()
+    W.poll_device_error()
