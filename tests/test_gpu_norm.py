@@ -181,10 +181,10 @@ def _midpoint_shift(K, n_mid, seed):
 
 @pytest.mark.parametrize("n_mid", [40, 4096])
 def test_unsettled_pairs(W, n_mid):
-    """Rows whose h are E4M3 ties at s = 1: with a few per row the kernel's
-    per-row list of unsettled pairs takes the division; with every element a
-    tie the list overflows and the whole row is redone.  Codes equal the
-    static quantization of h (ties to even)."""
+    """Rows whose h are E4M3 ties at s = 1: the bracket test cannot settle
+    them, so each thread recomputes its marked pairs after the row and stores
+    the division's codes (a few per row, or every element of the row).
+    Codes equal the static quantization of h (ties to even)."""
     M, K = 24, 4096
     x = np.repeat(O.bf16_round(np.linspace(-1, 1, M)).astype(np.uint16)[:, None], K, axis=1)   # constant rows
     shift = _midpoint_shift(K, n_mid, seed=n_mid)
@@ -197,8 +197,7 @@ def test_unsettled_pairs(W, n_mid):
 @pytest.mark.parametrize("s,K", [(2e38, 2048), (1e-39, 2048), (2e38, 8192), (1e-39, 200)])
 def test_scale_outside_fast_range(W, s, K):
     """Scales whose reciprocal is not a normal binary32 number: every pair
-    takes the division (through the list when a row has at most 128 pairs,
-    else by redoing the row)."""
+    takes the division, recomputed by its thread after the row."""
     M, S = 40, 2
     x, shift, scale = _problem(M, K, S, seed=13)
     q, h = _run(W, x, shift, scale, 1e-6, np.float32(s))

@@ -291,14 +291,16 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
 // h differs from the exactly computed value by a few binary32 ulps of its
 // terms, so it is the correctly rounded bf16 except where the exact value is
 // that close to a bf16 rounding boundary.  The E4M3 codes are the static
-// quantization of this bf16 h, bit for bit: the bracket test of quant_pair,
-// with the pairs it cannot settle collected in a per-row list and given the
-// correctly rounded division after the row's third barrier (so that the
-// division's code is not in the per-pair loop).
+// quantization of this bf16 h, bit for bit: the bracket test of quant_pair
+// in a branch-free per-pair loop that only marks, in a per-thread mask, the
+// pairs it cannot settle; after the row, a thread with marked pairs (rare:
+// values within 2^-21 of an E4M3 rounding boundary, or every pair when the
+// scale is outside the fast range) recomputes each of them from the row in
+// global memory by the same operations and stores the correctly rounded
+// division's code over the fast one.
 
 constexpr int kLnMaxStages = 8;
 constexpr int kLnRingBytes = 64 * 1024;       // row buffers per block, split among its row groups
-constexpr int kLnFixCap = 128;                // unsettled pairs listed per row
 constexpr uint64_t kLnWaitLimitNs = 2000000000ull;
 
 int ln_group_threads(int K) { return K <= 4096 ? 64 : 128; }
@@ -360,8 +362,42 @@ __device__ __forceinline__ void ln_modulation(bool from_table, const float4* tab
   }
 }
 
+// The exact codes of a thread's unsettled pairs (bit 4 i + c of `mask`: pair
+// c of its vector i) of one row: h recomputed from the row in global memory
+// by the main pass's operations (so it is the same bf16), then the correctly
+// rounded division.  This thread stored the fast codes of these pairs
+// before, so its own program order puts these stores after them.
+template <int kT, bool kTable>
+__device__ __noinline__ void ln_fix_pairs(uint32_t mask, const uint16_t* xrow, uint8_t* qrow, int lt, int nvec,
+                                          float minus_p, float r, float minus_mr, bool from_table,
+                                          const float4* table, const uint16_t* sh_row, const uint16_t* sc_row,
+                                          float s) {
+  while (mask != 0u) {
+    const int b = __ffs(mask) - 1;
+    mask &= mask - 1u;
+    const int j = lt + kT * (b >> 2), c = b & 3;
+    const int col = 8 * j + 2 * c;
+    const uint32_t xw = *reinterpret_cast<const uint32_t*>(xrow + col);
+    const F2 a = add2(F2{bf16_lo(xw), bf16_hi(xw)}, splat(minus_p));
+    F2 gc, sf;
+    if (kTable && from_table) {
+      const float4 v = table[c * nvec + j];
+      gc = F2{v.x, v.z};
+      sf = F2{v.y, v.w};
+    } else {
+      const uint32_t sw = *reinterpret_cast<const uint32_t*>(sh_row + col);
+      const uint32_t cw = *reinterpret_cast<const uint32_t*>(sc_row + col);
+      gc = add2(splat(1.0f), F2{bf16_lo(cw), bf16_hi(cw)});
+      sf = F2{bf16_lo(sw), bf16_hi(sw)};
+    }
+    const F2 hv = fma2(fma2(a, splat(r), splat(minus_mr)), gc, sf);
+    *reinterpret_cast<uint16_t*>(qrow + col) = (uint16_t)quant_pair_exact(cvt_bf16x2(hv.x, hv.y), s);
+  }
+}
+
 // kFull: K == 8 kT kV, every vector slot of every thread holds row data.
-template <int kT, int kV, bool kFull>
+// kOut: bit 0 the E4M3 codes q, bit 1 the bf16 h.
+template <int kT, int kV, bool kFull, int kOut>
 __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
     const uint16_t* __restrict__ x, int64_t M, int K, const uint16_t* __restrict__ shift,
     const uint16_t* __restrict__ scale, int64_t rows_per_sample, float eps, int stages,
@@ -370,6 +406,8 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
   constexpr int kW = kT / 32;                  // warps per row group
   constexpr int kP = 4 * kV;                   // binary32 pairs per thread
   constexpr bool kTable = (kT == 64);          // modulation table in shared memory
+  constexpr bool kQ = (kOut & 1) != 0, kH = (kOut & 2) != 0;
+  static_assert(kP <= 32, "one mask bit per pair");
   // dynamic shared memory: [table: K x (1 + scale, shift) binary32] then the
   // row rings, kG x stages x K bf16
   extern __shared__ __align__(128) uint8_t ln_smem[];
@@ -378,10 +416,6 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
   // next row's use different slots, so the row's own barriers keep them apart.
   __shared__ float red[kG][2][2][kW];
   __shared__ int bad[kG];
-  // Per-row list of the pairs whose fast code the bracket test could not
-  // settle (column, bf16 pair), by row parity like `red`.
-  __shared__ uint32_t fix_n[kG][2];
-  __shared__ uint2 fix[kG][2][kLnFixCap];
   const int g = (int)threadIdx.x / kT;
   const int lt = (int)threadIdx.x % kT;
   const uint32_t bar_id = 1u + (uint32_t)g;
@@ -413,7 +447,6 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
     for (int st = 0; st < stages; ++st) mbar_init(smem_u32(&full[g][st]), 1);
     fence_mbar_init();
     bad[g] = 0;
-    fix_n[g][0] = fix_n[g][1] = 0;
   }
   group_bar(bar_id, kT);
   int64_t issued = 0;                          // rows whose copy is out (lt 0's count)
@@ -426,11 +459,15 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
   }
   float s = 1.0f, rs = 1.0f;
   bool exact_only = false;
-  if (q != nullptr) {
+  if constexpr (kQ) {
     s = __ldg(s_in);
     rs = __frcp_rn(s);
     exact_only = !scale_is_fast(s, rs);
   }
+  uint32_t live = 0;                           // mask bits of the thread's pairs that hold row data
+#pragma unroll
+  for (int i = 0; i < kV; ++i)
+    if (kFull || lt + kT * i < nvec) live |= 0xFu << (4 * i);
   const float inv_k = __frcp_rn((float)K);     // exact when K is a power of two
   int never = 0;                               // nothing aborts these waits early
   int64_t k = 0;
@@ -468,8 +505,6 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
       for (int i = 0; i < w; ++i) t[i] = add2(t[i], t[i + w]);
     }
     const float m = __fmul_rn(group_sum<kW>(__fadd_rn(t[0].x, t[0].y), red[g][par][0], bar_id), inv_k);
-    // every thread is past the previous row's fix-up: its list may be reused
-    if (lt == 0) fix_n[g][par ^ 1] = 0;
     // every thread has its part of the row: the buffer takes the group's
     // row k + stages
     if (bad[g]) break;                         // uniform: set before the barrier above
@@ -501,6 +536,7 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
     // n = a r - m r in one rounding, h = bf16(n g + shift), then the codes
     const F2 r2 = splat(r), mr2 = splat(-__fmul_rn(m, r));
     const bool from_table = kTable && smp == table_smp;   // uniform over the group
+    uint32_t unsettled_mask = 0;
 #pragma unroll
     for (int i = 0; i < kV; ++i) {
       const int j = lt + kT * i;
@@ -513,53 +549,25 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
         const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), gc[c], sf[c]);
         hb[c] = cvt_bf16x2(hv.x, hv.y);
       }
-      if (h != nullptr) *reinterpret_cast<uint4*>(h + row * K + 8 * j) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
-      if (q != nullptr) {
+      if constexpr (kH) *reinterpret_cast<uint4*>(h + row * K + 8 * j) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+      if constexpr (kQ) {
         uint32_t code[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           bool unsettled;
           code[c] = e4m3x2_bracket(mul2(F2{bf16_lo(hb[c]), bf16_hi(hb[c])}, splat(rs)), kQuantBracketLo,
                                    kQuantBracketHi, unsettled);
-          if (unsettled | exact_only) {
-            const uint32_t slot = atomicAdd(&fix_n[g][par], 1u);
-            if (slot < kLnFixCap) fix[g][par][slot] = make_uint2((uint32_t)(8 * j + 2 * c), hb[c]);
-          }
+          unsettled_mask |= (uint32_t)unsettled << (4 * i + c);
         }
         *reinterpret_cast<uint2*>(q + row * K + 8 * j) =
             make_uint2(code[0] | (code[1] << 16), code[2] | (code[3] << 16));
       }
     }
-    if (q != nullptr) {
-      // the row's unsettled pairs: the fast codes above are stored; the
-      // barrier orders those stores before the exact ones
-      group_bar(bar_id, kT);
-      const uint32_t n = fix_n[g][par];
-      if (n <= (uint32_t)kLnFixCap) {
-        for (uint32_t e = (uint32_t)lt; e < n; e += kT) {
-          const uint2 f = fix[g][par][e];
-          *reinterpret_cast<uint16_t*>(q + row * K + f.x) = (uint16_t)quant_pair_exact(f.y, s);
-        }
-      } else {
-        // list overflow (a row with more than kLnFixCap unsettled pairs, as
-        // every pair is when the scale is outside the fast range): the group
-        // redoes the row's codes with the division
-#pragma unroll
-        for (int i = 0; i < kV; ++i) {
-          const int j = lt + kT * i;
-          if (!kFull && j >= nvec) break;
-          F2 gc[4], sf[4];
-          ln_modulation<kTable>(from_table, table, nvec, sh_row, sc_row, j, gc, sf);
-          uint32_t code[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const F2 hv = fma2(fma2(a[4 * i + c], r2, mr2), gc[c], sf[c]);
-            code[c] = quant_pair_exact(cvt_bf16x2(hv.x, hv.y), s);
-          }
-          *reinterpret_cast<uint2*>(q + row * K + 8 * j) =
-              make_uint2(code[0] | (code[1] << 16), code[2] | (code[3] << 16));
-        }
-      }
+    if constexpr (kQ) {
+      if (exact_only) unsettled_mask = live;
+      if (unsettled_mask != 0u)
+        ln_fix_pairs<kT, kTable>(unsettled_mask, x + row * K, q + row * K, lt, nvec, -p, r, mr2.x, from_table,
+                                 table, sh_row, sc_row, s);
     }
   }
   if (bad[g] && lt == 0) {
@@ -648,21 +656,27 @@ cudaError_t launch_ln_modulate_quant(const uint16_t* x, int64_t M, int K, const 
   // kG = 256 / kT rows per block at a time; as many blocks as fit at once
   // (the ring is the kernel's dynamic shared memory, opted in above the
   // default per-block limit).
-  static std::atomic<int> occ[10];
+  static std::atomic<int> occ[15];
   const int kt = ln_group_threads(K);
   const int groups = 256 / kt;
   const int stages = ln_stages(K);
   const int ring = ln_table_bytes(K) + groups * stages * 2 * K;
   const int64_t blocks_wanted = (M + groups - 1) / groups;
+  const int out = (q != nullptr ? 1 : 0) | (h != nullptr ? 2 : 0);
+  if (out == 0) return cudaErrorInvalidValue;   // the entry point refuses this first
+#define W8_LN_KERNEL(T, V, F)                                                                        \
+  (out == 1 ? ln_modulate_quant_kernel<T, V, F, 1>                                                   \
+            : out == 2 ? ln_modulate_quant_kernel<T, V, F, 2> : ln_modulate_quant_kernel<T, V, F, 3>)
 #define W8_LN_LAUNCH(T, V, SLOT)                                                                      \
   {                                                                                                  \
-    auto k = K == 8 * T * V ? ln_modulate_quant_kernel<T, V, true> : ln_modulate_quant_kernel<T, V, false>; \
+    auto k = K == 8 * T * V ? W8_LN_KERNEL(T, V, true) : W8_LN_KERNEL(T, V, false);                   \
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, ring);      \
     if (e != cudaSuccess) return e;                                                                  \
-    int b = occ[SLOT].load(std::memory_order_relaxed);                                               \
+    std::atomic<int>& o = occ[3 * (SLOT) + out - 1];                                                 \
+    int b = o.load(std::memory_order_relaxed);                                                       \
     if (b == 0) {                                                                                    \
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, 256, ring) != cudaSuccess || b < 1) b = 1; \
-      occ[SLOT].store(b, std::memory_order_relaxed);                                                 \
+      o.store(b, std::memory_order_relaxed);                                                         \
     }                                                                                                \
     const int64_t cap = (int64_t)sms * b;                                                            \
     const int grid = (int)(blocks_wanted < cap ? blocks_wanted : cap);                               \
@@ -674,6 +688,7 @@ cudaError_t launch_ln_modulate_quant(const uint16_t* x, int64_t M, int K, const 
   else if (K <= 4096) W8_LN_LAUNCH(64, 8, 3)
   else W8_LN_LAUNCH(128, 8, 4)
 #undef W8_LN_LAUNCH
+#undef W8_LN_KERNEL
   return cudaGetLastError();
 }
 
