@@ -1004,6 +1004,10 @@ def main():
                          "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one launch "
                                          "(ncu capture at M=20670, caches flushed per launch)",
                          "peak_note": f"{peaks['source']} bf16 burst x 2 (nominal FP8/BF16 ratio)"},
+            # the step against the nominal dense FP8 peaks: 4.5 PFLOP/s (2 x the
+            # 2.25 PFLOP/s dense bf16 of these parts) and 5.0 PFLOP/s (the
+            # GB300 NVL72 datasheet figure per GPU)
+            "pct_of_4p5pf_fp8": value / 4500.0,
             "pct_of_5pf_fp8": value / 5000.0,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOPS",
