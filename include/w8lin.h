@@ -189,6 +189,20 @@ w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int6
                                 uint8_t* ws, void* stream);
 
 /*
+ * fp8_e4m3_from_f32 — the E4M3 encoding step on its own: q[i] =
+ * E4M3_satRNE(x[i]) for binary32 x, the round-to-nearest-even to E4M3 with
+ * saturation at +-448 that ends the static quantization ([P2] Verification:
+ * div -> clamp -> round-to-float8) and every other code-producing kernel
+ * here (the same hardware conversion).  Infinities saturate to +-448; NaN
+ * gives a NaN code (0x7F or 0xFF); the sign of zero is kept.
+ *   x   binary32 [n], device, 16-byte aligned
+ *   q   E4M3 codes [n], device (written), 4-byte aligned
+ * n == 0 launches nothing.
+ * Errors: SHAPE (n < 0), NULL, ALIGN, ARCH, CUDA.
+ */
+w8_status fp8_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, void* stream);
+
+/*
  * fp8_dequant_weight — the dequantization step of the W8A16 path on its own
  * ([P3] Behavior: "dequant + F.linear"): Wd = bf16_RNE(fl32(dec(w) * s_w)).
  *   w    E4M3 weight [N, K], device;  s_w device float scalar

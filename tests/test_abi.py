@@ -35,7 +35,7 @@ def test_header_symbols_exported(L):
     for n in names:
         assert hasattr(L, n), n
         assert n in binding.SIGNATURES, n
-    assert L.w8_abi_version() == 4
+    assert L.w8_abi_version() == 5
 
 
 def test_policy_matches_oracle_everywhere(L):
@@ -101,6 +101,13 @@ def test_validation_before_any_cuda_call(L):
     assert L.bf16_linear_group(p16, 4, 16, 4, arr, ns, arr, None) == 2
     assert L.bf16_linear_group(p16, 4, 16, 3, None, ns, arr, None) == 1
     assert L.bf16_linear_group(p16, 0, 16, 3, arr, ns, arr, None) == 0
+    # binary32 -> E4M3 encoding: size, NULL and alignment checks
+    assert L.fp8_e4m3_from_f32(p16, -1, p16, None) == 2
+    assert L.fp8_e4m3_from_f32(None, 0, None, None) == 0
+    assert L.fp8_e4m3_from_f32(None, 8, p16, None) == 1
+    assert L.fp8_e4m3_from_f32(p16, 8, None, None) == 1
+    assert L.fp8_e4m3_from_f32(_u(0x10004), 8, p16, None) == 3
+    assert L.fp8_e4m3_from_f32(p16, 8, _u(0x10002), None) == 3
     # group-scale check arguments
     assert L.w8_check_group_scales(None, 3) == 1
     assert L.w8_check_group_scales(arr, 0) == 2

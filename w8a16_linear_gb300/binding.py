@@ -56,6 +56,7 @@ SIGNATURES = {
                                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
                                              _c_void_p, _c_void_p]),
     "fp8_dequant_weight": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "fp8_e4m3_from_f32": (ctypes.c_int, [_c_void_p, _i64, _c_void_p, _c_void_p]),
     "bf16_gate_up_swiglu": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i64, _c_void_p,
                                            _c_void_p]),
     "bf16_linear_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _i32, ctypes.POINTER(_c_void_p),
@@ -324,6 +325,21 @@ def qkv_shared_quant_gemm(mode, x, s_in, weights, weight_scales, outs=None, ws=N
     _check(lib().qkv_shared_quant_gemm(mode, _ptr(x2), M, K, s_in_p, G, arr_w, arr_n, arr_s, arr_y,
                                        ws_p, _stream(stream)))
     return outs
+
+
+def fp8_e4m3_from_f32(x, out=None, stream=None):
+    """E4M3 codes (uint8, same shape) of the float32 values of ``x``:
+    round to nearest even, saturating at +-448."""
+    if x.dtype != torch.float32:
+        raise W8Error(5, f"x: expected float32, got {x.dtype}")
+    _dense(x, "x")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    q = _as_u8(out, "out")
+    if q.shape != x.shape:
+        raise W8Error(2, f"out: shape {tuple(q.shape)} differs from x {tuple(x.shape)}")
+    _check(lib().fp8_e4m3_from_f32(_ptr(x), x.numel(), _ptr(q), _stream(stream)))
+    return out
 
 
 def fp8_dequant_weight(w, s_w, out=None, stream=None):

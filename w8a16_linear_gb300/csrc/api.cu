@@ -95,7 +95,7 @@ int query_device(int* sms) { return device_info(sms); }
 
 extern "C" {
 
-int w8_abi_version(void) { return 4; }
+int w8_abi_version(void) { return 5; }
 
 const char* w8_last_error(void) { return g_last_error; }
 
@@ -290,6 +290,19 @@ w8_status qkv_shared_quant_gemm(int32_t mode, const uint16_t* x, int64_t M, int6
   }
   if (terr) return fail(W8_ERR_ALIGN, "qkv_shared_quant_gemm: tensor map encoding rejected the operands");
   return cuda_status(e, "qkv_shared_quant_gemm: GEMM launch");
+}
+
+w8_status fp8_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, void* stream) {
+  if (n < 0) return fail(W8_ERR_SHAPE, "fp8_e4m3_from_f32: n=%lld", (long long)n);
+  if (n == 0) return ok();
+  if (!x || !q) return fail(W8_ERR_NULL, "fp8_e4m3_from_f32: NULL pointer");
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(q) & 3u))
+    return fail(W8_ERR_ALIGN, "fp8_e4m3_from_f32: x must be 16-byte and q 4-byte aligned");
+  int sms = 0;
+  w8_status st = device_info(&sms);
+  if (st != W8_OK) return st;
+  return cuda_status(w8::launch_e4m3_from_f32(x, n, q, sms, static_cast<cudaStream_t>(stream)),
+                     "fp8_e4m3_from_f32 launch");
 }
 
 w8_status fp8_dequant_weight(const uint8_t* w, int64_t N, int64_t K, const float* s_w, uint16_t* wd,

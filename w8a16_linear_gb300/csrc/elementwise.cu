@@ -623,6 +623,36 @@ cudaError_t launch_swiglu_ex(const uint16_t* g, const uint16_t* u, int64_t n, bo
   return cudaGetLastError();
 }
 
+// Binary32 -> E4M3, four values per thread per iteration (one 16-byte load,
+// one 4-byte store); the last n % 4 values by a second, one-thread-per-value
+// launch.
+__global__ void __launch_bounds__(256) e4m3_from_f32_kernel(const float4* __restrict__ x, int64_t n4,
+                                                            uint32_t* __restrict__ q) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 v = x[i];
+    q[i] = cvt_e4m3x2(v.x, v.y) | (cvt_e4m3x2(v.z, v.w) << 16);
+  }
+}
+
+__global__ void e4m3_from_f32_tail_kernel(const float* __restrict__ x, int64_t from, int64_t n,
+                                          uint8_t* __restrict__ q) {
+  const int64_t i = from + threadIdx.x;
+  if (i < n) q[i] = (uint8_t)(cvt_e4m3x2(x[i], 0.0f) & 0xFFu);
+}
+
+cudaError_t launch_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, int sms, cudaStream_t st) {
+  const int64_t n4 = n / 4;
+  if (n4 > 0) {
+    static std::atomic<int> occ{0};
+    auto k = e4m3_from_f32_kernel;
+    k<<<grid_for((const void*)k, &occ, n4, sms), 256, 0, st>>>(reinterpret_cast<const float4*>(x), n4,
+                                                                reinterpret_cast<uint32_t*>(q));
+  }
+  if (n % 4) e4m3_from_f32_tail_kernel<<<1, 4, 0, st>>>(x, 4 * n4, n, q);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w, uint16_t* wd, int sms,
                                   cudaStream_t st) {
   const int64_t n16 = n / 16;

@@ -21,6 +21,9 @@ cudaError_t launch_swiglu_fp8(const uint16_t* g, const uint16_t* u, int64_t n, c
 cudaError_t launch_swiglu_bf16(const uint16_t* g, const uint16_t* u, int64_t n, uint16_t* out,
                                int sms, cudaStream_t st);
 
+// Binary32 -> E4M3 codes (x 16-byte aligned, q 4-byte aligned).
+cudaError_t launch_e4m3_from_f32(const float* x, int64_t n, uint8_t* q, int sms, cudaStream_t st);
+
 cudaError_t launch_dequant_weight(const uint8_t* q, int64_t n, const float* s_w, uint16_t* wd, int sms,
                                   cudaStream_t st);
 
