@@ -171,41 +171,60 @@ __global__ void __launch_bounds__(256, kSwigluBlocks) swiglu_bf16_kernel(const u
 // ("dequant + F.linear").  E4M3 -> f16 is exact (cvt e4m3x2 -> f16x2), f16 ->
 // f32 exact, one correctly rounded binary32 multiply, one bf16 rounding.
 
+// Element layout by warp: a warp covers 512 consecutive elements per
+// iteration, lane t the 8-element chunks at 8 t and 256 + 8 t, so that every
+// 16-byte store instruction of the warp writes 512 contiguous bytes (whole
+// 32-byte sectors) and every 8-byte load of codes reads 256.  Two 16-byte
+// stores per thread 32 bytes apart (a thread's 16 consecutive outputs) left
+// each store instruction writing half of every sector it touched: 43.0
+// against 32.8 µs for a 16384 x 4096 weight.  (The read-heavy SwiGLU kernels
+// with 16-bit outputs measured 8-11% slower in this layout and keep theirs.)
+__device__ __forceinline__ int64_t chunk16_first(int64_t b, int64_t j, int64_t warps, int hh, int lane) {
+  return (b + j * warps) * 512 + hh * 256 + 8 * lane;
+}
+
 template <int U>
 __global__ void __launch_bounds__(256, kDequantBlocks) dequant_weight_kernel(const uint8_t* __restrict__ q, int64_t n16,
                                                                 const float* __restrict__ s_w,
                                                                 uint16_t* __restrict__ wd) {
   griddep_launch_dependents();   // a GEMM launched next may start its prologue
   const float sw = __ldg(s_w);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
-    uint4 c[U];
+  const int64_t n = n16 * 16;
+  const int lane = (int)(threadIdx.x & 31);
+  const int64_t nblk = (n + 511) / 512;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; b < nblk; b += U * warps) {
+    uint2 c[U][2];   // 8 codes per chunk
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-      const int64_t v = i + j * stride;
-      if (v < n16) c[j] = ldg16(q + v * 16);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int64_t e0 = chunk16_first(b, j, warps, hh, lane);
+        if (e0 + 8 <= n) c[j][hh] = __ldg(reinterpret_cast<const uint2*>(q + e0));
+      }
     }
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-      const int64_t v = i + j * stride;
-      if (v >= n16) break;
-      const uint32_t cw[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
-      uint32_t o[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] & 0xFFFF));
-        const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] >> 16));
-        F2 a, b;
-        f16x2_to_f32(f01, a.x, a.y);
-        f16x2_to_f32(f23, b.x, b.y);
-        a = mul2(a, splat(sw));
-        b = mul2(b, splat(sw));
-        o[2 * e] = cvt_bf16x2(a.x, a.y);
-        o[2 * e + 1] = cvt_bf16x2(b.x, b.y);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int64_t e0 = chunk16_first(b, j, warps, hh, lane);
+        if (e0 + 8 > n) continue;
+        const uint32_t cw[2] = {c[j][hh].x, c[j][hh].y};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t f01 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] & 0xFFFF));
+          const uint32_t f23 = cvt_e4m3x2_to_f16x2((uint16_t)(cw[e] >> 16));
+          F2 a, bq;
+          f16x2_to_f32(f01, a.x, a.y);
+          f16x2_to_f32(f23, bq.x, bq.y);
+          a = mul2(a, splat(sw));
+          bq = mul2(bq, splat(sw));
+          o[2 * e] = cvt_bf16x2(a.x, a.y);
+          o[2 * e + 1] = cvt_bf16x2(bq.x, bq.y);
+        }
+        *reinterpret_cast<uint4*>(wd + e0) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      uint4* dst = reinterpret_cast<uint4*>(wd + v * 16);
-      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
 }
