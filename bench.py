@@ -900,6 +900,13 @@ def run_case(args):
         def fn():
             W.swiglu_2in_fp8(gg, uu, s, out=h8)
             W.swiglu_2in_bf16(gg, uu, out=h16)
+    elif args.case == "dequant16k":
+        # one 16384 x 4096 weight (the gate or down projection's), its 134 MB
+        # bf16 output larger than L2 together with the 67 MB of codes
+        wq = (torch.randn((INTER, HID), generator=gen, device=dev) * 200).clamp(-448, 448) \
+            .to(torch.float8_e4m3fn).view(torch.uint8)
+        wdq = torch.empty((INTER, HID), dtype=torch.bfloat16, device=dev)
+        fn = lambda: W.fp8_dequant_weight(wq, ss[0], out=wdq)  # noqa: E731
     else:
         raise SystemExit(f"unknown case {args.case}")
     for _ in range(args.warmup + args.steps):
@@ -939,7 +946,7 @@ def main():
     ap.add_argument("--no-breakdown", action="store_true",
                     help="print the headline line without the breakdown (for launch-list captures)")
     ap.add_argument("--case", default=None,
-                    help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, block_gemms) instead of the bench")
+                    help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, ln20k, dequant16k, block_gemms, qkv_sustained, host_link) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.case:
