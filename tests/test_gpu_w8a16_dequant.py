@@ -26,6 +26,18 @@ def test_dequant_every_code(W, s_w):
     assert np.array_equal(got[~nan], want[~nan])
 
 
+@pytest.mark.parametrize("N,K", [(1, 16), (3, 592), (33, 48), (2000, 4112)])
+def test_dequant_ragged_sizes(W, N, K):
+    """Sizes that end inside a warp's 512-element block, and one that takes
+    two grid-stride iterations: every element bit-exact against the oracle."""
+    rng = np.random.default_rng(N + K)
+    q = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x10          # no NaN codes: compare bit for bit
+    s_w = np.float32(0.37)
+    got = host_bits(W.fp8_dequant_weight(dev_u8(q), dev_f32(s_w)))
+    assert np.array_equal(got, O.dequant_weight_bf16(q, s_w))
+
+
 def _group(M, K, Ns, seed=0):
     x = synth.activations_bf16(seed, (M, K), 0.25, outlier_frac=0.001)
     c = synth.uniform_f32(3, (len(Ns),), 0.5, 1.0)
