@@ -440,15 +440,31 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
   const uint32_t bar_id = 1u + (uint32_t)g;
   const int nvec = K / 8;                      // 16-byte vectors per row
   const uint32_t row_bytes = 2u * (uint32_t)K;
-  const int64_t G = (int64_t)gridDim.x * kG;   // rows between a group's consecutive rows
-  const int64_t first = (int64_t)blockIdx.x * kG + g;
+  // Rows of the group: first, first + G, ... below row_end.  With several
+  // samples and at least as many blocks, each block takes the rows of one
+  // sample (blocks [s bps, (s + 1) bps) sample s), so that its modulation
+  // table serves every row it works on; else the whole grid strides over M.
+  const int64_t nsmp = (M + rows_per_sample - 1) / rows_per_sample;
+  int64_t G, first, row_end, table_smp;
+  if (nsmp > 1 && (int64_t)gridDim.x >= nsmp) {
+    const int64_t bps = (int64_t)gridDim.x / nsmp;   // blocks per sample
+    table_smp = (int64_t)blockIdx.x / bps;
+    if (table_smp >= nsmp) return;             // the grid's remainder blocks (uniform per block)
+    G = bps * kG;
+    first = table_smp * rows_per_sample + ((int64_t)blockIdx.x % bps) * kG + g;
+    row_end = (table_smp + 1) * rows_per_sample < M ? (table_smp + 1) * rows_per_sample : M;
+  } else {
+    G = (int64_t)gridDim.x * kG;
+    first = (int64_t)blockIdx.x * kG + g;
+    row_end = M;
+    table_smp = ((int64_t)blockIdx.x * kG) / rows_per_sample;   // the sample of the block's first row
+  }
   const uint32_t table_bytes = kTable ? 8u * (uint32_t)K : 0u;
   float4* table = reinterpret_cast<float4*>(ln_smem);
   uint8_t* ln_ring = ln_smem + table_bytes;
-  // The table holds the sample of the block's first row: entry c * nvec + j
+  // The table holds the modulation of sample table_smp: entry c * nvec + j
   // = (1 + scale, shift) of columns 8 j + 2 c and 8 j + 2 c + 1, so that
   // the lanes of a warp (consecutive j) read consecutive 16-byte words.
-  const int64_t table_smp = ((int64_t)blockIdx.x * kG) / rows_per_sample;
   if constexpr (kTable) {
     const uint32_t* sh0 = reinterpret_cast<const uint32_t*>(shift + table_smp * K);
     const uint32_t* sc0 = reinterpret_cast<const uint32_t*>(scale + table_smp * K);
@@ -459,8 +475,8 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
     }
     __syncthreads();
   }
-  if (first >= M) return;                      // uniform over the group
-  const int64_t nrows = (M - 1 - first) / G + 1;
+  if (first >= row_end) return;                // uniform over the group
+  const int64_t nrows = (row_end - 1 - first) / G + 1;
   const uint32_t ring = smem_u32(ln_ring) + (uint32_t)(g * stages) * row_bytes;
   if (lt == 0) {
     for (int st = 0; st < stages; ++st) mbar_init(smem_u32(&full[g][st]), 1);
