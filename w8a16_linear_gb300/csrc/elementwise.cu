@@ -295,10 +295,12 @@ __global__ void __launch_bounds__(256, kSwigluExBlocks) swiglu_ex_kernel(const u
 // takes the row's 16-byte vectors t, t + kT, ... (kV of them, K <= 8 kT kV):
 // 64 elements per thread at K = 4096, so the per-row reductions and barriers
 // are spread over many elements.  For K <= 4096 the block keeps a table of
-// fl32(1 + scale) and shift in binary32 for the sample of its first row
-// (shared memory, filled once); rows of another sample, and all rows when
-// K > 4096, read the bf16 modulation from global memory where h is formed.  Statistics in binary32, taken about the row's first element
-// p = x_0 (so that a large common offset of the row does not enter their
+// fl32(1 + scale) and shift in binary32 for one sample (shared memory,
+// filled once); with several samples and enough blocks each block works on
+// the rows of its table's sample only, otherwise rows of another sample
+// (and all rows when K > 4096) read the bf16 modulation from global memory
+// where h is formed.  Statistics in binary32, taken about the row's first
+// element p = x_0 (so that a large common offset of the row does not enter their
 // rounding errors), with summation trees of depth <= 13 (the thread's 4 kV
 // pairs pairwise, the last pair's two halves, five butterfly levels, the
 // group's 2 or 4 warp sums pairwise):
