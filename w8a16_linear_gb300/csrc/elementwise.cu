@@ -19,8 +19,10 @@
 //    (the pages name the block's norm/modulation before the quantization
 //    without a formula; this is the diffusion-transformer form).
 //
-// Each thread moves 16 elements per step with 128-bit loads and stores in a
-// grid-stride loop over a grid of as many blocks as fit on the GPU at once.
+// Each thread moves 16 elements per step (the dequantization: two 8-element
+// chunks of its warp's 512-element block) with 64- or 128-bit loads and
+// 128-bit stores in a grid-stride loop over a grid of as many blocks as fit
+// on the GPU at once.
 // Every output is the specification's bit pattern: a fast value with a
 // proven error bound is kept only where it provably rounds to the same code,
 // everything else is recomputed with correctly rounded, never-fused scalar
