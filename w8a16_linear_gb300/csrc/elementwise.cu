@@ -368,9 +368,9 @@ __device__ __forceinline__ void ln_modulation(bool from_table, const float4* tab
   if (kTable && from_table) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const float4 v = table[c * nvec + j];    // columns 8j + 2c, + 1: (1 + scale, shift) each
-      gc[c] = F2{v.x, v.z};
-      sf[c] = F2{v.y, v.w};
+      const float4 v = table[c * nvec + j];    // columns 8j + 2c, + 1: (1 + scale) x2, shift x2
+      gc[c] = F2{v.x, v.y};
+      sf[c] = F2{v.z, v.w};
     }
   } else {
     const uint4 shv = ldg16(sh_row + 8 * j);
@@ -405,8 +405,8 @@ __device__ __noinline__ void ln_fix_pairs(uint32_t mask, const uint16_t* xrow, u
     F2 gc, sf;
     if (kTable && from_table) {
       const float4 v = table[c * nvec + j];
-      gc = F2{v.x, v.z};
-      sf = F2{v.y, v.w};
+      gc = F2{v.x, v.y};
+      sf = F2{v.z, v.w};
     } else {
       const uint32_t sw = *reinterpret_cast<const uint32_t*>(sh_row + col);
       const uint32_t cw = *reinterpret_cast<const uint32_t*>(sc_row + col);
@@ -467,15 +467,16 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
   float4* table = reinterpret_cast<float4*>(ln_smem);
   uint8_t* ln_ring = ln_smem + table_bytes;
   // The table holds the modulation of sample table_smp: entry c * nvec + j
-  // = (1 + scale, shift) of columns 8 j + 2 c and 8 j + 2 c + 1, so that
+  // = (1 + scale) of columns 8 j + 2 c and 8 j + 2 c + 1, then their shift
+  // (each pair lands in an aligned register pair for the packed FMAs), so that
   // the lanes of a warp (consecutive j) read consecutive 16-byte words.
   if constexpr (kTable) {
     const uint32_t* sh0 = reinterpret_cast<const uint32_t*>(shift + table_smp * K);
     const uint32_t* sc0 = reinterpret_cast<const uint32_t*>(scale + table_smp * K);
     for (int pi = (int)threadIdx.x; pi < K / 2; pi += 256) {
       const uint32_t sw = __ldg(sh0 + pi), cw = __ldg(sc0 + pi);
-      table[(pi & 3) * nvec + (pi >> 2)] = make_float4(__fadd_rn(1.0f, bf16_lo(cw)), bf16_lo(sw),
-                                                       __fadd_rn(1.0f, bf16_hi(cw)), bf16_hi(sw));
+      table[(pi & 3) * nvec + (pi >> 2)] = make_float4(__fadd_rn(1.0f, bf16_lo(cw)), __fadd_rn(1.0f, bf16_hi(cw)),
+                                                       bf16_lo(sw), bf16_hi(sw));
     }
     __syncthreads();
   }
