@@ -42,7 +42,8 @@ def test_linear_configs(W, M, K, N, kw):
 @pytest.mark.parametrize("M,K,N", [
     (1, 16, 16), (3, 48, 16), (127, 128, 256), (129, 144, 272), (200, 4112, 48),
     (333, 384, 512), (130, 64, 16 * 33),
-    # W8A16 CTA-pair tiles (256 weight rows x 384 tokens): ragged M, N and K
+    # ragged M, N and K against the W8A16 kernels' tiles (the fused kernel's
+    # 128 weight rows x 320 tokens, the bf16 GEMM's 256 x 256)
     (1000, 256, 400), (777, 4112, 272), (385, 64, 16 * 17),
 ])
 def test_linear_ragged_shapes(W, M, K, N):
@@ -52,6 +53,24 @@ def test_linear_ragged_shapes(W, M, K, N):
     r16, _ = O.linear_w8a16(x, qw, s_w)
     assert gemm_err(y8, r8) <= GEMM_TOL
     assert gemm_err(y16, r16) <= GEMM_TOL
+
+
+def test_pages_calibrated_scale_magnitudes(W):
+    """The calibrated maxima of one 4096 -> 4096 linear on the pages
+    (diffusers issue #15170, Logs: input amax 0.5430, weight amax 0.5039,
+    MaxCalibrator): s_in = 0.5430 / 448 and s_w = 0.5039 / 448, with the
+    activation and the weight drawn to exactly those maxima."""
+    M, K, N = 512, 4096, 4096
+    s_in, s_w = np.float32(0.5430 / 448), np.float32(0.5039 / 448)
+    xf = synth.normal_f32(41, (M, K), 0.12)
+    x = O.bf16_round(xf * np.float32(0.5430 / np.abs(xf).max()))
+    wf = synth.normal_f32(42, (N, K), 0.02)
+    qw = O.e4m3_encode((wf * np.float32(0.5039 / np.abs(wf).max())) / s_w)
+    y8, y16 = _run_both(W, x, qw, s_in, s_w)
+    r8, _ = O.linear_w8a8(O.quant_static(x, s_in), qw, s_in, s_w)
+    r16, _ = O.linear_w8a16(x, qw, s_w)
+    assert gemm_err(y8, r8) <= GEMM_TOL and gemm_err(y16, r16) <= GEMM_TOL
+    assert frac_rounded_equal(y8, r8) >= 0.98 and frac_rounded_equal(y16, r16) >= 0.98
 
 
 def test_w8a8_exact_sums_bit_exact(W):
