@@ -63,6 +63,18 @@ constexpr int kDequantU = 2, kDequantBlocks = 4;
 constexpr int kSwigluU = 1, kSwigluBlocks = 4;
 constexpr int kSwigluExU = 1, kSwigluExBlocks = 6;
 
+// A 16-byte streaming load that leaves no line in L1.  The quantization reads
+// each byte of x once; without L1 allocation it measured 36.9 against 38.9 µs
+// at 20670x4096 (same process, L2 flushed, both orders).  The two-input
+// SwiGLU kernels measured 0-1.6% slower with it and keep the plain load.
+__device__ __forceinline__ uint4 ldg16_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 template <int U>
 __global__ void __launch_bounds__(256, kQuantBlocks) quant_static_kernel(const uint16_t* __restrict__ x, int64_t n16,
                                                               const float* __restrict__ s_in,
@@ -78,8 +90,8 @@ __global__ void __launch_bounds__(256, kQuantBlocks) quant_static_kernel(const u
     for (int j = 0; j < U; ++j) {
       const int64_t v = i + j * stride;
       if (v < n16) {
-        a[j] = ldg16(x + v * 16);
-        b[j] = ldg16(x + v * 16 + 8);
+        a[j] = ldg16_stream(x + v * 16);
+        b[j] = ldg16_stream(x + v * 16 + 8);
       }
     }
 #pragma unroll
@@ -497,12 +509,19 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
       bulk_load(ring + (uint32_t)issued * row_bytes, x + (first + issued * G) * K, row_bytes, bar);
     }
   }
-  float s = 1.0f, rs = 1.0f;
+  // The bracket of the codes with the reciprocal folded into its ends:
+  // lo = fl(h * fl(rs (1 - 2^-21))), hi likewise.  The rounding of the
+  // scaled reciprocal takes the place of the rounding of h * rs, so the
+  // error against fl32(h / s) stays within the 4 * 2^-24 of the unfolded
+  // bracket; the ends stay normal while rs >= 2^-125.
+  float s = 1.0f, rlo = 1.0f, rhi = 1.0f;
   bool exact_only = false;
   if constexpr (kQ) {
     s = __ldg(s_in);
-    rs = __frcp_rn(s);
-    exact_only = !scale_is_fast(s, rs);
+    const float rs = __frcp_rn(s);
+    exact_only = !scale_is_fast(s, rs) || fabsf(rs) < 2.35098870e-38f;
+    rlo = __fmul_rn(rs, kQuantBracketLo);
+    rhi = __fmul_rn(rs, kQuantBracketHi);
   }
   uint32_t live = 0;                           // mask bits of the thread's pairs that hold row data
 #pragma unroll
@@ -595,8 +614,7 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           bool unsettled;
-          code[c] = e4m3x2_bracket(mul2(F2{bf16_lo(hb[c]), bf16_hi(hb[c])}, splat(rs)), kQuantBracketLo,
-                                   kQuantBracketHi, unsettled);
+          code[c] = e4m3x2_bracket(F2{bf16_lo(hb[c]), bf16_hi(hb[c])}, rlo, rhi, unsettled);
           unsettled_mask |= (uint32_t)unsettled << (4 * i + c);
         }
         *reinterpret_cast<uint2*>(q + row * K + 8 * j) =
