@@ -273,6 +273,40 @@ def _time(fn, flush, stream, n):
     return statistics.median(a.elapsed_time(b) for a, b in ev)
 
 
+# After a power-capped GEMM the SM clock stays near 1.46 GHz for some 50 ms
+# (sw_power_cap) and is back at 2.07 GHz after about 350 ms of idle.  An
+# elementwise kernel timed inside that window runs up to 1.4x slower (the
+# fused LayerNorm 84-88 against 61.4 us, the quantization 45-47 against
+# 37 us, at 20670 x 4096), so each is timed twice: alone, after an idle that
+# lets the clock recover (the state the measured HBM copy peak was taken
+# in), and right after a burst of headline steps (the clock it sees between
+# the GEMMs of a block step).
+SETTLE_S = 0.4
+GEMM_BURST_STEPS = 160              # about 100 ms of Q/K/V steps
+
+
+def _time_alone(fn, flush, stream, n):
+    torch.cuda.synchronize()
+    time.sleep(SETTLE_S)
+    return _time(fn, flush, stream, n)
+
+
+def _time_after_gemm(fn, blk, W, flush, stream, n):
+    torch.cuda.synchronize()
+    for _ in range(GEMM_BURST_STEPS):
+        blk.qkv_step(W)
+    return _time(fn, flush, stream, n)
+
+
+def _elementwise(fn, nbytes, blk, W, flush, stream, n, **extra):
+    """One elementwise line: time and bandwidth alone (the headline figures)
+    and right after GEMM work."""
+    ms = _time_alone(fn, flush, stream, n)
+    ms_g = _time_after_gemm(fn, blk, W, flush, stream, n)
+    return {"us": ms * 1e3, "GB_s": nbytes / ms / 1e6, "us_after_gemm": ms_g * 1e3,
+            "GB_s_after_gemm": nbytes / ms_g / 1e6, **extra}
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, dev):
@@ -460,23 +494,23 @@ def breakdown_ours(W, blk, flush, stream, args):
                flush, stream, n)
     out["fp8_linear_w8a8_4096x4096"] = {"us": ms * 1e3, "TFLOPS": lin_flops / ms / 1e9,
                                         "note": "one projection: quantization + W8A8 GEMM, M=20670"}
-    ms = _time(lambda: W.fp8_quant_static(blk.x_qkv, w.s_qkv, out=blk.ws), flush, stream, n)
-    out["fp8_quant_static"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6}
+    ew = dict(blk=blk, W=W, flush=flush, stream=stream, n=n)
+    out["fp8_quant_static"] = _elementwise(lambda: W.fp8_quant_static(blk.x_qkv, w.s_qkv, out=blk.ws),
+                                           3 * blk.x_qkv.numel(), **ew)
     gu = r.y_gu
     W.fp8_linear_w8a8_group(W.fp8_quant_static(blk.x_mlp, w.s_mlp), w.s_mlp, [q for q, _ in w.gu],
                             [s for _, s in w.gu], outs=gu)
-    ms = _time(lambda: W.swiglu_2in_fp8(gu[0], gu[1], w.s_h, out=r.h8), flush, stream, n)
-    out["swiglu_2in_fp8"] = {"us": ms * 1e3, "GB_s": 5 * r.h8.numel() / ms / 1e6}
-    ms = _time(lambda: W.swiglu_2in_bf16(gu[0], gu[1], out=r.h16), flush, stream, n)
-    out["swiglu_2in_bf16"] = {"us": ms * 1e3, "GB_s": 6 * r.h16.numel() / ms / 1e6}
+    out["swiglu_2in_fp8"] = _elementwise(lambda: W.swiglu_2in_fp8(gu[0], gu[1], w.s_h, out=r.h8),
+                                         5 * r.h8.numel(), **ew)
+    out["swiglu_2in_bf16"] = _elementwise(lambda: W.swiglu_2in_bf16(gu[0], gu[1], out=r.h16),
+                                          6 * r.h16.numel(), **ew)
     # the variant op with the limit / alpha / beta options on the same tensors
     opts = dict(limit=7.0, alpha=1.702, beta=1.0)
-    ms = _time(lambda: W.swiglu_2in_ex_fp8(gu[0], gu[1], w.s_h, out=r.h8, **opts), flush, stream, n)
-    out["swiglu_2in_ex_fp8"] = {"us": ms * 1e3, "GB_s": 5 * r.h8.numel() / ms / 1e6,
-                                "note": "limit 7, alpha 1.702, beta 1, bf16 in"}
-    ms = _time(lambda: W.swiglu_2in_ex_16(gu[0], gu[1], out=r.h16, **opts), flush, stream, n)
-    out["swiglu_2in_ex_16"] = {"us": ms * 1e3, "GB_s": 6 * r.h16.numel() / ms / 1e6,
-                               "note": "limit 7, alpha 1.702, beta 1, bf16 in and out"}
+    out["swiglu_2in_ex_fp8"] = _elementwise(lambda: W.swiglu_2in_ex_fp8(gu[0], gu[1], w.s_h, out=r.h8, **opts),
+                                            5 * r.h8.numel(), note="limit 7, alpha 1.702, beta 1, bf16 in", **ew)
+    out["swiglu_2in_ex_16"] = _elementwise(lambda: W.swiglu_2in_ex_16(gu[0], gu[1], out=r.h16, **opts),
+                                           6 * r.h16.numel(),
+                                           note="limit 7, alpha 1.702, beta 1, bf16 in and out", **ew)
     # library reference points on the Q/K/V shape (context only, not this path):
     # cuBLASLt FP8 through torch._scaled_mm on the pre-quantized activation,
     # cuBLAS bf16 through torch.matmul on weights dequantized beforehand
@@ -525,9 +559,9 @@ def breakdown_ours(W, blk, flush, stream, args):
                                                outs=[r.y_down], ws=blk.wsd), flush, stream, n)
     out["w8a16_down_16384x4096"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9,
                                     "note": "dequantization into the workspace + bf16 GEMM"}
-    ms = _time(lambda: W.fp8_dequant_weight(w.gu[0][0], w.gu[0][1], out=blk.wsd[:INTER * HID].view(INTER, HID)),
-               flush, stream, n)
-    out["fp8_dequant_weight_16384x4096"] = {"us": ms * 1e3, "GB_s": 3 * INTER * HID / ms / 1e6}
+    out["fp8_dequant_weight_16384x4096"] = _elementwise(
+        lambda: W.fp8_dequant_weight(w.gu[0][0], w.gu[0][1], out=blk.wsd[:INTER * HID].view(INTER, HID)),
+        3 * INTER * HID, **ew)
     # the producer of a linear input with the static quantization fused after
     # it (modulated LayerNorm -> bf16 -> E4M3), against the same two steps
     # run apart (bf16 h written and read back)
@@ -535,16 +569,15 @@ def breakdown_ours(W, blk, flush, stream, args):
     shift, scale = ((torch.randn((1, HID), generator=gen, device=blk.dev) * 0.5).to(torch.bfloat16)
                     for _ in range(2))
     hb = r.y_qkv[0]
-    ms = _time(lambda: W.ln_modulate_quant(blk.x_qkv, shift, scale, w.s_qkv, out=blk.ws), flush, stream, n)
-    out["ln_modulate_quant"] = {"us": ms * 1e3, "GB_s": 3 * blk.x_qkv.numel() / ms / 1e6,
-                                "note": "LayerNorm + shift/scale + bf16 + E4M3 in one pass, [20670, 4096]"}
+    out["ln_modulate_quant"] = _elementwise(
+        lambda: W.ln_modulate_quant(blk.x_qkv, shift, scale, w.s_qkv, out=blk.ws), 3 * blk.x_qkv.numel(),
+        note="LayerNorm + shift/scale + bf16 + E4M3 in one pass, [20670, 4096]", **ew)
 
     def ln_unfused():
         W.ln_modulate_bf16(blk.x_qkv, shift, scale, out=hb)
         W.fp8_quant_static(hb, w.s_qkv, out=blk.ws)
-    ms = _time(ln_unfused, flush, stream, n)
-    out["ln_modulate_then_quant"] = {"us": ms * 1e3, "GB_s": 7 * blk.x_qkv.numel() / ms / 1e6,
-                                     "note": "the same as two launches (bf16 h through HBM)"}
+    out["ln_modulate_then_quant"] = _elementwise(ln_unfused, 7 * blk.x_qkv.numel(),
+                                                 note="the same as two launches (bf16 h through HBM)", **ew)
     # configs 1 and 2 of the workload list on the GPU, next to their oracle
     # timings below
     for name, (M, K, N) in (("config1_64x256x256", (64, 256, 256)), ("config2_4096x4096x4096", (4096, 4096, 4096))):
@@ -891,6 +924,12 @@ def run_case(args):
         shift, scale = ((torch.randn((1, HID), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
                         for _ in range(2))
         fn = lambda: W.ln_modulate_quant(xl, shift, scale, s, out=ql)  # noqa: E731
+    elif args.case == "quant20k":
+        # the static quantization of the Q/K/V input at the bench's size (the
+        # 169 MB of x larger than L2)
+        xl = (torch.randn((M_TOK, HID), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
+        ql = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
+        fn = lambda: W.fp8_quant_static(xl, s, out=ql)  # noqa: E731
     elif args.case == "swiglu8k":
         gg = (torch.randn((M, INTER), generator=gen, device=dev) * 2).to(torch.bfloat16)
         uu = torch.randn((M, INTER), generator=gen, device=dev).to(torch.bfloat16)
@@ -946,7 +985,7 @@ def main():
     ap.add_argument("--no-breakdown", action="store_true",
                     help="print the headline line without the breakdown (for launch-list captures)")
     ap.add_argument("--case", default=None,
-                    help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, ln20k, dequant16k, block_gemms, qkv_sustained, host_link) instead of the bench")
+                    help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, ln20k, quant20k, dequant16k, block_gemms, qkv_sustained, host_link) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.case:
