@@ -179,25 +179,45 @@ def _midpoint_shift(K, n_mid, seed):
     return O.bf16_round(vals).astype(np.uint16)[None, :]
 
 
+def _near_tie_shift_448(K, n_mid, seed):
+    """A shift vector with n_mid entries +-3 * 2^k, k in [-16, -2]: their
+    quotients by fl32(1/448) lie within 2^-24 of the E4M3 midpoint
+    21 * 2^(k+6) in the normal range; the rest N(0, 0.05^2)."""
+    rng = np.random.default_rng(seed)
+    vals = rng.normal(0.0, 0.05, K)
+    vals[:n_mid] = 3.0 * np.exp2(rng.integers(-16, -1, n_mid)) * rng.choice([-1.0, 1.0], n_mid)
+    rng.shuffle(vals)
+    return O.bf16_round(vals).astype(np.uint16)[None, :]
+
+
 @pytest.mark.parametrize("n_mid", [40, 4096])
-def test_unsettled_pairs(W, n_mid):
-    """Rows whose h are E4M3 ties at s = 1: the bracket test cannot settle
-    them, so each thread recomputes its marked pairs after the row and stores
-    the division's codes (a few per row, or every element of the row).
-    Codes equal the static quantization of h (ties to even)."""
+@pytest.mark.parametrize("s", [1.0, 1.0 / 448])
+def test_unsettled_pairs(W, n_mid, s):
+    """Rows whose h sit on E4M3 rounding midpoints of h / s.  At s = 1 the
+    products h * (1/s) are h / s itself, so every pair settles on the fast
+    form (power-of-two scale).  At s = fl32(1/448) the quotients lie within
+    2^-24 of a midpoint: the bracket test cannot settle them, so each thread
+    recomputes its marked pairs after the row and stores the division's codes
+    (a few per row, or every element of the row).  Codes equal the static
+    quantization of h (ties to even)."""
     M, K = 24, 4096
     x = np.repeat(O.bf16_round(np.linspace(-1, 1, M)).astype(np.uint16)[:, None], K, axis=1)   # constant rows
-    shift = _midpoint_shift(K, n_mid, seed=n_mid)
+    shift = _midpoint_shift(K, n_mid, seed=n_mid) if s == 1.0 else _near_tie_shift_448(K, n_mid, seed=n_mid)
     scale = np.zeros((1, K), dtype=np.uint16)
-    q, h = _run(W, x, shift, scale, 1e-6, np.float32(1.0))
+    s_in = np.float32(s)
+    q, h = _run(W, x, shift, scale, 1e-6, s_in)
     assert np.array_equal(h, np.repeat(shift, M, axis=0))
-    assert np.array_equal(q, O.quant_static(h, np.float32(1.0)))
+    assert np.array_equal(q, O.quant_static(h, s_in))
 
 
-@pytest.mark.parametrize("s,K", [(2e38, 2048), (1e-39, 2048), (2e38, 8192), (1e-39, 200)])
+@pytest.mark.parametrize("s,K", [(2e38, 2048), (1e-39, 2048), (2e38, 8192), (1e-39, 200), (6e37, 2048),
+                                 (3e37, 1000)])
 def test_scale_outside_fast_range(W, s, K):
-    """Scales whose reciprocal is not a normal binary32 number: every pair
-    takes the division, recomputed by its thread after the row."""
+    """Scales whose reciprocal is not a normal binary32 number, or is normal
+    but below 2^-125 (6e37: the bracket's ends, the reciprocal times
+    1 -/+ 2^-21, could leave the normal range): every pair takes the
+    division, recomputed by its thread after the row.  3e37 is the nearest
+    side of that limit, where the folded ends are still used."""
     M, S = 40, 2
     x, shift, scale = _problem(M, K, S, seed=13)
     q, h = _run(W, x, shift, scale, 1e-6, np.float32(s))

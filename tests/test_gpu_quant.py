@@ -18,7 +18,8 @@ def _nan_ok(got, want, x_bits):
     assert np.all((got[isnan] & 0x7F) == 0x7F)
 
 
-@pytest.mark.parametrize("s", [0.5430 / 448, 0.5039 / 448, 2.0 ** -10, 1.0, 0.0123, 3.7, 1e-30, 2e38])
+@pytest.mark.parametrize("s", [0.5430 / 448, 0.5039 / 448, 2.0 ** -10, 1.0, 0.0123, 3.7, 1e-30, 2e38,
+                               2.0 ** 125, 2.0 ** 126, 2.0 ** -126, 6e37, 3e37])
 def test_quant_exhaustive_bf16(W, s):
     bits = np.arange(1 << 16, dtype=np.uint16).reshape(4096, 16)
     got = host_u8(W.fp8_quant_static(dev_bf16(bits), dev_f32(s)))

@@ -81,8 +81,7 @@ __global__ void __launch_bounds__(256, kQuantBlocks) quant_static_kernel(const u
                                                               uint8_t* __restrict__ q) {
   griddep_launch_dependents();   // a GEMM launched next may start its prologue
   const float s = __ldg(s_in);
-  const float r = __frcp_rn(s);
-  const bool exact_only = !scale_is_fast(s, r);
+  const QuantBracket br = quant_bracket(s);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += U * stride) {
     uint4 a[U], b[U];
@@ -99,10 +98,10 @@ __global__ void __launch_bounds__(256, kQuantBlocks) quant_static_kernel(const u
       const int64_t v = i + j * stride;
       if (v >= n16) break;
       uint4 o;
-      o.x = quant_pair(a[j].x, s, r, exact_only) | (quant_pair(a[j].y, s, r, exact_only) << 16);
-      o.y = quant_pair(a[j].z, s, r, exact_only) | (quant_pair(a[j].w, s, r, exact_only) << 16);
-      o.z = quant_pair(b[j].x, s, r, exact_only) | (quant_pair(b[j].y, s, r, exact_only) << 16);
-      o.w = quant_pair(b[j].z, s, r, exact_only) | (quant_pair(b[j].w, s, r, exact_only) << 16);
+      o.x = quant_pair(a[j].x, s, br) | (quant_pair(a[j].y, s, br) << 16);
+      o.y = quant_pair(a[j].z, s, br) | (quant_pair(a[j].w, s, br) << 16);
+      o.z = quant_pair(b[j].x, s, br) | (quant_pair(b[j].y, s, br) << 16);
+      o.w = quant_pair(b[j].z, s, br) | (quant_pair(b[j].w, s, br) << 16);
       *reinterpret_cast<uint4*>(q + v * 16) = o;
     }
   }
@@ -509,19 +508,15 @@ __global__ void __launch_bounds__(256, 2) ln_modulate_quant_kernel(
       bulk_load(ring + (uint32_t)issued * row_bytes, x + (first + issued * G) * K, row_bytes, bar);
     }
   }
-  // The bracket of the codes with the reciprocal folded into its ends:
-  // lo = fl(h * fl(rs (1 - 2^-21))), hi likewise.  The rounding of the
-  // scaled reciprocal takes the place of the rounding of h * rs, so the
-  // error against fl32(h / s) stays within the 4 * 2^-24 of the unfolded
-  // bracket; the ends stay normal while rs >= 2^-125.
+  // the codes' bracket ends, the reciprocal of s folded in (quant_spec.cuh)
   float s = 1.0f, rlo = 1.0f, rhi = 1.0f;
   bool exact_only = false;
   if constexpr (kQ) {
     s = __ldg(s_in);
-    const float rs = __frcp_rn(s);
-    exact_only = !scale_is_fast(s, rs) || fabsf(rs) < 2.35098870e-38f;
-    rlo = __fmul_rn(rs, kQuantBracketLo);
-    rhi = __fmul_rn(rs, kQuantBracketHi);
+    const QuantBracket br = quant_bracket(s);
+    rlo = br.lo;
+    rhi = br.hi;
+    exact_only = br.exact_only;
   }
   uint32_t live = 0;                           // mask bits of the thread's pairs that hold row data
 #pragma unroll
