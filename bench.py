@@ -926,10 +926,12 @@ def run_case(args):
         fn = lambda: W.ln_modulate_quant(xl, shift, scale, s, out=ql)  # noqa: E731
     elif args.case == "quant20k":
         # the static quantization of the Q/K/V input at the bench's size (the
-        # 169 MB of x larger than L2)
+        # 169 MB of x larger than L2), with a calibrated scale (amax / 448 of
+        # a separately drawn batch, as the bench's block uses)
         xl = (torch.randn((M_TOK, HID), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
         ql = torch.empty((M_TOK, HID), dtype=torch.uint8, device=dev)
-        fn = lambda: W.fp8_quant_static(xl, s, out=ql)  # noqa: E731
+        sq = _amax_scale(_act(gen, dev, 4096, HID))
+        fn = lambda: W.fp8_quant_static(xl, sq, out=ql)  # noqa: E731
     elif args.case == "swiglu8k":
         gg = (torch.randn((M, INTER), generator=gen, device=dev) * 2).to(torch.bfloat16)
         uu = torch.randn((M, INTER), generator=gen, device=dev).to(torch.bfloat16)
