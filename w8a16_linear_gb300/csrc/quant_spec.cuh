@@ -19,7 +19,7 @@ namespace {
 // the bracket are fl(x * fl(r (1 - 2^-21))) and fl(x * fl(r (1 + 2^-21))):
 // against the exact quotient, r, the scaled reciprocal and the product each
 // round once (2^-24), the specification's quotient once more, so the ends lie
-// below and above fl32(x / s) while 4 * 2^-24 < 2^-21.  That holds when s and
+// on either side of fl32(x / s) while 4 * 2^-24 < 2^-21.  That holds when s and
 // r are normal and r >= 2^-125, which keeps the scaled reciprocals normal (a
 // product in the binary32 subnormal range is below every E4M3 rounding
 // boundary, as is the specified value).  Equal codes at both ends are the
