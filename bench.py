@@ -755,6 +755,12 @@ def run_case(args):
         fn = lambda: blk.gemm_launches(W, *qa)  # noqa: E731
     elif args.case == "qkv8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A8, x, s, qs, ss, outs=ys, ws=qx)  # noqa: E731
+    elif args.case == "lin4k":
+        # the single 4096 -> 4096 linear at M = 4096 tokens: one W8A8 GEMM
+        # launch on E4M3 codes (operands 33.5 MB, output 33.5 MB)
+        q4 = W.fp8_quant_static(x[:4096], s)
+        y4 = ys[0][:4096]
+        fn = lambda: W.fp8_linear_w8a8_group(q4, s, qs[:1], ss[:1], outs=[y4])  # noqa: E731
     elif args.case == "w8a16_dq_8k":
         # dequant + F.linear: the three weights into a workspace, one bf16 group GEMM
         wsd = W.w8a16_workspace(qs)
@@ -987,7 +993,7 @@ def main():
     ap.add_argument("--no-breakdown", action="store_true",
                     help="print the headline line without the breakdown (for launch-list captures)")
     ap.add_argument("--case", default=None,
-                    help="run a profiling case (qkv8k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, ln20k, quant20k, dequant16k, block_gemms, qkv_sustained, host_link) instead of the bench")
+                    help="run a profiling case (qkv8k, lin4k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, ln20k, quant20k, dequant16k, block_gemms, qkv_sustained, host_link) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.case:

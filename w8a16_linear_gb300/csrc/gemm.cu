@@ -1026,15 +1026,15 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   l2_plan(w_bytes, (int64_t)BM * CG * p.K * kEl, tiles_m, args);
   const int max_clusters = sms / CG;
   const int clusters = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
-  // The last wave's tiles, if they fill at most half (a quarter) of the
-  // clusters, are cut in two (four) column slices (not GLU, whose tile
-  // columns pair gate with up; not single CTAs).
+  // The last wave's tiles, if they fill at most half of the clusters, are
+  // cut in two column slices (not GLU, whose tile columns pair gate with up;
+  // not single CTAs).  A slice is an N = 128 MMA, which does half a tile's
+  // work in about 0.8 of its time; N = 64 quarter slices took almost a whole
+  // tile's time, so cutting in four measured slower than in two (the Q/K/V
+  // group at M = 20670: 555 against 549-551 us) and is not used.
   const int tail = args.num_tiles % clusters;
   args.tail_split = 1;
-  if (!kGlu && CG == 2 && tail > 0) {
-    if (4 * tail <= clusters) args.tail_split = 4;
-    else if (2 * tail <= clusters) args.tail_split = 2;
-  }
+  if (!kGlu && CG == 2 && tail > 0 && 2 * tail <= clusters) args.tail_split = 2;
   args.num_full = args.num_tiles - (args.tail_split > 1 ? tail : 0);
   args.num_units = args.num_full + (args.num_tiles - args.num_full) * args.tail_split;
   return launch_cluster(gemm_kernel<MODE, CG>, clusters * CG, L::kThreads, L::kAlloc, CG, st, maps,
