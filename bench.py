@@ -1070,7 +1070,11 @@ def main():
                             "computes and its three outputs copied out while the next one computes (two "
                             "device buffer sets); inputs larger than L2"},
             "gpu_launches": r["launches"],
-            "clocks": r["clocks"],
+            "clocks": {**r["clocks"],
+                       "note": "nvidia-smi samples every 100 ms from just before the timed steps to 0.25 s "
+                               "after them; the steps take about 16 ms, so most samples fall around them. "
+                               "Inside, the GEMM runs at the power cap (about 1.4-1.5 GHz, sw_power_cap) "
+                               "within a few microseconds of its first MMAs."},
             "breakdown": bd,
         }
         print(json.dumps(line), flush=True)
