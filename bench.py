@@ -579,7 +579,8 @@ def breakdown_ours(W, blk, flush, stream, args):
     out["ln_modulate_then_quant"] = _elementwise(ln_unfused, 7 * blk.x_qkv.numel(),
                                                  note="the same as two launches (bf16 h through HBM)", **ew)
     # configs 1 and 2 of the workload list on the GPU, next to their oracle
-    # timings below
+    # timings below; each call is a short burst, timed alone (after an idle
+    # that lets the SM clock leave the power-cap state the lines above leave)
     for name, (M, K, N) in (("config1_64x256x256", (64, 256, 256)), ("config2_4096x4096x4096", (4096, 4096, 4096))):
         xs = blk.x_qkv[:M, :K].contiguous()
         wq0 = wq[0][:N, :K].contiguous()
@@ -587,8 +588,8 @@ def breakdown_ours(W, blk, flush, stream, args):
         ws0 = torch.empty((M, K), dtype=torch.uint8, device=blk.dev)
         wsd0 = torch.empty((N * K,), dtype=torch.bfloat16, device=blk.dev)
         fl = 2.0 * M * N * K
-        ms8 = _time(lambda: W.fp8_linear_w8a8(xs, wq0, w.s_qkv, sq[0], out=y0, ws=ws0), flush, stream, n)
-        ms16 = _time(lambda: W.fp8_linear_w8a16(xs, wq0, sq[0], out=y0, ws=wsd0), flush, stream, n)
+        ms8 = _time_alone(lambda: W.fp8_linear_w8a8(xs, wq0, w.s_qkv, sq[0], out=y0, ws=ws0), flush, stream, n)
+        ms16 = _time_alone(lambda: W.fp8_linear_w8a16(xs, wq0, sq[0], out=y0, ws=wsd0), flush, stream, n)
         out[name] = {"w8a8_us": ms8 * 1e3, "w8a8_TFLOPS": fl / ms8 / 1e9,
                      "w8a16_us": ms16 * 1e3, "w8a16_TFLOPS": fl / ms16 / 1e9}
     torch.cuda.synchronize()
