@@ -549,6 +549,11 @@ def breakdown_ours(W, blk, flush, stream, args):
                                             out=r.h8), flush, stream, n)
     out["glu_gate_up_swiglu_fp8"] = {"us": ms * 1e3, "TFLOPS": 4.0 * M_TOK * HID * INTER / ms / 1e9,
                                      "note": "fused gate+up GEMMs (E4M3 input) with SwiGLU->E4M3 epilogue"}
+    ms = _time(lambda: W.gate_up_swiglu_fp8(q, w.s_mlp, w.gu[0][0], w.gu[1][0], w.gu[0][1], w.gu[1][1], w.s_h,
+                                            out=r.h8, limit=7.0, alpha=1.702, beta=1.0), flush, stream, n)
+    out["glu_gate_up_swiglu_ex_fp8"] = {"us": ms * 1e3, "TFLOPS": 4.0 * M_TOK * HID * INTER / ms / 1e9,
+                                        "note": "the same with the SwiGLU options in the epilogue "
+                                                "(limit 7, alpha 1.702, beta 1)"}
     ms = _time(lambda: W.fp8_linear_w8a8_group(q, w.s_mlp, [w.gu[0][0]], [w.gu[0][1]], outs=[gu[0]]),
                flush, stream, n)
     out["w8a8_gate_4096x16384"] = {"us": ms * 1e3, "TFLOPS": 2.0 * M_TOK * HID * INTER / ms / 1e9}

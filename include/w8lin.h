@@ -351,6 +351,31 @@ w8_status swiglu_2in_ex_16(const void* gate, const void* up, int32_t in_dtype, i
                            const w8_swiglu_params* prm, void* out, void* stream);
 
 /*
+ * gate_up_swiglu_ex_fp8 — gate_up_swiglu_fp8 with the SwiGLU options in its
+ * epilogue ([P4] Test Coverage: swiglu_limit, swiglu_alpha + swiglu_beta).
+ * The bf16 gate and up values are those of the separate projections (as in
+ * gate_up_swiglu_fp8); the codes are swiglu_2in_ex_fp8's on them, bit for bit.
+ *   prm   host struct, read during the call only; {0, 0, 1, 0} gives
+ *         gate_up_swiglu_fp8's codes.
+ * Other arguments, layouts and errors as gate_up_swiglu_fp8, plus PARAM.
+ */
+w8_status gate_up_swiglu_ex_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t K,
+                                const float* s_in, const uint8_t* w_gate, const uint8_t* w_up,
+                                int64_t I, const float* s_w_gate, const float* s_w_up,
+                                const w8_swiglu_params* prm, const float* s_out, uint8_t* out,
+                                uint8_t* ws, void* stream);
+
+/*
+ * bf16_gate_up_swiglu_ex — bf16_gate_up_swiglu with the SwiGLU options: the
+ * bf16 outputs are swiglu_2in_ex_16's (bf16 inputs) on the bf16 gate and up
+ * values of the separate projections, bit for bit.  prm as above.
+ * Other arguments, layouts and errors as bf16_gate_up_swiglu, plus PARAM.
+ */
+w8_status bf16_gate_up_swiglu_ex(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wd_gate,
+                                 const uint16_t* wd_up, int64_t I, const w8_swiglu_params* prm,
+                                 uint16_t* out, void* stream);
+
+/*
  * ln_modulate_quant — the producer of a linear layer's input with the static
  * quantization fused after it.  The pages place the quantization right after
  * the block's norm/modulation ([P2] Verification: div -> clamp ->

@@ -35,7 +35,7 @@ def test_header_symbols_exported(L):
     for n in names:
         assert hasattr(L, n), n
         assert n in binding.SIGNATURES, n
-    assert L.w8_abi_version() == 5
+    assert L.w8_abi_version() == 6
 
 
 def test_policy_matches_oracle_everywhere(L):
@@ -210,3 +210,34 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         b.abi_version()
     with pytest.raises(ImportError):
         b.step_policy_dispatch(None, 0, 8)
+
+
+def test_fused_swiglu_options_validation_before_any_cuda_call(L):
+    """The fused gate/up entries with SwiGLU options refuse NULL or
+    out-of-range options (W8_ERR_NULL, W8_ERR_PARAM) before touching the
+    operands, and a zero-row call with valid options launches nothing."""
+    from w8a16_linear_gb300 import binding as b
+    p16 = _u(0x10000)
+    ref = ctypes.byref
+    ok = b.SwigluParams(1, 7.0, 1.702, 1.0)
+    bad = b.SwigluParams(1, -1.0, 1.0, 0.0)
+
+    def fp8(prm, M):
+        return L.gate_up_swiglu_ex_fp8(p16, 1, M, 16, p16, p16, p16, 16, p16, p16, prm, p16, p16, p16, None)
+
+    def bf16(prm, M):
+        return L.bf16_gate_up_swiglu_ex(p16, M, 16, p16, p16, 16, prm, p16, None)
+
+    assert fp8(None, 4) == 1
+    assert fp8(ref(bad), 4) == 11
+    assert b"gate_up_swiglu_ex_fp8" in L.w8_last_error()
+    assert fp8(ref(b.SwigluParams(0, 0.0, float("nan"), 0.0)), 4) == 11
+    assert fp8(ref(ok), 0) == 0
+    assert bf16(None, 4) == 1
+    assert bf16(ref(bad), 4) == 11
+    assert b"bf16_gate_up_swiglu_ex" in L.w8_last_error()
+    assert bf16(ref(ok), 0) == 0
+    # operand checks as the plain entries: K not a multiple of 16
+    assert L.gate_up_swiglu_ex_fp8(p16, 1, 4, 24, p16, p16, p16, 16, p16, p16, ref(ok), p16, p16, p16,
+                                   None) == L.gate_up_swiglu_fp8(p16, 1, 4, 24, p16, p16, p16, 16, p16, p16, p16,
+                                                                 p16, p16, None)

@@ -77,6 +77,11 @@ SIGNATURES = {
                                          _c_void_p, _c_void_p, _c_void_p]),
     "swiglu_2in_ex_16": (ctypes.c_int, [_c_void_p, _c_void_p, _i32, _i64, _i64, ctypes.POINTER(SwigluParams),
                                         _c_void_p, _c_void_p]),
+    "gate_up_swiglu_ex_fp8": (ctypes.c_int, [_c_void_p, _i32, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
+                                             _i64, _c_void_p, _c_void_p, ctypes.POINTER(SwigluParams),
+                                             _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "bf16_gate_up_swiglu_ex": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i64,
+                                              ctypes.POINTER(SwigluParams), _c_void_p, _c_void_p]),
     "ln_modulate_quant": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i64, ctypes.c_float,
                                          _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "step_policy_dispatch": (ctypes.c_int, [_c_void_p, _i32, _i32, ctypes.POINTER(_i32)]),
@@ -371,8 +376,10 @@ def bf16_linear_group(x, wds, outs=None, stream=None):
     return outs
 
 
-def bf16_gate_up_swiglu(x, wd_gate, wd_up, out=None, stream=None):
-    """bf16 SwiGLU of the gate/up pair on dequantized bf16 weights, one launch."""
+def bf16_gate_up_swiglu(x, wd_gate, wd_up, out=None, stream=None, limit=None, alpha=None, beta=None):
+    """bf16 SwiGLU of the gate/up pair on dequantized bf16 weights, one launch.
+    With any of ``limit``, ``alpha``, ``beta`` given, the SwiGLU takes those
+    options (``bf16_gate_up_swiglu_ex``)."""
     x = _as_bf16(x, "x")
     x2 = _flat2(x)
     M, K = x2.shape
@@ -382,8 +389,13 @@ def bf16_gate_up_swiglu(x, wd_gate, wd_up, out=None, stream=None):
     I = wg.shape[0]
     if out is None:
         out = torch.empty(*x.shape[:-1], I, dtype=torch.bfloat16, device=x.device)
-    _check(lib().bf16_gate_up_swiglu(_ptr(x2), M, K, _ptr(wg), _ptr(wu), I, _ptr(_as_bf16(out, "out")),
-                                     _stream(stream)))
+    if limit is None and alpha is None and beta is None:
+        _check(lib().bf16_gate_up_swiglu(_ptr(x2), M, K, _ptr(wg), _ptr(wu), I, _ptr(_as_bf16(out, "out")),
+                                         _stream(stream)))
+    else:
+        prm = _swiglu_params(limit, 1.0 if alpha is None else alpha, 0.0 if beta is None else beta)
+        _check(lib().bf16_gate_up_swiglu_ex(_ptr(x2), M, K, _ptr(wg), _ptr(wu), I, ctypes.byref(prm),
+                                            _ptr(_as_bf16(out, "out")), _stream(stream)))
     return out
 
 
@@ -414,8 +426,11 @@ def fp8_linear_w8a8_group(qx, s_in, weights, weight_scales, outs=None, stream=No
     return outs
 
 
-def gate_up_swiglu_fp8(x, s_in, w_gate, w_up, s_w_gate, s_w_up, s_out, out=None, ws=None, stream=None):
-    """Fused gate/up W8A8 GEMMs + SwiGLU -> E4M3 [M, I] for the down projection."""
+def gate_up_swiglu_fp8(x, s_in, w_gate, w_up, s_w_gate, s_w_up, s_out, out=None, ws=None, stream=None,
+                       limit=None, alpha=None, beta=None):
+    """Fused gate/up W8A8 GEMMs + SwiGLU -> E4M3 [M, I] for the down projection.
+    With any of ``limit``, ``alpha``, ``beta`` given, the SwiGLU takes those
+    options (``gate_up_swiglu_ex_fp8``; alpha defaults to 1, beta to 0)."""
     if x.dtype == torch.bfloat16:
         xd, dt = _as_bf16(x, "x"), DTYPE_BF16
     else:
@@ -431,10 +446,17 @@ def gate_up_swiglu_fp8(x, s_in, w_gate, w_up, s_w_gate, s_w_up, s_out, out=None,
     o = _as_u8(out, "out")
     if dt == DTYPE_BF16 and ws is None:
         ws = torch.empty((M, K), dtype=torch.uint8, device=x.device)
-    _check(lib().gate_up_swiglu_fp8(_ptr(x2), dt, M, K, _ptr(_scalar(s_in, "s_in")), _ptr(wg), _ptr(wu), I,
-                                    _ptr(_scalar(s_w_gate, "s_w_gate")), _ptr(_scalar(s_w_up, "s_w_up")),
-                                    _ptr(_scalar(s_out, "s_out")), _ptr(o),
-                                    _ptr(_as_u8(ws, "ws") if ws is not None else None), _stream(stream)))
+    wsp = _ptr(_as_u8(ws, "ws") if ws is not None else None)
+    if limit is None and alpha is None and beta is None:
+        _check(lib().gate_up_swiglu_fp8(_ptr(x2), dt, M, K, _ptr(_scalar(s_in, "s_in")), _ptr(wg), _ptr(wu), I,
+                                        _ptr(_scalar(s_w_gate, "s_w_gate")), _ptr(_scalar(s_w_up, "s_w_up")),
+                                        _ptr(_scalar(s_out, "s_out")), _ptr(o), wsp, _stream(stream)))
+    else:
+        prm = _swiglu_params(limit, 1.0 if alpha is None else alpha, 0.0 if beta is None else beta)
+        _check(lib().gate_up_swiglu_ex_fp8(_ptr(x2), dt, M, K, _ptr(_scalar(s_in, "s_in")), _ptr(wg), _ptr(wu),
+                                           I, _ptr(_scalar(s_w_gate, "s_w_gate")),
+                                           _ptr(_scalar(s_w_up, "s_w_up")), ctypes.byref(prm),
+                                           _ptr(_scalar(s_out, "s_out")), _ptr(o), wsp, _stream(stream)))
     return out
 
 

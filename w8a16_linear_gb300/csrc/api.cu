@@ -95,7 +95,7 @@ int query_device(int* sms) { return device_info(sms); }
 
 extern "C" {
 
-int w8_abi_version(void) { return 5; }
+int w8_abi_version(void) { return 6; }
 
 const char* w8_last_error(void) { return g_last_error; }
 
@@ -350,14 +350,30 @@ w8_status bf16_linear_group(const uint16_t* x, int64_t M, int64_t K, int32_t G, 
   return cuda_status(e, "bf16_linear_group: GEMM launch");
 }
 
-w8_status bf16_gate_up_swiglu(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wd_gate,
-                              const uint16_t* wd_up, int64_t I, uint16_t* out, void* stream) {
+// The SwiGLU options, checked and copied (the standalone and the fused
+// forms share them).
+static w8_status check_swiglu_params(const char* fn, const w8_swiglu_params* prm, w8::SwigluExArgs* a) {
+  if (!prm) return fail(W8_ERR_NULL, "%s: NULL params", fn);
+  if (!std::isfinite(prm->alpha) || !std::isfinite(prm->beta))
+    return fail(W8_ERR_PARAM, "%s: alpha and beta must be finite", fn);
+  if (prm->has_limit && !(std::isfinite(prm->limit) && prm->limit > 0.0f))
+    return fail(W8_ERR_PARAM, "%s: limit must be finite and > 0", fn);
+  a->has_limit = prm->has_limit != 0;
+  a->limit = prm->limit;
+  a->alpha = prm->alpha;
+  a->beta = prm->beta;
+  return W8_OK;
+}
+
+static w8_status bf16_gate_up_swiglu_impl(const char* fn, const uint16_t* x, int64_t M, int64_t K,
+                                          const uint16_t* wd_gate, const uint16_t* wd_up, int64_t I,
+                                          const w8::SwigluExArgs* ex, uint16_t* out, void* stream) {
   static const float kOne = 1.0f;  // placeholder scale: the common check wants a pointer
   const uint8_t* wg = reinterpret_cast<const uint8_t*>(wd_gate);
   const uint8_t* wu = reinterpret_cast<const uint8_t*>(wd_up);
-  w8_status st = check_linear_common("bf16_gate_up_swiglu", x, M, K, wg, I, &kOne, out);
+  w8_status st = check_linear_common(fn, x, M, K, wg, I, &kOne, out);
   if (st != W8_OK) return st;
-  if ((st = check_linear_common("bf16_gate_up_swiglu", x, M, K, wu, I, &kOne, out)) != W8_OK) return st;
+  if ((st = check_linear_common(fn, x, M, K, wu, I, &kOne, out)) != W8_OK) return st;
   if (M == 0) return ok();
   int sms = 0;
   if ((st = device_info(&sms)) != W8_OK) return st;
@@ -371,10 +387,25 @@ w8_status bf16_gate_up_swiglu(const uint16_t* x, int64_t M, int64_t K, const uin
   p.N[0] = I;
   p.N[1] = I;
   p.y[0] = out;
+  p.ex = ex;
   int terr = 0;
   cudaError_t e = w8::launch_gemm_glu16(p, sms, static_cast<cudaStream_t>(stream), &terr);
-  if (terr) return fail(W8_ERR_ALIGN, "bf16_gate_up_swiglu: tensor map encoding rejected the operands");
+  if (terr) return fail(W8_ERR_ALIGN, "%s: tensor map encoding rejected the operands", fn);
   return cuda_status(e, "bf16_gate_up_swiglu: GEMM launch");
+}
+
+w8_status bf16_gate_up_swiglu(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wd_gate,
+                              const uint16_t* wd_up, int64_t I, uint16_t* out, void* stream) {
+  return bf16_gate_up_swiglu_impl("bf16_gate_up_swiglu", x, M, K, wd_gate, wd_up, I, nullptr, out, stream);
+}
+
+w8_status bf16_gate_up_swiglu_ex(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wd_gate,
+                                 const uint16_t* wd_up, int64_t I, const w8_swiglu_params* prm,
+                                 uint16_t* out, void* stream) {
+  w8::SwigluExArgs a{};
+  w8_status st = check_swiglu_params("bf16_gate_up_swiglu_ex", prm, &a);
+  if (st != W8_OK) return st;
+  return bf16_gate_up_swiglu_impl("bf16_gate_up_swiglu_ex", x, M, K, wd_gate, wd_up, I, &a, out, stream);
 }
 
 w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const float* s_in,
@@ -410,21 +441,21 @@ w8_status fp8_linear_w8a8_group(const uint8_t* qx, int64_t M, int64_t K, const f
   return cuda_status(e, "fp8_linear_w8a8_group: GEMM launch");
 }
 
-w8_status gate_up_swiglu_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t K,
-                             const float* s_in, const uint8_t* w_gate, const uint8_t* w_up,
-                             int64_t I, const float* s_w_gate, const float* s_w_up,
-                             const float* s_out, uint8_t* out, uint8_t* ws, void* stream) {
+static w8_status gate_up_swiglu_fp8_impl(const char* fn, const void* x, int32_t x_dtype, int64_t M,
+                                         int64_t K, const float* s_in, const uint8_t* w_gate,
+                                         const uint8_t* w_up, int64_t I, const float* s_w_gate,
+                                         const float* s_w_up, const w8::SwigluExArgs* ex, const float* s_out,
+                                         uint8_t* out, uint8_t* ws, void* stream) {
   if (x_dtype != W8_DTYPE_BF16 && x_dtype != W8_DTYPE_E4M3)
-    return fail(W8_ERR_DTYPE, "gate_up_swiglu_fp8: unknown activation dtype %d", x_dtype);
-  w8_status st = check_linear_common("gate_up_swiglu_fp8", x, M, K, w_gate, I, s_w_gate,
-                                     reinterpret_cast<const uint16_t*>(out));
+    return fail(W8_ERR_DTYPE, "%s: unknown activation dtype %d", fn, x_dtype);
+  w8_status st = check_linear_common(fn, x, M, K, w_gate, I, s_w_gate, reinterpret_cast<const uint16_t*>(out));
   if (st != W8_OK) return st;
   if (M == 0) return ok();
-  if (!w_up || !s_w_up || !s_in || !s_out) return fail(W8_ERR_NULL, "gate_up_swiglu_fp8: NULL pointer");
-  if (!aligned16(w_up)) return fail(W8_ERR_ALIGN, "gate_up_swiglu_fp8: w_up must be 16-byte aligned");
+  if (!w_up || !s_w_up || !s_in || !s_out) return fail(W8_ERR_NULL, "%s: NULL pointer", fn);
+  if (!aligned16(w_up)) return fail(W8_ERR_ALIGN, "%s: w_up must be 16-byte aligned", fn);
   if (x_dtype == W8_DTYPE_BF16) {
-    if (!ws) return fail(W8_ERR_NULL, "gate_up_swiglu_fp8: bf16 input needs the [M,K] E4M3 workspace");
-    if (!aligned16(ws)) return fail(W8_ERR_ALIGN, "gate_up_swiglu_fp8: ws must be 16-byte aligned");
+    if (!ws) return fail(W8_ERR_NULL, "%s: bf16 input needs the [M,K] E4M3 workspace", fn);
+    if (!aligned16(ws)) return fail(W8_ERR_ALIGN, "%s: ws must be 16-byte aligned", fn);
   }
   int sms = 0;
   if ((st = device_info(&sms)) != W8_OK) return st;
@@ -448,10 +479,31 @@ w8_status gate_up_swiglu_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t 
   p.s_w[1] = s_w_up;
   p.y[0] = out;
   p.s_out = s_out;
+  p.ex = ex;
   int terr = 0;
   cudaError_t e = w8::launch_gemm_glu(p, sms, s, &terr);
-  if (terr) return fail(W8_ERR_ALIGN, "gate_up_swiglu_fp8: tensor map encoding rejected the operands");
+  if (terr) return fail(W8_ERR_ALIGN, "%s: tensor map encoding rejected the operands", fn);
   return cuda_status(e, "gate_up_swiglu_fp8: GEMM launch");
+}
+
+w8_status gate_up_swiglu_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t K,
+                             const float* s_in, const uint8_t* w_gate, const uint8_t* w_up,
+                             int64_t I, const float* s_w_gate, const float* s_w_up,
+                             const float* s_out, uint8_t* out, uint8_t* ws, void* stream) {
+  return gate_up_swiglu_fp8_impl("gate_up_swiglu_fp8", x, x_dtype, M, K, s_in, w_gate, w_up, I, s_w_gate,
+                                 s_w_up, nullptr, s_out, out, ws, stream);
+}
+
+w8_status gate_up_swiglu_ex_fp8(const void* x, int32_t x_dtype, int64_t M, int64_t K,
+                                const float* s_in, const uint8_t* w_gate, const uint8_t* w_up,
+                                int64_t I, const float* s_w_gate, const float* s_w_up,
+                                const w8_swiglu_params* prm, const float* s_out, uint8_t* out,
+                                uint8_t* ws, void* stream) {
+  w8::SwigluExArgs a{};
+  w8_status st = check_swiglu_params("gate_up_swiglu_ex_fp8", prm, &a);
+  if (st != W8_OK) return st;
+  return gate_up_swiglu_fp8_impl("gate_up_swiglu_ex_fp8", x, x_dtype, M, K, s_in, w_gate, w_up, I, s_w_gate,
+                                 s_w_up, &a, s_out, out, ws, stream);
 }
 
 static w8_status check_swiglu(const char* fn, const uint16_t* g, const uint16_t* u, int64_t M,
@@ -497,16 +549,7 @@ static w8_status check_swiglu_ex(const char* fn, const void* g, const void* u, i
   if (st != W8_OK) return st;
   if (in_dtype != W8_DTYPE_BF16 && in_dtype != W8_DTYPE_F16)
     return fail(W8_ERR_DTYPE, "%s: in_dtype %d is neither bf16 nor f16", fn, in_dtype);
-  if (!prm) return fail(W8_ERR_NULL, "%s: NULL params", fn);
-  if (!std::isfinite(prm->alpha) || !std::isfinite(prm->beta))
-    return fail(W8_ERR_PARAM, "%s: alpha and beta must be finite", fn);
-  if (prm->has_limit && !(std::isfinite(prm->limit) && prm->limit > 0.0f))
-    return fail(W8_ERR_PARAM, "%s: limit must be finite and > 0", fn);
-  a->has_limit = prm->has_limit != 0;
-  a->limit = prm->limit;
-  a->alpha = prm->alpha;
-  a->beta = prm->beta;
-  return W8_OK;
+  return check_swiglu_params(fn, prm, a);
 }
 
 w8_status swiglu_2in_ex_fp8(const void* gate, const void* up, int32_t in_dtype, int64_t M, int64_t I,

@@ -26,11 +26,15 @@
 //  GLU16 (kind::f16): the gate and up projections of a 16-bit step on
 //        dequantized weights, with the SwiGLU written as bf16 -- the values
 //        swiglu_2in_bf16 would produce from the bf16 outputs of BF16.
+//  GLUX / GLU16X: GLU / GLU16 with the SwiGLU options (limit, alpha, beta;
+//        TensorRT-LLM PR #17476, section Test Coverage) in the epilogue -- the
+//        values swiglu_2in_ex_fp8 / swiglu_2in_ex_16 would produce from the
+//        same bf16 gate and up.
 //  W8A16 (kind::f16, gemm_a16t_kernel below): the same product with the
 //        dequantized weight formed in TMEM inside the GEMM, for calls that
 //        provide no workspace.
 //
-// W8A8 / GLU / BF16 / GLU16 kernel shapes (template parameter CG):
+// W8A8 / GLU / BF16 / GLU16 (and GLUX / GLU16X) kernel shapes (template parameter CG):
 //   CG = 1  one CTA per SM computes a 128-row output tile.
 //   CG = 2  a cluster of two CTAs on two SMs computes a 256-row tile with
 //           CTA-pair MMAs (tcgen05 cta_group::2): each CTA stages its 128
@@ -71,17 +75,20 @@ constexpr uint32_t kAccCols = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kEpiBufBytes = 32 * 128;            // W8A8 staging: 32 rows x 64 bf16
 
-enum class Mode { W8A8, GLU, BF16, GLU16 };
+enum class Mode { W8A8, GLU, BF16, GLU16, GLUX, GLU16X };
 
 template <Mode MODE, int CG>
 struct Cfg {
-  static constexpr bool kGlu = (MODE == Mode::GLU || MODE == Mode::GLU16);
+  // GLUX / GLU16X: GLU / GLU16 with the SwiGLU options (limit, alpha, beta)
+  // in the epilogue; separate kernels, so that the plain forms keep theirs.
+  static constexpr bool kEx = (MODE == Mode::GLUX || MODE == Mode::GLU16X);
+  static constexpr bool kGlu = (MODE == Mode::GLU || MODE == Mode::GLU16 || kEx);
   // BF16: the W8A16 product on an already dequantized weight (bf16 x bf16,
   // kind::f16): the same tiles and pipeline (a 128-byte swizzle atom holds
   // 64 K-values instead of 128) and an unscaled epilogue.  GLU16: the gate/up pair of a 16-bit
   // step on dequantized weights, with the SwiGLU written as bf16.
-  static constexpr bool kBf16 = (MODE == Mode::BF16 || MODE == Mode::GLU16);
-  static constexpr bool kOut16 = (MODE == Mode::GLU16);
+  static constexpr bool kBf16 = (MODE == Mode::BF16 || MODE == Mode::GLU16 || MODE == Mode::GLU16X);
+  static constexpr bool kOut16 = (MODE == Mode::GLU16 || MODE == Mode::GLU16X);
   // W8A8: 256 output columns per tile.  GLU: 128 intermediate columns per
   // tile, computed by one N = 256 MMA whose B operand is [128 gate rows | 128
   // up rows] of the slice: D columns 0-127 hold gate, 128-255 hold up, and
@@ -159,6 +166,7 @@ struct Args {
   const float* s_in;
   const float* s_w[kMaxGroup];
   const float* s_out;  // GLU: the down projection's input scale
+  SwigluParams pr;     // GLUX / GLU16X: the SwiGLU options
   // L2 policies of the operand loads and the output stores (kL2Normal,
   // kL2Keep, kL2Stream), chosen per launch from what fits in L2
   int l2_a, l2_b, l2_y;
@@ -525,7 +533,8 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
                 // the bf16 values the separate gate / up GEMMs would have written
                 const uint32_t gw = cvt_bf16x2(__uint_as_float(rg[e]), __uint_as_float(rg[e + 1]));
                 const uint32_t uw = cvt_bf16x2(__uint_as_float(ru[e]), __uint_as_float(ru[e + 1]));
-                hw[j] = swiglu_bf16_pair(gw, uw);
+                if constexpr (C::kEx) hw[j] = swiglu_ex_16_pair<false>(gw, uw, args.pr);
+                else hw[j] = swiglu_bf16_pair(gw, uw);
               }
               const int j0 = 4 * lc + 2 * hh;
               *reinterpret_cast<uint4*>(bp + ((j0 ^ (lane & 7)) * 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -583,7 +592,16 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
                                    __fmul_rn(__uint_as_float(ru[e + 1]), alpha_u));
               }
               uint32_t c4[4];
-              swiglu_fp8_x16(gw, uw, s_out, rs_out, exact_only, c4);
+              if constexpr (C::kEx) {   // the options' specification, pair by pair
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  c4[j] = swiglu_ex_fp8_pair<false>(gw[2 * j], uw[2 * j], args.pr, s_out, rs_out, exact_only) |
+                          (swiglu_ex_fp8_pair<false>(gw[2 * j + 1], uw[2 * j + 1], args.pr, s_out, rs_out,
+                                                     exact_only)
+                           << 16);
+              } else {
+                swiglu_fp8_x16(gw, uw, s_out, rs_out, exact_only, c4);
+              }
 #pragma unroll
               for (int j = 0; j < 4; ++j) codes[4 * hh + j] = c4[j];
             }
@@ -992,6 +1010,9 @@ cudaError_t launch(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err
   args.num_kb = (int)((p.K + C::kBK - 1) / C::kBK);
   args.s_in = p.s_in;
   args.s_out = p.s_out;
+  if (C::kEx)
+    args.pr = SwigluParams{p.ex->limit, p.ex->alpha, p.ex->beta, p.ex->has_limit ? 1 : 0,
+                           p.ex->beta != 0.0f ? 1 : 0};
   const int tiles_m = (int)((p.M + BM * CG - 1) / (BM * CG));
   constexpr int kEl = C::kBf16 ? 2 : 1;  // operand element bytes
   const CUtensorMapDataType dt = C::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -1119,11 +1140,17 @@ cudaError_t launch_gemm_bf16(const GemmProblem& p, int sms, cudaStream_t st, int
 }
 
 cudaError_t launch_gemm_glu16(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  if (p.ex)
+    return use_pair(p) ? launch<Mode::GLU16X, 2>(p, sms, st, tmap_err)
+                       : launch<Mode::GLU16X, 1>(p, sms, st, tmap_err);
   return use_pair(p) ? launch<Mode::GLU16, 2>(p, sms, st, tmap_err)
                      : launch<Mode::GLU16, 1>(p, sms, st, tmap_err);
 }
 
 cudaError_t launch_gemm_glu(const GemmProblem& p, int sms, cudaStream_t st, int* tmap_err) {
+  if (p.ex)
+    return use_pair(p) ? launch<Mode::GLUX, 2>(p, sms, st, tmap_err)
+                       : launch<Mode::GLUX, 1>(p, sms, st, tmap_err);
   return use_pair(p) ? launch<Mode::GLU, 2>(p, sms, st, tmap_err)
                      : launch<Mode::GLU, 1>(p, sms, st, tmap_err);
 }

@@ -58,6 +58,7 @@ struct GemmProblem {
   const float* s_w[kMaxGroup];
   void* y[kMaxGroup];            // bf16 [M, N_g] (GLU: E4M3 [M, I])
   const float* s_out;            // GLU: input scale of the down projection
+  const SwigluExArgs* ex;        // GLU / GLU16: SwiGLU options, or nullptr for the plain form
 };
 
 // Returns cudaSuccess or the CUDA error; *tmap_err is set non-zero when a
