@@ -1,8 +1,9 @@
 """The path's entry points only enqueue work on the caller's stream, so a
 whole W8A8 block (shared-quant Q/K/V group, out-projection, fused gate/up +
 SwiGLU, down projection), a W8A16 block (fused, and through the
-dequantization workspace) and the input producer (modulated LayerNorm with
-the quantization fused) can be captured in a CUDA graph;
+dequantization workspace), the fused gate/up GEMMs with the SwiGLU options
+and the input producer (modulated LayerNorm with the quantization fused)
+can be captured in a CUDA graph;
 replaying the graph reproduces the eager results bit for bit."""
 
 import numpy as np
@@ -43,6 +44,8 @@ def test_block_in_cuda_graph(W):
         "qkv16w": [torch.empty((M, H), **bf) for _ in range(3)],
         "y16w": torch.empty((M, H), **bf),
         "h16f": torch.empty((M, I), **bf),
+        "h8x": torch.empty((M, I), dtype=torch.uint8, device="cuda"),
+        "h16x": torch.empty((M, I), **bf),
         "qn": torch.empty((M, H), dtype=torch.uint8, device="cuda"),
         "hn": torch.empty((M, H), **bf),
     }
@@ -66,6 +69,10 @@ def test_block_in_cuda_graph(W):
                                 ws=wsd)
         W.qkv_shared_quant_gemm(W.MODE_A16, outs["h16"], None, [wd[0]], [wd[1]], outs=[outs["y16w"]], ws=wsd)
         W.bf16_gate_up_swiglu(x, wdg, wdu, out=outs["h16f"])
+        # the fused gate/up with the SwiGLU options, both forms
+        W.gate_up_swiglu_fp8(x, s_in, wg[0], wu[0], wg[1], wu[1], s_h, out=outs["h8x"], ws=ws,
+                             limit=7.0, alpha=1.702, beta=1.0)
+        W.bf16_gate_up_swiglu(x, wdg, wdu, out=outs["h16x"], limit=3.0, alpha=1.0, beta=0.5)
         # the input producer with the quantization fused (two samples of 500 rows)
         W.ln_modulate_quant(x, mod[0], mod[1], s_in, out=outs["qn"], h_out=outs["hn"])
 
