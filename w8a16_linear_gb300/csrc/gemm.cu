@@ -592,13 +592,8 @@ __global__ void __launch_bounds__(Layout<MODE, CG>::kThreads, 1)
                                    __fmul_rn(__uint_as_float(ru[e + 1]), alpha_u));
               }
               uint32_t c4[4];
-              if constexpr (C::kEx) {   // the options' specification, pair by pair
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  c4[j] = swiglu_ex_fp8_pair<false>(gw[2 * j], uw[2 * j], args.pr, s_out, rs_out, exact_only) |
-                          (swiglu_ex_fp8_pair<false>(gw[2 * j + 1], uw[2 * j + 1], args.pr, s_out, rs_out,
-                                                     exact_only)
-                           << 16);
+              if constexpr (C::kEx) {   // the options' specification, 8 pairs at a time
+                swiglu_ex_fp8_x16<false>(gw, uw, args.pr, s_out, rs_out, exact_only, c4);
               } else {
                 swiglu_fp8_x16(gw, uw, s_out, rs_out, exact_only, c4);
               }

@@ -380,6 +380,49 @@ __device__ __forceinline__ uint32_t swiglu_ex_fp8_pair(uint32_t gw, uint32_t uw,
   return code;
 }
 
+// The specification's codes of one pair with the options (the rare path of
+// swiglu_ex_fp8_x16): the operands again, the specified denominator, the
+// correctly rounded divisions.
+template <bool kF16>
+__device__ __forceinline__ uint32_t swiglu_ex_fp8_exact_pair(uint32_t gw, uint32_t uw, const SwigluParams& pr,
+                                                             float s) {
+  F2 t, p;
+  swiglu_ex_operands<kF16>(gw, uw, pr, t, p);
+  const F2 de = add2(splat(1.0f), exp_spec2(neg(t)));
+  return cvt_e4m3x2(__fdiv_rn(__fdiv_rn(p.x, de.x), s), __fdiv_rn(__fdiv_rn(p.y, de.y), s));
+}
+
+// swiglu_ex_fp8_pair over 8 packed pairs: the fast codes of all of them,
+// then one rarely taken branch for the pairs the bracket cannot settle (or
+// whose gate is below -16), as swiglu_fp8_x16 does for the plain form.  The
+// codes are swiglu_ex_fp8_pair's, bit for bit.  For callers with registers to
+// spare (the fused gate/up GEMM's epilogue).
+template <bool kF16>
+__device__ __forceinline__ void swiglu_ex_fp8_x16(const uint32_t (&gw)[8], const uint32_t (&uw)[8],
+                                                  const SwigluParams& pr, float s, float rs, bool exact_only,
+                                                  uint32_t (&codes)[4]) {
+  uint32_t c[8];
+  uint32_t bad = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    F2 t, p;
+    swiglu_ex_operands<kF16>(gw[j], uw[j], pr, t, p);
+    const F2 d = add2(splat(1.0f), F2{__expf(-t.x), __expf(-t.y)});
+    const F2 hf = mul2(p, F2{rcp_approx(d.x), rcp_approx(d.y)});
+    bool unsettled;
+    c[j] = e4m3x2_bracket(mul2(hf, splat(rs)), kFp8BracketLo, kFp8BracketHi, unsettled);
+    bad |= (uint32_t)(unsettled | (t.x < -16.0f) | (t.y < -16.0f)) << j;
+  }
+  if (exact_only) bad = 0xFFu;
+  if (bad) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (bad & (1u << j)) c[j] = swiglu_ex_fp8_exact_pair<kF16>(gw[j], uw[j], pr, s);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) codes[j] = c[2 * j] | (c[2 * j + 1] << 16);
+}
+
 __device__ __forceinline__ uint32_t cvt16x2(bool f16, float lo, float hi) {
   return f16 ? cvt_f16x2(lo, hi) : cvt_bf16x2(lo, hi);
 }
