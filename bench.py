@@ -793,7 +793,7 @@ def run_case(args):
             W.swiglu_2in_ex_16(gg, uu, out=h16, **opts)
     elif args.case == "w8a16_8k":
         fn = lambda: W.qkv_shared_quant_gemm(W.MODE_A16, x, None, qs, ss, outs=ys)  # noqa: E731
-    elif args.case == "glu8k":
+    elif args.case in ("glu8k", "glu_ex8k"):
         # weights as in the bench: N(0, 0.02^2) with amax/448 scales, so the
         # SwiGLU inputs have a realistic spread (the exact-division fallback of
         # the epilogue is data dependent)
@@ -805,7 +805,11 @@ def run_case(args):
         s_x = (x.float().abs().amax() / 448).reshape(1).contiguous()
         s_h = torch.tensor([0.02], device=dev)
         h8 = torch.empty((M, INTER), dtype=torch.uint8, device=dev)
-        fn = lambda: W.gate_up_swiglu_fp8(x, s_x, wg, wu, sg, su, s_h, out=h8, ws=qx)  # noqa: E731
+        if args.case == "glu_ex8k":   # the same with the SwiGLU options in the epilogue
+            fn = lambda: W.gate_up_swiglu_fp8(x, s_x, wg, wu, sg, su, s_h, out=h8, ws=qx,  # noqa: E731
+                                              limit=7.0, alpha=1.702, beta=1.0)
+        else:
+            fn = lambda: W.gate_up_swiglu_fp8(x, s_x, wg, wu, sg, su, s_h, out=h8, ws=qx)  # noqa: E731
     elif args.case == "qkv_sustained":
         # Sustained comparison under the power cap: the Q/K/V group launch
         # (20670 x 4096 -> 3 x 4096, E4M3 input) against cuBLASLt FP8 on the
@@ -999,7 +1003,7 @@ def main():
     ap.add_argument("--no-breakdown", action="store_true",
                     help="print the headline line without the breakdown (for launch-list captures)")
     ap.add_argument("--case", default=None,
-                    help="run a profiling case (qkv8k, lin4k, w8a16_8k, w8a16_dq_8k, glu8k, glu16_8k, swiglu8k, swiglu_ex8k, ln20k, quant20k, dequant16k, block_gemms, qkv_sustained, host_link) instead of the bench")
+                    help="run a profiling case (qkv8k, lin4k, w8a16_8k, w8a16_dq_8k, glu8k, glu_ex8k, glu16_8k, swiglu8k, swiglu_ex8k, ln20k, quant20k, dequant16k, block_gemms, qkv_sustained, host_link) instead of the bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.case:
